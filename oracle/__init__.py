@@ -1,0 +1,10 @@
+"""Reference oracle for the attention library's parity tests.
+
+TEST INFRASTRUCTURE ONLY: imported by ``tests/``, the smoke check and the
+benchmark's CPU-baseline leg, never by the library itself.
+"""
+
+from .mqa import (  # noqa: F401
+    attention, block_status, pad_rows, pair_visibility, raw_visible, comp_visible,
+    padded_lengths, ceil_to, H, D, BLOCK,
+)
