@@ -1,0 +1,523 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused multi-query attention path on GB300.
+
+One step = one decode attention call over the decode workload at 32768
+context on a ratio-128 layer (T = 1, 64 heads, D = 512, 128 raw + 256
+compressed rows): the split-KV tcgen05 kernel plus the log-sum-exp merge.
+Prints ONE JSON line (rank 0).  See ``--help``.
+
+Timing: W eager warm-up steps, then exactly K steps replayed from CUDA graphs
+captured over R rotating input sets whose total size is several times the
+129 MB L2, bracketed by a barrier and a synchronize, CUDA events on the
+launching stream, max over ranks.  ``--gpus N`` under torchrun runs N
+independent replicas (the path has no exchange step).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode attn HBM GB/s (% of 8 TB/s); prefill attn TFLOP/s (% fp16 peak)"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_SOURCES = ["attn_kernel.cuh", "attn_params.h", "ptx.cuh", "attn.cu"]
+
+
+# ------------------------------------------------------------------ workload arithmetic
+
+def visible_rows(L: dict, t: int) -> int:
+    """Rows token t sees under the structural rule (window + pooled rows)."""
+    p = L["q_pos0"] + t
+    lo = max(0, p - L["window"] + 1 - L["raw_pos0"])
+    hi = min(L["n_raw"], p + 1 - L["raw_pos0"])
+    comp = min(L["n_comp"], (p + 1) // L["ratio"]) if L["n_comp"] else 0
+    return max(0, hi - lo) + comp
+
+
+def decode_bytes(L: dict) -> int:
+    """Compulsory HBM bytes of one decode call: Q, the visible K and V rows, O."""
+    rows = sum(visible_rows(L, t) for t in range(L["T"]))
+    return rows * 2 * 1024 + L["T"] * 2 * 64 * 512 * 2
+
+
+def attn_flops(L: dict, rows_per_token=None) -> float:
+    """4 * H * D flops per (token, visible row): QK^T and PV."""
+    rows = rows_per_token if rows_per_token is not None else sum(visible_rows(L, t) for t in range(L["T"]))
+    return 4.0 * 64 * 512 * rows
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "mqa_flash_attention_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per launch of the attention kernel from the committed ncu
+    summary, if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    if not e or e.get("kernel_hash") != kernel_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples every 100 ms while running; keeps those inside [t0, t1]."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        inside = [r for ts, r in self.rows if t0 <= ts <= t1]
+        window = "timed region"
+        if not inside and self.rows:
+            # a short timed region can fall between two samples: take the nearest ones
+            inside = [min(self.rows, key=lambda x: abs(x[0] - (t0 + t1) / 2))[1]]
+            window = "nearest sample to the timed region"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "window": "no nvidia-smi"}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        sm, smax, pw = [], [], []
+        for r in inside:
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+                pw.append(float(r[3]))
+            except (ValueError, IndexError):
+                continue
+            for i, n in enumerate(names):
+                if len(r) > 5 + i and r[5 + i].lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(pw) if pw else None, "reasons": sorted(reasons), "samples": len(inside),
+                "window": window}
+
+
+# ------------------------------------------------------------------ CPU oracle legs
+
+def oracle_leg(workload: str, seconds: float, heads: int | None = None) -> dict:
+    """Times the fp64 oracle (as it stands) on this process's host threads."""
+    import numpy as np
+    import oracle
+    from mqa_flash_attention_gb300 import workloads as W
+    wl = getattr(W, workload)()
+    L = wl.layout
+    q = wl.q if heads is None else np.ascontiguousarray(wl.q[:, :heads])
+    frac = 1.0 if heads is None else heads / 64.0
+    calls, t0 = 0, time.perf_counter()
+    while True:
+        oracle.attention(L, q, wl.k_raw, wl.v_raw, wl.k_comp, wl.v_comp)
+        calls += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    per_call = el / calls
+    return {"seconds_per_call": per_call, "calls": calls, "fraction_of_call": frac}
+
+
+def run_oracle_subprocess(workload: str, seconds: float, heads=None) -> dict:
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    cmd = [sys.executable, os.path.abspath(__file__), "--_oracle-leg", workload, "--_seconds", str(seconds)]
+    if heads:
+        cmd += ["--_heads", str(heads)]
+    r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=600)
+    if r.returncode != 0:
+        raise RuntimeError(f"oracle leg failed: {r.stderr[-2000:]}")
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_ours(args) -> None:
+    import numpy as np
+    import torch
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    from mqa_flash_attention_gb300 import build, ds4a
+    from mqa_flash_attention_gb300 import workloads as W
+    build.build()
+    lib = ds4a.lib()
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(x: float) -> float:
+        if world == 1:
+            return x
+        import torch.distributed as dist
+        t = torch.tensor([x], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    wl = W.decode_r128_32k()
+    L = wl.layout
+    step_bytes = decode_bytes(L)
+    set_bytes = sum(a.nbytes for a in (wl.q, wl.k_raw, wl.v_raw, wl.k_comp, wl.v_comp)) + wl.q.nbytes
+    R = max(8, math.ceil(4 * L2_BYTES / set_bytes))
+    dev = torch.device("cuda", local)
+
+    def to_dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    base = [to_dev(a) for a in (wl.q, wl.k_raw, wl.v_raw, wl.k_comp, wl.v_comp)]
+    sets = []
+    for i in range(R):
+        # distinct buffers per set (same values): every step reads memory the previous steps did not touch
+        sets.append([b.clone() for b in base] + [torch.empty_like(base[0])])
+    n_splits = ds4a.decode_default_splits(L)
+    ws = torch.empty(ds4a.decode_workspace_bytes(L, n_splits), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(i):
+        q, kr, vr, kc, vc, o = sets[i % R]
+        ds4a.attn_decode(L, q, kr, vr, kc, vc, n_splits=n_splits, workspace=ws, out=o, stream=stream)
+
+    def partial_step(i):
+        q, kr, vr, kc, vc, _ = sets[i % R]
+        ds4a.attn_decode_partials(L, q, kr, vr, kc, vc, n_splits=n_splits, workspace=ws, stream=stream)
+
+    K, Wm = args.steps, args.warmup
+    with torch.cuda.stream(stream):
+        for i in range(Wm):
+            step(i)
+    torch.cuda.synchronize()
+
+    def capture(fn, n, offset=0):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                fn(offset + i)
+        return g
+
+    g_full = capture(step, min(R, K))
+    g_tail = capture(step, K % R) if K > R and K % R else None
+    n_full = K // R if K >= R else 1
+    g_full.replay()
+    if g_tail is not None:
+        g_tail.replay()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.25)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_host0 = time.time()
+    e0.record(stream)
+    for _ in range(n_full):
+        g_full.replay()
+    if g_tail is not None:
+        g_tail.replay()
+    e1.record(stream)
+    barrier()
+    t_host1 = time.time()
+    sampler.stop()
+    elapsed_ms = max_over_ranks(e0.elapsed_time(e1))
+    ms_per_step = elapsed_ms / K
+    value = step_bytes * K * world / (elapsed_ms * 1e-3) / 1e9
+    clocks = sampler.summary(t_host0, t_host1)
+
+    # Dominant kernel alone (split-KV attention, no merge): graph of R launches.
+    gp = capture(partial_step, R)
+    gp.replay()
+    torch.cuda.synchronize()
+    reps = max(1, min(50, 20000 // R))
+    p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    p0.record(stream)
+    for _ in range(reps):
+        gp.replay()
+    p1.record(stream)
+    torch.cuda.synchronize()
+    kernel_us = p0.elapsed_time(p1) * 1e3 / (reps * R)
+    pk, pk_kind = peaks()
+    achieved = step_bytes / (kernel_us * 1e-6) / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": ncu_traffic("decode_r128_32k"),
+                "kernel": "ds4a::attn_fwd_kernel (split-KV partials)", "kernel_us": round(kernel_us, 3),
+                "peak_kind": f"{pk_kind} hbm_gbs (copy bandwidth)",
+                "algorithmic_bytes_per_launch": step_bytes}
+
+    # End to end through the API with host buffers: H2D inputs, call, D2H output, every step.
+    host_in = [torch.from_numpy(np.ascontiguousarray(a)).pin_memory() for a in (wl.q, wl.k_raw, wl.v_raw,
+                                                                                wl.k_comp, wl.v_comp)]
+    host_out = torch.empty(tuple(wl.q.shape), dtype=torch.float16).pin_memory()
+    dq, dkr, dvr, dkc, dvc, do = sets[0]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = host_out.numel() * host_out.element_size()
+    Ke = min(K, 2000)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            for d, h in zip((dq, dkr, dvr, dkc, dvc), host_in):
+                d.copy_(h, non_blocking=True)
+            ds4a.attn_decode(L, dq, dkr, dvr, dkc, dvc, n_splits=n_splits, workspace=ws, out=do, stream=stream)
+            host_out.copy_(do, non_blocking=True)
+    barrier()
+    x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        x0.record(stream)
+        for _ in range(Ke):
+            for d, h in zip((dq, dkr, dvr, dkc, dvc), host_in):
+                d.copy_(h, non_blocking=True)
+            ds4a.attn_decode(L, dq, dkr, dvr, dkc, dvc, n_splits=n_splits, workspace=ws, out=do, stream=stream)
+            host_out.copy_(do, non_blocking=True)
+        x1.record(stream)
+    barrier()
+    e2e_ms = max_over_ranks(x0.elapsed_time(x1)) / Ke
+    e2e = {"value": round(step_bytes * world / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": Ke, "ms_per_step": round(e2e_ms, 5)}
+
+    # Correctness guard on the timed outputs (decode of set 0 vs the kernel's own eager result).
+    ref = torch.empty_like(sets[0][5])
+    ds4a.attn_decode(L, *sets[0][:5], n_splits=n_splits, workspace=ws, out=ref, stream=stream)
+    torch.cuda.synchronize()
+    if not torch.equal(ref, sets[0][5]) or ds4a.device_status() != ds4a.OK:
+        raise RuntimeError("timed outputs differ from an eager call or a device wait ran out")
+
+    also = None
+    if rank == 0 and not args.no_also:
+        also = run_also(torch, ds4a, W, dev, stream, pk, pk_kind)
+
+    cpu = None
+    if rank == 0:
+        leg = run_oracle_subprocess("decode_r128_32k", args.cpu_seconds)
+        cpu = {"value": round(step_bytes / leg["seconds_per_call"] / 1e9, 4), "unit": "GB/s", "cores": 1,
+               "kind": "oracle",
+               "sample": f"full decode call (T=1, 384 rows) x {leg['calls']} calls, "
+                         f"{leg['seconds_per_call'] * 1e3:.2f} ms per call, fp64 numpy, 1 thread"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
+            "warmup": Wm, "ms_per_step": round(ms_per_step, 6), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+            "config": {"workload": "decode_ratio128_ctx32768: T=1, 64 q-heads, 1 KV head, D=512, 128 raw + "
+                                   "256 compressed rows (all visible), fp16 N(0,1)",
+                       "global_batch": world, "seq_len": 32768, "parallelism": f"replicas{world}",
+                       "n_splits": n_splits, "rotating_input_sets": R,
+                       "l2": f"inputs rotate over {R} sets ({R * set_bytes / 2**20:.0f} MiB > L2)",
+                       "timing": "CUDA graphs of the decode call, CUDA events on the launching stream",
+                       "step": "ds4a_attn_decode = split-KV tcgen05 attention (in-kernel block selection, "
+                               "TMA zero-filled ragged tiles) + LSE merge"},
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 2 * K, "clocks": clocks,
+        }
+        if also is not None:
+            line["also"] = also
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_also(torch, ds4a, W, dev, stream, pk, pk_kind):
+    """The other headline shapes, each timed alone: prefill TFLOP/s, indexed
+    TFLOP/s, long decode GB/s, with their roofline fractions."""
+    import numpy as np
+    out = []
+
+    def timed(fn, n):
+        for _ in range(2):
+            fn(0)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                fn(i)
+        g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) * 1e-3 / n
+
+    def up(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    # prefill, raw-only, T = 2048 (two input sets alternate: each is ~270 MB > L2)
+    wl = W.prefill_raw_2048()
+    sets = [[up(wl.q), up(wl.k_raw), up(wl.v_raw), torch.empty(wl.q.shape, dtype=torch.float16, device=dev)]
+            for _ in range(2)]
+    sec = timed(lambda i: ds4a.attn_prefill(wl.layout, sets[i % 2][0], sets[i % 2][1], sets[i % 2][2],
+                                            out=sets[i % 2][3], stream=stream), 10)
+    fl = attn_flops(wl.layout)
+    by = 2 * wl.q.nbytes + wl.k_raw.nbytes + wl.v_raw.nbytes
+    out.append({"workload": wl.name, "us_per_call": round(sec * 1e6, 2),
+                "tflops": round(fl / sec / 1e12, 1), "frac_tensor": round(fl / sec / 1e12 / pk["bf16_tflops"], 4),
+                "hbm_gbs": round(by / sec / 1e9, 1), "frac_hbm": round(by / sec / 1e9 / pk["hbm_gbs"], 4),
+                "algorithmic_flops": fl, "algorithmic_bytes": by})
+    del sets
+    # indexed ratio-4, T = 2048, top-512
+    wl = W.indexed_r4_2048()
+    sets = [[up(wl.q), up(wl.k_raw), up(wl.v_raw), up(wl.k_comp), up(wl.v_comp), up(wl.idx),
+             torch.empty(wl.q.shape, dtype=torch.float16, device=dev)] for _ in range(2)]
+    sec = timed(lambda i: ds4a.attn_indexed(wl.layout, *sets[i % 2][:6], out=sets[i % 2][6], stream=stream), 6)
+    rows = sum(min(wl.layout["n_raw"], 128) + int((wl.idx[t] >= 0).sum()) for t in range(wl.layout["T"]))
+    fl = attn_flops(wl.layout, rows)
+    out.append({"workload": wl.name, "us_per_call": round(sec * 1e6, 2),
+                "tflops": round(fl / sec / 1e12, 1), "frac_tensor": round(fl / sec / 1e12 / pk["bf16_tflops"], 4),
+                "algorithmic_flops": fl})
+    del sets
+    # long decode, 262144 compressed rows (537 MB of K/V > L2)
+    wl = W.decode_long(262144)
+    d = [up(a) for a in (wl.q, wl.k_raw, wl.v_raw, wl.k_comp, wl.v_comp)]
+    o = torch.empty(wl.q.shape, dtype=torch.float16, device=dev)
+    ws = torch.empty(ds4a.decode_workspace_bytes(wl.layout), dtype=torch.uint8, device=dev)
+    sec = timed(lambda i: ds4a.attn_decode(wl.layout, *d, workspace=ws, out=o, stream=stream), 10)
+    by = decode_bytes(wl.layout)
+    out.append({"workload": wl.name, "us_per_call": round(sec * 1e6, 2), "hbm_gbs": round(by / sec / 1e9, 1),
+                "frac_hbm": round(by / sec / 1e9 / pk["hbm_gbs"], 4), "algorithmic_bytes": by})
+    for e in out:
+        e["peak_kind"] = pk_kind
+    return out
+
+
+# ------------------------------------------------------------------ reference arm
+
+def run_reference(args) -> None:
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return
+    from mqa_flash_attention_gb300 import workloads as W
+    wl = W.decode_r128_32k()
+    L = wl.layout
+    step_bytes = decode_bytes(L)
+    probe = oracle_leg("decode_r128_32k", 0.5)
+    per_call = probe["seconds_per_call"]
+    budget = 90.0
+    heads = None
+    if (args.steps + args.warmup) * per_call > budget:
+        heads = max(1, min(64, int(64 * budget / ((args.steps + args.warmup) * per_call))))
+    import numpy as np  # noqa: F401
+    import oracle
+    q = wl.q if heads is None else np.ascontiguousarray(wl.q[:, :heads])
+    for _ in range(args.warmup):
+        oracle.attention(L, q, wl.k_raw, wl.v_raw, wl.k_comp, wl.v_comp)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.attention(L, q, wl.k_raw, wl.v_raw, wl.k_comp, wl.v_comp)
+    el = time.perf_counter() - t0
+    frac = 1.0 if heads is None else heads / 64.0
+    value = step_bytes * frac * args.steps / el / 1e9
+    sample = ("full decode call (T=1, 384 rows) per step" if heads is None else
+              f"{heads} of 64 heads of the decode call per step (bytes scaled by {frac:.3f})")
+    cores = 1
+    line = {"metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(el * 1e3 / args.steps, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "decode_ratio128_ctx32768: T=1, 64 q-heads, 1 KV head, D=512, 128 raw + "
+                                   "256 compressed rows (all visible), fp16 N(0,1)",
+                       "global_batch": 1, "seq_len": 32768, "parallelism": "host"},
+            "impl": "reference",
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-also", action="store_true", help="skip the prefill / indexed / long-decode lines")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="length of the CPU oracle baseline")
+    ap.add_argument("--_oracle-leg", dest="oracle_leg", default=None, help=argparse.SUPPRESS)
+    ap.add_argument("--_seconds", dest="leg_seconds", type=float, default=10.0, help=argparse.SUPPRESS)
+    ap.add_argument("--_heads", dest="leg_heads", type=int, default=None, help=argparse.SUPPRESS)
+    args = ap.parse_args()
+    if args.oracle_leg:
+        print(json.dumps(oracle_leg(args.oracle_leg, args.leg_seconds, args.leg_heads)))
+        return
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    if "--impl" in sys.argv and "reference" in sys.argv:
+        for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+            os.environ[v] = "1"
+    main()

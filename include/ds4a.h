@@ -1,0 +1,269 @@
+/*
+ * ds4a.h - C ABI of the GB300 fused multi-query attention forward used by the
+ * DeepSeek V4 Flash layers of the ds4 engine.
+ *
+ * Sources of the operation (page titles and sections):
+ *  [P1] "How DeepSeek V4 Flash Model Inference Works on Apple Silicon with
+ *       Metal Backend": "KV-Cache Management on Metal Device Buffers" (K/V rows
+ *       padded to a multiple of 32), "FlashAttention Kernel Architecture" (pad,
+ *       block-scan and fused attention kernels; Q.K, softmax and V weighting in
+ *       one dispatch), "Mask Handling and Block Skipping" (one status byte per
+ *       block, fully masked blocks skipped), "Memory Layout and Zero-Copy Buffer
+ *       Access" (raw byte buffers with host-computed byte strides).
+ *  [P2] "DwarfStar 4 (DS4) - DeepSeek V4 Flash Inference Engine": "Fixed Model
+ *       Shape" (64 query heads, 1 K/V head, head dim 512, 128-token sliding
+ *       window), "Layer Compression" (raw-only layers, ratio-4 layers with a
+ *       top-512 index list, ratio-128 layers), "GPU Backend Architecture"
+ *       (raw / mixed / indexed mixed heads and prefill attention ops), "KV Cache
+ *       Design" (raw ring rows, compressed rows pooled every 4 or 128 tokens),
+ *       "Whole-Model Graph Execution" (2048-token prefill chunks, one-token
+ *       decode).
+ *
+ * What every attention call computes, for each query token t at position
+ * p = q_pos0 + t and each head h < 64:
+ *
+ *     o[t][h] = sum_j softmax_j( scale * q[t][h] . k_j + bias_j ) * v_j
+ *
+ * over the rows j the token may see:
+ *   - raw row i (position raw_pos0 + i) when p - window + 1 <= raw_pos0 + i <= p;
+ *   - structural mode: compressed row c when (c + 1) * ratio <= p + 1
+ *     (its pooled span c*ratio .. (c+1)*ratio-1 has ended);
+ *   - indexed mode: compressed row idx[t][k] for every list entry >= 0 (each
+ *     entry counts once per occurrence);
+ *   - dense-mask mode: every real row of the padded logical sequence whose
+ *     mask entry is not -inf; the entry is bias_j (natural-log units).
+ * bias_j = 0 outside dense-mask mode.  A token with no visible row gets o = 0
+ * and lse = -inf.  lse[t][h] = log(sum_j exp(scale*q.k_j + bias_j)).
+ *
+ * Logical sequence (block numbering, dense masks):
+ *     [ raw rows, padded to a multiple of 32 | compressed rows, padded to 32 ]
+ * Pad rows are never visible.  Block b covers logical rows 32b .. 32b+31.
+ *
+ * Conventions shared by all calls
+ *   - Head count H = 64 and head dim D = 512 are fixed.  Every tensor is fp16
+ *     (IEEE binary16) unless stated.  All arithmetic after the fp16 loads is
+ *     fp32; outputs are rounded to fp16 to nearest-even.
+ *   - Every tensor pointer is a DEVICE pointer owned by the caller.  The
+ *     library keeps no reference after the call returns and allocates no
+ *     device memory.
+ *   - A row of K or V is 512 contiguous fp16 (1024 bytes).  Row strides are in
+ *     BYTES, must be >= 1024 and multiples of 16; base pointers must be
+ *     16-byte aligned.  Q and O are [T][64][512]: heads contiguous (1024 bytes
+ *     apart), token stride in bytes (>= 65536, multiple of 16).
+ *   - K and V may alias (k == v), as in an engine that stores one KV row.
+ *   - Rows that a token cannot see must still hold finite values (pad rows
+ *     written by ds4a_pad_kv are +0.0): an invisible row gets weight 0, and
+ *     0 * inf or 0 * nan would poison the sum.
+ *   - Calls are asynchronous on `stream` (NULL = legacy default stream).  Bad
+ *     arguments are reported synchronously, before anything is launched.  A
+ *     failed launch returns DS4A_ERR_CUDA.  Kernels never trap: every device
+ *     wait is bounded, and a wait that runs out records an error word read by
+ *     ds4a_device_status().
+ *   - The calls hold no mutable host state and are safe to issue from several
+ *     host threads on different streams.
+ */
+#ifndef DS4A_H
+#define DS4A_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DS4A_HEADS 64
+#define DS4A_HEAD_DIM 512
+#define DS4A_BLOCK_ROWS 32
+#define DS4A_ROW_BYTES 1024
+
+/* A CUDA stream handle (cudaStream_t / CUstream). */
+typedef struct CUstream_st *ds4a_stream_t;
+
+typedef enum {
+  DS4A_OK = 0,
+  DS4A_ERR_INVALID_ARG = 1, /* an argument breaks the contract; nothing launched */
+  DS4A_ERR_UNSUPPORTED = 2, /* valid request this build does not serve (e.g. no sm_103a device) */
+  DS4A_ERR_WORKSPACE = 3,   /* workspace missing or smaller than ds4a_attn_decode_workspace_size() */
+  DS4A_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed (launch, tensor-map encode, ...) */
+  DS4A_ERR_TIMEOUT = 5      /* a bounded device wait ran out (reported by ds4a_device_status) */
+} ds4a_status;
+
+/* Static message for a status code; never NULL. */
+const char *ds4a_status_string(int status);
+
+/* Library version string, e.g. "ds4a 0.1 sm_103a". */
+const char *ds4a_version(void);
+
+/*
+ * Query geometry.  All positions are absolute token positions ([P2] "KV Cache
+ * Design": raw rows are kept in logical order; compressed rows are numbered
+ * from the start of the sequence).
+ *   T        query tokens in this call (>= 0); token t is at q_pos0 + t.
+ *   q_pos0   position of token 0 (>= 0).
+ *   n_raw    raw rows passed (>= 0); raw row i is at position raw_pos0 + i.
+ *   raw_pos0 position of raw row 0 (>= 0).
+ *   n_comp   compressed rows passed (>= 0; 0 = none).
+ *   ratio    pooling ratio of the compressed rows (>= 1 when n_comp > 0; the
+ *            model uses 4 and 128).
+ *   window   sliding-window length in positions, self included (>= 1; the
+ *            model uses 128).
+ *   scale    softmax scale applied to q.k (the model uses 1/sqrt(512)).
+ */
+typedef struct {
+  int32_t T, q_pos0;
+  int32_t n_raw, raw_pos0;
+  int32_t n_comp, ratio;
+  int32_t window;
+  float scale;
+} ds4a_layout;
+
+/*
+ * Operands of one attention call (device pointers, byte strides).
+ *   q      fp16 [T][64][512]; token stride q_tok_stride.
+ *   k_raw, v_raw   fp16 [n_raw][512]; row stride raw_row_stride.  May be NULL
+ *          when n_raw == 0.
+ *   k_comp, v_comp fp16 [n_comp][512]; row stride comp_row_stride.  May be NULL
+ *          when n_comp == 0.
+ *   o      fp16 [T][64][512] output; token stride o_tok_stride.  Must not
+ *          overlap any input.
+ *   lse    fp32 [T][64] output (natural log), or NULL.
+ */
+typedef struct {
+  const void *q;
+  int64_t q_tok_stride;
+  const void *k_raw, *v_raw;
+  int64_t raw_row_stride;
+  const void *k_comp, *v_comp;
+  int64_t comp_row_stride;
+  void *o;
+  int64_t o_tok_stride;
+  float *lse;
+} ds4a_tensors;
+
+/*
+ * ds4a_pad_kv - [P1] "KV-Cache Management on Metal Device Buffers" and
+ * "FlashAttention Kernel Architecture" (the pad kernel): writes
+ *     dst[i] = src[i]  for i <  n_rows,
+ *     dst[i] = +0.0    for n_rows <= i < ceil(n_rows / 32) * 32,
+ * row by row (512 fp16 per row).  dst must hold ceil(n_rows/32)*32 rows at
+ * dst_row_stride.  In-place use (dst == src, equal strides) only writes the
+ * zero tail.  Other overlaps are invalid.  n_rows == 0 is a no-op.
+ */
+ds4a_status ds4a_pad_kv(const void *src, int64_t src_row_stride, int32_t n_rows,
+                        void *dst, int64_t dst_row_stride, ds4a_stream_t stream);
+
+/* Number of 32-row blocks of the padded logical sequence of L
+ * (ceil(n_raw/32) + ceil(n_comp/32)), or -1 if L is NULL. */
+int32_t ds4a_block_count(const ds4a_layout *L);
+
+/*
+ * ds4a_block_mask - [P1] "Mask Handling and Block Skipping" (the block-scan
+ * kernel): one status byte per (q-tile of q_tile consecutive tokens, 32-row
+ * block of the logical sequence), row-major [ceil(T/q_tile)][block_count]:
+ *     0 = no (token, row) pair of the tile and block is visible (skippable),
+ *     2 = every pair is visible with zero bias,
+ *     1 = otherwise.
+ * dense_mask == NULL: the structural rule (window + pooled compressed rows).
+ * Otherwise dense_mask is fp16 [T][block_count*32] at mask_row_stride bytes
+ * (>= block_count*64, multiple of 16); a pair is visible iff its entry is not
+ * -inf and the row is real; "zero bias" means the entry is +0.0 or -0.0.
+ * q_tile >= 1.  The result is exact (integer work).
+ */
+ds4a_status ds4a_block_mask(const ds4a_layout *L, const void *dense_mask, int64_t mask_row_stride,
+                            int32_t q_tile, uint8_t *status, ds4a_stream_t stream);
+
+/*
+ * ds4a_attn_prefill - [P1] "FlashAttention Kernel Architecture" (the fused
+ * attention kernel) with [P2] "GPU Backend Architecture" (raw heads, mixed
+ * heads, flash attention prefill) and "Whole-Model Graph Execution"
+ * (2048-token prefill chunks).  One pass per query token over its visible
+ * rows; the output is normalised in the same kernel.
+ *   dense_mask / mask_row_stride: NULL for the structural rule, else as in
+ *          ds4a_block_mask (the mask replaces the structural rule).
+ *   status / q_tile: optional block-status bytes as written by
+ *          ds4a_block_mask for the same layout, mask and q_tile.  With a
+ *          dense mask, blocks marked 0 are skipped and mask entries of blocks
+ *          marked 2 are not read.  Without a mask the kernel derives the same
+ *          skips from the layout (it never reads a row of a block marked 0), so
+ *          status is not needed and, if given, must agree with the layout.
+ * Any T >= 0 is accepted.
+ */
+ds4a_status ds4a_attn_prefill(const ds4a_layout *L, const ds4a_tensors *X,
+                              const void *dense_mask, int64_t mask_row_stride,
+                              const uint8_t *status, int32_t q_tile, ds4a_stream_t stream);
+
+/*
+ * ds4a_attn_decode - the same result as ds4a_attn_prefill for few query
+ * tokens and many rows ([P2] "Whole-Model Graph Execution": decode processes
+ * single tokens): each token's visible rows are split into n_splits ranges
+ * processed by different SMs, and a second kernel merges the partial results
+ * by their log-sum-exp.  Structural rule only (no dense mask).
+ *   n_splits   ranges per token, >= 1, or <= 0 for the library's choice
+ *              (ds4a_attn_decode_default_splits).
+ *   workspace  device scratch of at least ds4a_attn_decode_workspace_size()
+ *              bytes, 256-byte aligned, owned by the caller; it is fully
+ *              overwritten and need not be initialised.  Two calls in flight
+ *              at the same time must not share a workspace.
+ */
+int32_t ds4a_attn_decode_default_splits(const ds4a_layout *L);
+size_t ds4a_attn_decode_workspace_size(const ds4a_layout *L, int32_t n_splits);
+ds4a_status ds4a_attn_decode(const ds4a_layout *L, const ds4a_tensors *X, int32_t n_splits,
+                             void *workspace, size_t workspace_bytes, ds4a_stream_t stream);
+
+/*
+ * ds4a_attn_decode_partials / ds4a_attn_decode_merge - the two halves of
+ * ds4a_attn_decode, for callers that merge partial results themselves (for
+ * instance across devices that each hold part of the compressed rows).
+ * Workspace layout, with I = T * n_splits items (item = t * n_splits + s):
+ *   float O_part[I][64][512]   unnormalised sum_j p_j v_j of split s of token t
+ *   float2 ml[I][64]           (m, l): p_j = 2^(log2(e) * (scale q.k_j + bias_j) - m),
+ *                              l = sum_j p_j; m = -inf and l = 0 for a split with
+ *                              no visible row (its O_part is then not written)
+ * The merge computes o = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s with
+ * M = max_s m_s, and lse = (M + log2 L) * ln 2.  decode_partials ignores X->o
+ * and X->lse; decode_merge reads only the workspace and writes X->o / X->lse
+ * (X->q and the K/V pointers are not used and may be NULL).
+ */
+ds4a_status ds4a_attn_decode_partials(const ds4a_layout *L, const ds4a_tensors *X, int32_t n_splits,
+                                      void *workspace, size_t workspace_bytes, ds4a_stream_t stream);
+ds4a_status ds4a_attn_decode_merge(const ds4a_layout *L, const ds4a_tensors *X, int32_t n_splits,
+                                   const void *workspace, size_t workspace_bytes, ds4a_stream_t stream);
+
+/*
+ * ds4a_attn_indexed - [P2] "Layer Compression" (ratio-4 layers: an indexer
+ * selects the top-512 compressed rows) and "GPU Backend Architecture"
+ * (indexed mixed heads): each token sees its raw window rows plus the
+ * compressed rows its own index list names.
+ *   idx        int32 [T][top_k] at idx_row_stride bytes (>= 4*top_k, multiple
+ *              of 16).  Entries < 0 are empty slots; entries >= n_comp are
+ *              treated as empty.  Order does not matter.  The entries are not
+ *              checked against the causal rule: the caller's indexer owns that.
+ *   top_k      list length, 1 .. 4096 (the model uses 512).
+ */
+ds4a_status ds4a_attn_indexed(const ds4a_layout *L, const ds4a_tensors *X,
+                              const int32_t *idx, int64_t idx_row_stride, int32_t top_k,
+                              ds4a_stream_t stream);
+
+/*
+ * ds4a_device_status - synchronises `stream`, then reports the device error
+ * word the kernels set when a bounded wait runs out (DS4A_ERR_TIMEOUT) or
+ * DS4A_OK.  clear != 0 resets the word.  A CUDA error from the
+ * synchronisation is DS4A_ERR_CUDA.
+ */
+ds4a_status ds4a_device_status(ds4a_stream_t stream, int clear);
+
+/*
+ * ds4a_selftest_wait_timeout - diagnostic: launches one CTA that waits on a
+ * barrier nothing ever completes, with the given bound (nanoseconds, 1e3 ..
+ * 1e10).  The wait runs out, the kernel records DS4A_ERR_TIMEOUT in the
+ * device error word and returns normally.  Used by the tests to show that a
+ * stuck wait ends as a status, not a hang.
+ */
+ds4a_status ds4a_selftest_wait_timeout(uint64_t timeout_ns, ds4a_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DS4A_H */

@@ -1,0 +1,436 @@
+// C ABI of the library (declared in include/ds4a.h): argument checks, TMA
+// tensor maps, work splitting and kernel launches.  No device memory is
+// allocated here; every buffer belongs to the caller.
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "ds4a.h"
+#include "internal.h"
+
+// Device error word: set by a kernel whose bounded wait ran out.  Its address
+// is looked up once per device and handed to the kernels as a parameter.
+__device__ unsigned int g_ds4a_device_error;
+
+namespace {
+
+using ds4a::AttnParams;
+
+constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;  // 2 s per wait
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  bool ready = false;
+  bool supported = false;
+  int sm_count = 0;
+  unsigned int *err = nullptr;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+// Looks up the current device once: compute capability, SM count, the error
+// word's address, the kernel's shared-memory opt-in and the tensor-map encoder.
+ds4a_status current_device(DeviceState **out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DS4A_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return DS4A_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState &d = g_dev[dev];
+  if (!d.ready) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return DS4A_ERR_CUDA;
+    d.sm_count = sms;
+    d.supported = (major == 10 && minor == 3);
+    if (d.supported) {
+      if (ds4a::prepare_attn_kernel() != cudaSuccess) return DS4A_ERR_CUDA;
+      if (cudaGetSymbolAddress(reinterpret_cast<void **>(&d.err), g_ds4a_device_error) != cudaSuccess)
+        return DS4A_ERR_CUDA;
+      if (g_encode == nullptr) {
+        cudaDriverEntryPointQueryResult q;
+        void *fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || fn == nullptr)
+          return DS4A_ERR_CUDA;
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+      }
+    }
+    d.ready = true;
+  }
+  if (!d.supported) return DS4A_ERR_UNSUPPORTED;
+  *out = &d;
+  return DS4A_OK;
+}
+
+cudaStream_t as_cuda(ds4a_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+bool row_stride_ok(int64_t s) { return s >= DS4A_ROW_BYTES && s % 16 == 0 && s < (1LL << 39); }
+bool tok_stride_ok(int64_t s) { return s >= 64LL * DS4A_ROW_BYTES && s % 16 == 0 && s < (1LL << 39); }
+int32_t ceil_div(int64_t a, int64_t b) { return (int32_t)((a + b - 1) / b); }
+
+ds4a_status check_layout(const ds4a_layout *L) {
+  if (L == nullptr) return DS4A_ERR_INVALID_ARG;
+  if (L->T < 0 || L->q_pos0 < 0 || L->n_raw < 0 || L->raw_pos0 < 0 || L->n_comp < 0) return DS4A_ERR_INVALID_ARG;
+  if (L->window < 1) return DS4A_ERR_INVALID_ARG;
+  if (L->n_comp > 0 && L->ratio < 1) return DS4A_ERR_INVALID_ARG;
+  if (!std::isfinite(L->scale)) return DS4A_ERR_INVALID_ARG;
+  // Positions and row counts must stay inside int32 arithmetic.
+  if ((int64_t)L->q_pos0 + L->T > INT32_MAX - 1 || (int64_t)L->raw_pos0 + L->n_raw > INT32_MAX - 1)
+    return DS4A_ERR_INVALID_ARG;
+  if (L->n_raw > (1 << 30) || L->n_comp > (1 << 30)) return DS4A_ERR_INVALID_ARG;
+  return DS4A_OK;
+}
+
+ds4a_status check_tensors(const ds4a_layout *L, const ds4a_tensors *X) {
+  if (X == nullptr) return DS4A_ERR_INVALID_ARG;
+  if (X->q == nullptr || !aligned(X->q, 16) || !tok_stride_ok(X->q_tok_stride)) return DS4A_ERR_INVALID_ARG;
+  if (X->o == nullptr || !aligned(X->o, 16) || !tok_stride_ok(X->o_tok_stride)) return DS4A_ERR_INVALID_ARG;
+  if (X->lse != nullptr && !aligned(X->lse, 4)) return DS4A_ERR_INVALID_ARG;
+  if (L->n_raw > 0) {
+    if (X->k_raw == nullptr || X->v_raw == nullptr || !aligned(X->k_raw, 16) || !aligned(X->v_raw, 16) ||
+        !row_stride_ok(X->raw_row_stride))
+      return DS4A_ERR_INVALID_ARG;
+  }
+  if (L->n_comp > 0) {
+    if (X->k_comp == nullptr || X->v_comp == nullptr || !aligned(X->k_comp, 16) || !aligned(X->v_comp, 16) ||
+        !row_stride_ok(X->comp_row_stride))
+      return DS4A_ERR_INVALID_ARG;
+  }
+  return DS4A_OK;
+}
+
+ds4a_status encode(CUtensorMap *m, const void *base, int rank, const cuuint64_t *dims, const cuuint64_t *strides,
+                   const cuuint32_t *box) {
+  const cuuint32_t es[3] = {1, 1, 1};
+  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, (cuuint32_t)rank, const_cast<void *>(base), dims,
+                              strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DS4A_OK : DS4A_ERR_CUDA;
+}
+
+// K/V rows: {512 dims, rows}, box {64 dims, box_rows rows}, 128-byte swizzle.
+ds4a_status encode_rows(CUtensorMap *m, const void *base, int rows, int64_t stride, unsigned box_rows) {
+  const cuuint64_t dims[2] = {DS4A_HEAD_DIM, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)stride};
+  const cuuint32_t box[2] = {64, box_rows};
+  return encode(m, base, 2, dims, strides, box);
+}
+
+// Fills the parts of the kernel parameters every attention mode shares.
+ds4a_status fill_params(AttnParams &p, const ds4a_layout *L, const ds4a_tensors *X, int mode, DeviceState *d) {
+  std::memset(&p, 0, sizeof(p));
+  {
+    const cuuint64_t dims[3] = {DS4A_HEAD_DIM, DS4A_HEADS, (cuuint64_t)L->T};
+    const cuuint64_t strides[2] = {DS4A_ROW_BYTES, (cuuint64_t)X->q_tok_stride};
+    const cuuint32_t box[3] = {64, 64, 1};
+    ds4a_status st = encode(&p.tm_q, X->q, 3, dims, strides, box);
+    if (st != DS4A_OK) return st;
+  }
+  if (L->n_raw > 0) {
+    ds4a_status st = encode_rows(&p.tm_k[0], X->k_raw, L->n_raw, X->raw_row_stride, 128);
+    if (st == DS4A_OK) st = encode_rows(&p.tm_v[0], X->v_raw, L->n_raw, X->raw_row_stride, 128);
+    if (st != DS4A_OK) return st;
+  }
+  if (L->n_comp > 0) {
+    ds4a_status st = encode_rows(&p.tm_k[1], X->k_comp, L->n_comp, X->comp_row_stride, 128);
+    if (st == DS4A_OK) st = encode_rows(&p.tm_v[1], X->v_comp, L->n_comp, X->comp_row_stride, 128);
+    if (st == DS4A_OK && mode == ds4a::MODE_INDEXED) {
+      st = encode_rows(&p.tm_kg, X->k_comp, L->n_comp, X->comp_row_stride, 1);
+      if (st == DS4A_OK) st = encode_rows(&p.tm_vg, X->v_comp, L->n_comp, X->comp_row_stride, 1);
+    }
+    if (st != DS4A_OK) return st;
+  }
+  p.T = L->T;
+  p.q_pos0 = L->q_pos0;
+  p.n_raw = L->n_raw;
+  p.raw_pos0 = L->raw_pos0;
+  p.n_comp = L->n_comp;
+  p.ratio = L->n_comp > 0 ? L->ratio : 1;
+  p.window = L->window;
+  p.scale_log2 = L->scale * 1.4426950408889634f;
+  p.mode = mode;
+  p.n_splits = 1;
+  p.q_tile = 1;
+  p.nbr = ceil_div(L->n_raw, DS4A_BLOCK_ROWS);
+  p.n_blocks = p.nbr + ceil_div(L->n_comp, DS4A_BLOCK_ROWS);
+  p.o = static_cast<__half *>(X->o);
+  p.o_tok_stride = X->o_tok_stride / 2;
+  p.lse = X->lse;
+  p.timeout_ns = kDefaultTimeoutNs;
+  p.err = d->err;
+  return DS4A_OK;
+}
+
+ds4a_status launched(cudaError_t e) { return e == cudaSuccess ? DS4A_OK : DS4A_ERR_CUDA; }
+
+int32_t max_tiles_per_token(const ds4a_layout *L) {
+  const int64_t raw = L->window < L->n_raw ? L->window : L->n_raw;
+  return ceil_div(raw, 128) + ceil_div(L->n_comp, 128);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *ds4a_status_string(int status) {
+  switch (status) {
+    case DS4A_OK: return "ok";
+    case DS4A_ERR_INVALID_ARG: return "invalid argument";
+    case DS4A_ERR_UNSUPPORTED: return "unsupported (needs an sm_103a device)";
+    case DS4A_ERR_WORKSPACE: return "workspace missing or too small";
+    case DS4A_ERR_CUDA: return "CUDA error";
+    case DS4A_ERR_TIMEOUT: return "a bounded device wait ran out";
+    default: return "unknown status";
+  }
+}
+
+const char *ds4a_version(void) { return "ds4a 0.1 sm_103a"; }
+
+ds4a_status ds4a_pad_kv(const void *src, int64_t src_row_stride, int32_t n_rows, void *dst, int64_t dst_row_stride,
+                        ds4a_stream_t stream) {
+  if (n_rows < 0) return DS4A_ERR_INVALID_ARG;
+  if (n_rows == 0) return DS4A_OK;
+  if (src == nullptr || dst == nullptr || !aligned(src, 16) || !aligned(dst, 16) || !row_stride_ok(src_row_stride) ||
+      !row_stride_ok(dst_row_stride))
+    return DS4A_ERR_INVALID_ARG;
+  const bool in_place = src == dst;
+  if (in_place && src_row_stride != dst_row_stride) return DS4A_ERR_INVALID_ARG;
+  if (!in_place) {
+    // Other overlaps are not allowed.
+    const uintptr_t s0 = reinterpret_cast<uintptr_t>(src), d0 = reinterpret_cast<uintptr_t>(dst);
+    const uintptr_t s1 = s0 + (uintptr_t)(n_rows - 1) * src_row_stride + DS4A_ROW_BYTES;
+    const uintptr_t d1 = d0 + (uintptr_t)(ceil_div(n_rows, 32) * 32 - 1) * dst_row_stride + DS4A_ROW_BYTES;
+    if (s0 < d1 && d0 < s1) return DS4A_ERR_INVALID_ARG;
+  }
+  DeviceState *d = nullptr;
+  ds4a_status st = current_device(&d);
+  if (st != DS4A_OK) return st;
+  return launched(ds4a::launch_pad(src, src_row_stride, n_rows, dst, dst_row_stride, in_place ? n_rows : 0,
+                                   as_cuda(stream)));
+}
+
+int32_t ds4a_block_count(const ds4a_layout *L) {
+  if (L == nullptr || L->n_raw < 0 || L->n_comp < 0) return -1;
+  return ceil_div(L->n_raw, DS4A_BLOCK_ROWS) + ceil_div(L->n_comp, DS4A_BLOCK_ROWS);
+}
+
+ds4a_status ds4a_block_mask(const ds4a_layout *L, const void *dense_mask, int64_t mask_row_stride, int32_t q_tile,
+                            uint8_t *status, ds4a_stream_t stream) {
+  ds4a_status st = check_layout(L);
+  if (st != DS4A_OK) return st;
+  if (q_tile < 1) return DS4A_ERR_INVALID_ARG;
+  const int32_t n_blocks = ds4a_block_count(L);
+  if (L->T == 0 || n_blocks == 0) return DS4A_OK;
+  if (status == nullptr) return DS4A_ERR_INVALID_ARG;
+  if (dense_mask != nullptr &&
+      (!aligned(dense_mask, 16) || mask_row_stride < (int64_t)n_blocks * 64 || mask_row_stride % 16 != 0))
+    return DS4A_ERR_INVALID_ARG;
+  DeviceState *d = nullptr;
+  st = current_device(&d);
+  if (st != DS4A_OK) return st;
+  const ds4a::GeomScalars g{L->T, L->q_pos0, L->n_raw, L->raw_pos0, L->n_comp, L->n_comp > 0 ? L->ratio : 1,
+                            L->window};
+  if (dense_mask == nullptr) return launched(ds4a::launch_block_mask_struct(g, q_tile, status, as_cuda(stream)));
+  return launched(ds4a::launch_block_mask_dense(g, static_cast<const __half *>(dense_mask), mask_row_stride / 2,
+                                                q_tile, status, as_cuda(stream)));
+}
+
+ds4a_status ds4a_attn_prefill(const ds4a_layout *L, const ds4a_tensors *X, const void *dense_mask,
+                              int64_t mask_row_stride, const uint8_t *status, int32_t q_tile, ds4a_stream_t stream) {
+  ds4a_status st = check_layout(L);
+  if (st != DS4A_OK) return st;
+  if (L->T == 0) return DS4A_OK;
+  st = check_tensors(L, X);
+  if (st != DS4A_OK) return st;
+  const int32_t n_blocks = ds4a_block_count(L);
+  if (dense_mask != nullptr &&
+      (!aligned(dense_mask, 16) || mask_row_stride < (int64_t)n_blocks * 64 || mask_row_stride % 16 != 0))
+    return DS4A_ERR_INVALID_ARG;
+  if (status != nullptr && q_tile < 1) return DS4A_ERR_INVALID_ARG;
+  DeviceState *d = nullptr;
+  st = current_device(&d);
+  if (st != DS4A_OK) return st;
+  AttnParams p;
+  st = fill_params(p, L, X, dense_mask != nullptr ? ds4a::MODE_MASK : ds4a::MODE_STRUCT, d);
+  if (st != DS4A_OK) return st;
+  if (dense_mask != nullptr) {
+    p.mask = static_cast<const __half *>(dense_mask);
+    p.mask_stride = mask_row_stride / 2;
+    p.status = status;
+    p.q_tile = status != nullptr ? q_tile : 1;
+  }
+  const int grid = L->T < d->sm_count ? L->T : d->sm_count;
+  return launched(ds4a::launch_attn(p, grid, as_cuda(stream)));
+}
+
+int32_t ds4a_attn_decode_default_splits(const ds4a_layout *L) {
+  if (check_layout(L) != DS4A_OK || L->T == 0) return 1;
+  int sms = 148;
+  int dev = -1;
+  if (cudaGetDevice(&dev) == cudaSuccess) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0) sms = v;
+  }
+  int32_t s = ceil_div(sms, L->T);
+  const int32_t mt = max_tiles_per_token(L);
+  if (s > mt) s = mt;
+  return s < 1 ? 1 : s;
+}
+
+size_t ds4a_attn_decode_workspace_size(const ds4a_layout *L, int32_t n_splits) {
+  if (check_layout(L) != DS4A_OK) return 0;
+  if (n_splits <= 0) n_splits = ds4a_attn_decode_default_splits(L);
+  return (size_t)L->T * (size_t)n_splits * DS4A_HEADS * (DS4A_HEAD_DIM * sizeof(float) + 2 * sizeof(float));
+}
+
+namespace {
+
+// Shared checks of the decode calls; fills the partial-output pointers.
+ds4a_status decode_setup(const ds4a_layout *L, const ds4a_tensors *X, int32_t &n_splits, const void *workspace,
+                         size_t workspace_bytes, bool need_inputs, bool need_outputs, float **ws_o,
+                         float2 **ws_ml) {
+  ds4a_status st = check_layout(L);
+  if (st != DS4A_OK) return st;
+  if (L->T == 0) return DS4A_OK;
+  if (X == nullptr) return DS4A_ERR_INVALID_ARG;
+  if (need_inputs) {
+    ds4a_tensors probe = *X;
+    if (!need_outputs) {  // the outputs are not touched: check the inputs only
+      probe.o = const_cast<void *>(X->q);
+      probe.o_tok_stride = X->q_tok_stride;
+      probe.lse = nullptr;
+    }
+    st = check_tensors(L, &probe);
+    if (st != DS4A_OK) return st;
+  } else {
+    if (X->o == nullptr || !aligned(X->o, 16) || !tok_stride_ok(X->o_tok_stride)) return DS4A_ERR_INVALID_ARG;
+    if (X->lse != nullptr && !aligned(X->lse, 4)) return DS4A_ERR_INVALID_ARG;
+  }
+  if (n_splits <= 0) n_splits = ds4a_attn_decode_default_splits(L);
+  if (n_splits > 4096) return DS4A_ERR_INVALID_ARG;
+  const size_t need = ds4a_attn_decode_workspace_size(L, n_splits);
+  if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256)) return DS4A_ERR_WORKSPACE;
+  const size_t n_items = (size_t)L->T * n_splits;
+  if (n_items > (size_t)INT32_MAX) return DS4A_ERR_INVALID_ARG;
+  *ws_o = static_cast<float *>(const_cast<void *>(workspace));
+  *ws_ml = reinterpret_cast<float2 *>(static_cast<uint8_t *>(const_cast<void *>(workspace)) +
+                                      n_items * DS4A_HEADS * DS4A_HEAD_DIM * sizeof(float));
+  return DS4A_OK;
+}
+
+ds4a_status decode_partials(const ds4a_layout *L, const ds4a_tensors *X, int32_t n_splits, float *ws_o,
+                            float2 *ws_ml, ds4a_stream_t stream) {
+  DeviceState *d = nullptr;
+  ds4a_status st = current_device(&d);
+  if (st != DS4A_OK) return st;
+  ds4a_tensors Xi = *X;
+  if (Xi.o == nullptr) {  // the partial kernel never writes o; the tensor map needs none either
+    Xi.o = const_cast<void *>(X->q);
+    Xi.o_tok_stride = X->q_tok_stride;
+  }
+  AttnParams p;
+  st = fill_params(p, L, &Xi, ds4a::MODE_STRUCT, d);
+  if (st != DS4A_OK) return st;
+  const size_t n_items = (size_t)L->T * n_splits;
+  p.n_splits = n_splits;
+  p.partial = 1;
+  p.o = nullptr;
+  p.lse = nullptr;
+  p.ws_o = ws_o;
+  p.ws_ml = ws_ml;
+  const int grid = (int)(n_items < (size_t)d->sm_count ? n_items : (size_t)d->sm_count);
+  return launched(ds4a::launch_attn(p, grid, as_cuda(stream)));
+}
+
+}  // namespace
+
+ds4a_status ds4a_attn_decode_partials(const ds4a_layout *L, const ds4a_tensors *X, int32_t n_splits,
+                                      void *workspace, size_t workspace_bytes, ds4a_stream_t stream) {
+  float *ws_o = nullptr;
+  float2 *ws_ml = nullptr;
+  ds4a_status st = decode_setup(L, X, n_splits, workspace, workspace_bytes, true, false, &ws_o, &ws_ml);
+  if (st != DS4A_OK || L->T == 0) return st;
+  return decode_partials(L, X, n_splits, ws_o, ws_ml, stream);
+}
+
+ds4a_status ds4a_attn_decode_merge(const ds4a_layout *L, const ds4a_tensors *X, int32_t n_splits,
+                                   const void *workspace, size_t workspace_bytes, ds4a_stream_t stream) {
+  float *ws_o = nullptr;
+  float2 *ws_ml = nullptr;
+  ds4a_status st = decode_setup(L, X, n_splits, workspace, workspace_bytes, false, true, &ws_o, &ws_ml);
+  if (st != DS4A_OK || L->T == 0) return st;
+  DeviceState *d = nullptr;
+  st = current_device(&d);
+  if (st != DS4A_OK) return st;
+  return launched(ds4a::launch_combine(ws_o, ws_ml, n_splits, L->T, static_cast<__half *>(X->o),
+                                       X->o_tok_stride / 2, X->lse, as_cuda(stream)));
+}
+
+ds4a_status ds4a_attn_decode(const ds4a_layout *L, const ds4a_tensors *X, int32_t n_splits, void *workspace,
+                             size_t workspace_bytes, ds4a_stream_t stream) {
+  float *ws_o = nullptr;
+  float2 *ws_ml = nullptr;
+  ds4a_status st = decode_setup(L, X, n_splits, workspace, workspace_bytes, true, true, &ws_o, &ws_ml);
+  if (st != DS4A_OK || L->T == 0) return st;
+  st = decode_partials(L, X, n_splits, ws_o, ws_ml, stream);
+  if (st != DS4A_OK) return st;
+  return launched(ds4a::launch_combine(ws_o, ws_ml, n_splits, L->T, static_cast<__half *>(X->o),
+                                       X->o_tok_stride / 2, X->lse, as_cuda(stream)));
+}
+
+ds4a_status ds4a_attn_indexed(const ds4a_layout *L, const ds4a_tensors *X, const int32_t *idx,
+                              int64_t idx_row_stride, int32_t top_k, ds4a_stream_t stream) {
+  ds4a_status st = check_layout(L);
+  if (st != DS4A_OK) return st;
+  if (top_k < 1 || top_k > 4096) return DS4A_ERR_INVALID_ARG;
+  if (L->T == 0) return DS4A_OK;
+  st = check_tensors(L, X);
+  if (st != DS4A_OK) return st;
+  if (idx == nullptr || !aligned(idx, 16) || idx_row_stride < 4LL * top_k || idx_row_stride % 16 != 0)
+    return DS4A_ERR_INVALID_ARG;
+  DeviceState *d = nullptr;
+  st = current_device(&d);
+  if (st != DS4A_OK) return st;
+  AttnParams p;
+  st = fill_params(p, L, X, ds4a::MODE_INDEXED, d);
+  if (st != DS4A_OK) return st;
+  p.idx = idx;
+  p.idx_stride = idx_row_stride / 4;
+  p.top_k = top_k;
+  const int grid = L->T < d->sm_count ? L->T : d->sm_count;
+  return launched(ds4a::launch_attn(p, grid, as_cuda(stream)));
+}
+
+ds4a_status ds4a_device_status(ds4a_stream_t stream, int clear) {
+  DeviceState *d = nullptr;
+  ds4a_status st = current_device(&d);
+  if (st != DS4A_OK) return st;
+  if (cudaStreamSynchronize(as_cuda(stream)) != cudaSuccess) return DS4A_ERR_CUDA;
+  unsigned int v = 0;
+  if (cudaMemcpy(&v, d->err, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return DS4A_ERR_CUDA;
+  if (clear && v != 0) {
+    const unsigned int zero = 0;
+    if (cudaMemcpy(d->err, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return DS4A_ERR_CUDA;
+  }
+  return v != 0 ? DS4A_ERR_TIMEOUT : DS4A_OK;
+}
+
+ds4a_status ds4a_selftest_wait_timeout(uint64_t timeout_ns, ds4a_stream_t stream) {
+  if (timeout_ns < 1000ull || timeout_ns > 10000000000ull) return DS4A_ERR_INVALID_ARG;
+  DeviceState *d = nullptr;
+  ds4a_status st = current_device(&d);
+  if (st != DS4A_OK) return st;
+  return launched(ds4a::launch_selftest_wait(timeout_ns, d->err, as_cuda(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,601 @@
+// Fused multi-query attention forward for sm_103a (tcgen05 + TMEM + TMA).
+//
+// What it computes: for every query token t and head h,
+//   o[t][h] = sum_j softmax_j(scale * q[t][h].k_j + bias_j) v_j
+// over the rows the token may see (ds4 page "DwarfStar 4 (DS4) - DeepSeek V4
+// Flash Inference Engine", sections "Fixed Model Shape" and "Layer
+// Compression"; fused as in "How DeepSeek V4 Flash Model Inference Works on
+// Apple Silicon with Metal Backend", section "FlashAttention Kernel
+// Architecture").
+//
+// Orientation.  The 64 heads share one K/V row, so a token's scores against a
+// 128-row K tile form a 128 x 64 product.  The kernel keeps the KV rows on the
+// M side of every MMA, so each instruction is a full M = 128 tcgen05 tile:
+//   S^T[128 rows][64 heads]  = K_tile[128][512] . Q_t[64][512]^T   (K-major A, K-major B)
+//   O^T[512 dims][64 heads] += V_tile^T[512][128] . P^T[64][128]^T (MN-major A, MN-major B)
+// TMEM holds O^T (4 x 64 columns, fp32) and two S^T buffers (64 columns each):
+// 384 of the 512 columns.  Lane r of TMEM is KV row r (for S) or dim r of a
+// 128-dim slice (for O).  The softmax is over TMEM lanes, i.e. across threads:
+// a warp reduce-scatter gives each lane two heads, a 4-warp exchange in shared
+// memory finishes the per-head max.
+//
+// Rows are loaded by TMA at the exact row where a token's window starts (a
+// tile need not be 32-row aligned), so a raw-only token issues exactly its 128
+// window rows.  The pages' 32-row block skip is kept for dense masks, where the
+// caller's status bytes decide which 128-row tiles are loaded at all.
+//
+// Online softmax with a lazy reference: the running reference max of a head
+// moves only when a tile's max exceeds it by more than 2^8 (kTau in log2
+// units); then O^T and the partial sums are rescaled.  Values of P stay below
+// 2^8 and are stored as fp16, and the row sums add the same fp16 values, so
+// o = sum(p v) / sum(p) is an exact convex combination up to fp32 rounding.
+//
+// Warp roles (192 threads, one CTA per SM, persistent over work items):
+//   warps 0-3  softmax + epilogue (thread r owns TMEM lane r)
+//   warp  4    TMA producer (Q once per item, K/V in 32 KB stages)
+//   warp  5    TMEM allocator and tcgen05.mma issuer
+#pragma once
+
+#include "attn_params.h"
+#include "ptx.cuh"
+
+namespace ds4a {
+
+// ------------------------------------------------------------------ tile plan
+
+struct Tile {
+  int seg;    // 0 raw rows, 1 compressed rows, 2 compressed rows named by the index list
+  int start;  // first row (seg 0/1) or first list slot (seg 2)
+  int count;  // rows (or slots) of the tile that exist, <= 128
+  int open;   // dense mask: every covered block has status 2 (visible, zero bias)
+};
+
+struct TokenTiles {
+  int t, pos;
+  int raw_lo, raw_hi;  // raw rows [raw_lo, raw_hi)
+  int comp_rows;       // compressed rows (seg 1) or list slots (seg 2)
+  int n_rt, n_ct;      // raw / compressed tile candidates
+};
+
+__device__ __forceinline__ TokenTiles token_tiles(const AttnParams &p, int t) {
+  TokenTiles z;
+  z.t = t;
+  z.pos = p.q_pos0 + t;
+  if (p.mode == MODE_MASK) {
+    z.raw_lo = 0;
+    z.raw_hi = p.n_raw;
+    z.comp_rows = p.n_comp;
+  } else {
+    // Raw row i sits at raw_pos0 + i; the window is pos - window + 1 .. pos.
+    const long long a = (long long)z.pos - p.window + 1 - p.raw_pos0;
+    const long long b = (long long)z.pos + 1 - p.raw_pos0;
+    long long lo = a < 0 ? 0 : a;
+    long long hi = b > p.n_raw ? p.n_raw : b;
+    if (hi < lo) hi = lo;
+    z.raw_lo = (int)lo;
+    z.raw_hi = (int)hi;
+    if (p.mode == MODE_INDEXED) {
+      z.comp_rows = p.n_comp > 0 ? p.top_k : 0;
+    } else {
+      // Compressed row c is pooled from positions c*ratio .. (c+1)*ratio-1.
+      const long long c = p.n_comp > 0 ? ((long long)z.pos + 1) / p.ratio : 0;
+      z.comp_rows = (int)(c < p.n_comp ? c : p.n_comp);
+    }
+  }
+  z.n_rt = (z.raw_hi - z.raw_lo + kTile - 1) / kTile;
+  z.n_ct = (z.comp_rows + kTile - 1) / kTile;
+  return z;
+}
+
+__device__ __forceinline__ Tile tile_candidate(const AttnParams &p, const TokenTiles &z, int i, bool &skip) {
+  Tile tl;
+  skip = false;
+  tl.open = 0;
+  if (i < z.n_rt) {
+    tl.seg = 0;
+    tl.start = z.raw_lo + i * kTile;
+    tl.count = min(kTile, z.raw_hi - tl.start);
+  } else {
+    tl.seg = p.mode == MODE_INDEXED ? 2 : 1;
+    tl.start = (i - z.n_rt) * kTile;
+    tl.count = min(kTile, z.comp_rows - tl.start);
+  }
+  if (p.mode == MODE_MASK && p.status != nullptr) {
+    const int base = tl.seg == 0 ? 0 : p.nbr;
+    const int b0 = base + tl.start / 32;
+    const int b1 = base + (tl.start + tl.count - 1) / 32;
+    const uint8_t *srow = p.status + (long long)(z.t / p.q_tile) * p.n_blocks;
+    bool all0 = true, all2 = true;
+    for (int b = b0; b <= b1; ++b) {
+      const uint8_t s = srow[b];
+      all0 = all0 && s == 0;
+      all2 = all2 && s == 2;
+    }
+    skip = all0;
+    tl.open = all2 ? 1 : 0;
+  }
+  return tl;
+}
+
+__device__ __forceinline__ int count_tiles(const AttnParams &p, const TokenTiles &z) {
+  const int n = z.n_rt + z.n_ct;
+  if (p.mode != MODE_MASK || p.status == nullptr) return n;
+  int c = 0;
+  for (int i = 0; i < n; ++i) {
+    bool skip;
+    tile_candidate(p, z, i, skip);
+    c += skip ? 0 : 1;
+  }
+  return c;
+}
+
+struct TileCursor {
+  TokenTiles z;
+  int cand;
+  __device__ __forceinline__ Tile next(const AttnParams &p) {
+    const int n = z.n_rt + z.n_ct;
+    while (cand < n) {
+      bool skip;
+      Tile tl = tile_candidate(p, z, cand++, skip);
+      if (!skip) return tl;
+    }
+    Tile none{0, 0, 0, 0};
+    return none;
+  }
+};
+
+// Work item -> token, tile range [j0, j1) and a cursor positioned at j0.
+struct ItemPlan {
+  int t, j0, j1;
+  TileCursor cur;
+};
+
+__device__ __forceinline__ ItemPlan plan_item(const AttnParams &p, int item) {
+  ItemPlan ip;
+  ip.t = item / p.n_splits;
+  const int sp = item - ip.t * p.n_splits;
+  ip.cur.z = token_tiles(p, ip.t);
+  ip.cur.cand = 0;
+  const int n = count_tiles(p, ip.cur.z);
+  ip.j0 = (int)(((long long)sp * n) / p.n_splits);
+  ip.j1 = (int)(((long long)(sp + 1) * n) / p.n_splits);
+  for (int j = 0; j < ip.j0; ++j) ip.cur.next(p);
+  return ip;
+}
+
+// ------------------------------------------------------------------ warp reductions
+
+// Lane l ends with the max (or sum) over the warp's 32 rows of heads 2l and 2l+1.
+template <bool kMax>
+__device__ __forceinline__ float2 warp_reduce_scatter(const float (&s)[64], int lane) {
+  float a[32];
+  {
+    const bool up = lane & 16;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float send = up ? s[i] : s[i + 32];
+      const float keep = up ? s[i + 32] : s[i];
+      const float got = __shfl_xor_sync(0xffffffffu, send, 16);
+      a[i] = kMax ? fmaxf(keep, got) : keep + got;
+    }
+  }
+#pragma unroll
+  for (int c = 32; c >= 4; c >>= 1) {  // 32 -> 16 -> 8 -> 4 -> 2 values, xor 8, 4, 2, 1
+    const int half = c / 2;
+    const bool up = lane & (c / 4);
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const float send = up ? a[i] : a[i + half];
+      const float keep = up ? a[i + half] : a[i];
+      const float got = __shfl_xor_sync(0xffffffffu, send, c / 4);
+      a[i] = kMax ? fmaxf(keep, got) : keep + got;
+    }
+  }
+  return make_float2(a[0], a[1]);
+}
+
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// ------------------------------------------------------------------ producer
+
+__device__ __forceinline__ void producer_role(const AttnParams &p, uint32_t sbase, Misc &ms, int lane) {
+  volatile int *abrt = &ms.abort_flag;
+  const uint32_t b_q_full = smem_u32(&ms.q_full), b_q_empty = smem_u32(&ms.q_empty);
+  uint32_t st = 0, ph = 0, n_item = 0;
+  uint32_t filled = 0, last_par = 0;
+  bool q_issued = false;
+  uint32_t q_par = 0;
+  bool ok = true;
+  const int n_items = p.T * p.n_splits;
+  for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+    ItemPlan ip = plan_item(p, item);
+    if (ip.j1 == ip.j0) continue;
+    if (lane == 0) ok = mbar_wait(b_q_empty, (n_item & 1) ^ 1, abrt, p.timeout_ns, p.err, SITE_Q_EMPTY);
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    if (!ok) break;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(b_q_full, kQBytes);
+#pragma unroll 1
+      for (int b = 0; b < 8; ++b)
+        tma_load_3d(sbase + kOffQ + b * kQBoxBytes, &p.tm_q, b_q_full, 64 * b, 0, ip.t);
+    }
+    q_issued = true;
+    q_par = n_item & 1;
+    for (int j = ip.j0; j < ip.j1 && ok; ++j) {
+      const Tile tl = ip.cur.next(p);
+      int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
+      if (tl.seg == 2) {
+        const int32_t *lst = p.idx + (long long)ip.t * p.idx_stride;
+        int rr[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int k = tl.start + 4 * lane + i;
+          int c = k < p.top_k ? __ldg(lst + k) : -1;
+          rr[i] = (c >= 0 && c < p.n_comp) ? c : 0;  // empty slots load row 0, masked later
+        }
+        r0 = rr[0]; r1 = rr[1]; r2 = rr[2]; r3 = rr[3];
+      }
+#pragma unroll 1
+      for (int part = 0; part < 8; ++part) {  // parts 0-3: K dims 128*part, parts 4-7: V
+        const uint32_t b_full = smem_u32(&ms.kv_full[st]);
+        if (lane == 0) ok = mbar_wait(smem_u32(&ms.kv_empty[st]), ph ^ 1, abrt, p.timeout_ns, p.err, SITE_KV_EMPTY);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        const uint32_t dst = sbase + kOffKV + st * kStageBytes;
+        const int dim0 = 128 * (part & 3);
+        const bool is_v = part >= 4;
+        if (lane == 0) mbar_arrive_expect_tx(b_full, kStageBytes);
+        __syncwarp();
+        if (tl.seg == 2) {
+          const CUtensorMap *m = is_v ? &p.tm_vg : &p.tm_kg;
+          tma_gather4(dst + lane * 512, m, b_full, dim0, r0, r1, r2, r3);
+          tma_gather4(dst + kBoxBytes + lane * 512, m, b_full, dim0 + 64, r0, r1, r2, r3);
+        } else if (lane == 0) {
+          const CUtensorMap *m = is_v ? &p.tm_v[tl.seg] : &p.tm_k[tl.seg];
+          tma_load_2d(dst, m, b_full, dim0, tl.start);
+          tma_load_2d(dst + kBoxBytes, m, b_full, dim0 + 64, tl.start);
+        }
+        filled |= 1u << st;
+        last_par = (last_par & ~(1u << st)) | (ph << st);
+        if (++st == kStages) {
+          st = 0;
+          ph ^= 1;
+        }
+      }
+    }
+    ++n_item;
+  }
+  if (!ok && lane == 0) {
+    // Let every copy already issued land before the CTA's shared memory goes away.
+    volatile int never = 0;
+    for (int s = 0; s < kStages; ++s)
+      if (filled & (1u << s))
+        mbar_wait(smem_u32(&ms.kv_full[s]), (last_par >> s) & 1, &never, 100000000ull, p.err, SITE_DRAIN);
+    if (q_issued) mbar_wait(b_q_full, q_par, &never, 100000000ull, p.err, SITE_DRAIN);
+  }
+  __syncwarp();
+}
+
+// ------------------------------------------------------------------ MMA issuer
+
+__device__ __forceinline__ void mma_role(const AttnParams &p, uint32_t sbase, uint32_t tmem, Misc &ms, int lane) {
+  if (lane == 0) {
+    volatile int *abrt = &ms.abort_flag;
+    constexpr uint32_t kIdescQK = idesc_f16_f32(128, 64, false, false);
+    constexpr uint32_t kIdescPV = idesc_f16_f32(128, 64, true, true);
+    uint32_t st = 0, ph = 0, g = 0, n_item = 0;
+    bool ok = true;
+    const int n_items = p.T * p.n_splits;
+    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+      ItemPlan ip = plan_item(p, item);
+      if (ip.j1 == ip.j0) continue;
+      ok = mbar_wait(smem_u32(&ms.q_full), n_item & 1, abrt, p.timeout_ns, p.err, SITE_Q_FULL);
+      if (!ok) break;
+      const int nt = ip.j1 - ip.j0;
+      for (int jj = 0; jj < nt && ok; ++jj) {
+        const uint32_t sb = g & 1;
+        ok = mbar_wait(smem_u32(&ms.s_empty[sb]), ((g >> 1) & 1) ^ 1, abrt, p.timeout_ns, p.err, SITE_S_EMPTY);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t d_s = tmem + kTmemS + 64 * sb;
+        // S^T = K_tile . Q^T over the 512 dims, 128 dims per stage.
+        for (int c = 0; c < 4 && ok; ++c) {
+          ok = mbar_wait(smem_u32(&ms.kv_full[st]), ph, abrt, p.timeout_ns, p.err, SITE_KV_FULL);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t stage = sbase + kOffKV + st * kStageBytes;
+#pragma unroll
+          for (int b2 = 0; b2 < 2; ++b2) {
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+              const uint64_t a = sdesc_sw128(stage + b2 * kBoxBytes + ks * 32, 16, 1024);
+              const uint64_t b = sdesc_sw128(sbase + kOffQ + (2 * c + b2) * kQBoxBytes + ks * 32, 16, 1024);
+              umma_f16(d_s, a, b, kIdescQK, (c | b2 | ks) != 0 ? 1u : 0u);
+            }
+          }
+          umma_commit(smem_u32(&ms.kv_empty[st]));
+          if (++st == kStages) {
+            st = 0;
+            ph ^= 1;
+          }
+        }
+        if (!ok) break;
+        umma_commit(smem_u32(&ms.s_full[sb]));
+        if (jj == nt - 1) umma_commit(smem_u32(&ms.q_empty));
+        ok = mbar_wait(smem_u32(&ms.p_full), g & 1, abrt, p.timeout_ns, p.err, SITE_P_FULL);
+        if (!ok) break;
+        if (jj == 0) {
+          ok = mbar_wait(smem_u32(&ms.o_empty), (n_item & 1) ^ 1, abrt, p.timeout_ns, p.err, SITE_O_EMPTY);
+          if (!ok) break;
+        }
+        tc_fence_after();
+        // O^T[m] += V_tile^T[dims 128m..] . P^T, 16 rows per instruction.
+        for (int m = 0; m < 4 && ok; ++m) {
+          ok = mbar_wait(smem_u32(&ms.kv_full[st]), ph, abrt, p.timeout_ns, p.err, SITE_KV_FULL);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t stage = sbase + kOffKV + st * kStageBytes;
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint64_t a = sdesc_sw128(stage + ks * 2048, kBoxBytes, 1024);
+            const uint64_t b = sdesc_sw128(sbase + kOffP + ks * 2048, 16, 1024);  // one 64-head MN atom: LBO unused
+            umma_f16(tmem + 64 * m, a, b, kIdescPV, (jj > 0 || ks > 0) ? 1u : 0u);
+          }
+          umma_commit(smem_u32(&ms.kv_empty[st]));
+          if (++st == kStages) {
+            st = 0;
+            ph ^= 1;
+          }
+        }
+        if (!ok) break;
+        umma_commit(smem_u32(&ms.p_empty));
+        ++g;
+      }
+      if (!ok) break;
+      umma_commit(smem_u32(&ms.o_full));
+      ++n_item;
+    }
+    // Every MMA issued so far must finish before TMEM is released.
+    umma_commit(smem_u32(&ms.mma_done));
+    volatile int never = 0;
+    mbar_wait(smem_u32(&ms.mma_done), 0, &never, 100000000ull, p.err, SITE_DRAIN);
+  }
+  __syncwarp();
+}
+
+// ------------------------------------------------------------------ softmax / epilogue
+
+__device__ __forceinline__ void row_visibility(const AttnParams &p, int t, const Tile &tl, int r, bool &vis,
+                                               float &bias_l2) {
+  bias_l2 = 0.f;
+  vis = r < tl.count;
+  if (!vis) return;
+  if (p.mode == MODE_MASK) {
+    if (tl.open) return;
+    const int col = (tl.seg == 0 ? 0 : p.nbr * 32) + tl.start + r;
+    const float m = __half2float(p.mask[(long long)t * p.mask_stride + col]);
+    vis = m != -INFINITY;
+    bias_l2 = vis ? m * kLog2e : 0.f;
+  } else if (tl.seg == 2) {
+    const int c = __ldg(p.idx + (long long)t * p.idx_stride + tl.start + r);
+    vis = c >= 0 && c < p.n_comp;
+  }
+}
+
+__device__ __forceinline__ void write_empty_item(const AttnParams &p, int item, int t, int tid) {
+  if (p.partial) {
+    if (tid < kH) p.ws_ml[(long long)item * kH + tid] = make_float2(-INFINITY, 0.f);
+    return;
+  }
+  __half *orow = p.o + (long long)t * p.o_tok_stride;
+  for (int h = 0; h < kH; ++h)
+    for (int m = 0; m < 4; ++m) orow[h * kD + 128 * m + tid] = __float2half_rn(0.f);
+  if (p.lse != nullptr && tid < kH) p.lse[(long long)t * kH + tid] = -INFINITY;
+}
+
+__device__ __forceinline__ void compute_role(const AttnParams &p, uint8_t *smem, uint32_t tmem, Misc &ms, int tid) {
+  volatile int *abrt = &ms.abort_flag;
+  const int w = tid >> 5, l = tid & 31;
+  const uint32_t lane_base = static_cast<uint32_t>(32 * w) << 16;
+  uint32_t g = 0, n_item = 0;
+  bool bad = false, aborted = false;
+  const int n_items = p.T * p.n_splits;
+  for (int item = blockIdx.x; item < n_items && !aborted; item += gridDim.x) {
+    ItemPlan ip = plan_item(p, item);
+    const int t = ip.t;
+    if (ip.j1 == ip.j0) {
+      write_empty_item(p, item, t, tid);
+      continue;
+    }
+    float m_ref = -INFINITY;  // reference max of head `tid` (threads < 64), log2 units
+    float lpart[64];
+#pragma unroll
+    for (int h = 0; h < 64; ++h) lpart[h] = 0.f;
+    const int nt = ip.j1 - ip.j0;
+    for (int jj = 0; jj < nt; ++jj) {
+      const Tile tl = ip.cur.next(p);
+      const uint32_t sb = g & 1;
+      bad = bad || !mbar_wait(smem_u32(&ms.s_full[sb]), (g >> 1) & 1, abrt, p.timeout_ns, p.err, SITE_S_FULL);
+      tc_fence_after();
+      float s[64];
+      tmem_ld64(tmem + kTmemS + 64 * sb + lane_base, s);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&ms.s_empty[sb]));
+
+      bool vis;
+      float bias;
+      row_visibility(p, t, tl, tid, vis, bias);
+#pragma unroll
+      for (int h = 0; h < 64; ++h) s[h] = vis ? fmaf(s[h], p.scale_log2, bias) : -INFINITY;
+
+      const float2 mx = warp_reduce_scatter<true>(s, l);
+      *reinterpret_cast<float2 *>(&ms.red[w][2 * l]) = mx;
+      if (bar_red_or(1, 128, bad)) {
+        aborted = true;
+        break;
+      }
+      if (tid < kH) {
+        const float tmax = fmaxf(fmaxf(ms.red[0][tid], ms.red[1][tid]), fmaxf(ms.red[2][tid], ms.red[3][tid]));
+        float alpha = 1.f;
+        if (m_ref == -INFINITY) {
+          m_ref = tmax;
+        } else if (tmax > m_ref + kTau) {
+          alpha = exp2f(m_ref - tmax);
+          m_ref = tmax;
+        }
+        ms.m_use[tid] = m_ref == -INFINITY ? 0.f : m_ref;
+        ms.alpha[tid] = alpha;
+        if (alpha != 1.f) ms.resc_flag[g & 1] = 1;
+      }
+      named_bar_sync(1, 128);
+      const int resc = ms.resc_flag[g & 1];
+      if (tid == 0) ms.resc_flag[(g + 1) & 1] = 0;
+
+      // P (fp16) may only be rewritten once the previous PV has consumed it.
+      bad = bad || !mbar_wait(smem_u32(&ms.p_empty), (g & 1) ^ 1, abrt, p.timeout_ns, p.err, SITE_P_EMPTY);
+      if (resc) {
+#pragma unroll
+        for (int h = 0; h < 64; ++h) lpart[h] *= ms.alpha[h];
+      }
+      // P^T row `tid` (64 heads, 128 bytes) with the 128-byte swizzle: the
+      // 16-byte chunk c (heads 8c .. 8c+7) goes to chunk c ^ (row & 7).
+      {
+        uint8_t *prow = smem + kOffP + tid * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const float4 m0 = reinterpret_cast<const float4 *>(ms.m_use)[2 * c];
+          const float4 m1 = reinterpret_cast<const float4 *>(ms.m_use)[2 * c + 1];
+          const float mu[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+          uint32_t w4[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int h = 8 * c + 2 * i;
+            const __half2 hp = __floats2half2_rn(exp2f(s[h] - mu[2 * i]), exp2f(s[h + 1] - mu[2 * i + 1]));
+            const float2 f = __half22float2(hp);
+            lpart[h] += f.x;
+            lpart[h + 1] += f.y;
+            w4[i] = *reinterpret_cast<const uint32_t *>(&hp);
+          }
+          *reinterpret_cast<uint4 *>(prow + ((c ^ (tid & 7)) << 4)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+        }
+      }
+      if (resc && jj > 0) {
+        // O^T holds the previous tiles against the old reference: scale column h by alpha[h].
+        tc_fence_after();
+#pragma unroll 1
+        for (int m = 0; m < 4; ++m) {
+          float o[64];
+          tmem_ld64(tmem + 64 * m + lane_base, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int h = 0; h < 64; ++h) o[h] *= ms.alpha[h];
+          tmem_st64(tmem + 64 * m + lane_base, o);
+        }
+        tmem_wait_st();
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&ms.p_full));
+      ++g;
+    }
+    if (aborted) break;
+
+    // Epilogue: sum the row partials per head, normalise (or hand out partials).
+    bad = bad || !mbar_wait(smem_u32(&ms.o_full), n_item & 1, abrt, p.timeout_ns, p.err, SITE_O_FULL);
+    tc_fence_after();
+    const float2 ls = warp_reduce_scatter<false>(lpart, l);
+    *reinterpret_cast<float2 *>(&ms.red[w][2 * l]) = ls;
+    if (bar_red_or(1, 128, bad)) {
+      aborted = true;
+      break;
+    }
+    if (tid < kH) {
+      const float lsum = ms.red[0][tid] + ms.red[1][tid] + ms.red[2][tid] + ms.red[3][tid];
+      if (p.partial) {
+        p.ws_ml[(long long)item * kH + tid] = make_float2(lsum > 0.f ? m_ref : -INFINITY, lsum);
+      } else {
+        ms.inv_l[tid] = lsum > 0.f ? 1.f / lsum : 0.f;
+        if (p.lse != nullptr)
+          p.lse[(long long)t * kH + tid] = lsum > 0.f ? (m_ref + log2f(lsum)) * kLn2 : -INFINITY;
+      }
+    }
+    named_bar_sync(1, 128);
+#pragma unroll 1
+    for (int m = 0; m < 4; ++m) {
+      float o[64];
+      tmem_ld64(tmem + 64 * m + lane_base, o);
+      tmem_wait_ld();
+      const int d = 128 * m + tid;
+      if (p.partial) {
+        float *dst = p.ws_o + (long long)item * kH * kD + d;
+#pragma unroll
+        for (int h = 0; h < 64; ++h) dst[h * kD] = o[h];
+      } else {
+        __half *dst = p.o + (long long)t * p.o_tok_stride + d;
+#pragma unroll
+        for (int h = 0; h < 64; ++h) dst[h * kD] = __float2half_rn(o[h] * ms.inv_l[h]);
+      }
+    }
+    tc_fence_before();
+    mbar_arrive(smem_u32(&ms.o_empty));
+    ++n_item;
+  }
+}
+
+// ------------------------------------------------------------------ kernel
+
+__global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ AttnParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  Misc &ms = *reinterpret_cast<Misc *>(smem + kOffMisc);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&ms.q_full), 1);
+    mbar_init(smem_u32(&ms.q_empty), 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&ms.kv_full[s]), 1);
+      mbar_init(smem_u32(&ms.kv_empty[s]), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&ms.s_full[s]), 1);
+      mbar_init(smem_u32(&ms.s_empty[s]), 128);
+    }
+    mbar_init(smem_u32(&ms.p_full), 128);
+    mbar_init(smem_u32(&ms.p_empty), 1);
+    mbar_init(smem_u32(&ms.o_full), 1);
+    mbar_init(smem_u32(&ms.o_empty), 128);
+    mbar_init(smem_u32(&ms.mma_done), 1);
+    ms.abort_flag = 0;
+    ms.resc_flag[0] = 0;
+    ms.resc_flag[1] = 0;
+    fence_barrier_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(&ms.tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ms.tmem_base;
+
+  if (warp < 4) {
+    compute_role(p, smem, tmem, ms, threadIdx.x);
+  } else if (warp == kProducerWarp) {
+    producer_role(p, sbase, ms, lane);
+  } else {
+    mma_role(p, sbase, tmem, ms, lane);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace ds4a

@@ -1,0 +1,89 @@
+// Constants, shared-memory bookkeeping and launch parameters of the fused
+// attention kernel.  Included by the kernel's translation unit and by the host
+// code that fills the parameters.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_fp16.h>
+
+namespace ds4a {
+
+constexpr int kH = 64;
+constexpr int kD = 512;
+constexpr int kTile = 128;
+constexpr int kThreads = 192;
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr int kStages = 4;
+constexpr uint32_t kQBytes = 65536;     // 8 boxes of [64 heads][64 dims] fp16
+constexpr uint32_t kQBoxBytes = 8192;
+constexpr uint32_t kBoxBytes = 16384;   // [128 rows][64 dims] fp16
+constexpr uint32_t kStageBytes = 32768; // two boxes: 128 dims of a 128-row tile
+constexpr uint32_t kPBytes = 16384;     // P^T [128 rows][64 heads] fp16
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffKV = kOffQ + kQBytes;
+constexpr uint32_t kOffP = kOffKV + kStages * kStageBytes;
+constexpr uint32_t kOffMisc = kOffP + kPBytes;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemS = 256;        // S^T buffers at columns 256 and 320
+constexpr float kTau = 8.0f;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+enum Mode : int { MODE_STRUCT = 0, MODE_INDEXED = 1, MODE_MASK = 2 };
+
+// Wait-site ids recorded with a timeout.
+enum : unsigned int {
+  SITE_Q_EMPTY = 1, SITE_KV_EMPTY, SITE_Q_FULL, SITE_S_EMPTY, SITE_KV_FULL, SITE_P_FULL, SITE_O_EMPTY,
+  SITE_S_FULL, SITE_P_EMPTY, SITE_O_FULL, SITE_DRAIN, SITE_SELFTEST
+};
+
+struct Misc {
+  alignas(16) float red[4][kH];   // per-warp partial max / sum of each head
+  alignas(16) float m_use[kH];    // reference max used for P (log2 units)
+  alignas(16) float alpha[kH];    // rescale factor of the previous reference
+  alignas(16) float inv_l[kH];
+  alignas(8) uint64_t q_full, q_empty;
+  uint64_t kv_full[kStages], kv_empty[kStages];
+  uint64_t s_full[2], s_empty[2];
+  uint64_t p_full, p_empty, o_full, o_empty, mma_done;
+  uint32_t tmem_base;
+  int abort_flag;
+  int resc_flag[2];
+};
+static_assert(offsetof(Misc, red) % 16 == 0 && offsetof(Misc, m_use) % 16 == 0 &&
+                  offsetof(Misc, q_full) % 8 == 0,
+              "shared-memory bookkeeping must stay aligned");
+
+constexpr uint32_t kSmemBytes = kOffMisc + ((sizeof(Misc) + 127) / 128) * 128 + 1024;
+
+struct AttnParams {
+  CUtensorMap tm_q;        // 3-D {512, 64, T}, box {64, 64, 1}
+  CUtensorMap tm_k[2];     // [raw, comp] 2-D {512, rows}, box {64, 128}
+  CUtensorMap tm_v[2];
+  CUtensorMap tm_kg, tm_vg;  // compressed rows, box {64, 1} (gather4)
+  int T, q_pos0, n_raw, raw_pos0, n_comp, ratio, window;
+  float scale_log2;
+  int mode;
+  int n_splits;            // row ranges per token
+  int partial;             // 1: unnormalised partials to the workspace
+  int top_k;
+  const int32_t *idx;
+  long long idx_stride;    // elements
+  const __half *mask;
+  long long mask_stride;   // elements
+  const uint8_t *status;
+  int q_tile, n_blocks, nbr;  // nbr = raw blocks (ceil(n_raw / 32))
+  int pad_;
+  __half *o;
+  long long o_tok_stride;  // elements
+  float *lse;
+  float *ws_o;             // [T * n_splits][64][512]
+  float2 *ws_ml;           // [T * n_splits][64] (m in log2 units, l)
+  unsigned long long timeout_ns;
+  unsigned int *err;       // device error word
+};
+
+}  // namespace ds4a

@@ -1,0 +1,191 @@
+// Small kernels around the fused attention: K/V padding, block status,
+// split-KV merge and the bounded-wait self test.
+#include <cuda_fp16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace ds4a {
+
+// ------------------------------------------------------------------ pad
+// "How DeepSeek V4 Flash Model Inference Works on Apple Silicon with Metal
+// Backend", sections "KV-Cache Management on Metal Device Buffers" and
+// "FlashAttention Kernel Architecture" (the pad kernel): rows are copied and
+// the block is completed with +0.0 rows up to a multiple of 32.  Each thread
+// moves 16-byte chunks (64 per 1024-byte row), grid-stride, coalesced.
+
+__global__ void pad_kernel(const uint8_t *__restrict__ src, long long src_stride, int n_rows,
+                           uint8_t *__restrict__ dst, long long dst_stride, int first_row, int n_out) {
+  const long long n_chunks = (long long)(n_out - first_row) * 64;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n_chunks;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int row = first_row + (int)(i >> 6);
+    const int c = (int)(i & 63);
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (row < n_rows) v = __ldg(reinterpret_cast<const uint4 *>(src + row * src_stride) + c);
+    reinterpret_cast<uint4 *>(dst + row * dst_stride)[c] = v;
+  }
+}
+
+cudaError_t launch_pad(const void *src, long long src_stride, int n_rows, void *dst, long long dst_stride,
+                       int first_row, cudaStream_t s) {
+  const int n_out = (n_rows + 31) / 32 * 32;
+  const long long n_chunks = (long long)(n_out - first_row) * 64;
+  if (n_chunks <= 0) return cudaSuccess;
+  long long blocks = (n_chunks + 255) / 256;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  pad_kernel<<<(int)blocks, 256, 0, s>>>(static_cast<const uint8_t *>(src), src_stride, n_rows,
+                                         static_cast<uint8_t *>(dst), dst_stride, first_row, n_out);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ block status
+// Same page, section "Mask Handling and Block Skipping": one byte per (q-tile,
+// 32-row block): 0 = no visible pair, 2 = every pair visible with zero bias,
+// 1 = otherwise.  Blocks number [raw rows padded to 32 | compressed rows padded
+// to 32]; pad rows are never visible.
+
+// Structural rule by interval arithmetic.  A raw row at position x is seen by
+// positions x .. x+window-1; compressed row c by positions >= (c+1)*ratio - 1.
+// The q-tile covers positions P0 .. P1.
+__global__ void block_mask_struct_kernel(GeomScalars g, int q_tile, int n_qt, int nbr, int nbc,
+                                         uint8_t *__restrict__ status) {
+  const int n_blocks = nbr + nbc;
+  const long long total = (long long)n_qt * n_blocks;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int b = (int)(i / n_blocks);
+    const int k = (int)(i - (long long)b * n_blocks);
+    const long long P0 = (long long)g.q_pos0 + (long long)b * q_tile;
+    const long long t_end = min((long long)g.T, (long long)(b + 1) * q_tile);
+    const long long P1 = (long long)g.q_pos0 + t_end - 1;
+    bool some, every;
+    if (k < nbr) {
+      const long long lo = 32LL * k, hi = min(32LL * k + 31, (long long)g.n_raw - 1);
+      const long long x0 = g.raw_pos0 + lo, x1 = g.raw_pos0 + hi;
+      some = x0 <= P1 && x1 + g.window - 1 >= P0;
+      every = (hi - lo == 31) && x1 <= P0 && x0 + g.window - 1 >= P1;
+    } else {
+      const long long kc = k - nbr;
+      const long long lo = 32LL * kc, hi = min(32LL * kc + 31, (long long)g.n_comp - 1);
+      some = (lo + 1) * g.ratio - 1 <= P1;
+      every = (hi - lo == 31) && (hi + 1) * g.ratio - 1 <= P0;
+    }
+    status[i] = every ? 2 : (some ? 1 : 0);
+  }
+}
+
+// Dense mask: one warp per (q-tile, block); lane = row of the block.
+__global__ void block_mask_dense_kernel(GeomScalars g, const __half *__restrict__ mask, long long mask_stride,
+                                        int q_tile, int n_qt, int nbr, int nbc, uint8_t *__restrict__ status) {
+  const int n_blocks = nbr + nbc;
+  const long long total = (long long)n_qt * n_blocks;
+  const int lane = threadIdx.x & 31;
+  const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
+  for (long long i = blockIdx.x * (long long)(blockDim.x >> 5) + (threadIdx.x >> 5); i < total; i += warps) {
+    const int b = (int)(i / n_blocks);
+    const int k = (int)(i - (long long)b * n_blocks);
+    const bool real = k < nbr ? (32 * k + lane < g.n_raw) : (32 * (k - nbr) + lane < g.n_comp);
+    const int col = 32 * k + lane;
+    const int t0 = b * q_tile, t1 = min(g.T, (b + 1) * q_tile);
+    bool any_vis = false, all_zero = real;
+    if (real) {
+      for (int t = t0; t < t1; ++t) {
+        const __half hv = mask[(long long)t * mask_stride + col];
+        const float m = __half2float(hv);
+        const bool vis = m != -INFINITY;
+        any_vis = any_vis || vis;
+        all_zero = all_zero && vis && m == 0.f;
+      }
+    }
+    const bool some = __any_sync(0xffffffffu, any_vis);
+    const bool every = __all_sync(0xffffffffu, all_zero);
+    if (lane == 0) status[i] = every ? 2 : (some ? 1 : 0);
+  }
+}
+
+static int grid_for(long long work, int per_block) {
+  long long b = (work + per_block - 1) / per_block;
+  if (b < 1) b = 1;
+  if (b > 152 * 8) b = 152 * 8;
+  return (int)b;
+}
+
+cudaError_t launch_block_mask_struct(const GeomScalars &g, int q_tile, uint8_t *status, cudaStream_t s) {
+  const int n_qt = (g.T + q_tile - 1) / q_tile;
+  const int nbr = (g.n_raw + 31) / 32, nbc = (g.n_comp + 31) / 32;
+  const long long total = (long long)n_qt * (nbr + nbc);
+  if (total == 0) return cudaSuccess;
+  block_mask_struct_kernel<<<grid_for(total, 256), 256, 0, s>>>(g, q_tile, n_qt, nbr, nbc, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_block_mask_dense(const GeomScalars &g, const __half *mask, long long mask_stride, int q_tile,
+                                    uint8_t *status, cudaStream_t s) {
+  const int n_qt = (g.T + q_tile - 1) / q_tile;
+  const int nbr = (g.n_raw + 31) / 32, nbc = (g.n_comp + 31) / 32;
+  const long long total = (long long)n_qt * (nbr + nbc);
+  if (total == 0) return cudaSuccess;
+  block_mask_dense_kernel<<<grid_for(total, 8), 256, 0, s>>>(g, mask, mask_stride, q_tile, n_qt, nbr, nbc,
+                                                             status);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ split merge
+// Each split s of a token left an unnormalised O_s (fp32, relative to its
+// reference max m_s in log2 units) and l_s.  With M = max_s m_s:
+//   o = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s,  lse = (M + log2 L) ln 2.
+// Grid (4 dim quarters, 64 heads, T tokens), 128 threads: one dim each.
+
+__global__ void combine_kernel(const float *__restrict__ ws_o, const float2 *__restrict__ ws_ml, int n_splits,
+                               __half *__restrict__ o, long long o_tok_stride, float *__restrict__ lse) {
+  const int q4 = blockIdx.x, h = blockIdx.y, t = blockIdx.z;
+  const int d = 128 * q4 + threadIdx.x;
+  const long long base = (long long)t * n_splits;
+  float M = -INFINITY;
+  for (int s = 0; s < n_splits; ++s) M = fmaxf(M, ws_ml[(base + s) * 64 + h].x);
+  float L = 0.f, acc = 0.f;
+  if (M != -INFINITY) {
+    for (int s = 0; s < n_splits; ++s) {
+      const float2 ml = ws_ml[(base + s) * 64 + h];
+      if (ml.x == -INFINITY) continue;
+      const float w = exp2f(ml.x - M);
+      L += w * ml.y;
+      acc += w * ws_o[((base + s) * 64 + h) * 512 + d];
+    }
+  }
+  o[(long long)t * o_tok_stride + h * 512 + d] = __float2half_rn(L > 0.f ? acc / L : 0.f);
+  if (lse != nullptr && q4 == 0 && threadIdx.x == 0)
+    lse[(long long)t * 64 + h] = L > 0.f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
+}
+
+cudaError_t launch_combine(const float *ws_o, const float2 *ws_ml, int n_splits, int T, __half *o,
+                           long long o_tok_stride, float *lse, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  combine_kernel<<<dim3(4, 64, T), 128, 0, s>>>(ws_o, ws_ml, n_splits, o, o_tok_stride, lse);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ self test
+// One CTA waits on a barrier that nothing ever completes; the bounded wait runs
+// out, records the timeout and the kernel returns.
+
+__global__ void selftest_wait_kernel(unsigned long long timeout_ns, unsigned int *err) {
+  __shared__ alignas(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(smem_u32(&bar), 0, &abort_flag, timeout_ns, err, SITE_SELFTEST);
+  __syncthreads();
+}
+
+cudaError_t launch_selftest_wait(unsigned long long timeout_ns, unsigned int *err, cudaStream_t s) {
+  selftest_wait_kernel<<<1, 32, 0, s>>>(timeout_ns, err);
+  return cudaGetLastError();
+}
+
+}  // namespace ds4a

@@ -1,0 +1,29 @@
+// Launchers shared between the kernel translation units and the C ABI.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "attn_params.h"
+
+namespace ds4a {
+
+struct GeomScalars {
+  int T, q_pos0, n_raw, raw_pos0, n_comp, ratio, window;
+};
+
+// attn.cu
+cudaError_t prepare_attn_kernel();
+cudaError_t launch_attn(const AttnParams &p, int grid, cudaStream_t s);
+
+// aux.cu
+cudaError_t launch_pad(const void *src, long long src_stride, int n_rows, void *dst, long long dst_stride,
+                       int first_row, cudaStream_t s);
+cudaError_t launch_block_mask_struct(const GeomScalars &g, int q_tile, uint8_t *status, cudaStream_t s);
+cudaError_t launch_block_mask_dense(const GeomScalars &g, const __half *mask, long long mask_stride, int q_tile,
+                                    uint8_t *status, cudaStream_t s);
+cudaError_t launch_combine(const float *ws_o, const float2 *ws_ml, int n_splits, int T, __half *o,
+                           long long o_tok_stride, float *lse, cudaStream_t s);
+cudaError_t launch_selftest_wait(unsigned long long timeout_ns, unsigned int *err, cudaStream_t s);
+
+}  // namespace ds4a

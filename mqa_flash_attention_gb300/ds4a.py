@@ -1,0 +1,275 @@
+"""Python binding of ``libds4a.so`` (the C ABI in ``include/ds4a.h``).
+
+Argument marshalling only: every step of the attention path runs in the
+library's CUDA kernels.  PyTorch supplies device memory and the current
+stream.  There is no fallback: if the library is missing, importing the
+functions raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+from .workloads import H, D
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libds4a.so")
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = range(6)
+BLOCK_ROWS = 32
+ROW_BYTES = 1024
+
+
+class Ds4aError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+
+
+class Layout(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("q_pos0", ctypes.c_int32),
+                ("n_raw", ctypes.c_int32), ("raw_pos0", ctypes.c_int32),
+                ("n_comp", ctypes.c_int32), ("ratio", ctypes.c_int32),
+                ("window", ctypes.c_int32), ("scale", ctypes.c_float)]
+
+
+class Tensors(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("q_tok_stride", ctypes.c_int64),
+                ("k_raw", ctypes.c_void_p), ("v_raw", ctypes.c_void_p), ("raw_row_stride", ctypes.c_int64),
+                ("k_comp", ctypes.c_void_p), ("v_comp", ctypes.c_void_p), ("comp_row_stride", ctypes.c_int64),
+                ("o", ctypes.c_void_p), ("o_tok_stride", ctypes.c_int64),
+                ("lse", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """Loads the library once; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise ImportError(f"{_LIB_PATH} is missing: build it with `python -m mqa_flash_attention_gb300.build`")
+        L = ctypes.CDLL(_LIB_PATH)
+        vp, i32, i64, st = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_int
+        PL, PT = ctypes.POINTER(Layout), ctypes.POINTER(Tensors)
+        L.ds4a_status_string.restype = ctypes.c_char_p
+        L.ds4a_status_string.argtypes = [ctypes.c_int]
+        L.ds4a_version.restype = ctypes.c_char_p
+        L.ds4a_version.argtypes = []
+        L.ds4a_pad_kv.restype = st
+        L.ds4a_pad_kv.argtypes = [vp, i64, i32, vp, i64, vp]
+        L.ds4a_block_count.restype = i32
+        L.ds4a_block_count.argtypes = [PL]
+        L.ds4a_block_mask.restype = st
+        L.ds4a_block_mask.argtypes = [PL, vp, i64, i32, vp, vp]
+        L.ds4a_attn_prefill.restype = st
+        L.ds4a_attn_prefill.argtypes = [PL, PT, vp, i64, vp, i32, vp]
+        L.ds4a_attn_decode_default_splits.restype = i32
+        L.ds4a_attn_decode_default_splits.argtypes = [PL]
+        L.ds4a_attn_decode_workspace_size.restype = ctypes.c_size_t
+        L.ds4a_attn_decode_workspace_size.argtypes = [PL, i32]
+        L.ds4a_attn_decode.restype = st
+        L.ds4a_attn_decode.argtypes = [PL, PT, i32, vp, ctypes.c_size_t, vp]
+        L.ds4a_attn_decode_partials.restype = st
+        L.ds4a_attn_decode_partials.argtypes = [PL, PT, i32, vp, ctypes.c_size_t, vp]
+        L.ds4a_attn_decode_merge.restype = st
+        L.ds4a_attn_decode_merge.argtypes = [PL, PT, i32, vp, ctypes.c_size_t, vp]
+        L.ds4a_attn_indexed.restype = st
+        L.ds4a_attn_indexed.argtypes = [PL, PT, vp, i64, i32, vp]
+        L.ds4a_device_status.restype = st
+        L.ds4a_device_status.argtypes = [vp, ctypes.c_int]
+        L.ds4a_selftest_wait_timeout.restype = st
+        L.ds4a_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().ds4a_status_string(int(status)).decode()
+
+
+def version() -> str:
+    return lib().ds4a_version().decode()
+
+
+def _check(status: int, what: str) -> None:
+    if status != OK:
+        raise Ds4aError(status, what)
+
+
+def make_layout(layout) -> Layout:
+    """A ``Layout`` from a dict with the ``ds4a_layout`` fields (or a ``Layout``)."""
+    if isinstance(layout, Layout):
+        return layout
+    return Layout(int(layout["T"]), int(layout["q_pos0"]), int(layout["n_raw"]), int(layout["raw_pos0"]),
+                  int(layout["n_comp"]), int(layout.get("ratio", 1) or 1), int(layout["window"]),
+                  float(layout.get("scale", 1.0 / math.sqrt(D))))
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _rows(t, name):
+    """A [rows, 512] fp16 tensor with contiguous rows -> (pointer, byte stride)."""
+    import torch
+    if t is None:
+        return None, ROW_BYTES
+    if t.dtype != torch.float16 or t.dim() != 2 or t.shape[1] != D or t.stride(1) != 1:
+        raise ValueError(f"{name} must be fp16 [rows, 512] with contiguous rows")
+    return _ptr(t), t.stride(0) * 2
+
+
+def _tokens(t, name):
+    import torch
+    if t.dtype != torch.float16 or t.dim() != 3 or t.shape[1:] != (H, D) or t.stride(2) != 1 or t.stride(1) != D:
+        raise ValueError(f"{name} must be fp16 [T, 64, 512] with contiguous heads")
+    return _ptr(t), t.stride(0) * 2
+
+
+def _tensors(q, k_raw, v_raw, k_comp, v_comp, out, lse) -> Tensors:
+    qp, qs = _tokens(q, "q")
+    op, os_ = _tokens(out, "out")
+    krp, rs = _rows(k_raw, "k_raw")
+    vrp, rs2 = _rows(v_raw, "v_raw")
+    kcp, cs = _rows(k_comp, "k_comp")
+    vcp, cs2 = _rows(v_comp, "v_comp")
+    if rs != rs2 or cs != cs2:
+        raise ValueError("K and V of a segment must share the row stride")
+    return Tensors(qp, qs, krp, vrp, rs, kcp, vcp, cs, op, os_, _ptr(lse))
+
+
+def _outputs(q, out, lse, want_lse):
+    import torch
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((q.shape[0], H), dtype=torch.float32, device=q.device)
+    return out, lse
+
+
+# ------------------------------------------------------------------ calls
+
+def pad_kv(src, n_rows: int | None = None, dst=None, stream=None):
+    """Rows ``0 .. n_rows-1`` of ``src`` followed by zero rows up to a multiple
+    of 32.  ``dst`` defaults to a new tensor; ``dst is src`` pads in place."""
+    import torch
+    n = src.shape[0] if n_rows is None else int(n_rows)
+    n_pad = -(-n // BLOCK_ROWS) * BLOCK_ROWS
+    if dst is None:
+        dst = torch.empty((n_pad, D), dtype=torch.float16, device=src.device)
+    sp, ss = _rows(src, "src")
+    dp, ds = _rows(dst, "dst")
+    _check(lib().ds4a_pad_kv(sp, ss, n, dp, ds, _stream(stream)), "ds4a_pad_kv")
+    return dst
+
+
+def block_count(layout) -> int:
+    return lib().ds4a_block_count(ctypes.byref(make_layout(layout)))
+
+
+def block_mask(layout, q_tile: int, mask=None, out=None, stream=None):
+    """Status bytes ``uint8 [ceil(T/q_tile), block_count]``."""
+    import torch
+    L = make_layout(layout)
+    nb = block_count(L)
+    if out is None:
+        out = torch.empty((-(-L.T // q_tile), nb), dtype=torch.uint8, device="cuda")
+    ms = 0 if mask is None else mask.stride(0) * 2
+    _check(lib().ds4a_block_mask(ctypes.byref(L), _ptr(mask), ms, int(q_tile), _ptr(out), _stream(stream)),
+           "ds4a_block_mask")
+    return out
+
+
+def attn_prefill(layout, q, k_raw, v_raw, k_comp=None, v_comp=None, *, mask=None, status=None, q_tile=1,
+                 out=None, lse=None, want_lse=False, stream=None):
+    L = make_layout(layout)
+    out, lse = _outputs(q, out, lse, want_lse)
+    X = _tensors(q, k_raw, v_raw, k_comp, v_comp, out, lse)
+    ms = 0 if mask is None else mask.stride(0) * 2
+    _check(lib().ds4a_attn_prefill(ctypes.byref(L), ctypes.byref(X), _ptr(mask), ms, _ptr(status), int(q_tile),
+                                   _stream(stream)), "ds4a_attn_prefill")
+    return (out, lse) if (want_lse or lse is not None) else out
+
+
+def decode_workspace_bytes(layout, n_splits: int = 0) -> int:
+    return lib().ds4a_attn_decode_workspace_size(ctypes.byref(make_layout(layout)), int(n_splits))
+
+
+def decode_default_splits(layout) -> int:
+    return lib().ds4a_attn_decode_default_splits(ctypes.byref(make_layout(layout)))
+
+
+def attn_decode(layout, q, k_raw, v_raw, k_comp=None, v_comp=None, *, n_splits=0, workspace=None, out=None,
+                lse=None, want_lse=False, stream=None):
+    import torch
+    L = make_layout(layout)
+    out, lse = _outputs(q, out, lse, want_lse)
+    X = _tensors(q, k_raw, v_raw, k_comp, v_comp, out, lse)
+    need = decode_workspace_bytes(L, n_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _check(lib().ds4a_attn_decode(ctypes.byref(L), ctypes.byref(X), int(n_splits), _ptr(workspace),
+                                  workspace.numel() * workspace.element_size(), _stream(stream)),
+           "ds4a_attn_decode")
+    return (out, lse) if (want_lse or lse is not None) else out
+
+
+def attn_decode_partials(layout, q, k_raw, v_raw, k_comp=None, v_comp=None, *, n_splits=0, workspace=None,
+                         stream=None):
+    """First half of :func:`attn_decode`: per-split partials into ``workspace``."""
+    import torch
+    L = make_layout(layout)
+    X = _tensors(q, k_raw, v_raw, k_comp, v_comp, q, None)
+    X.o = None
+    if workspace is None:
+        workspace = torch.empty(max(decode_workspace_bytes(L, n_splits), 256), dtype=torch.uint8, device=q.device)
+    _check(lib().ds4a_attn_decode_partials(ctypes.byref(L), ctypes.byref(X), int(n_splits), _ptr(workspace),
+                                           workspace.numel() * workspace.element_size(), _stream(stream)),
+           "ds4a_attn_decode_partials")
+    return workspace
+
+
+def attn_decode_merge(layout, workspace, *, n_splits=0, out, lse=None, stream=None):
+    """Second half of :func:`attn_decode`: merges the partials into ``out``."""
+    L = make_layout(layout)
+    op, os_ = _tokens(out, "out")
+    X = Tensors(None, 0, None, None, ROW_BYTES, None, None, ROW_BYTES, op, os_, _ptr(lse))
+    _check(lib().ds4a_attn_decode_merge(ctypes.byref(L), ctypes.byref(X), int(n_splits), _ptr(workspace),
+                                        workspace.numel() * workspace.element_size(), _stream(stream)),
+           "ds4a_attn_decode_merge")
+    return out
+
+
+def attn_indexed(layout, q, k_raw, v_raw, k_comp, v_comp, idx, *, out=None, lse=None, want_lse=False, stream=None):
+    import torch
+    L = make_layout(layout)
+    if idx.dtype != torch.int32 or idx.dim() != 2 or idx.stride(1) != 1:
+        raise ValueError("idx must be int32 [T, top_k] with contiguous rows")
+    out, lse = _outputs(q, out, lse, want_lse)
+    X = _tensors(q, k_raw, v_raw, k_comp, v_comp, out, lse)
+    _check(lib().ds4a_attn_indexed(ctypes.byref(L), ctypes.byref(X), _ptr(idx), idx.stride(0) * 4, idx.shape[1],
+                                   _stream(stream)), "ds4a_attn_indexed")
+    return (out, lse) if (want_lse or lse is not None) else out
+
+
+def device_status(clear: bool = True, stream=None) -> int:
+    """Synchronises the stream and returns the device error status code."""
+    return lib().ds4a_device_status(_stream(stream), 1 if clear else 0)
+
+
+def selftest_wait_timeout(timeout_ns: int, stream=None) -> None:
+    _check(lib().ds4a_selftest_wait_timeout(int(timeout_ns), _stream(stream)), "ds4a_selftest_wait_timeout")

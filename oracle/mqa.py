@@ -120,11 +120,11 @@ def listed_rows(lst) -> np.ndarray:
 # ------------------------------------------------------------------ attention
 
 def _softmax_weighted(q_t, keys, vals, bias, scale):
-    """Plain softmax attention of the 64 heads of one token over given rows.
+    """Plain softmax attention of the heads of one token over given rows.
 
-    ``q_t`` [64, 512], ``keys``/``vals`` [n, 512], ``bias`` [n]; float64."""
+    ``q_t`` [heads, 512], ``keys``/``vals`` [n, 512], ``bias`` [n]; float64."""
     if keys.shape[0] == 0:
-        return np.zeros((H, D)), np.full(H, -np.inf)
+        return np.zeros(q_t.shape), np.full(q_t.shape[0], -np.inf)
     s = scale * (q_t @ keys.T) + bias[None, :]          # [64, n]
     m = s.max(axis=1, keepdims=True)
     w = np.exp(s - m)
@@ -153,8 +153,9 @@ def attention(layout: dict, q, k_raw, v_raw, k_comp=None, v_comp=None, *,
     vc = np.zeros((0, D)) if v_comp is None else np.asarray(v_comp, dtype=f)
     npr, npc = padded_lengths(layout)
     n_raw, n_comp = layout["n_raw"], layout["n_comp"]
-    out_o = np.zeros((len(toks), H, D))
-    out_l = np.zeros((len(toks), H))
+    n_heads = np.shape(q)[1]            # 64 for the model; a smaller sample of heads is allowed
+    out_o = np.zeros((len(toks), n_heads, D))
+    out_l = np.zeros((len(toks), n_heads))
     for n, t in enumerate(toks):
         p = layout["q_pos0"] + t
         qt = np.asarray(q[t], dtype=f)

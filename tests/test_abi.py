@@ -1,0 +1,153 @@
+"""The C ABI without a GPU: the library loads, exports every declared symbol,
+and rejects bad arguments before touching CUDA."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from mqa_flash_attention_gb300 import build as ds4a_build
+from mqa_flash_attention_gb300 import ds4a
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ds4a.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    ds4a_build.build()
+    return ds4a.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ds4a_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_calls():
+    names = declared_functions()
+    for n in ("ds4a_pad_kv", "ds4a_block_mask", "ds4a_attn_prefill", "ds4a_attn_decode", "ds4a_attn_indexed"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert ds4a.status_string(s)
+    assert ds4a.status_string(99) == "unknown status"
+    assert "sm_103a" in ds4a.version()
+
+
+def _layout(**kw):
+    base = dict(T=4, q_pos0=100, n_raw=50, raw_pos0=60, n_comp=0, ratio=128, window=128, scale=0.0441941738)
+    base.update(kw)
+    return ds4a.make_layout(base)
+
+
+def test_block_count(lib):
+    assert ds4a.block_count(_layout(n_raw=0, n_comp=0)) == 0
+    assert ds4a.block_count(_layout(n_raw=1, n_comp=0)) == 1
+    assert ds4a.block_count(_layout(n_raw=32, n_comp=33)) == 1 + 2
+    assert ds4a.block_count(_layout(n_raw=2175, n_comp=8192)) == 68 + 256
+    assert lib.ds4a_block_count(None) == -1
+
+
+def test_decode_workspace_size(lib):
+    L = _layout(T=3, n_comp=1000, ratio=128)
+    per_split = 64 * (512 * 4 + 8)
+    assert lib.ds4a_attn_decode_workspace_size(ctypes.byref(L), 5) == 3 * 5 * per_split
+    assert lib.ds4a_attn_decode_workspace_size(None, 5) == 0
+
+
+FAKE = ctypes.c_void_p(1 << 20)       # never dereferenced: validation fails first
+MISALIGNED = ctypes.c_void_p((1 << 20) + 8)
+
+
+def _tensors(**kw):
+    base = dict(q=FAKE, q_tok_stride=65536, k_raw=FAKE, v_raw=FAKE, raw_row_stride=1024, k_comp=None, v_comp=None,
+                comp_row_stride=1024, o=FAKE, o_tok_stride=65536, lse=None)
+    base.update(kw)
+    return ds4a.Tensors(**base)
+
+
+def _prefill(lib, L, X):
+    return lib.ds4a_attn_prefill(ctypes.byref(L), ctypes.byref(X), None, 0, None, 1, None)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(T=-1), dict(q_pos0=-3), dict(n_raw=-1), dict(window=0), dict(n_comp=5, ratio=0),
+    dict(scale=float("inf")), dict(scale=float("nan")), dict(q_pos0=2**31 - 2),
+])
+def test_bad_layout_is_rejected(lib, bad):
+    assert _prefill(lib, _layout(**bad), _tensors()) == ds4a.ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("bad", [
+    dict(q=None), dict(q=MISALIGNED), dict(q_tok_stride=65535), dict(q_tok_stride=4096),
+    dict(o=None), dict(o_tok_stride=65536 + 8), dict(k_raw=None), dict(v_raw=MISALIGNED),
+    dict(raw_row_stride=1000), dict(raw_row_stride=1032), dict(lse=ctypes.c_void_p((1 << 20) + 2)),
+])
+def test_bad_tensors_are_rejected(lib, bad):
+    assert _prefill(lib, _layout(), _tensors(**bad)) == ds4a.ERR_INVALID_ARG
+
+
+def test_compressed_rows_need_pointers(lib):
+    L = _layout(n_comp=10, ratio=4)
+    assert _prefill(lib, L, _tensors()) == ds4a.ERR_INVALID_ARG
+    assert _prefill(lib, L, _tensors(k_comp=FAKE, v_comp=FAKE, comp_row_stride=16)) == ds4a.ERR_INVALID_ARG
+
+
+def test_empty_call_is_a_no_op(lib):
+    assert _prefill(lib, _layout(T=0), _tensors(q=None, o=None)) == ds4a.OK
+    assert lib.ds4a_pad_kv(None, 0, 0, None, 0, None) == ds4a.OK
+    L = _layout(T=0)
+    assert lib.ds4a_attn_indexed(ctypes.byref(L), ctypes.byref(_tensors()), None, 0, 512, None) == ds4a.OK
+
+
+def test_dense_mask_stride_is_checked(lib):
+    L = _layout()
+    X = _tensors()
+    # 2 blocks of 32 rows need 128 bytes per mask row
+    assert lib.ds4a_attn_prefill(ctypes.byref(L), ctypes.byref(X), FAKE, 64, None, 1, None) == ds4a.ERR_INVALID_ARG
+    assert lib.ds4a_block_mask(ctypes.byref(L), FAKE, 112, 1, FAKE, None) == ds4a.ERR_INVALID_ARG
+    assert lib.ds4a_block_mask(ctypes.byref(L), None, 0, 0, FAKE, None) == ds4a.ERR_INVALID_ARG
+
+
+def test_decode_workspace_is_checked(lib):
+    L = _layout(T=1, n_comp=300, ratio=128)
+    X = _tensors(k_comp=FAKE, v_comp=FAKE)
+    assert lib.ds4a_attn_decode(ctypes.byref(L), ctypes.byref(X), 2, None, 0, None) == ds4a.ERR_WORKSPACE
+    small = lib.ds4a_attn_decode_workspace_size(ctypes.byref(L), 2) - 1
+    assert lib.ds4a_attn_decode(ctypes.byref(L), ctypes.byref(X), 2, FAKE, small, None) == ds4a.ERR_WORKSPACE
+    assert lib.ds4a_attn_decode(ctypes.byref(L), ctypes.byref(X), 2, ctypes.c_void_p((1 << 20) + 128), 1 << 30,
+                                None) == ds4a.ERR_WORKSPACE
+
+
+def test_indexed_arguments_are_checked(lib):
+    L = _layout(n_comp=64, ratio=4)
+    X = _tensors(k_comp=FAKE, v_comp=FAKE)
+    assert lib.ds4a_attn_indexed(ctypes.byref(L), ctypes.byref(X), FAKE, 2048, 0, None) == ds4a.ERR_INVALID_ARG
+    assert lib.ds4a_attn_indexed(ctypes.byref(L), ctypes.byref(X), FAKE, 2048, 4097, None) == ds4a.ERR_INVALID_ARG
+    assert lib.ds4a_attn_indexed(ctypes.byref(L), ctypes.byref(X), None, 2048, 512, None) == ds4a.ERR_INVALID_ARG
+    assert lib.ds4a_attn_indexed(ctypes.byref(L), ctypes.byref(X), FAKE, 2040, 512, None) == ds4a.ERR_INVALID_ARG
+    assert lib.ds4a_attn_indexed(ctypes.byref(L), ctypes.byref(X), FAKE, 2056, 512, None) == ds4a.ERR_INVALID_ARG
+
+
+def test_pad_arguments_are_checked(lib):
+    assert lib.ds4a_pad_kv(FAKE, 1024, -1, FAKE, 1024, None) == ds4a.ERR_INVALID_ARG
+    assert lib.ds4a_pad_kv(FAKE, 1024, 10, None, 1024, None) == ds4a.ERR_INVALID_ARG
+    assert lib.ds4a_pad_kv(FAKE, 1000, 10, ctypes.c_void_p(1 << 30), 1024, None) == ds4a.ERR_INVALID_ARG
+    # in place needs equal strides; overlapping distinct ranges are refused
+    assert lib.ds4a_pad_kv(FAKE, 1024, 10, FAKE, 2048, None) == ds4a.ERR_INVALID_ARG
+    assert lib.ds4a_pad_kv(FAKE, 1024, 10, ctypes.c_void_p((1 << 20) + 4096), 1024, None) == ds4a.ERR_INVALID_ARG
+
+
+def test_selftest_bound_is_checked(lib):
+    assert lib.ds4a_selftest_wait_timeout(10, None) == ds4a.ERR_INVALID_ARG
+    assert lib.ds4a_selftest_wait_timeout(10**11, None) == ds4a.ERR_INVALID_ARG

@@ -1,0 +1,404 @@
+"""CUDA path against the fp64 oracle, element by element (needs a GB300).
+
+Tolerance (fp16 inputs and outputs, fp32 accumulation): max |gpu - oracle| <=
+5e-3 and mean |gpu - oracle| <= 5e-4 over every output element compared.
+Integer and byte results (block status, padding) must match bit for bit.
+"""
+
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from mqa_flash_attention_gb300 import synth, workloads as W
+from mqa_flash_attention_gb300.workloads import make_layout
+
+pytestmark = pytest.mark.gpu
+
+MAX_ABS = 5e-3
+MEAN_ABS = 5e-4
+
+
+@pytest.fixture(scope="module")
+def torch():
+    import torch as _torch
+    from mqa_flash_attention_gb300 import build
+    build.build()
+    assert _torch.cuda.is_available()
+    return _torch
+
+
+@pytest.fixture(scope="module")
+def ds4a(torch):
+    from mqa_flash_attention_gb300 import ds4a as _ds4a
+    _ds4a.lib()
+    return _ds4a
+
+
+def dev(torch, a):
+    return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def host(t):
+    return t.detach().cpu().numpy()
+
+
+def assert_close(got, want, what):
+    got = np.asarray(got, dtype=np.float64)
+    err = np.abs(got - want)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    assert err.max() <= MAX_ABS, f"{what}: max abs err {err.max():.3e}"
+    assert err.mean() <= MEAN_ABS, f"{what}: mean abs err {err.mean():.3e}"
+
+
+def assert_lse_close(got, want, what):
+    got = np.asarray(got, dtype=np.float64)
+    fin = np.isfinite(want)
+    assert np.array_equal(np.isfinite(got), fin), f"{what}: lse finiteness differs"
+    if fin.any():
+        assert np.abs(got[fin] - want[fin]).max() <= 1e-3, what
+
+
+def upload(torch, wl):
+    return dict(q=dev(torch, wl.q), k_raw=dev(torch, wl.k_raw), v_raw=dev(torch, wl.v_raw),
+                k_comp=dev(torch, wl.k_comp) if wl.layout["n_comp"] else None,
+                v_comp=dev(torch, wl.v_comp) if wl.layout["n_comp"] else None)
+
+
+def oracle_out(wl, tokens=None, idx=None, mask=None):
+    return oracle.attention(wl.layout, wl.q, wl.k_raw, wl.v_raw, wl.k_comp, wl.v_comp, idx=idx, mask=mask,
+                            tokens=tokens)
+
+
+# ------------------------------------------------------------------ pad
+
+@pytest.mark.parametrize("n", [1, 31, 32, 33, 160, 2175])
+def test_pad_matches_oracle_bitwise(torch, ds4a, n):
+    src = synth.normal_f16(40 + n, 2, (n + 7, 512))
+    want = oracle.pad_rows(src, n)
+    got = host(ds4a.pad_kv(dev(torch, src), n))
+    assert got.shape == want.shape
+    assert np.array_equal(got.view(np.uint16), want.view(np.uint16))
+
+
+def test_pad_in_place_and_strided(torch, ds4a):
+    n = 45
+    buf = synth.normal_f16(41, 2, (64, 512))
+    t = dev(torch, buf)
+    ds4a.pad_kv(t[:64], n, dst=t[:64])
+    want = oracle.pad_rows(buf, n)
+    assert np.array_equal(host(t).view(np.uint16), want.view(np.uint16))
+    # rows with a 2048-byte stride (every other row of a wider buffer)
+    wide = dev(torch, synth.normal_f16(42, 2, (80, 1024)))
+    src = wide[:, :512]
+    got = host(ds4a.pad_kv(src, 70))
+    assert np.array_equal(got.view(np.uint16), oracle.pad_rows(host(src), 70).view(np.uint16))
+
+
+# ------------------------------------------------------------------ block status
+
+def _status_layouts():
+    out = [(W.tiny().layout, q) for q in (1, 2, 4, 16, 64)]
+    out += [(W.decode_r128_32k().layout, 1), (W.prefill_raw_2048().layout, 2),
+            (W.prefill_raw_2048().layout, 16), (make_layout(T=2048, q_pos0=30720, n_raw=2175, raw_pos0=30593,
+                                                            n_comp=8192, ratio=4), 64)]
+    u = iter(synth.uniform(43, 1, 2000))
+
+    def ri(lo, hi):
+        return lo + int(next(u) * (hi - lo + 1))
+
+    for _ in range(25):
+        out.append((make_layout(T=ri(1, 70), q_pos0=ri(0, 500), n_raw=ri(0, 300), raw_pos0=ri(0, 400),
+                                n_comp=ri(0, 200), ratio=(4, 128, 7)[ri(0, 2)], window=ri(1, 200)),
+                    (1, 2, 3, 16, 64)[ri(0, 4)]))
+    return out
+
+
+def test_block_status_structural_bitwise(torch, ds4a):
+    for L, qt in _status_layouts():
+        if oracle.padded_lengths(L) == (0, 0) or L["T"] == 0:
+            continue
+        want = oracle.block_status(L, qt)
+        got = host(ds4a.block_mask(L, qt))
+        assert np.array_equal(got, want), (L, qt)
+
+
+def _random_mask(seed, L, p_open=0.6, p_bias=0.1):
+    npr, npc = oracle.padded_lengths(L)
+    u = synth.uniform(seed, synth.STREAM_MASK, L["T"] * (npr + npc)).reshape(L["T"], npr + npc)
+    m = np.where(u < p_open, 0.0, -np.inf)
+    m = np.where((u < p_bias), (u - 0.05) * 10, m)      # a few biased entries in (-0.5, 0.5)
+    return m.astype(np.float16)
+
+
+def test_block_status_dense_mask_bitwise(torch, ds4a):
+    L = make_layout(T=37, q_pos0=500, n_raw=150, raw_pos0=0, n_comp=70, ratio=4)
+    npr, npc = oracle.padded_lengths(L)
+    m = _random_mask(44, L)
+    m[:, 0:32] = -np.inf                 # a closed block
+    m[:, 64:96] = 0.0                    # a fully open block
+    m[5:9, 96:128] = -np.inf
+    for qt in (1, 4, 37):
+        want = oracle.block_status(L, qt, mask=m)
+        got = host(ds4a.block_mask(L, qt, mask=dev(torch, m)))
+        assert np.array_equal(got, want), qt
+        assert (want == 0).any() and (want == 2).any()
+
+
+# ------------------------------------------------------------------ prefill
+
+def test_prefill_tiny(torch, ds4a):
+    wl = W.tiny()
+    d = upload(torch, wl)
+    o, lse = ds4a.attn_prefill(wl.layout, d["q"], d["k_raw"], d["v_raw"], want_lse=True)
+    want, wlse = oracle_out(wl)
+    assert_close(host(o), want, "tiny prefill")
+    assert_lse_close(host(lse), wlse, "tiny prefill lse")
+
+
+def test_prefill_raw_2048_sampled(torch, ds4a):
+    """Full-size 2048-token raw-only chunk; outputs compared on sampled tokens."""
+    wl = W.prefill_raw_2048()
+    d = upload(torch, wl)
+    o, lse = ds4a.attn_prefill(wl.layout, d["q"], d["k_raw"], d["v_raw"], want_lse=True)
+    toks = sorted(set([0, 1, 2, 126, 127, 128, 1023, 2046, 2047] + list(range(5, 2048, 97))))
+    want, wlse = oracle_out(wl, tokens=toks)
+    assert_close(host(o)[toks], want, "prefill 2048")
+    assert_lse_close(host(lse)[toks], wlse, "prefill 2048 lse")
+
+
+def _ragged_cases():
+    return [
+        make_layout(T=3, q_pos0=5, n_raw=9, raw_pos0=0),                       # windows shorter than 128
+        make_layout(T=5, q_pos0=300, n_raw=260, raw_pos0=50, window=128),      # window inside, unaligned
+        make_layout(T=2, q_pos0=1000, n_raw=40, raw_pos0=990, n_comp=7, ratio=128),
+        make_layout(T=4, q_pos0=999, n_raw=128, raw_pos0=872, n_comp=250, ratio=4),   # 2 compressed tiles
+        make_layout(T=3, q_pos0=700, n_raw=300, raw_pos0=400, window=200),     # window > 128: two raw tiles
+        make_layout(T=1, q_pos0=64, n_raw=1, raw_pos0=64, window=1),           # single row
+        make_layout(T=130, q_pos0=200, n_raw=330, raw_pos0=0, n_comp=50, ratio=4),    # > one wave of tokens
+    ]
+
+
+@pytest.mark.parametrize("case", range(7))
+def test_prefill_ragged(torch, ds4a, case):
+    L = _ragged_cases()[case]
+    wl = W.draw(f"ragged{case}", 50 + case, L)
+    d = upload(torch, wl)
+    o, lse = ds4a.attn_prefill(L, d["q"], d["k_raw"], d["v_raw"], d["k_comp"], d["v_comp"], want_lse=True)
+    want, wlse = oracle_out(wl)
+    assert_close(host(o), want, f"ragged {case}")
+    assert_lse_close(host(lse), wlse, f"ragged {case} lse")
+
+
+def test_prefill_strided_tokens_and_rows(torch, ds4a):
+    """Q/O token strides and K/V row strides larger than the packed ones."""
+    L = make_layout(T=6, q_pos0=150, n_raw=160, raw_pos0=0, n_comp=40, ratio=4)
+    wl = W.draw("strided", 60, L)
+    qbig = torch.zeros((6, 80, 512), dtype=torch.float16, device="cuda")
+    qbig[:, :64] = dev(torch, wl.q)
+    kbig = torch.zeros((160, 768), dtype=torch.float16, device="cuda")
+    vbig = torch.zeros((160, 768), dtype=torch.float16, device="cuda")
+    kbig[:, :512] = dev(torch, wl.k_raw)
+    vbig[:, :512] = dev(torch, wl.v_raw)
+    obig = torch.full((6, 70, 512), 7.0, dtype=torch.float16, device="cuda")
+    ds4a.attn_prefill(L, qbig[:, :64], kbig[:, :512], vbig[:, :512], dev(torch, wl.k_comp), dev(torch, wl.v_comp),
+                      out=obig[:, :64])
+    want, _ = oracle_out(wl)
+    assert_close(host(obig[:, :64]), want, "strided")
+    assert np.all(host(obig[:, 64:]) == 7.0), "wrote outside the output rows"
+
+
+def test_invisible_rows_do_not_change_output_bitwise(torch, ds4a):
+    """Rows outside every window set to +-65504 (finite): bit-identical output."""
+    L = make_layout(T=8, q_pos0=400, n_raw=500, raw_pos0=0, n_comp=0)
+    wl = W.draw("invis", 61, L)
+    d = upload(torch, wl)
+    base = host(ds4a.attn_prefill(L, d["q"], d["k_raw"], d["v_raw"]))
+    k2, v2 = wl.k_raw.copy(), wl.v_raw.copy()
+    k2[:400 - 127] = 65504.0           # before the first window
+    v2[:400 - 127] = -65504.0
+    k2[408:] = -65504.0                # after the last token
+    v2[408:] = 65504.0
+    got = host(ds4a.attn_prefill(L, d["q"], dev(torch, k2), dev(torch, v2)))
+    assert np.array_equal(got.view(np.uint16), base.view(np.uint16))
+
+
+def test_aliased_k_and_v(torch, ds4a):
+    L = make_layout(T=4, q_pos0=300, n_raw=310, raw_pos0=0)
+    wl = W.draw("alias", 62, L)
+    kv = dev(torch, wl.k_raw)
+    got = host(ds4a.attn_prefill(L, dev(torch, wl.q), kv, kv))
+    want, _ = oracle.attention(L, wl.q, wl.k_raw, wl.k_raw)
+    assert_close(got, want, "k == v")
+
+
+def test_large_score_rescale_path(torch, ds4a):
+    """Rows whose scores jump far above the running max in later tiles force
+    the lazy reference to move and O to be rescaled (twice for token 0)."""
+    L = make_layout(T=2, q_pos0=900, n_raw=129, raw_pos0=772, n_comp=225, ratio=4, window=129)
+    wl = W.draw("rescale", 63, L)
+    qsum = wl.q[0].astype(np.float32).sum(0)           # scores ~ c * 22.6 for every head of token 0
+    k_comp = wl.k_comp.copy()
+    k_comp[10] = (0.4 * qsum).astype(np.float16)       # 3rd tile: jump of ~9 (natural log units)
+    k_comp[200] = (1.0 * qsum).astype(np.float16)      # 4th tile: jump of ~13 more
+    wl.k_comp = k_comp
+    d = upload(torch, wl)
+    o, lse = ds4a.attn_prefill(L, d["q"], d["k_raw"], d["v_raw"], d["k_comp"], d["v_comp"], want_lse=True)
+    want, wlse = oracle_out(wl)
+    assert_close(host(o), want, "rescale")
+    assert_lse_close(host(lse), wlse, "rescale lse")
+
+
+# ------------------------------------------------------------------ dense mask
+
+def test_prefill_dense_mask(torch, ds4a):
+    L = make_layout(T=40, q_pos0=600, n_raw=300, raw_pos0=0, n_comp=90, ratio=4)
+    wl = W.draw("mask", 64, L)
+    m = _random_mask(65, L)
+    m[3] = -np.inf                     # a token that sees nothing
+    d = upload(torch, wl)
+    dm = dev(torch, m)
+    o, lse = ds4a.attn_prefill(L, d["q"], d["k_raw"], d["v_raw"], d["k_comp"], d["v_comp"], mask=dm,
+                               want_lse=True)
+    want, wlse = oracle_out(wl, mask=m)
+    assert_close(host(o), want, "dense mask")
+    assert_lse_close(host(lse), wlse, "dense mask lse")
+    # with status bytes: skipped blocks and unread open blocks change nothing
+    for qt in (1, 8):
+        st = ds4a.block_mask(L, qt, mask=dm)
+        o2 = ds4a.attn_prefill(L, d["q"], d["k_raw"], d["v_raw"], d["k_comp"], d["v_comp"], mask=dm, status=st,
+                               q_tile=qt)
+        assert np.array_equal(host(o2).view(np.uint16), host(o).view(np.uint16)), qt
+    ones = torch.ones_like(ds4a.block_mask(L, 8, mask=dm))
+    o3 = ds4a.attn_prefill(L, d["q"], d["k_raw"], d["v_raw"], d["k_comp"], d["v_comp"], mask=dm, status=ones,
+                           q_tile=8)
+    assert np.array_equal(host(o3).view(np.uint16), host(o).view(np.uint16))
+
+
+def test_dense_mask_of_the_window_equals_structural(torch, ds4a):
+    wl = W.tiny()
+    L = wl.layout
+    vis, _ = oracle.pair_visibility(L)
+    m = np.where(vis, 0.0, -np.inf).astype(np.float16)
+    d = upload(torch, wl)
+    a = host(ds4a.attn_prefill(L, d["q"], d["k_raw"], d["v_raw"]))
+    b = host(ds4a.attn_prefill(L, d["q"], d["k_raw"], d["v_raw"], mask=dev(torch, m)))
+    assert_close(b.astype(np.float64), a.astype(np.float64), "mask == window")
+
+
+# ------------------------------------------------------------------ decode
+
+def test_decode_r128_32k(torch, ds4a):
+    wl = W.decode_r128_32k()
+    d = upload(torch, wl)
+    want, wlse = oracle_out(wl)
+    for splits in (0, 1, 2, 3, 5):
+        o, lse = ds4a.attn_decode(wl.layout, d["q"], d["k_raw"], d["v_raw"], d["k_comp"], d["v_comp"],
+                                  n_splits=splits, want_lse=True)
+        assert_close(host(o), want, f"decode splits={splits}")
+        assert_lse_close(host(lse), wlse, f"decode lse splits={splits}")
+
+
+@pytest.mark.parametrize("n_comp", W.LONG_DECODE_SIZES)
+def test_decode_long(torch, ds4a, n_comp):
+    wl = W.decode_long(n_comp)
+    d = upload(torch, wl)
+    o, lse = ds4a.attn_decode(wl.layout, d["q"], d["k_raw"], d["v_raw"], d["k_comp"], d["v_comp"], want_lse=True)
+    want, wlse = oracle_out(wl)
+    assert_close(host(o), want, f"decode N={n_comp}")
+    assert_lse_close(host(lse), wlse, f"decode N={n_comp} lse")
+
+
+def test_decode_equals_last_prefill_row(torch, ds4a):
+    L = make_layout(T=4, q_pos0=2000, n_raw=260, raw_pos0=1744, n_comp=15, ratio=128)
+    wl = W.draw("dec_vs_pre", 66, L)
+    d = upload(torch, wl)
+    full = host(ds4a.attn_prefill(L, d["q"], d["k_raw"], d["v_raw"], d["k_comp"], d["v_comp"]))
+    L1 = dict(L, T=1, q_pos0=2003)
+    one = host(ds4a.attn_decode(L1, d["q"][3:4], d["k_raw"], d["v_raw"], d["k_comp"], d["v_comp"], n_splits=2))
+    err = np.abs(one[0].astype(np.float64) - full[3].astype(np.float64))
+    assert err.max() <= 2 * MAX_ABS
+
+
+def test_decode_several_tokens(torch, ds4a):
+    L = make_layout(T=3, q_pos0=5000, n_raw=200, raw_pos0=4850, n_comp=39, ratio=128)
+    wl = W.draw("dec3", 67, L)
+    d = upload(torch, wl)
+    want, _ = oracle_out(wl)
+    for s in (1, 2, 7):
+        o = ds4a.attn_decode(L, d["q"], d["k_raw"], d["v_raw"], d["k_comp"], d["v_comp"], n_splits=s)
+        assert_close(host(o), want, f"decode T=3 splits={s}")
+
+
+# ------------------------------------------------------------------ indexed
+
+def test_indexed_ratio4_sampled(torch, ds4a):
+    wl = W.indexed_r4_2048()
+    d = upload(torch, wl)
+    idx = dev(torch, wl.idx)
+    o, lse = ds4a.attn_indexed(wl.layout, d["q"], d["k_raw"], d["v_raw"], d["k_comp"], d["v_comp"], idx,
+                               want_lse=True)
+    toks = sorted(set([0, 1, 127, 128, 1000, 2046, 2047] + list(range(3, 2048, 131))))
+    want, wlse = oracle_out(wl, tokens=toks, idx=wl.idx)
+    assert_close(host(o)[toks], want, "indexed")
+    assert_lse_close(host(lse)[toks], wlse, "indexed lse")
+
+
+def test_indexed_edge_cases(torch, ds4a):
+    L = make_layout(T=5, q_pos0=700, n_raw=140, raw_pos0=600, n_comp=175, ratio=4)
+    wl = W.draw("idx_edge", 68, L)
+    idx = np.full((5, 200), -1, np.int32)
+    idx[0, :3] = [4, 4, 9]                         # duplicates
+    idx[1, 50:60] = np.arange(10)                  # -1 around the entries
+    idx[2, :] = np.arange(200) % 175               # every row, some twice
+    idx[3, 0] = 174
+    idx[4, 199] = 0                                # last slot only
+    d = upload(torch, wl)
+    o = ds4a.attn_indexed(L, d["q"], d["k_raw"], d["v_raw"], d["k_comp"], d["v_comp"], dev(torch, idx))
+    want, _ = oracle_out(wl, idx=idx)
+    assert_close(host(o), want, "indexed edges")
+
+
+def test_indexed_all_available_equals_dense(torch, ds4a):
+    """Index lists naming every pooled row once give the dense (ratio rule) result."""
+    L = make_layout(T=6, q_pos0=1000, n_raw=200, raw_pos0=850, n_comp=300, ratio=4)
+    wl = W.draw("idx_all", 69, L)
+    idx = np.full((6, 256), -1, np.int32)
+    for t in range(6):
+        n = min(300, (1000 + t + 1) // 4)
+        assert n <= 256
+        idx[t, :n] = np.arange(n)
+    d = upload(torch, wl)
+    o = host(ds4a.attn_indexed(L, d["q"], d["k_raw"], d["v_raw"], d["k_comp"], d["v_comp"], dev(torch, idx)))
+    want, _ = oracle_out(wl, idx=idx)
+    assert_close(o, want, "indexed all")
+    dense = host(ds4a.attn_prefill(L, d["q"], d["k_raw"], d["v_raw"], d["k_comp"], d["v_comp"]))
+    assert_close(o.astype(np.float64), dense.astype(np.float64), "indexed all vs dense kernel")
+
+
+# ------------------------------------------------------------------ bounded waits
+
+def test_stuck_wait_ends_as_a_status(torch, ds4a):
+    assert ds4a.device_status(clear=True) == ds4a.OK
+    ds4a.selftest_wait_timeout(2_000_000)          # 2 ms bound
+    assert ds4a.device_status(clear=True) == ds4a.ERR_TIMEOUT
+    assert ds4a.device_status(clear=True) == ds4a.OK
+    # the context is still usable
+    wl = W.tiny()
+    d = upload(torch, wl)
+    o = ds4a.attn_prefill(wl.layout, d["q"], d["k_raw"], d["v_raw"])
+    assert_close(host(o), oracle_out(wl)[0], "after timeout")
+    assert ds4a.device_status() == ds4a.OK
+
+
+def test_decode_partials_then_merge(torch, ds4a):
+    wl = W.decode_long(1024)
+    d = upload(torch, wl)
+    ws = ds4a.attn_decode_partials(wl.layout, d["q"], d["k_raw"], d["v_raw"], d["k_comp"], d["v_comp"], n_splits=4)
+    out = torch.empty_like(d["q"])
+    lse = torch.empty((1, 64), dtype=torch.float32, device="cuda")
+    ds4a.attn_decode_merge(wl.layout, ws, n_splits=4, out=out, lse=lse)
+    want, wlse = oracle_out(wl)
+    assert_close(host(out), want, "partials + merge")
+    assert_lse_close(host(lse), wlse, "partials + merge lse")
