@@ -93,7 +93,7 @@ def ncu_traffic(workload: str):
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
-    """nvidia-smi samples every 100 ms while running; keeps those inside [t0, t1]."""
+    """nvidia-smi samples every 20 ms while running; keeps those inside [t0, t1]."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -109,7 +109,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
             return
@@ -270,9 +270,10 @@ def run_ours(args) -> None:
     g_full = capture(step, min(R, K))
     g_tail = capture(step, K % R) if K > R and K % R else None
     n_full = K // R if K >= R else 1
-    g_full.replay()
-    if g_tail is not None:
-        g_tail.replay()
+    with torch.cuda.stream(stream):
+        g_full.replay()
+        if g_tail is not None:
+            g_tail.replay()
     torch.cuda.synchronize()
 
     sampler = ClockSampler(local)
@@ -281,12 +282,13 @@ def run_ours(args) -> None:
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t_host0 = time.time()
-    e0.record(stream)
-    for _ in range(n_full):
-        g_full.replay()
-    if g_tail is not None:
-        g_tail.replay()
-    e1.record(stream)
+    with torch.cuda.stream(stream):  # a graph replays on the current stream
+        e0.record(stream)
+        for _ in range(n_full):
+            g_full.replay()
+        if g_tail is not None:
+            g_tail.replay()
+        e1.record(stream)
     barrier()
     t_host1 = time.time()
     sampler.stop()
@@ -297,14 +299,15 @@ def run_ours(args) -> None:
 
     # Dominant kernel alone (split-KV attention, no merge): graph of R launches.
     gp = capture(partial_step, R)
-    gp.replay()
-    torch.cuda.synchronize()
     reps = max(1, min(50, 20000 // R))
     p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    p0.record(stream)
-    for _ in range(reps):
+    with torch.cuda.stream(stream):
         gp.replay()
-    p1.record(stream)
+        torch.cuda.synchronize()
+        p0.record(stream)
+        for _ in range(reps):
+            gp.replay()
+        p1.record(stream)
     torch.cuda.synchronize()
     kernel_us = p0.elapsed_time(p1) * 1e3 / (reps * R)
     pk, pk_kind = peaks()
@@ -400,12 +403,13 @@ def run_also(torch, ds4a, W, dev, stream, pk, pk_kind):
         with torch.cuda.graph(g, stream=stream):
             for i in range(n):
                 fn(i)
-        g.replay()
-        torch.cuda.synchronize()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        g.replay()
-        b.record(stream)
+        with torch.cuda.stream(stream):
+            g.replay()
+            torch.cuda.synchronize()
+            a.record(stream)
+            g.replay()
+            b.record(stream)
         torch.cuda.synchronize()
         return a.elapsed_time(b) * 1e-3 / n
 
@@ -448,6 +452,39 @@ def run_also(torch, ds4a, W, dev, stream, pk, pk_kind):
     for e in out:
         e["peak_kind"] = pk_kind
     return out
+
+
+# ------------------------------------------------------------------ profiling cases
+
+CASES = ("tiny", "decode_r128_32k", "prefill_raw_2048", "indexed_r4_2048", "decode_long_262144")
+
+
+def run_case(name: str, calls: int) -> None:
+    """Runs `calls` calls of one workload and exits: the program ncu captures."""
+    import numpy as np
+    import torch
+    from mqa_flash_attention_gb300 import build, ds4a
+    from mqa_flash_attention_gb300 import workloads as W
+    build.build()
+    wl = W.decode_long(262144) if name == "decode_long_262144" else getattr(W, name)()
+    L = wl.layout
+
+    def up(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+    d = [up(a) for a in (wl.q, wl.k_raw, wl.v_raw, wl.k_comp, wl.v_comp)]
+    outs = [torch.empty_like(d[0]) for _ in range(calls)]
+    for i in range(calls):
+        if name == "indexed_r4_2048":
+            ds4a.attn_indexed(L, *d, up(wl.idx), out=outs[i])
+        elif name.startswith("decode"):
+            ds4a.attn_decode(L, *d, out=outs[i])
+        else:
+            ds4a.attn_prefill(L, *d[:3], *(d[3:] if L["n_comp"] else []), out=outs[i])
+    torch.cuda.synchronize()
+    if ds4a.device_status() != ds4a.OK:
+        raise RuntimeError("device wait ran out")
+    print(f"{name}: {calls} calls ok")
 
 
 # ------------------------------------------------------------------ reference arm
@@ -501,12 +538,18 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-also", action="store_true", help="skip the prefill / indexed / long-decode lines")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="length of the CPU oracle baseline")
+    ap.add_argument("--case", choices=CASES, default=None,
+                    help="run --calls calls of one workload and exit (the program ncu captures)")
+    ap.add_argument("--calls", type=int, default=3)
     ap.add_argument("--_oracle-leg", dest="oracle_leg", default=None, help=argparse.SUPPRESS)
     ap.add_argument("--_seconds", dest="leg_seconds", type=float, default=10.0, help=argparse.SUPPRESS)
     ap.add_argument("--_heads", dest="leg_heads", type=int, default=None, help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args.oracle_leg:
         print(json.dumps(oracle_leg(args.oracle_leg, args.leg_seconds, args.leg_heads)))
+        return
+    if args.case:
+        run_case(args.case, args.calls)
         return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
