@@ -191,6 +191,25 @@ def run_oracle_subprocess(workload: str, seconds: float, heads=None) -> dict:
     return json.loads(r.stdout.strip().splitlines()[-1])
 
 
+# ------------------------------------------------------------------ ranks
+
+def max_over_ranks(x: float, device="cpu") -> float:
+    """The slowest rank's value (timings are reported as the max over ranks)."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_step: float, steps: int, world: int, max_elapsed_s: float) -> float:
+    """Units all ranks processed divided by the slowest rank's time (weak scaling:
+    every rank runs its own replica of the step)."""
+    return units_per_step * steps * world / max_elapsed_s
+
+
 # ------------------------------------------------------------------ GPU arm
 
 def dist_setup():
@@ -218,14 +237,6 @@ def run_ours(args) -> None:
             import torch.distributed as dist
             dist.barrier()
         torch.cuda.synchronize()
-
-    def max_over_ranks(x: float) -> float:
-        if world == 1:
-            return x
-        import torch.distributed as dist
-        t = torch.tensor([x], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
 
     wl = W.decode_r128_32k()
     L = wl.layout
@@ -292,9 +303,9 @@ def run_ours(args) -> None:
     barrier()
     t_host1 = time.time()
     sampler.stop()
-    elapsed_ms = max_over_ranks(e0.elapsed_time(e1))
+    elapsed_ms = max_over_ranks(e0.elapsed_time(e1), dev)
     ms_per_step = elapsed_ms / K
-    value = step_bytes * K * world / (elapsed_ms * 1e-3) / 1e9
+    value = whole_job_rate(step_bytes, K, world, elapsed_ms * 1e-3) / 1e9
     clocks = sampler.summary(t_host0, t_host1)
 
     # Dominant kernel alone (split-KV attention, no merge): graph of R launches.
@@ -343,7 +354,7 @@ def run_ours(args) -> None:
             host_out.copy_(do, non_blocking=True)
         x1.record(stream)
     barrier()
-    e2e_ms = max_over_ranks(x0.elapsed_time(x1)) / Ke
+    e2e_ms = max_over_ranks(x0.elapsed_time(x1), dev) / Ke
     e2e = {"value": round(step_bytes * world / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": Ke, "ms_per_step": round(e2e_ms, 5)}
 

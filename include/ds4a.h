@@ -254,6 +254,16 @@ ds4a_status ds4a_attn_indexed(const ds4a_layout *L, const ds4a_tensors *X,
 ds4a_status ds4a_device_status(ds4a_stream_t stream, int clear);
 
 /*
+ * ds4a_device_error_word - like ds4a_device_status, but returns the raw error
+ * word in *word (0 = no error).  For a wait that ran out the word is
+ * 0x01000000 | site, where site names the barrier that was waited on (1 Q
+ * buffer free, 2 K/V stage free, 3 Q loaded, 4 S buffer free, 5 K/V stage
+ * loaded, 6 P written, 7 O read, 8 S computed, 9 P consumed, 10 O complete,
+ * 11 draining copies, 12 self test).  clear != 0 resets the word.
+ */
+ds4a_status ds4a_device_error_word(ds4a_stream_t stream, uint32_t *word, int clear);
+
+/*
  * ds4a_selftest_wait_timeout - diagnostic: launches one CTA that waits on a
  * barrier nothing ever completes, with the given bound (nanoseconds, 1e3 ..
  * 1e10).  The wait runs out, the kernel records DS4A_ERR_TIMEOUT in the

@@ -110,10 +110,10 @@ ds4a_status check_tensors(const ds4a_layout *L, const ds4a_tensors *X) {
 }
 
 ds4a_status encode(CUtensorMap *m, const void *base, int rank, const cuuint64_t *dims, const cuuint64_t *strides,
-                   const cuuint32_t *box) {
+                   const cuuint32_t *box, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   const cuuint32_t es[3] = {1, 1, 1};
   const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, (cuuint32_t)rank, const_cast<void *>(base), dims,
-                              strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? DS4A_OK : DS4A_ERR_CUDA;
 }
@@ -136,6 +136,14 @@ ds4a_status fill_params(AttnParams &p, const ds4a_layout *L, const ds4a_tensors 
     ds4a_status st = encode(&p.tm_q, X->q, 3, dims, strides, box);
     if (st != DS4A_OK) return st;
   }
+  if (X->o != nullptr) {
+    // Output: fp16 [T][64][512]; the epilogue stores [64 heads][128 dims] boxes.
+    const cuuint64_t dims[3] = {DS4A_HEAD_DIM, DS4A_HEADS, (cuuint64_t)L->T};
+    const cuuint64_t strides[2] = {DS4A_ROW_BYTES, (cuuint64_t)X->o_tok_stride};
+    const cuuint32_t box[3] = {128, 64, 1};
+    ds4a_status st = encode(&p.tm_o, X->o, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (st != DS4A_OK) return st;
+  }
   if (L->n_raw > 0) {
     ds4a_status st = encode_rows(&p.tm_k[0], X->k_raw, L->n_raw, X->raw_row_stride, 128);
     if (st == DS4A_OK) st = encode_rows(&p.tm_v[0], X->v_raw, L->n_raw, X->raw_row_stride, 128);
@@ -144,12 +152,11 @@ ds4a_status fill_params(AttnParams &p, const ds4a_layout *L, const ds4a_tensors 
   if (L->n_comp > 0) {
     ds4a_status st = encode_rows(&p.tm_k[1], X->k_comp, L->n_comp, X->comp_row_stride, 128);
     if (st == DS4A_OK) st = encode_rows(&p.tm_v[1], X->v_comp, L->n_comp, X->comp_row_stride, 128);
-    if (st == DS4A_OK && mode == ds4a::MODE_INDEXED) {
-      st = encode_rows(&p.tm_kg, X->k_comp, L->n_comp, X->comp_row_stride, 1);
-      if (st == DS4A_OK) st = encode_rows(&p.tm_vg, X->v_comp, L->n_comp, X->comp_row_stride, 1);
-    }
     if (st != DS4A_OK) return st;
   }
+  p.k_comp = X->k_comp;
+  p.v_comp = X->v_comp;
+  p.comp_row_stride = X->comp_row_stride;
   p.T = L->T;
   p.q_pos0 = L->q_pos0;
   p.n_raw = L->n_raw;
@@ -411,7 +418,9 @@ ds4a_status ds4a_attn_indexed(const ds4a_layout *L, const ds4a_tensors *X, const
   return launched(ds4a::launch_attn(p, grid, as_cuda(stream)));
 }
 
-ds4a_status ds4a_device_status(ds4a_stream_t stream, int clear) {
+ds4a_status ds4a_device_error_word(ds4a_stream_t stream, uint32_t *word, int clear) {
+  if (word == nullptr) return DS4A_ERR_INVALID_ARG;
+  *word = 0;
   DeviceState *d = nullptr;
   ds4a_status st = current_device(&d);
   if (st != DS4A_OK) return st;
@@ -422,6 +431,14 @@ ds4a_status ds4a_device_status(ds4a_stream_t stream, int clear) {
     const unsigned int zero = 0;
     if (cudaMemcpy(d->err, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return DS4A_ERR_CUDA;
   }
+  *word = v;
+  return DS4A_OK;
+}
+
+ds4a_status ds4a_device_status(ds4a_stream_t stream, int clear) {
+  uint32_t v = 0;
+  const ds4a_status st = ds4a_device_error_word(stream, &v, clear);
+  if (st != DS4A_OK) return st;
   return v != 0 ? DS4A_ERR_TIMEOUT : DS4A_OK;
 }
 

@@ -30,10 +30,15 @@
 // 2^8 and are stored as fp16, and the row sums add the same fp16 values, so
 // o = sum(p v) / sum(p) is an exact convex combination up to fp32 rounding.
 //
-// Warp roles (192 threads, one CTA per SM, persistent over work items):
-//   warps 0-3  softmax + epilogue (thread r owns TMEM lane r)
-//   warp  4    TMA producer (Q once per item, K/V in 32 KB stages)
-//   warp  5    TMEM allocator and tcgen05.mma issuer
+// Warp roles (384 threads, one CTA per SM, persistent over work items):
+//   warps 0-7   softmax + epilogue: warp w owns TMEM lane quarter w % 4 (32
+//               KV rows or dims) and heads 32*(w/4) .. +31
+//   warps 8-9   loaders: Q once per item, every K/V stage in ring order (TMA
+//               tiles, or 16-byte cp.async gathers of index-listed rows: a
+//               TMA gather moves only 512 bytes per instruction)
+//   warp  10    TMEM allocator and tcgen05.mma issuer
+// Each mbarrier is waited on only by a role that cannot fall more than one
+// phase behind it, which a parity wait needs.
 #pragma once
 
 #include "attn_params.h"
@@ -165,57 +170,122 @@ __device__ __forceinline__ ItemPlan plan_item(const AttnParams &p, int item) {
 
 // ------------------------------------------------------------------ warp reductions
 
-// Lane l ends with the max (or sum) over the warp's 32 rows of heads 2l and 2l+1.
+// Lane l ends with the max (or sum) over the warp's 32 rows of head l of the
+// 32 heads held in s[0..31].
 template <bool kMax>
-__device__ __forceinline__ float2 warp_reduce_scatter(const float (&s)[64], int lane) {
-  float a[32];
+__device__ __forceinline__ float warp_reduce_scatter32(const float (&s)[32], int lane) {
+  float a[16];
   {
     const bool up = lane & 16;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const float send = up ? s[i] : s[i + 32];
-      const float keep = up ? s[i + 32] : s[i];
+    for (int i = 0; i < 16; ++i) {
+      const float send = up ? s[i] : s[i + 16];
+      const float keep = up ? s[i + 16] : s[i];
       const float got = __shfl_xor_sync(0xffffffffu, send, 16);
       a[i] = kMax ? fmaxf(keep, got) : keep + got;
     }
   }
 #pragma unroll
-  for (int c = 32; c >= 4; c >>= 1) {  // 32 -> 16 -> 8 -> 4 -> 2 values, xor 8, 4, 2, 1
+  for (int c = 16; c >= 2; c >>= 1) {  // 16 -> 8 -> 4 -> 2 -> 1 values, xor 8, 4, 2, 1
     const int half = c / 2;
-    const bool up = lane & (c / 4);
+    const bool up = lane & half;
 #pragma unroll
     for (int i = 0; i < half; ++i) {
       const float send = up ? a[i] : a[i + half];
       const float keep = up ? a[i + half] : a[i];
-      const float got = __shfl_xor_sync(0xffffffffu, send, c / 4);
+      const float got = __shfl_xor_sync(0xffffffffu, send, half);
       a[i] = kMax ? fmaxf(keep, got) : keep + got;
     }
   }
-  return make_float2(a[0], a[1]);
+  return a[0];
 }
 
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
-// ------------------------------------------------------------------ producer
+// Ring position bookkeeping shared by every role.
+struct Ring {
+  uint32_t st = 0, ph = 0;
+  __device__ __forceinline__ void advance() {
+    if (++st == kStages) {
+      st = 0;
+      ph ^= 1;
+    }
+  }
+};
 
-__device__ __forceinline__ void producer_role(const AttnParams &p, uint32_t sbase, Misc &ms, int lane) {
+// ------------------------------------------------------------------ loaders
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Warps 8-9 fill Q (once per work item) and every K/V ring stage, in ring
+// order.  Only the filler of a stage waits on its "stage free" barrier: a
+// parity wait is unambiguous only for a waiter at most one phase behind, and
+// the filler cannot fall behind a barrier that only advances after its own
+// fills.
+//
+// TMA tiles: thread 0 issues two 16 KB box loads per 32 KB stage.
+// Gathered tiles (index-listed compressed rows): per stage (128 rows x 128
+// dims) each of the 64 threads copies 32 chunks of 16 bytes; a warp
+// instruction covers two rows x 256 contiguous bytes.  Chunk (row r, 16-byte
+// column c of a 64-dim box) lands at column c ^ (r & 7): the 128-byte swizzle
+// TMA applies, so the MMA reads gathered and TMA-loaded stages alike.
+// cp.async writes through the generic proxy, so a gathered stage is announced
+// (fence to the async proxy, one arrival) once its copies are complete,
+// kGatherLag stages behind the newest.
+__device__ __forceinline__ void loader_role(const AttnParams &p, uint32_t sbase, Misc &ms, int ltid) {
   volatile int *abrt = &ms.abort_flag;
+  const bool group = p.mode == MODE_INDEXED && p.n_comp > 0;  // all 64 threads needed
+  if (!group && ltid != 0) return;
   const uint32_t b_q_full = smem_u32(&ms.q_full), b_q_empty = smem_u32(&ms.q_empty);
-  uint32_t st = 0, ph = 0, n_item = 0;
-  uint32_t filled = 0, last_par = 0;
+  Ring ring;
+  uint32_t n_item = 0;
+  uint32_t filled = 0, last_par = 0;  // TMA stages issued (thread 0), for draining on abort
   bool q_issued = false;
   uint32_t q_par = 0;
   bool ok = true;
+  uint32_t pend[kGatherLag + 1];
+  int n_pend = 0;
+  const int c16 = ltid & 15;   // 16-byte column within a stage's 256-byte row slice
+  const int rsub = ltid >> 4;  // row within each group of 4
+  const uint8_t *kbase = reinterpret_cast<const uint8_t *>(p.k_comp);
+  const uint8_t *vbase = reinterpret_cast<const uint8_t *>(p.v_comp);
+
+  // Bounded wait by thread 0, decision shared by the group.
+  auto wait0 = [&](uint32_t bar, uint32_t parity, unsigned int site) -> bool {
+    bool bad = false;
+    if (ltid == 0) bad = !mbar_wait(bar, parity, abrt, p.timeout_ns, p.err, site);
+    if (group) bad = bar_red_or(2, kLoaderThreads, bad);
+    return !bad;
+  };
+  // Arrive for all but the newest `keep` pending gathered stages.
+  auto announce = [&](int keep) {
+    if (n_pend <= keep) return;
+    if (keep == 0) cp_async_wait<0>(); else cp_async_wait<kGatherLag>();
+    fence_proxy_async_smem();
+    named_bar_sync(2, kLoaderThreads);
+    while (n_pend > keep) {
+      if (ltid == 0) mbar_arrive(smem_u32(&ms.kv_full[pend[0]]));
+      for (int i = 0; i < kGatherLag; ++i) pend[i] = pend[i + 1];
+      --n_pend;
+    }
+  };
+
   const int n_items = p.T * p.n_splits;
   for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
     ItemPlan ip = plan_item(p, item);
     if (ip.j1 == ip.j0) continue;
-    if (lane == 0) ok = mbar_wait(b_q_empty, (n_item & 1) ^ 1, abrt, p.timeout_ns, p.err, SITE_Q_EMPTY);
-    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    ok = wait0(b_q_empty, (n_item & 1) ^ 1, SITE_Q_EMPTY);
     if (!ok) break;
-    if (lane == 0) {
+    if (ltid == 0) {
       mbar_arrive_expect_tx(b_q_full, kQBytes);
 #pragma unroll 1
       for (int b = 0; b < 8; ++b)
@@ -225,57 +295,61 @@ __device__ __forceinline__ void producer_role(const AttnParams &p, uint32_t sbas
     q_par = n_item & 1;
     for (int j = ip.j0; j < ip.j1 && ok; ++j) {
       const Tile tl = ip.cur.next(p);
-      int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
       if (tl.seg == 2) {
+        named_bar_sync(2, kLoaderThreads);  // every thread is done with the previous list
         const int32_t *lst = p.idx + (long long)ip.t * p.idx_stride;
-        int rr[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int k = tl.start + 4 * lane + i;
-          int c = k < p.top_k ? __ldg(lst + k) : -1;
-          rr[i] = (c >= 0 && c < p.n_comp) ? c : 0;  // empty slots load row 0, masked later
+        for (int k = ltid; k < 128; k += kLoaderThreads) {
+          const int slot = tl.start + k;
+          const int c = slot < p.top_k ? __ldg(lst + slot) : -1;
+          ms.idx_s[k] = (c >= 0 && c < p.n_comp) ? c : 0;  // empty slots load row 0, masked later
         }
-        r0 = rr[0]; r1 = rr[1]; r2 = rr[2]; r3 = rr[3];
+        named_bar_sync(2, kLoaderThreads);
       }
 #pragma unroll 1
       for (int part = 0; part < 8; ++part) {  // parts 0-3: K dims 128*part, parts 4-7: V
-        const uint32_t b_full = smem_u32(&ms.kv_full[st]);
-        if (lane == 0) ok = mbar_wait(smem_u32(&ms.kv_empty[st]), ph ^ 1, abrt, p.timeout_ns, p.err, SITE_KV_EMPTY);
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        ok = wait0(smem_u32(&ms.kv_empty[ring.st]), ring.ph ^ 1, SITE_KV_EMPTY);
         if (!ok) break;
-        const uint32_t dst = sbase + kOffKV + st * kStageBytes;
-        const int dim0 = 128 * (part & 3);
-        const bool is_v = part >= 4;
-        if (lane == 0) mbar_arrive_expect_tx(b_full, kStageBytes);
-        __syncwarp();
-        if (tl.seg == 2) {
-          const CUtensorMap *m = is_v ? &p.tm_vg : &p.tm_kg;
-          tma_gather4(dst + lane * 512, m, b_full, dim0, r0, r1, r2, r3);
-          tma_gather4(dst + kBoxBytes + lane * 512, m, b_full, dim0 + 64, r0, r1, r2, r3);
-        } else if (lane == 0) {
-          const CUtensorMap *m = is_v ? &p.tm_v[tl.seg] : &p.tm_k[tl.seg];
-          tma_load_2d(dst, m, b_full, dim0, tl.start);
-          tma_load_2d(dst + kBoxBytes, m, b_full, dim0 + 64, tl.start);
+        const uint32_t stage = sbase + kOffKV + ring.st * kStageBytes;
+        if (tl.seg != 2) {
+          if (ltid == 0) {
+            const uint32_t b_full = smem_u32(&ms.kv_full[ring.st]);
+            const int dim0 = 128 * (part & 3);
+            const CUtensorMap *m = part >= 4 ? &p.tm_v[tl.seg] : &p.tm_k[tl.seg];
+            mbar_arrive_expect_tx(b_full, kStageBytes);
+            tma_load_2d(stage, m, b_full, dim0, tl.start);
+            tma_load_2d(stage + kBoxBytes, m, b_full, dim0 + 64, tl.start);
+            filled |= 1u << ring.st;
+            last_par = (last_par & ~(1u << ring.st)) | (ring.ph << ring.st);
+          }
+        } else {
+          const uint8_t *base = (part >= 4 ? vbase : kbase) + 256 * (part & 3) + 16 * c16;
+          const uint32_t col_box = (c16 >> 3) * kBoxBytes;
+          const uint32_t col = c16 & 7;
+#pragma unroll 8
+          for (int it = 0; it < 32; ++it) {
+            const int row = 4 * it + rsub;
+            const uint8_t *src = base + (long long)ms.idx_s[row] * p.comp_row_stride;
+            cp_async16(stage + col_box + row * 128 + ((col ^ (row & 7)) << 4), src);
+          }
+          cp_async_commit();
+          pend[n_pend++] = ring.st;
+          announce(kGatherLag);
         }
-        filled |= 1u << st;
-        last_par = (last_par & ~(1u << st)) | (ph << st);
-        if (++st == kStages) {
-          st = 0;
-          ph ^= 1;
-        }
+        ring.advance();
       }
+      if (ok && tl.seg == 2) announce(0);
     }
     ++n_item;
   }
-  if (!ok && lane == 0) {
-    // Let every copy already issued land before the CTA's shared memory goes away.
+  if (group) cp_async_wait<0>();  // no gathered copy may still be landing at exit
+  if (!ok && ltid == 0) {
+    // Let every TMA copy already issued land before the CTA's shared memory goes away.
     volatile int never = 0;
     for (int s = 0; s < kStages; ++s)
       if (filled & (1u << s))
         mbar_wait(smem_u32(&ms.kv_full[s]), (last_par >> s) & 1, &never, 100000000ull, p.err, SITE_DRAIN);
     if (q_issued) mbar_wait(b_q_full, q_par, &never, 100000000ull, p.err, SITE_DRAIN);
   }
-  __syncwarp();
 }
 
 // ------------------------------------------------------------------ MMA issuer
@@ -285,7 +359,8 @@ __device__ __forceinline__ void mma_role(const AttnParams &p, uint32_t sbase, ui
     volatile int *abrt = &ms.abort_flag;
     constexpr uint32_t kIdescQK = idesc_f16_f32(128, 64, false, false);
     constexpr uint32_t kIdescPV = idesc_f16_f32(128, 64, true, true);
-    uint32_t st = 0, ph = 0, g = 0, n_item = 0;
+    Ring ring;
+    uint32_t g = 0, n_item = 0;
     bool ok = true;
     const int n_items = p.T * p.n_splits;
     for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
@@ -302,10 +377,10 @@ __device__ __forceinline__ void mma_role(const AttnParams &p, uint32_t sbase, ui
         const uint32_t d_s = tmem + kTmemS + 64 * sb;
         // S^T = K_tile . Q^T over the 512 dims, 128 dims per stage.
         for (int c = 0; c < 4 && ok; ++c) {
-          ok = mbar_wait(smem_u32(&ms.kv_full[st]), ph, abrt, p.timeout_ns, p.err, SITE_KV_FULL);
+          ok = mbar_wait(smem_u32(&ms.kv_full[ring.st]), ring.ph, abrt, p.timeout_ns, p.err, SITE_KV_FULL);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t stage = sbase + kOffKV + st * kStageBytes;
+          const uint32_t stage = sbase + kOffKV + ring.st * kStageBytes;
 #pragma unroll
           for (int b2 = 0; b2 < 2; ++b2) {
 #pragma unroll
@@ -315,11 +390,8 @@ __device__ __forceinline__ void mma_role(const AttnParams &p, uint32_t sbase, ui
               umma_f16(d_s, a, b, kIdescQK, (c | b2 | ks) != 0 ? 1u : 0u);
             }
           }
-          umma_commit(smem_u32(&ms.kv_empty[st]));
-          if (++st == kStages) {
-            st = 0;
-            ph ^= 1;
-          }
+          umma_commit(smem_u32(&ms.kv_empty[ring.st]));
+          ring.advance();
         }
         if (!ok) break;
         umma_commit(smem_u32(&ms.s_full[sb]));
@@ -333,21 +405,18 @@ __device__ __forceinline__ void mma_role(const AttnParams &p, uint32_t sbase, ui
         tc_fence_after();
         // O^T[m] += V_tile^T[dims 128m..] . P^T, 16 rows per instruction.
         for (int m = 0; m < 4 && ok; ++m) {
-          ok = mbar_wait(smem_u32(&ms.kv_full[st]), ph, abrt, p.timeout_ns, p.err, SITE_KV_FULL);
+          ok = mbar_wait(smem_u32(&ms.kv_full[ring.st]), ring.ph, abrt, p.timeout_ns, p.err, SITE_KV_FULL);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t stage = sbase + kOffKV + st * kStageBytes;
+          const uint32_t stage = sbase + kOffKV + ring.st * kStageBytes;
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
             const uint64_t a = sdesc_sw128(stage + ks * 2048, kBoxBytes, 1024);
             const uint64_t b = sdesc_sw128(sbase + kOffP + ks * 2048, 16, 1024);  // one 64-head MN atom: LBO unused
             umma_f16(tmem + 64 * m, a, b, kIdescPV, (jj > 0 || ks > 0) ? 1u : 0u);
           }
-          umma_commit(smem_u32(&ms.kv_empty[st]));
-          if (++st == kStages) {
-            st = 0;
-            ph ^= 1;
-          }
+          umma_commit(smem_u32(&ms.kv_empty[ring.st]));
+          ring.advance();
         }
         if (!ok) break;
         umma_commit(smem_u32(&ms.p_empty));
@@ -390,15 +459,26 @@ __device__ __forceinline__ void write_empty_item(const AttnParams &p, int item, 
     return;
   }
   __half *orow = p.o + (long long)t * p.o_tok_stride;
-  for (int h = 0; h < kH; ++h)
-    for (int m = 0; m < 4; ++m) orow[h * kD + 128 * m + tid] = __float2half_rn(0.f);
+  for (int i = tid; i < kH * kD; i += kComputeThreads) orow[(i >> 9) * kD + (i & 511)] = __float2half_rn(0.f);
   if (p.lse != nullptr && tid < kH) p.lse[(long long)t * kH + tid] = -INFINITY;
+}
+
+__device__ __forceinline__ void load32(const float *src, float (&v)[32]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float4 x = reinterpret_cast<const float4 *>(src)[i];
+    v[4 * i] = x.x; v[4 * i + 1] = x.y; v[4 * i + 2] = x.z; v[4 * i + 3] = x.w;
+  }
 }
 
 __device__ __forceinline__ void compute_role(const AttnParams &p, uint8_t *smem, uint32_t tmem, Misc &ms, int tid) {
   volatile int *abrt = &ms.abort_flag;
   const int w = tid >> 5, l = tid & 31;
-  const uint32_t lane_base = static_cast<uint32_t>(32 * w) << 16;
+  const int q = w & 3;            // TMEM lane quarter: rows (or dims) 32q .. 32q+31
+  const int hh = w >> 2;          // head half: heads 32hh .. 32hh+31
+  const int r = 32 * q + l;       // this thread's TMEM lane
+  const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+  const uint32_t col0 = 32 * hh;
   uint32_t g = 0, n_item = 0;
   bool bad = false, aborted = false;
   const int n_items = p.T * p.n_splits;
@@ -410,30 +490,29 @@ __device__ __forceinline__ void compute_role(const AttnParams &p, uint8_t *smem,
       continue;
     }
     float m_ref = -INFINITY;  // reference max of head `tid` (threads < 64), log2 units
-    float lpart[64];
+    float lpart[32];
 #pragma unroll
-    for (int h = 0; h < 64; ++h) lpart[h] = 0.f;
+    for (int h = 0; h < 32; ++h) lpart[h] = 0.f;
     const int nt = ip.j1 - ip.j0;
     for (int jj = 0; jj < nt; ++jj) {
       const Tile tl = ip.cur.next(p);
       const uint32_t sb = g & 1;
       bad = bad || !mbar_wait(smem_u32(&ms.s_full[sb]), (g >> 1) & 1, abrt, p.timeout_ns, p.err, SITE_S_FULL);
       tc_fence_after();
-      float s[64];
-      tmem_ld64(tmem + kTmemS + 64 * sb + lane_base, s);
+      float s[32];
+      tmem_ld32(tmem + kTmemS + 64 * sb + col0 + lane_base, s);
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(smem_u32(&ms.s_empty[sb]));
 
       bool vis;
       float bias;
-      row_visibility(p, t, tl, tid, vis, bias);
+      row_visibility(p, t, tl, r, vis, bias);
 #pragma unroll
-      for (int h = 0; h < 64; ++h) s[h] = vis ? fmaf(s[h], p.scale_log2, bias) : -INFINITY;
+      for (int h = 0; h < 32; ++h) s[h] = vis ? fmaf(s[h], p.scale_log2, bias) : -INFINITY;
 
-      const float2 mx = warp_reduce_scatter<true>(s, l);
-      *reinterpret_cast<float2 *>(&ms.red[w][2 * l]) = mx;
-      if (bar_red_or(1, 128, bad)) {
+      ms.red[q][col0 + l] = warp_reduce_scatter32<true>(s, l);
+      if (bar_red_or(1, kComputeThreads, bad)) {
         aborted = true;
         break;
       }
@@ -450,24 +529,26 @@ __device__ __forceinline__ void compute_role(const AttnParams &p, uint8_t *smem,
         ms.alpha[tid] = alpha;
         if (alpha != 1.f) ms.resc_flag[g & 1] = 1;
       }
-      named_bar_sync(1, 128);
+      named_bar_sync(1, kComputeThreads);
       const int resc = ms.resc_flag[g & 1];
       if (tid == 0) ms.resc_flag[(g + 1) & 1] = 0;
 
       // P (fp16) may only be rewritten once the previous PV has consumed it.
       bad = bad || !mbar_wait(smem_u32(&ms.p_empty), (g & 1) ^ 1, abrt, p.timeout_ns, p.err, SITE_P_EMPTY);
       if (resc) {
+        float al[32];
+        load32(ms.alpha + col0, al);
 #pragma unroll
-        for (int h = 0; h < 64; ++h) lpart[h] *= ms.alpha[h];
+        for (int h = 0; h < 32; ++h) lpart[h] *= al[h];
       }
-      // P^T row `tid` (64 heads, 128 bytes) with the 128-byte swizzle: the
-      // 16-byte chunk c (heads 8c .. 8c+7) goes to chunk c ^ (row & 7).
+      // P^T row r, heads 32hh .. +31 = 16-byte chunks 4hh .. 4hh+3 of the
+      // 128-byte row, stored at chunk c ^ (r & 7) (128-byte swizzle).
       {
-        uint8_t *prow = smem + kOffP + tid * 128;
+        uint8_t *prow = smem + kOffP + r * 128;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const float4 m0 = reinterpret_cast<const float4 *>(ms.m_use)[2 * c];
-          const float4 m1 = reinterpret_cast<const float4 *>(ms.m_use)[2 * c + 1];
+        for (int c = 0; c < 4; ++c) {
+          const float4 m0 = reinterpret_cast<const float4 *>(ms.m_use + col0)[2 * c];
+          const float4 m1 = reinterpret_cast<const float4 *>(ms.m_use + col0)[2 * c + 1];
           const float mu[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
           uint32_t w4[4];
 #pragma unroll
@@ -479,20 +560,23 @@ __device__ __forceinline__ void compute_role(const AttnParams &p, uint8_t *smem,
             lpart[h + 1] += f.y;
             w4[i] = *reinterpret_cast<const uint32_t *>(&hp);
           }
-          *reinterpret_cast<uint4 *>(prow + ((c ^ (tid & 7)) << 4)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+          const int chunk = 4 * hh + c;
+          *reinterpret_cast<uint4 *>(prow + ((chunk ^ (r & 7)) << 4)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
         }
       }
       if (resc && jj > 0) {
         // O^T holds the previous tiles against the old reference: scale column h by alpha[h].
+        float al[32];
+        load32(ms.alpha + col0, al);
         tc_fence_after();
 #pragma unroll 1
         for (int m = 0; m < 4; ++m) {
-          float o[64];
-          tmem_ld64(tmem + 64 * m + lane_base, o);
+          float o[32];
+          tmem_ld32(tmem + 64 * m + col0 + lane_base, o);
           tmem_wait_ld();
 #pragma unroll
-          for (int h = 0; h < 64; ++h) o[h] *= ms.alpha[h];
-          tmem_st64(tmem + 64 * m + lane_base, o);
+          for (int h = 0; h < 32; ++h) o[h] *= al[h];
+          tmem_st32(tmem + 64 * m + col0 + lane_base, o);
         }
         tmem_wait_st();
       }
@@ -506,9 +590,8 @@ __device__ __forceinline__ void compute_role(const AttnParams &p, uint8_t *smem,
     // Epilogue: sum the row partials per head, normalise (or hand out partials).
     bad = bad || !mbar_wait(smem_u32(&ms.o_full), n_item & 1, abrt, p.timeout_ns, p.err, SITE_O_FULL);
     tc_fence_after();
-    const float2 ls = warp_reduce_scatter<false>(lpart, l);
-    *reinterpret_cast<float2 *>(&ms.red[w][2 * l]) = ls;
-    if (bar_red_or(1, 128, bad)) {
+    ms.red[q][col0 + l] = warp_reduce_scatter32<false>(lpart, l);
+    if (bar_red_or(1, kComputeThreads, bad)) {
       aborted = true;
       break;
     }
@@ -522,34 +605,57 @@ __device__ __forceinline__ void compute_role(const AttnParams &p, uint8_t *smem,
           p.lse[(long long)t * kH + tid] = lsum > 0.f ? (m_ref + log2f(lsum)) * kLn2 : -INFINITY;
       }
     }
-    named_bar_sync(1, 128);
+    named_bar_sync(1, kComputeThreads);
+    if (p.partial) {
 #pragma unroll 1
-    for (int m = 0; m < 4; ++m) {
-      float o[64];
-      tmem_ld64(tmem + 64 * m + lane_base, o);
-      tmem_wait_ld();
-      const int d = 128 * m + tid;
-      if (p.partial) {
-        float *dst = p.ws_o + (long long)item * kH * kD + d;
+      for (int m = 0; m < 4; ++m) {
+        float o[32];
+        tmem_ld32(tmem + 64 * m + col0 + lane_base, o);
+        tmem_wait_ld();
+        float *dst = p.ws_o + ((long long)item * kH + col0) * kD + 128 * m + r;
 #pragma unroll
-        for (int h = 0; h < 64; ++h) dst[h * kD] = o[h];
-      } else {
-        __half *dst = p.o + (long long)t * p.o_tok_stride + d;
-#pragma unroll
-        for (int h = 0; h < 64; ++h) dst[h * kD] = __float2half_rn(o[h] * ms.inv_l[h]);
+        for (int h = 0; h < 32; ++h) dst[h * kD] = o[h];
       }
+    } else {
+      // O^T[128 dims][64 heads] -> fp16 O[64 heads][128 dims] staged in the P
+      // buffer (free once o_full has fired), then one TMA store per dim slice.
+      float inv[32];
+      load32(ms.inv_l + col0, inv);
+      __half *stg = reinterpret_cast<__half *>(smem + kOffP);
+#pragma unroll 1
+      for (int m = 0; m < 4; ++m) {
+        float o[32];
+        tmem_ld32(tmem + 64 * m + col0 + lane_base, o);
+        tmem_wait_ld();
+        if (m > 0) {
+          if (tid == 0) bulk_wait_read_all();
+          named_bar_sync(1, kComputeThreads);
+        }
+#pragma unroll
+        for (int h = 0; h < 32; ++h) stg[(col0 + h) * 128 + r] = __float2half_rn(o[h] * inv[h]);
+        fence_proxy_async_smem();
+        named_bar_sync(1, kComputeThreads);
+        if (tid == 0) {
+          tma_store_3d(&p.tm_o, smem_u32(stg), 128 * m, 0, t);
+          bulk_commit_group();
+        }
+      }
+      if (tid == 0) bulk_wait_read_all();  // the P buffer is reused by the next item
     }
     tc_fence_before();
     mbar_arrive(smem_u32(&ms.o_empty));
     ++n_item;
   }
+  if (tid == 0) bulk_wait_all();
 }
 
 // ------------------------------------------------------------------ kernel
 
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ AttnParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // Align by pointer arithmetic on the __shared__ array (not through an
+  // integer cast) so every access below stays a shared-memory access.
+  uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
   Misc &ms = *reinterpret_cast<Misc *>(smem + kOffMisc);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -563,12 +669,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&ms.s_full[s]), 1);
-      mbar_init(smem_u32(&ms.s_empty[s]), 128);
+      mbar_init(smem_u32(&ms.s_empty[s]), kComputeThreads);
     }
-    mbar_init(smem_u32(&ms.p_full), 128);
+    mbar_init(smem_u32(&ms.p_full), kComputeThreads);
     mbar_init(smem_u32(&ms.p_empty), 1);
     mbar_init(smem_u32(&ms.o_full), 1);
-    mbar_init(smem_u32(&ms.o_empty), 128);
+    mbar_init(smem_u32(&ms.o_empty), kComputeThreads);
     mbar_init(smem_u32(&ms.mma_done), 1);
     ms.abort_flag = 0;
     ms.resc_flag[0] = 0;
@@ -579,17 +685,34 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     tmem_alloc(smem_u32(&ms.tmem_base), kTmemCols);
     tmem_relinquish();
   }
+  if (warp == kLoaderWarp0 && lane == 0) {
+    // Fetch the tensor maps this call uses while the prologue runs.
+    tma_prefetch_desc(&p.tm_q);
+    if (p.n_raw > 0) {
+      tma_prefetch_desc(&p.tm_k[0]);
+      tma_prefetch_desc(&p.tm_v[0]);
+    }
+    if (p.n_comp > 0 && p.mode != MODE_INDEXED) {
+      tma_prefetch_desc(&p.tm_k[1]);
+      tma_prefetch_desc(&p.tm_v[1]);
+    }
+    if (!p.partial) tma_prefetch_desc(&p.tm_o);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ms.tmem_base;
+  // Inputs may come from the previous kernel in the stream: wait for it here,
+  // after the prologue, and let the next kernel start its own prologue.
+  grid_dependency_wait();
+  grid_launch_dependents();
 
-  if (warp < 4) {
+  if (warp < kComputeWarps) {
     compute_role(p, smem, tmem, ms, threadIdx.x);
-  } else if (warp == kProducerWarp) {
-    producer_role(p, sbase, ms, lane);
-  } else {
+  } else if (warp == kMmaWarp) {
     mma_role(p, sbase, tmem, ms, lane);
+  } else {
+    loader_role(p, sbase, ms, threadIdx.x - 32 * kLoaderWarp0);
   }
 
   tc_fence_before();

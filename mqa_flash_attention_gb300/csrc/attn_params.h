@@ -13,9 +13,17 @@ namespace ds4a {
 constexpr int kH = 64;
 constexpr int kD = 512;
 constexpr int kTile = 128;
-constexpr int kThreads = 192;
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
+// Warps 0-7: softmax + epilogue.  Warp w reads TMEM lane quarter (w % 4) and
+// owns heads 32*(w / 4) .. +31 of those rows.  Warps 8-9: loaders (Q and every
+// K/V stage: TMA tiles, or 16-byte cp.async gathers of index-listed rows).
+// Warp 10: TMEM allocator and MMA issuer.
+constexpr int kComputeWarps = 8;
+constexpr int kComputeThreads = 32 * kComputeWarps;
+constexpr int kLoaderWarp0 = 8;
+constexpr int kLoaderThreads = 64;
+constexpr int kMmaWarp = 10;
+constexpr int kThreads = 352;
+constexpr int kGatherLag = 2;     // gathered stages kept in flight before their barrier arrives
 constexpr int kStages = 4;
 constexpr uint32_t kQBytes = 65536;     // 8 boxes of [64 heads][64 dims] fp16
 constexpr uint32_t kQBoxBytes = 8192;
@@ -45,6 +53,7 @@ struct Misc {
   alignas(16) float m_use[kH];    // reference max used for P (log2 units)
   alignas(16) float alpha[kH];    // rescale factor of the previous reference
   alignas(16) float inv_l[kH];
+  alignas(16) int idx_s[128];     // compressed rows of the tile being gathered
   alignas(8) uint64_t q_full, q_empty;
   uint64_t kv_full[kStages], kv_empty[kStages];
   uint64_t s_full[2], s_empty[2];
@@ -64,12 +73,15 @@ struct AttnParams {
   CUtensorMap tm_k[2];     // [raw, comp] 2-D {512, rows}, box {64, 128}
   CUtensorMap tm_v[2];
   CUtensorMap tm_kg, tm_vg;  // compressed rows, box {64, 1} (gather4)
+  CUtensorMap tm_o;        // 3-D {512, 64, T}, box {128, 64, 1}, no swizzle (epilogue stores)
   int T, q_pos0, n_raw, raw_pos0, n_comp, ratio, window;
   float scale_log2;
   int mode;
   int n_splits;            // row ranges per token
   int partial;             // 1: unnormalised partials to the workspace
   int top_k;
+  const void *k_comp, *v_comp;  // compressed rows (read directly by the gather warps)
+  long long comp_row_stride;    // bytes
   const int32_t *idx;
   long long idx_stride;    // elements
   const __half *mask;

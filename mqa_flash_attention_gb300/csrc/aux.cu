@@ -139,6 +139,8 @@ cudaError_t launch_block_mask_dense(const GeomScalars &g, const __half *mask, lo
 
 __global__ void combine_kernel(const float *__restrict__ ws_o, const float2 *__restrict__ ws_ml, int n_splits,
                                __half *__restrict__ o, long long o_tok_stride, float *__restrict__ lse) {
+  grid_dependency_wait();  // the partials come from the previous kernel
+  grid_launch_dependents();
   const int q4 = blockIdx.x, h = blockIdx.y, t = blockIdx.z;
   const int d = 128 * q4 + threadIdx.x;
   const long long base = (long long)t * n_splits;
@@ -162,8 +164,18 @@ __global__ void combine_kernel(const float *__restrict__ ws_o, const float2 *__r
 cudaError_t launch_combine(const float *ws_o, const float2 *ws_ml, int n_splits, int T, __half *o,
                            long long o_tok_stride, float *lse, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  combine_kernel<<<dim3(4, 64, T), 128, 0, s>>>(ws_o, ws_ml, n_splits, o, o_tok_stride, lse);
-  return cudaGetLastError();
+  // Programmatic dependent launch: the merge is scheduled while the partial
+  // kernel runs and waits for it inside (griddepcontrol.wait).
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(4, 64, T);
+  cfg.blockDim = dim3(128);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, combine_kernel, ws_o, ws_ml, n_splits, o, o_tok_stride, lse);
 }
 
 // ------------------------------------------------------------------ self test

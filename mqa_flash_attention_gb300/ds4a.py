@@ -84,6 +84,8 @@ def lib() -> ctypes.CDLL:
         L.ds4a_attn_indexed.argtypes = [PL, PT, vp, i64, i32, vp]
         L.ds4a_device_status.restype = st
         L.ds4a_device_status.argtypes = [vp, ctypes.c_int]
+        L.ds4a_device_error_word.restype = st
+        L.ds4a_device_error_word.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
         L.ds4a_selftest_wait_timeout.restype = st
         L.ds4a_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
         _lib = L
@@ -269,6 +271,14 @@ def attn_indexed(layout, q, k_raw, v_raw, k_comp, v_comp, idx, *, out=None, lse=
 def device_status(clear: bool = True, stream=None) -> int:
     """Synchronises the stream and returns the device error status code."""
     return lib().ds4a_device_status(_stream(stream), 1 if clear else 0)
+
+
+def device_error_word(clear: bool = True, stream=None) -> int:
+    """Synchronises the stream and returns the raw device error word (0 = none)."""
+    w = ctypes.c_uint32(0)
+    _check(lib().ds4a_device_error_word(_stream(stream), ctypes.byref(w), 1 if clear else 0),
+           "ds4a_device_error_word")
+    return w.value
 
 
 def selftest_wait_timeout(timeout_ns: int, stream=None) -> None:

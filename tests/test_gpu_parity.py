@@ -36,6 +36,16 @@ def ds4a(torch):
     return _ds4a
 
 
+@pytest.fixture(autouse=True)
+def device_error_word_stays_clear(ds4a):
+    """Every GPU test must leave the device error word clear: a bounded wait
+    that ran out would otherwise go unnoticed by tests that check values only."""
+    ds4a.device_error_word(clear=True)
+    yield
+    w = ds4a.device_error_word(clear=True)
+    assert w == 0, f"a device wait ran out during this test: error word {w:#010x}"
+
+
 def dev(torch, a):
     return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).cuda()
 
@@ -382,6 +392,7 @@ def test_indexed_all_available_equals_dense(torch, ds4a):
 def test_stuck_wait_ends_as_a_status(torch, ds4a):
     assert ds4a.device_status(clear=True) == ds4a.OK
     ds4a.selftest_wait_timeout(2_000_000)          # 2 ms bound
+    assert ds4a.device_error_word(clear=False) == 0x01000000 | 12   # the self test's wait site
     assert ds4a.device_status(clear=True) == ds4a.ERR_TIMEOUT
     assert ds4a.device_status(clear=True) == ds4a.OK
     # the context is still usable
