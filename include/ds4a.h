@@ -231,6 +231,28 @@ ds4a_status ds4a_attn_decode_merge(const ds4a_layout *L, const ds4a_tensors *X, 
                                    const void *workspace, size_t workspace_bytes, ds4a_stream_t stream);
 
 /*
+ * ds4a_attn_decode_noalloc - ds4a_attn_decode for callers that cannot
+ * allocate device memory: code living inside a host framework whose memory
+ * pool owns the device, or a serving loop that forbids allocations once it is
+ * running, has no way to hand this library a workspace.  The pages have no
+ * counterpart of this call; it exists for those callers.
+ *   The split-KV partials go to an 8 MiB array inside the library (a
+ *   file-scope device array that every device loading the library holds until
+ *   the process exits), so T * n_splits * 131584 bytes must fit in 8 MiB
+ *   (T * n_splits <= 63).  n_splits <= 0 picks the usual split count, capped to
+ *   fit; a T or n_splits that cannot fit returns DS4A_ERR_WORKSPACE before any
+ *   launch.  Nothing is allocated: no cudaMalloc, no cudaFree.
+ *   The array needs no clearing: every byte a call reads was written earlier
+ *   in the same call.  All calls share the one array, so calls whose kernels
+ *   overlap on the GPU (different streams, or different host threads) race on
+ *   it and must be serialised by the caller.
+ *   The first call of the library on a device (any entry point) looks up the
+ *   array's device address; make that first call before any stream capture.
+ */
+ds4a_status ds4a_attn_decode_noalloc(const ds4a_layout *L, const ds4a_tensors *X, int32_t n_splits,
+                                     ds4a_stream_t stream);
+
+/*
  * ds4a_attn_indexed - [P2] "Layer Compression" (ratio-4 layers: an indexer
  * selects the top-512 compressed rows) and "GPU Backend Architecture"
  * (indexed mixed heads): each token sees its raw window rows plus the

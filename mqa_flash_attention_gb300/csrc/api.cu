@@ -16,6 +16,13 @@
 // is looked up once per device and handed to the kernels as a parameter.
 __device__ unsigned int g_ds4a_device_error;
 
+// Split-KV scratch of ds4a_attn_decode_noalloc, for callers that cannot
+// allocate device memory.  Every device that loads the library holds these
+// 8 MiB until the process exits.  In host code the name is only a stand-in:
+// the device address comes from cudaGetSymbolAddress (see current_device).
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;
+static __device__ __align__(256) unsigned char g_decode_scratch[kNoAllocScratchBytes];
+
 namespace {
 
 using ds4a::AttnParams;
@@ -28,6 +35,7 @@ struct DeviceState {
   bool supported = false;
   int sm_count = 0;
   unsigned int *err = nullptr;
+  void *scratch = nullptr;  // device address of g_decode_scratch
 };
 
 std::mutex g_mu;
@@ -54,6 +62,7 @@ ds4a_status current_device(DeviceState **out) {
       if (ds4a::prepare_attn_kernel() != cudaSuccess) return DS4A_ERR_CUDA;
       if (cudaGetSymbolAddress(reinterpret_cast<void **>(&d.err), g_ds4a_device_error) != cudaSuccess)
         return DS4A_ERR_CUDA;
+      if (cudaGetSymbolAddress(&d.scratch, g_decode_scratch) != cudaSuccess) return DS4A_ERR_CUDA;
       if (g_encode == nullptr) {
         cudaDriverEntryPointQueryResult q;
         void *fn = nullptr;
@@ -389,6 +398,35 @@ ds4a_status ds4a_attn_decode(const ds4a_layout *L, const ds4a_tensors *X, int32_
   float2 *ws_ml = nullptr;
   ds4a_status st = decode_setup(L, X, n_splits, workspace, workspace_bytes, true, true, &ws_o, &ws_ml);
   if (st != DS4A_OK || L->T == 0) return st;
+  st = decode_partials(L, X, n_splits, ws_o, ws_ml, stream);
+  if (st != DS4A_OK) return st;
+  return launched(ds4a::launch_combine(ws_o, ws_ml, n_splits, L->T, static_cast<__half *>(X->o),
+                                       X->o_tok_stride / 2, X->lse, as_cuda(stream)));
+}
+
+ds4a_status ds4a_attn_decode_noalloc(const ds4a_layout *L, const ds4a_tensors *X, int32_t n_splits,
+                                     ds4a_stream_t stream) {
+  ds4a_status st = check_layout(L);
+  if (st != DS4A_OK) return st;
+  if (L->T == 0) return DS4A_OK;
+  // Items (token, split) that fit in the scratch array.
+  const size_t per_item = ds4a_attn_decode_workspace_size(L, 1) / (size_t)L->T;
+  const size_t max_items = kNoAllocScratchBytes / per_item;
+  if ((size_t)L->T > max_items) return DS4A_ERR_WORKSPACE;
+  if (n_splits <= 0) {
+    n_splits = ds4a_attn_decode_default_splits(L);
+    const int32_t cap = (int32_t)(max_items / (size_t)L->T);
+    if (n_splits > cap) n_splits = cap;
+  } else if ((size_t)L->T * (size_t)n_splits > max_items) {
+    return DS4A_ERR_WORKSPACE;
+  }
+  DeviceState *d = nullptr;
+  st = current_device(&d);  // the first call on a device looks up the scratch address
+  if (st != DS4A_OK) return st;
+  float *ws_o = nullptr;
+  float2 *ws_ml = nullptr;
+  st = decode_setup(L, X, n_splits, d->scratch, kNoAllocScratchBytes, true, true, &ws_o, &ws_ml);
+  if (st != DS4A_OK) return st;
   st = decode_partials(L, X, n_splits, ws_o, ws_ml, stream);
   if (st != DS4A_OK) return st;
   return launched(ds4a::launch_combine(ws_o, ws_ml, n_splits, L->T, static_cast<__half *>(X->o),

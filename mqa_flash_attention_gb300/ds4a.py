@@ -80,6 +80,8 @@ def lib() -> ctypes.CDLL:
         L.ds4a_attn_decode_partials.argtypes = [PL, PT, i32, vp, ctypes.c_size_t, vp]
         L.ds4a_attn_decode_merge.restype = st
         L.ds4a_attn_decode_merge.argtypes = [PL, PT, i32, vp, ctypes.c_size_t, vp]
+        L.ds4a_attn_decode_noalloc.restype = st
+        L.ds4a_attn_decode_noalloc.argtypes = [PL, PT, i32, vp]
         L.ds4a_attn_indexed.restype = st
         L.ds4a_attn_indexed.argtypes = [PL, PT, vp, i64, i32, vp]
         L.ds4a_device_status.restype = st
@@ -254,6 +256,18 @@ def attn_decode_merge(layout, workspace, *, n_splits=0, out, lse=None, stream=No
                                         workspace.numel() * workspace.element_size(), _stream(stream)),
            "ds4a_attn_decode_merge")
     return out
+
+
+def attn_decode_noalloc(layout, q, k_raw, v_raw, k_comp=None, v_comp=None, *, n_splits=0, out=None, lse=None,
+                        want_lse=False, stream=None):
+    """:func:`attn_decode` without a workspace: the library's own 8 MiB scratch
+    array holds the split partials (for callers that cannot allocate)."""
+    L = make_layout(layout)
+    out, lse = _outputs(q, out, lse, want_lse)
+    X = _tensors(q, k_raw, v_raw, k_comp, v_comp, out, lse)
+    _check(lib().ds4a_attn_decode_noalloc(ctypes.byref(L), ctypes.byref(X), int(n_splits), _stream(stream)),
+           "ds4a_attn_decode_noalloc")
+    return (out, lse) if (want_lse or lse is not None) else out
 
 
 def attn_indexed(layout, q, k_raw, v_raw, k_comp, v_comp, idx, *, out=None, lse=None, want_lse=False, stream=None):
