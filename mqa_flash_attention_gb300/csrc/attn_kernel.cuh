@@ -30,13 +30,13 @@
 // 2^8 and are stored as fp16, and the row sums add the same fp16 values, so
 // o = sum(p v) / sum(p) is an exact convex combination up to fp32 rounding.
 //
-// Warp roles (384 threads, one CTA per SM, persistent over work items):
+// Warp roles (416 threads, one CTA per SM, persistent over work items):
 //   warps 0-7   softmax + epilogue: warp w owns TMEM lane quarter w % 4 (32
 //               KV rows or dims) and heads 32*(w/4) .. +31
-//   warps 8-9   loaders: Q once per item, every K/V stage in ring order (TMA
+//   warps 8-11  loaders: Q once per item, every K/V stage in ring order (TMA
 //               tiles, or 16-byte cp.async gathers of index-listed rows: a
 //               TMA gather moves only 512 bytes per instruction)
-//   warp  10    TMEM allocator and tcgen05.mma issuer
+//   warp  12    TMEM allocator and tcgen05.mma issuer
 // Each mbarrier is waited on only by a role that cannot fall more than one
 // phase behind it, which a parity wait needs.
 #pragma once
@@ -164,7 +164,11 @@ __device__ __forceinline__ ItemPlan plan_item(const AttnParams &p, int item) {
   const int n = count_tiles(p, ip.cur.z);
   ip.j0 = (int)(((long long)sp * n) / p.n_splits);
   ip.j1 = (int)(((long long)(sp + 1) * n) / p.n_splits);
-  for (int j = 0; j < ip.j0; ++j) ip.cur.next(p);
+  if (p.mode == MODE_MASK && p.status != nullptr) {
+    for (int j = 0; j < ip.j0; ++j) ip.cur.next(p);  // skipped blocks: walk the candidates
+  } else {
+    ip.cur.cand = ip.j0;  // every candidate is a tile: jump straight to the split's first
+  }
   return ip;
 }
 
@@ -225,25 +229,31 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
+// Arrive on `bar` when every cp.async this thread issued so far has completed;
+// the arrival counts toward the barrier's expected count (.noinc).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
 
-// Warps 8-9 fill Q (once per work item) and every K/V ring stage, in ring
-// order.  Only the filler of a stage waits on its "stage free" barrier: a
-// parity wait is unambiguous only for a waiter at most one phase behind, and
-// the filler cannot fall behind a barrier that only advances after its own
-// fills.
+// The loader warps fill Q (once per work item) and every K/V ring stage, in
+// ring order.  Only fillers wait on a "stage free" barrier: a parity wait is
+// unambiguous only for a waiter at most one phase behind, and a filler cannot
+// fall behind a barrier that only advances after its own fills.
 //
 // TMA tiles: thread 0 issues two 16 KB box loads per 32 KB stage.
 // Gathered tiles (index-listed compressed rows): per stage (128 rows x 128
-// dims) each of the 64 threads copies 32 chunks of 16 bytes; a warp
-// instruction covers two rows x 256 contiguous bytes.  Chunk (row r, 16-byte
-// column c of a 64-dim box) lands at column c ^ (r & 7): the 128-byte swizzle
-// TMA applies, so the MMA reads gathered and TMA-loaded stages alike.
-// cp.async writes through the generic proxy, so a gathered stage is announced
-// (fence to the async proxy, one arrival) once its copies are complete,
-// kGatherLag stages behind the newest.
+// dims) the loader threads copy 2048 chunks of 16 bytes; a warp instruction
+// covers two rows x 256 contiguous bytes.  Chunk (row r, 16-byte column c of a
+// 64-dim box) lands at column c ^ (r & 7): the 128-byte swizzle TMA applies, so
+// the MMA reads gathered and TMA-loaded stages alike.  Each thread's copies
+// arrive on the stage's barrier by themselves when they complete
+// (cp.async.mbarrier.arrive.noinc), so no loader thread waits for its own
+// copies and stages stay in flight up to the ring depth.  In this mode a
+// stage barrier expects one arrival per loader thread (TMA stages: thread 0's
+// arrive.expect_tx plus a plain arrival from every other thread).
 __device__ __forceinline__ void loader_role(const AttnParams &p, uint32_t sbase, Misc &ms, int ltid) {
   volatile int *abrt = &ms.abort_flag;
-  const bool group = p.mode == MODE_INDEXED && p.n_comp > 0;  // all 64 threads needed
+  const bool group = p.mode == MODE_INDEXED && p.n_comp > 0;  // all loader threads needed
   if (!group && ltid != 0) return;
   const uint32_t b_q_full = smem_u32(&ms.q_full), b_q_empty = smem_u32(&ms.q_empty);
   Ring ring;
@@ -252,39 +262,23 @@ __device__ __forceinline__ void loader_role(const AttnParams &p, uint32_t sbase,
   bool q_issued = false;
   uint32_t q_par = 0;
   bool ok = true;
-  uint32_t pend[kGatherLag + 1];
-  int n_pend = 0;
+  constexpr int kRowStep = kLoaderThreads / 16;  // rows copied per pass of the group
   const int c16 = ltid & 15;   // 16-byte column within a stage's 256-byte row slice
-  const int rsub = ltid >> 4;  // row within each group of 4
+  const int rsub = ltid >> 4;  // row within each group of kRowStep
   const uint8_t *kbase = reinterpret_cast<const uint8_t *>(p.k_comp);
   const uint8_t *vbase = reinterpret_cast<const uint8_t *>(p.v_comp);
-
-  // Bounded wait by thread 0, decision shared by the group.
-  auto wait0 = [&](uint32_t bar, uint32_t parity, unsigned int site) -> bool {
-    bool bad = false;
-    if (ltid == 0) bad = !mbar_wait(bar, parity, abrt, p.timeout_ns, p.err, site);
-    if (group) bad = bar_red_or(2, kLoaderThreads, bad);
-    return !bad;
-  };
-  // Arrive for all but the newest `keep` pending gathered stages.
-  auto announce = [&](int keep) {
-    if (n_pend <= keep) return;
-    if (keep == 0) cp_async_wait<0>(); else cp_async_wait<kGatherLag>();
-    fence_proxy_async_smem();
-    named_bar_sync(2, kLoaderThreads);
-    while (n_pend > keep) {
-      if (ltid == 0) mbar_arrive(smem_u32(&ms.kv_full[pend[0]]));
-      for (int i = 0; i < kGatherLag; ++i) pend[i] = pend[i + 1];
-      --n_pend;
-    }
-  };
 
   const int n_items = p.T * p.n_splits;
   for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
     ItemPlan ip = plan_item(p, item);
     if (ip.j1 == ip.j0) continue;
-    ok = wait0(b_q_empty, (n_item & 1) ^ 1, SITE_Q_EMPTY);
-    if (!ok) break;
+    bool bad = false;
+    if (ltid == 0) bad = !mbar_wait(b_q_empty, (n_item & 1) ^ 1, abrt, p.timeout_ns, p.err, SITE_Q_EMPTY);
+    if (group) bad = bar_red_or(2, kLoaderThreads, bad);
+    if (bad) {
+      ok = false;
+      break;
+    }
     if (ltid == 0) {
       mbar_arrive_expect_tx(b_q_full, kQBytes);
 #pragma unroll 1
@@ -307,12 +301,16 @@ __device__ __forceinline__ void loader_role(const AttnParams &p, uint32_t sbase,
       }
 #pragma unroll 1
       for (int part = 0; part < 8; ++part) {  // parts 0-3: K dims 128*part, parts 4-7: V
-        ok = wait0(smem_u32(&ms.kv_empty[ring.st]), ring.ph ^ 1, SITE_KV_EMPTY);
-        if (!ok) break;
+        // Every thread waits for the slot itself (bounded); a thread that gives
+        // up stops filling, and the group meets at the next tile's barrier.
+        if (!mbar_wait(smem_u32(&ms.kv_empty[ring.st]), ring.ph ^ 1, abrt, p.timeout_ns, p.err, SITE_KV_EMPTY)) {
+          ok = false;
+          break;
+        }
         const uint32_t stage = sbase + kOffKV + ring.st * kStageBytes;
+        const uint32_t b_full = smem_u32(&ms.kv_full[ring.st]);
         if (tl.seg != 2) {
           if (ltid == 0) {
-            const uint32_t b_full = smem_u32(&ms.kv_full[ring.st]);
             const int dim0 = 128 * (part & 3);
             const CUtensorMap *m = part >= 4 ? &p.tm_v[tl.seg] : &p.tm_k[tl.seg];
             mbar_arrive_expect_tx(b_full, kStageBytes);
@@ -320,24 +318,24 @@ __device__ __forceinline__ void loader_role(const AttnParams &p, uint32_t sbase,
             tma_load_2d(stage + kBoxBytes, m, b_full, dim0 + 64, tl.start);
             filled |= 1u << ring.st;
             last_par = (last_par & ~(1u << ring.st)) | (ring.ph << ring.st);
+          } else {
+            mbar_arrive(b_full);
           }
         } else {
           const uint8_t *base = (part >= 4 ? vbase : kbase) + 256 * (part & 3) + 16 * c16;
           const uint32_t col_box = (c16 >> 3) * kBoxBytes;
           const uint32_t col = c16 & 7;
 #pragma unroll 8
-          for (int it = 0; it < 32; ++it) {
-            const int row = 4 * it + rsub;
+          for (int it = 0; it < 128 / kRowStep; ++it) {
+            const int row = kRowStep * it + rsub;
             const uint8_t *src = base + (long long)ms.idx_s[row] * p.comp_row_stride;
             cp_async16(stage + col_box + row * 128 + ((col ^ (row & 7)) << 4), src);
           }
-          cp_async_commit();
-          pend[n_pend++] = ring.st;
-          announce(kGatherLag);
+          cp_async_arrive_noinc(b_full);
         }
         ring.advance();
       }
-      if (ok && tl.seg == 2) announce(0);
+      if (group) ok = !bar_red_or(2, kLoaderThreads, !ok);  // uniform decision before the next list
     }
     ++n_item;
   }
@@ -617,30 +615,19 @@ __device__ __forceinline__ void compute_role(const AttnParams &p, uint8_t *smem,
         for (int h = 0; h < 32; ++h) dst[h * kD] = o[h];
       }
     } else {
-      // O^T[128 dims][64 heads] -> fp16 O[64 heads][128 dims] staged in the P
-      // buffer (free once o_full has fired), then one TMA store per dim slice.
+      // O^T[128 dims][64 heads] -> fp16 O: for each head a warp writes 32
+      // consecutive dims (64 contiguous bytes).
       float inv[32];
       load32(ms.inv_l + col0, inv);
-      __half *stg = reinterpret_cast<__half *>(smem + kOffP);
+      __half *orow = p.o + (long long)t * p.o_tok_stride + (long long)col0 * kD + r;
 #pragma unroll 1
       for (int m = 0; m < 4; ++m) {
         float o[32];
         tmem_ld32(tmem + 64 * m + col0 + lane_base, o);
         tmem_wait_ld();
-        if (m > 0) {
-          if (tid == 0) bulk_wait_read_all();
-          named_bar_sync(1, kComputeThreads);
-        }
 #pragma unroll
-        for (int h = 0; h < 32; ++h) stg[(col0 + h) * 128 + r] = __float2half_rn(o[h] * inv[h]);
-        fence_proxy_async_smem();
-        named_bar_sync(1, kComputeThreads);
-        if (tid == 0) {
-          tma_store_3d(&p.tm_o, smem_u32(stg), 128 * m, 0, t);
-          bulk_commit_group();
-        }
+        for (int h = 0; h < 32; ++h) orow[h * kD + 128 * m] = __float2half_rn(o[h] * inv[h]);
       }
-      if (tid == 0) bulk_wait_read_all();  // the P buffer is reused by the next item
     }
     tc_fence_before();
     mbar_arrive(smem_u32(&ms.o_empty));
@@ -663,8 +650,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&ms.q_full), 1);
     mbar_init(smem_u32(&ms.q_empty), 1);
+    const uint32_t fill_count = (p.mode == MODE_INDEXED && p.n_comp > 0) ? kLoaderThreads : 1;
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_u32(&ms.kv_full[s]), 1);
+      mbar_init(smem_u32(&ms.kv_full[s]), fill_count);
       mbar_init(smem_u32(&ms.kv_empty[s]), 1);
     }
     for (int s = 0; s < 2; ++s) {

@@ -14,16 +14,16 @@ constexpr int kH = 64;
 constexpr int kD = 512;
 constexpr int kTile = 128;
 // Warps 0-7: softmax + epilogue.  Warp w reads TMEM lane quarter (w % 4) and
-// owns heads 32*(w / 4) .. +31 of those rows.  Warps 8-9: loaders (Q and every
-// K/V stage: TMA tiles, or 16-byte cp.async gathers of index-listed rows).
-// Warp 10: TMEM allocator and MMA issuer.
+// owns heads 32*(w / 4) .. +31 of those rows.  Warps 8-11: loaders (Q and
+// every K/V stage: TMA tiles, or 16-byte cp.async gathers of index-listed
+// rows).  Warp 12: TMEM allocator and MMA issuer.
 constexpr int kComputeWarps = 8;
 constexpr int kComputeThreads = 32 * kComputeWarps;
 constexpr int kLoaderWarp0 = 8;
-constexpr int kLoaderThreads = 64;
-constexpr int kMmaWarp = 10;
-constexpr int kThreads = 352;
-constexpr int kGatherLag = 2;     // gathered stages kept in flight before their barrier arrives
+constexpr int kLoaderWarps = 4;
+constexpr int kLoaderThreads = 32 * kLoaderWarps;
+constexpr int kMmaWarp = kLoaderWarp0 + kLoaderWarps;
+constexpr int kThreads = 32 * (kMmaWarp + 1);
 constexpr int kStages = 4;
 constexpr uint32_t kQBytes = 65536;     // 8 boxes of [64 heads][64 dims] fp16
 constexpr uint32_t kQBoxBytes = 8192;

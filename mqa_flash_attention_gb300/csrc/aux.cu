@@ -135,40 +135,84 @@ cudaError_t launch_block_mask_dense(const GeomScalars &g, const __half *mask, lo
 // Each split s of a token left an unnormalised O_s (fp32, relative to its
 // reference max m_s in log2 units) and l_s.  With M = max_s m_s:
 //   o = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s,  lse = (M + log2 L) ln 2.
-// Grid (4 dim quarters, 64 heads, T tokens), 128 threads: one dim each.
+// One block per (token, head, half of the dims), 256 threads, one dim each.
+// The split weights are computed once into shared memory; the partials are
+// then streamed with eight independent loads in flight per thread.
 
-__global__ void combine_kernel(const float *__restrict__ ws_o, const float2 *__restrict__ ws_ml, int n_splits,
-                               __half *__restrict__ o, long long o_tok_stride, float *__restrict__ lse) {
+constexpr int kCombineThreads = 256;
+constexpr int kCombineMaxSplits = 4096;
+
+__device__ __forceinline__ float block_reduce(float v, bool is_max, float *red) {
+  for (int o = 16; o > 0; o >>= 1) {
+    const float x = __shfl_xor_sync(0xffffffffu, v, o);
+    v = is_max ? fmaxf(v, x) : v + x;
+  }
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  __syncthreads();
+  if (l == 0) red[w] = v;
+  __syncthreads();
+  v = l < kCombineThreads / 32 ? red[l] : (is_max ? -INFINITY : 0.f);
+  for (int o = 4; o > 0; o >>= 1) {
+    const float x = __shfl_xor_sync(0xffffffffu, v, o);
+    v = is_max ? fmaxf(v, x) : v + x;
+  }
+  return __shfl_sync(0xffffffffu, v, 0);
+}
+
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float *__restrict__ ws_o,
+                                                                  const float2 *__restrict__ ws_ml, int n_splits,
+                                                                  __half *__restrict__ o, long long o_tok_stride,
+                                                                  float *__restrict__ lse) {
+  __shared__ float w_s[kCombineMaxSplits];
+  __shared__ float red[kCombineThreads / 32];
   grid_dependency_wait();  // the partials come from the previous kernel
   grid_launch_dependents();
-  const int q4 = blockIdx.x, h = blockIdx.y, t = blockIdx.z;
-  const int d = 128 * q4 + threadIdx.x;
+  const int half = blockIdx.x, h = blockIdx.y, t = blockIdx.z;
   const long long base = (long long)t * n_splits;
-  float M = -INFINITY;
-  for (int s = 0; s < n_splits; ++s) M = fmaxf(M, ws_ml[(base + s) * 64 + h].x);
-  float L = 0.f, acc = 0.f;
-  if (M != -INFINITY) {
-    for (int s = 0; s < n_splits; ++s) {
-      const float2 ml = ws_ml[(base + s) * 64 + h];
-      if (ml.x == -INFINITY) continue;
-      const float w = exp2f(ml.x - M);
-      L += w * ml.y;
-      acc += w * ws_o[((base + s) * 64 + h) * 512 + d];
+  float mx = -INFINITY;
+  for (int s = threadIdx.x; s < n_splits; s += kCombineThreads) mx = fmaxf(mx, ws_ml[(base + s) * 64 + h].x);
+  const float M = block_reduce(mx, true, red);
+  float lsum = 0.f;
+  for (int s = threadIdx.x; s < n_splits; s += kCombineThreads) {
+    const float2 ml = ws_ml[(base + s) * 64 + h];
+    const float wgt = (ml.x == -INFINITY || M == -INFINITY) ? 0.f : exp2f(ml.x - M);
+    w_s[s] = wgt;
+    lsum += wgt * ml.y;
+  }
+  const float L = block_reduce(lsum, false, red);  // also orders the w_s writes before the reads below
+  const int d = 256 * half + threadIdx.x;
+  const float *src = ws_o + (base * 64 + h) * 512 + d;
+  const long long step = 64LL * 512;
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+  int s = 0;
+  for (; s + 8 <= n_splits; s += 8) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float wgt = w_s[s + i];  // same for every thread: no divergence
+      if (wgt != 0.f) acc[i] += wgt * __ldg(src + (long long)(s + i) * step);
     }
   }
-  o[(long long)t * o_tok_stride + h * 512 + d] = __float2half_rn(L > 0.f ? acc / L : 0.f);
-  if (lse != nullptr && q4 == 0 && threadIdx.x == 0)
+  for (; s < n_splits; ++s) {
+    const float wgt = w_s[s];
+    if (wgt != 0.f) acc[0] += wgt * __ldg(src + (long long)s * step);
+  }
+  const float sum = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+  o[(long long)t * o_tok_stride + h * 512 + d] = __float2half_rn(L > 0.f ? sum / L : 0.f);
+  if (lse != nullptr && half == 0 && threadIdx.x == 0)
     lse[(long long)t * 64 + h] = L > 0.f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
 }
 
 cudaError_t launch_combine(const float *ws_o, const float2 *ws_ml, int n_splits, int T, __half *o,
                            long long o_tok_stride, float *lse, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
+  if (n_splits > kCombineMaxSplits) return cudaErrorInvalidValue;
   // Programmatic dependent launch: the merge is scheduled while the partial
   // kernel runs and waits for it inside (griddepcontrol.wait).
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(4, 64, T);
-  cfg.blockDim = dim3(128);
+  cfg.gridDim = dim3(2, 64, T);
+  cfg.blockDim = dim3(kCombineThreads);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
