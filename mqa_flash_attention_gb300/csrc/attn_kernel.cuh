@@ -615,18 +615,26 @@ __device__ __forceinline__ void compute_role(const AttnParams &p, uint8_t *smem,
         for (int h = 0; h < 32; ++h) dst[h * kD] = o[h];
       }
     } else {
-      // O^T[128 dims][64 heads] -> fp16 O: for each head a warp writes 32
-      // consecutive dims (64 contiguous bytes).
+      // O^T[128 dims][64 heads] -> fp16 O.  Lanes 2k and 2k+1 hold adjacent
+      // dims: for each pair of heads they swap one value, so the even lane
+      // writes both dims of the first head and the odd lane both dims of the
+      // second (32-bit stores, 64 contiguous bytes per head per warp).
       float inv[32];
       load32(ms.inv_l + col0, inv);
-      __half *orow = p.o + (long long)t * p.o_tok_stride + (long long)col0 * kD + r;
+      const bool odd = l & 1;
+      __half *obase = p.o + (long long)t * p.o_tok_stride + (long long)col0 * kD + (r & ~1);
 #pragma unroll 1
       for (int m = 0; m < 4; ++m) {
         float o[32];
         tmem_ld32(tmem + 64 * m + col0 + lane_base, o);
         tmem_wait_ld();
 #pragma unroll
-        for (int h = 0; h < 32; ++h) orow[h * kD + 128 * m] = __float2half_rn(o[h] * inv[h]);
+        for (int h = 0; h < 32; h += 2) {
+          const float a = o[h] * inv[h], b = o[h + 1] * inv[h + 1];
+          const float got = __shfl_xor_sync(0xffffffffu, odd ? a : b, 1);
+          const __half2 v = odd ? __floats2half2_rn(got, b) : __floats2half2_rn(a, got);
+          *reinterpret_cast<__half2 *>(obase + (h + (odd ? 1 : 0)) * kD + 128 * m) = v;
+        }
       }
     }
     tc_fence_before();
