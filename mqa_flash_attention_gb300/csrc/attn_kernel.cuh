@@ -357,6 +357,13 @@ __device__ __forceinline__ void mma_role(const AttnParams &p, uint32_t sbase, ui
     volatile int *abrt = &ms.abort_flag;
     constexpr uint32_t kIdescQK = idesc_f16_f32(128, 64, false, false);
     constexpr uint32_t kIdescPV = idesc_f16_f32(128, 64, true, true);
+    // Base descriptors, built once; the issue loops only add byte offsets.
+    // K tiles and Q: K-major.  V tiles: MN-major, LBO = one 64-dim box.
+    // P^T: one 64-head MN atom, LBO unused.
+    const uint64_t k_desc = sdesc_sw128(sbase + kOffKV, 16, 1024);
+    const uint64_t v_desc = sdesc_sw128(sbase + kOffKV, kBoxBytes, 1024);
+    const uint64_t q_desc = sdesc_sw128(sbase + kOffQ, 16, 1024);
+    const uint64_t p_desc = sdesc_sw128(sbase + kOffP, 16, 1024);
     Ring ring;
     uint32_t g = 0, n_item = 0;
     bool ok = true;
@@ -378,14 +385,18 @@ __device__ __forceinline__ void mma_role(const AttnParams &p, uint32_t sbase, ui
           ok = mbar_wait(smem_u32(&ms.kv_full[ring.st]), ring.ph, abrt, p.timeout_ns, p.err, SITE_KV_FULL);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t stage = sbase + kOffKV + ring.st * kStageBytes;
+          const uint64_t a0 = sdesc_add(k_desc, ring.st * kStageBytes);
+          const uint64_t b0 = sdesc_add(q_desc, 2 * c * kQBoxBytes);
 #pragma unroll
           for (int b2 = 0; b2 < 2; ++b2) {
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
-              const uint64_t a = sdesc_sw128(stage + b2 * kBoxBytes + ks * 32, 16, 1024);
-              const uint64_t b = sdesc_sw128(sbase + kOffQ + (2 * c + b2) * kQBoxBytes + ks * 32, 16, 1024);
-              umma_f16(d_s, a, b, kIdescQK, (c | b2 | ks) != 0 ? 1u : 0u);
+              const uint64_t a = sdesc_add(a0, b2 * kBoxBytes + ks * 32);
+              const uint64_t b = sdesc_add(b0, b2 * kQBoxBytes + ks * 32);
+              if (b2 == 0 && ks == 0)
+                umma_f16(d_s, a, b, kIdescQK, c != 0 ? 1u : 0u);
+              else
+                umma_f16_acc(d_s, a, b, kIdescQK);
             }
           }
           umma_commit(smem_u32(&ms.kv_empty[ring.st]));
@@ -406,12 +417,15 @@ __device__ __forceinline__ void mma_role(const AttnParams &p, uint32_t sbase, ui
           ok = mbar_wait(smem_u32(&ms.kv_full[ring.st]), ring.ph, abrt, p.timeout_ns, p.err, SITE_KV_FULL);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t stage = sbase + kOffKV + ring.st * kStageBytes;
+          const uint64_t a0 = sdesc_add(v_desc, ring.st * kStageBytes);
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
-            const uint64_t a = sdesc_sw128(stage + ks * 2048, kBoxBytes, 1024);
-            const uint64_t b = sdesc_sw128(sbase + kOffP + ks * 2048, 16, 1024);  // one 64-head MN atom: LBO unused
-            umma_f16(tmem + 64 * m, a, b, kIdescPV, (jj > 0 || ks > 0) ? 1u : 0u);
+            const uint64_t a = sdesc_add(a0, ks * 2048);
+            const uint64_t b = sdesc_add(p_desc, ks * 2048);
+            if (ks == 0)
+              umma_f16(tmem + 64 * m, a, b, kIdescPV, jj > 0 ? 1u : 0u);
+            else
+              umma_f16_acc(tmem + 64 * m, a, b, kIdescPV);
           }
           umma_commit(smem_u32(&ms.kv_empty[ring.st]));
           ring.advance();

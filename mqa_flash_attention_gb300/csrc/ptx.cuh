@@ -201,6 +201,14 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64
       : "memory");
 }
 
+// D(tmem) += A * B^T with the accumulate flag as an immediate (no predicate
+// set-up on the issue path).
+__device__ __forceinline__ void umma_f16_acc(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc) {
+  asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, 1;" ::"r"(d_tmem), "l"(adesc), "l"(bdesc),
+               "r"(idesc)
+               : "memory");
+}
+
 // Arrive on `bar` once every tcgen05 operation issued so far by this thread
 // has completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
@@ -290,6 +298,16 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
   return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) |
          (static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16) |
          (static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// The same descriptor moved by `bytes` (a multiple of 16).  The start address
+// sits in the low 14 bits in 16-byte units and shared addresses stay below
+// 256 KB, so the move is one 32-bit add on the low word with no carry into
+// the other fields.  On the MMA issue path this matters: rebuilding each
+// descriptor from an address (shift, mask, or, 64-bit assemble) before every
+// 128x64x16 MMA costs more single-thread issue cycles than the MMA takes.
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t desc, uint32_t bytes) {
+  return (desc & 0xFFFFFFFF00000000ull) | static_cast<uint32_t>(static_cast<uint32_t>(desc) + (bytes >> 4));
 }
 
 // Instruction descriptor of tcgen05.mma kind::f16: fp16 A and B, fp32 D.
