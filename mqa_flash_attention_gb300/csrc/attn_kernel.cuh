@@ -269,9 +269,12 @@ __device__ __forceinline__ void loader_role(const AttnParams &p, uint32_t sbase,
   const uint8_t *vbase = reinterpret_cast<const uint8_t *>(p.v_comp);
 
   const int n_items = p.T * p.n_splits;
+  const bool plan_reads_status = p.mode == MODE_MASK && p.status != nullptr;
+  if (plan_reads_status) grid_dependency_wait();  // the plan reads the caller's status bytes
   for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
     ItemPlan ip = plan_item(p, item);
     if (ip.j1 == ip.j0) continue;
+    if (n_item == 0 && !plan_reads_status) grid_dependency_wait();  // first global read follows
     bool bad = false;
     if (ltid == 0) bad = !mbar_wait(b_q_empty, (n_item & 1) ^ 1, abrt, p.timeout_ns, p.err, SITE_Q_EMPTY);
     if (group) bad = bar_red_or(2, kLoaderThreads, bad);
@@ -368,6 +371,7 @@ __device__ __forceinline__ void mma_role(const AttnParams &p, uint32_t sbase, ui
     uint32_t g = 0, n_item = 0;
     bool ok = true;
     const int n_items = p.T * p.n_splits;
+    if (p.mode == MODE_MASK && p.status != nullptr) grid_dependency_wait();  // the plan reads status bytes
     for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
       ItemPlan ip = plan_item(p, item);
       if (ip.j1 == ip.j0) continue;
@@ -428,6 +432,9 @@ __device__ __forceinline__ void mma_role(const AttnParams &p, uint32_t sbase, ui
               umma_f16_acc(tmem + 64 * m, a, b, kIdescPV);
           }
           umma_commit(smem_u32(&ms.kv_empty[ring.st]));
+          // After the item's last tile, block m of O^T is final: the epilogue
+          // drains it while the remaining blocks are still being computed.
+          if (jj == nt - 1) umma_commit(smem_u32(&ms.o_full[m]));
           ring.advance();
         }
         if (!ok) break;
@@ -435,7 +442,6 @@ __device__ __forceinline__ void mma_role(const AttnParams &p, uint32_t sbase, ui
         ++g;
       }
       if (!ok) break;
-      umma_commit(smem_u32(&ms.o_full));
       ++n_item;
     }
     // Every MMA issued so far must finish before TMEM is released.
@@ -494,6 +500,7 @@ __device__ __forceinline__ void compute_role(const AttnParams &p, uint8_t *smem,
   uint32_t g = 0, n_item = 0;
   bool bad = false, aborted = false;
   const int n_items = p.T * p.n_splits;
+  grid_dependency_wait();  // outputs and index lists may be shared with the previous kernel
   for (int item = blockIdx.x; item < n_items && !aborted; item += gridDim.x) {
     ItemPlan ip = plan_item(p, item);
     const int t = ip.t;
@@ -599,9 +606,9 @@ __device__ __forceinline__ void compute_role(const AttnParams &p, uint8_t *smem,
     }
     if (aborted) break;
 
-    // Epilogue: sum the row partials per head, normalise (or hand out partials).
-    bad = bad || !mbar_wait(smem_u32(&ms.o_full), n_item & 1, abrt, p.timeout_ns, p.err, SITE_O_FULL);
-    tc_fence_after();
+    // Epilogue: sum the row partials per head (they do not depend on O), then
+    // normalise (or hand out partials) one O^T block at a time as each block
+    // of the last PV completes.
     ms.red[q][col0 + l] = warp_reduce_scatter32<false>(lpart, l);
     if (bar_red_or(1, kComputeThreads, bad)) {
       aborted = true;
@@ -621,6 +628,8 @@ __device__ __forceinline__ void compute_role(const AttnParams &p, uint8_t *smem,
     if (p.partial) {
 #pragma unroll 1
       for (int m = 0; m < 4; ++m) {
+        bad = bad || !mbar_wait(smem_u32(&ms.o_full[m]), n_item & 1, abrt, p.timeout_ns, p.err, SITE_O_FULL);
+        tc_fence_after();
         float o[32];
         tmem_ld32(tmem + 64 * m + col0 + lane_base, o);
         tmem_wait_ld();
@@ -639,6 +648,8 @@ __device__ __forceinline__ void compute_role(const AttnParams &p, uint8_t *smem,
       __half *obase = p.o + (long long)t * p.o_tok_stride + (long long)col0 * kD + (r & ~1);
 #pragma unroll 1
       for (int m = 0; m < 4; ++m) {
+        bad = bad || !mbar_wait(smem_u32(&ms.o_full[m]), n_item & 1, abrt, p.timeout_ns, p.err, SITE_O_FULL);
+        tc_fence_after();
         float o[32];
         tmem_ld32(tmem + 64 * m + col0 + lane_base, o);
         tmem_wait_ld();
@@ -654,6 +665,10 @@ __device__ __forceinline__ void compute_role(const AttnParams &p, uint8_t *smem,
     tc_fence_before();
     mbar_arrive(smem_u32(&ms.o_empty));
     ++n_item;
+    if (bar_red_or(1, kComputeThreads, bad)) {  // a block wait ran out: leave together
+      aborted = true;
+      break;
+    }
   }
   if (tid == 0) bulk_wait_all();
 }
@@ -683,7 +698,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     }
     mbar_init(smem_u32(&ms.p_full), kComputeThreads);
     mbar_init(smem_u32(&ms.p_empty), 1);
-    mbar_init(smem_u32(&ms.o_full), 1);
+    for (int m = 0; m < 4; ++m) mbar_init(smem_u32(&ms.o_full[m]), 1);
     mbar_init(smem_u32(&ms.o_empty), kComputeThreads);
     mbar_init(smem_u32(&ms.mma_done), 1);
     ms.abort_flag = 0;
@@ -712,9 +727,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ms.tmem_base;
-  // Inputs may come from the previous kernel in the stream: wait for it here,
-  // after the prologue, and let the next kernel start its own prologue.
-  grid_dependency_wait();
+  // Let the next kernel in the stream start its own prologue.  Inputs may come
+  // from the previous kernel: each role waits for it just before its first
+  // global access (the loader after planning its first item, so that work
+  // overlaps the previous kernel's tail; the MMA warp touches no global memory
+  // except the status bytes its plan reads in dense-mask mode).
   grid_launch_dependents();
 
   if (warp < kComputeWarps) {

@@ -57,7 +57,8 @@ struct Misc {
   alignas(8) uint64_t q_full, q_empty;
   uint64_t kv_full[kStages], kv_empty[kStages];
   uint64_t s_full[2], s_empty[2];
-  uint64_t p_full, p_empty, o_full, o_empty, mma_done;
+  uint64_t o_full[4];              // O^T block m (dims 128m ..) final for the item
+  uint64_t p_full, p_empty, o_empty, mma_done;
   uint32_t tmem_base;
   int abort_flag;
   int resc_flag[2];
