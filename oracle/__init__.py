@@ -8,3 +8,4 @@ from .mqa import (  # noqa: F401
     attention, block_status, pad_rows, pair_visibility, raw_visible, comp_visible,
     padded_lengths, ceil_to, H, D, BLOCK,
 )
+from . import indexer  # noqa: F401,E402
