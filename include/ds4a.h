@@ -268,6 +268,53 @@ ds4a_status ds4a_attn_indexed(const ds4a_layout *L, const ds4a_tensors *X,
                               ds4a_stream_t stream);
 
 /*
+ * ds4a_indexer_scores - [P2] "Layer Compression" (on ratio-4 layers a learned
+ * indexer selects the top-512 compressed rows for each query) and "GPU
+ * Backend Architecture" (indexer scoring among the GPU ops).  The pages give
+ * no score formula; this library's reading is
+ *     s[t][c] = sum_h w[t][h] * f(scale * q[t][h][:] . k[c][:]),
+ * with f = max(0, x) when relu != 0 and the identity otherwise, for every
+ * compressed row c whose pooled span has ended, (c+1)*ratio <= q_pos0+t+1;
+ * every other row of the token gets -inf.  One head, w = 1 and relu = 0 is the
+ * plain dot product.  fp16 inputs, fp32 accumulation (tensor cores).
+ *   L             T, q_pos0, n_comp and ratio are used (the layer's attention
+ *                 layout); T = 0 or n_comp = 0 does nothing.
+ *   q_idx         fp16 [T][n_heads][head_dim], heads contiguous, token stride
+ *                 q_tok_stride bytes (multiple of 16, >= 2*n_heads*head_dim).
+ *   n_heads       1, 2, 4, 8, 16, 32, 64 or 128.   head_dim: 64, 128 or 256.
+ *   k_idx         fp16 [n_comp][head_dim], row stride k_row_stride bytes
+ *                 (multiple of 16, >= 2*head_dim): the indexer's own
+ *                 compressed rows ([P2] "KV Cache Design": index_comp_kv),
+ *                 not the attention's.
+ *   head_weights  fp32 [T][n_heads], contiguous.
+ *   scale         finite.
+ *   scores        fp32 [T][n_comp] out, row stride score_row_stride bytes
+ *                 (multiple of 16, >= 4*n_comp).
+ * Device pointers owned by the caller, 16-byte aligned (head_weights 4-byte).
+ */
+ds4a_status ds4a_indexer_scores(const ds4a_layout *L, const void *q_idx, int64_t q_tok_stride, int32_t n_heads,
+                                int32_t head_dim, const void *k_idx, int64_t k_row_stride,
+                                const float *head_weights, float scale, int32_t relu, float *scores,
+                                int64_t score_row_stride, ds4a_stream_t stream);
+
+/*
+ * ds4a_indexer_topk - the selection half of the indexer ([P2] "Layer
+ * Compression": the top-512 compressed rows; "GPU Backend Architecture":
+ * indexer top-k).  For each token, the top_k candidate rows (as above) with
+ * the largest scores; equal scores go to the lower row; a NaN score counts as
+ * -inf.  The chosen rows are written in ascending order, then -1 when a token
+ * has fewer than top_k candidates: the index lists ds4a_attn_indexed takes.
+ * The result is exact (integer work) for the scores given.
+ *   scores   fp32 [T][>= n_comp] at score_row_stride bytes (multiple of 4,
+ *            >= 4*n_comp); only the candidates of each token are read.
+ *   top_k    1 .. 4096.
+ *   idx      int32 [T][top_k] out at idx_row_stride bytes (multiple of 16,
+ *            >= 4*top_k).
+ */
+ds4a_status ds4a_indexer_topk(const ds4a_layout *L, const float *scores, int64_t score_row_stride, int32_t top_k,
+                              int32_t *idx, int64_t idx_row_stride, ds4a_stream_t stream);
+
+/*
  * ds4a_device_status - synchronises `stream`, then reports the device error
  * word the kernels set when a bounded wait runs out (DS4A_ERR_TIMEOUT) or
  * DS4A_OK.  clear != 0 resets the word.  A CUDA error from the

@@ -489,3 +489,103 @@ ds4a_status ds4a_selftest_wait_timeout(uint64_t timeout_ns, ds4a_stream_t stream
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------ indexer
+
+namespace {
+
+bool indexer_heads_ok(int32_t n) { return n >= 1 && n <= 128 && (n & (n - 1)) == 0; }
+
+}  // namespace
+
+ds4a_status ds4a_indexer_scores(const ds4a_layout *L, const void *q_idx, int64_t q_tok_stride, int32_t n_heads,
+                                int32_t head_dim, const void *k_idx, int64_t k_row_stride,
+                                const float *head_weights, float scale, int32_t relu, float *scores,
+                                int64_t score_row_stride, ds4a_stream_t stream) {
+  ds4a_status st = check_layout(L);
+  if (st != DS4A_OK) return st;
+  if (!indexer_heads_ok(n_heads) || (head_dim != 64 && head_dim != 128 && head_dim != 256)) return DS4A_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return DS4A_ERR_INVALID_ARG;
+  if (L->T == 0 || L->n_comp == 0) return DS4A_OK;
+  const int64_t q_row = 2LL * n_heads * head_dim;
+  if (q_idx == nullptr || !aligned(q_idx, 16) || q_tok_stride % 16 != 0 || q_tok_stride < q_row ||
+      q_tok_stride >= (1LL << 39))
+    return DS4A_ERR_INVALID_ARG;
+  if (k_idx == nullptr || !aligned(k_idx, 16) || k_row_stride % 16 != 0 || k_row_stride < 2LL * head_dim ||
+      k_row_stride >= (1LL << 39))
+    return DS4A_ERR_INVALID_ARG;
+  if (head_weights == nullptr || !aligned(head_weights, 4)) return DS4A_ERR_INVALID_ARG;
+  if (scores == nullptr || !aligned(scores, 16) || score_row_stride % 16 != 0 ||
+      score_row_stride < 4LL * L->n_comp || score_row_stride >= (1LL << 39))
+    return DS4A_ERR_INVALID_ARG;
+  DeviceState *d = nullptr;
+  st = current_device(&d);
+  if (st != DS4A_OK) return st;
+  ds4a::ScoreParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.g = ds4a::IndexerGeom{L->T, L->q_pos0, L->n_comp, L->ratio};
+  const int G = 256 / n_heads;
+  {
+    const cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)n_heads, (cuuint64_t)L->T};
+    const cuuint64_t strides[2] = {(cuuint64_t)(2 * head_dim), (cuuint64_t)q_tok_stride};
+    const cuuint32_t box[3] = {64, (cuuint32_t)n_heads, (cuuint32_t)G};
+    if ((st = encode(&p.tm_q, q_idx, 3, dims, strides, box)) != DS4A_OK) return st;
+  }
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)head_dim, (cuuint64_t)L->n_comp};
+    const cuuint64_t strides[1] = {(cuuint64_t)k_row_stride};
+    const cuuint32_t box[2] = {64, 128};
+    if ((st = encode(&p.tm_k, k_idx, 2, dims, strides, box)) != DS4A_OK) return st;
+  }
+  p.w = head_weights;
+  p.scores = scores;
+  p.score_stride = score_row_stride / 4;
+  p.scale = scale;
+  p.relu = relu != 0;
+  p.head_dim = head_dim;
+  p.n_groups = ceil_div(L->T, G);
+  p.n_row_tiles = ceil_div(L->n_comp, 128);
+  // Cut each group's row tiles into items so that there are a few per SM.
+  int ipg = ceil_div(4LL * d->sm_count, p.n_groups);
+  if (ipg < 1) ipg = 1;
+  if (ipg > p.n_row_tiles) ipg = p.n_row_tiles;
+  p.tiles_per_item = ceil_div(p.n_row_tiles, ipg);
+  p.items_per_group = ceil_div(p.n_row_tiles, p.tiles_per_item);
+  p.timeout_ns = kDefaultTimeoutNs;
+  p.err = d->err;
+  const long long items = (long long)p.n_groups * p.items_per_group;
+  if (items > INT32_MAX) return DS4A_ERR_INVALID_ARG;
+  const int grid = (int)(items < d->sm_count ? items : d->sm_count);
+  return launched(ds4a::launch_indexer_scores(p, n_heads, grid, as_cuda(stream)));
+}
+
+ds4a_status ds4a_indexer_topk(const ds4a_layout *L, const float *scores, int64_t score_row_stride, int32_t top_k,
+                              int32_t *idx, int64_t idx_row_stride, ds4a_stream_t stream) {
+  ds4a_status st = check_layout(L);
+  if (st != DS4A_OK) return st;
+  if (top_k < 1 || top_k > 4096) return DS4A_ERR_INVALID_ARG;
+  if (L->T == 0) return DS4A_OK;
+  if (idx == nullptr || !aligned(idx, 16) || idx_row_stride % 16 != 0 || idx_row_stride < 4LL * top_k ||
+      idx_row_stride >= (1LL << 39))
+    return DS4A_ERR_INVALID_ARG;
+  if (L->n_comp > 0 && (scores == nullptr || !aligned(scores, 4) || score_row_stride % 4 != 0 ||
+                        score_row_stride < 4LL * L->n_comp || score_row_stride >= (1LL << 39)))
+    return DS4A_ERR_INVALID_ARG;
+  DeviceState *d = nullptr;
+  st = current_device(&d);
+  if (st != DS4A_OK) return st;
+  ds4a::TopkParams p;
+  std::memset(&p, 0, sizeof(p));
+  const int ratio = L->n_comp > 0 ? L->ratio : 1;
+  p.g = ds4a::IndexerGeom{L->T, L->q_pos0, L->n_comp, ratio};
+  p.scores = scores;
+  p.score_stride = score_row_stride / 4;
+  p.idx = idx;
+  p.idx_stride = idx_row_stride / 4;
+  p.top_k = top_k;
+  // The last token has the most candidates.
+  int64_t max_n = ((int64_t)L->q_pos0 + L->T) / ratio;
+  if (max_n > L->n_comp) max_n = L->n_comp;
+  p.cached_keys = max_n <= top_k ? 0 : (int)(max_n < ds4a::kTopkMaxCachedKeys ? max_n : ds4a::kTopkMaxCachedKeys);
+  return launched(ds4a::launch_indexer_topk(p, p.cached_keys * 4, as_cuda(stream)));
+}

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include "attn_params.h"
+#include "indexer_params.h"
 
 namespace ds4a {
 
@@ -25,5 +26,10 @@ cudaError_t launch_block_mask_dense(const GeomScalars &g, const __half *mask, lo
 cudaError_t launch_combine(const float *ws_o, const float2 *ws_ml, int n_splits, int T, __half *o,
                            long long o_tok_stride, float *lse, cudaStream_t s);
 cudaError_t launch_selftest_wait(unsigned long long timeout_ns, unsigned int *err, cudaStream_t s);
+
+// indexer.cu
+constexpr int kTopkMaxCachedKeys = 32768;  // candidate keys a top-k CTA keeps in shared memory
+cudaError_t launch_indexer_topk(const TopkParams &p, int dyn_smem, cudaStream_t s);
+cudaError_t launch_indexer_scores(const ScoreParams &p, int n_heads, int grid, cudaStream_t s);
 
 }  // namespace ds4a

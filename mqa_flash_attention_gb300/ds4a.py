@@ -84,6 +84,10 @@ def lib() -> ctypes.CDLL:
         L.ds4a_attn_decode_noalloc.argtypes = [PL, PT, i32, vp]
         L.ds4a_attn_indexed.restype = st
         L.ds4a_attn_indexed.argtypes = [PL, PT, vp, i64, i32, vp]
+        L.ds4a_indexer_scores.restype = st
+        L.ds4a_indexer_scores.argtypes = [PL, vp, i64, i32, i32, vp, i64, vp, ctypes.c_float, i32, vp, i64, vp]
+        L.ds4a_indexer_topk.restype = st
+        L.ds4a_indexer_topk.argtypes = [PL, vp, i64, i32, vp, i64, vp]
         L.ds4a_device_status.restype = st
         L.ds4a_device_status.argtypes = [vp, ctypes.c_int]
         L.ds4a_device_error_word.restype = st
@@ -280,6 +284,47 @@ def attn_indexed(layout, q, k_raw, v_raw, k_comp, v_comp, idx, *, out=None, lse=
     _check(lib().ds4a_attn_indexed(ctypes.byref(L), ctypes.byref(X), _ptr(idx), idx.stride(0) * 4, idx.shape[1],
                                    _stream(stream)), "ds4a_attn_indexed")
     return (out, lse) if (want_lse or lse is not None) else out
+
+
+def indexer_scores(layout, q_idx, k_idx, head_weights, *, scale, relu=True, out=None, stream=None):
+    """Indexer scores: fp32 [T, n_comp] (non-candidate rows -inf).
+
+    q_idx: fp16 [T, n_heads, head_dim] with contiguous heads; k_idx: fp16
+    [n_comp, head_dim] with contiguous rows; head_weights: fp32 [T, n_heads].
+    """
+    import torch
+    L = make_layout(layout)
+    T, n_heads, head_dim = q_idx.shape
+    if q_idx.dtype != torch.float16 or q_idx.stride(2) != 1 or q_idx.stride(1) != head_dim:
+        raise ValueError("q_idx must be fp16 [T, n_heads, head_dim] with contiguous heads")
+    if k_idx.dtype != torch.float16 or k_idx.dim() != 2 or k_idx.stride(1) != 1 or k_idx.shape[1] != head_dim:
+        raise ValueError("k_idx must be fp16 [n_comp, head_dim] with contiguous rows")
+    w = head_weights
+    if w.dtype != torch.float32 or not w.is_contiguous() or tuple(w.shape) != (T, n_heads):
+        raise ValueError("head_weights must be contiguous fp32 [T, n_heads]")
+    n_comp = L.n_comp
+    if out is None:
+        stride = (n_comp + 3) // 4 * 4
+        out = torch.empty((T, stride), dtype=torch.float32, device=q_idx.device)[:, :n_comp]
+    _check(lib().ds4a_indexer_scores(ctypes.byref(L), _ptr(q_idx), q_idx.stride(0) * 2, n_heads, head_dim,
+                                     _ptr(k_idx), k_idx.stride(0) * 2, _ptr(w), float(scale), 1 if relu else 0,
+                                     _ptr(out), out.stride(0) * 4, _stream(stream)), "ds4a_indexer_scores")
+    return out
+
+
+def indexer_topk(layout, scores, top_k, *, out=None, stream=None):
+    """Index lists: int32 [T, top_k], ascending rows, -1 padded."""
+    import torch
+    L = make_layout(layout)
+    if scores.dtype != torch.float32 or scores.dim() != 2 or scores.stride(1) != 1:
+        raise ValueError("scores must be fp32 [T, >= n_comp] with contiguous rows")
+    T = scores.shape[0]
+    if out is None:
+        stride = (top_k + 3) // 4 * 4
+        out = torch.empty((T, stride), dtype=torch.int32, device=scores.device)[:, :top_k]
+    _check(lib().ds4a_indexer_topk(ctypes.byref(L), _ptr(scores), scores.stride(0) * 4, int(top_k), _ptr(out),
+                                   out.stride(0) * 4, _stream(stream)), "ds4a_indexer_topk")
+    return out
 
 
 def device_status(clear: bool = True, stream=None) -> int:

@@ -33,6 +33,9 @@ STREAM_K_COMP = 4
 STREAM_V_COMP = 5
 STREAM_IDX = 6
 STREAM_MASK = 7
+STREAM_IDX_Q = 8      # indexer query vectors
+STREAM_IDX_K = 9      # indexer compressed rows
+STREAM_IDX_W = 10     # indexer head weights
 
 
 def _mix64(z: np.ndarray) -> np.ndarray:
@@ -70,6 +73,12 @@ def normal_f64(seed: int, stream: int, n: int) -> np.ndarray:
     z[0::2] = r * np.cos(2.0 * np.pi * u2)
     z[1::2] = r * np.sin(2.0 * np.pi * u2)
     return z[:n]
+
+
+def normal_f32(seed: int, stream: int, shape) -> np.ndarray:
+    """N(0, 1) rounded to fp32, C-contiguous."""
+    n = int(np.prod(shape))
+    return normal_f64(seed, stream, n).astype(np.float32).reshape(shape)
 
 
 def normal_f16(seed: int, stream: int, shape) -> np.ndarray:

@@ -119,3 +119,37 @@ def decode_long(n_comp: int) -> Workload:
 
 
 LONG_DECODE_SIZES = (1024, 8192, 65536, 262144)
+
+
+@dataclasses.dataclass
+class IndexerWorkload:
+    """Inputs of the indexer (scoring + top-k) of one ratio-4 layer."""
+    name: str
+    seed: int
+    layout: dict
+    q_idx: np.ndarray   # fp16 [T, n_heads, head_dim]
+    k_idx: np.ndarray   # fp16 [n_comp, head_dim]: the indexer's own compressed rows
+    w: np.ndarray       # fp32 [T, n_heads]
+    scale: float
+    relu: bool
+    top_k: int
+
+
+def draw_indexer(name: str, seed: int, layout: dict, n_heads: int, head_dim: int, top_k: int,
+                 relu: bool = True) -> IndexerWorkload:
+    T, n = layout["T"], layout["n_comp"]
+    return IndexerWorkload(name, seed, layout,
+                           synth.normal_f16(seed, synth.STREAM_IDX_Q, (T, n_heads, head_dim)),
+                           synth.normal_f16(seed, synth.STREAM_IDX_K, (n, head_dim)),
+                           synth.normal_f32(seed, synth.STREAM_IDX_W, (T, n_heads)),
+                           1.0 / math.sqrt(head_dim), relu, top_k)
+
+
+def indexer_r4_2048(n_heads: int = 64, head_dim: int = 128) -> IndexerWorkload:
+    """Indexer of the indexed ratio-4 layer: 2048 tokens at context 32768 over
+    8192 indexer rows, top-512.  The pages give no indexer shape; 64 heads of
+    128 dims with max(0, x) is the multi-head reading (one head is the plain
+    dot product)."""
+    return draw_indexer("indexer_ratio4_T2048_ctx32768", 12,
+                        make_layout(T=2048, q_pos0=30720, n_raw=2175, raw_pos0=30593, n_comp=8192, ratio=4),
+                        n_heads, head_dim, 512)
