@@ -460,6 +460,26 @@ def run_also(torch, ds4a, W, dev, stream, pk, pk_kind):
     by = decode_bytes(wl.layout)
     out.append({"workload": wl.name, "us_per_call": round(sec * 1e6, 2), "hbm_gbs": round(by / sec / 1e9, 1),
                 "frac_hbm": round(by / sec / 1e9 / pk["hbm_gbs"], 4), "algorithmic_bytes": by})
+    del d, o, ws
+    # indexer of the ratio-4 layer: scores (64 heads x 128 dims, max(0, x)) and top-512
+    wx = W.indexer_r4_2048()
+    L = wx.layout
+    qx, kx, wx_w = up(wx.q_idx), up(wx.k_idx), up(wx.w)
+    sc = [torch.empty((L["T"], L["n_comp"]), dtype=torch.float32, device=dev) for _ in range(2)]
+    sec = timed(lambda i: ds4a.indexer_scores(L, qx, kx, wx_w, scale=wx.scale, relu=True, out=sc[i % 2],
+                                              stream=stream), 10)
+    n_cand = sum(min(L["n_comp"], (L["q_pos0"] + t + 1) // L["ratio"]) for t in range(L["T"]))
+    n_heads, head_dim = wx.q_idx.shape[1], wx.q_idx.shape[2]
+    fl = 2.0 * n_cand * n_heads * head_dim
+    out.append({"workload": wx.name + "_scores", "us_per_call": round(sec * 1e6, 2),
+                "tflops": round(fl / sec / 1e12, 1), "frac_tensor": round(fl / sec / 1e12 / pk["bf16_tflops"], 4),
+                "algorithmic_flops": fl, "shape": f"{n_heads} heads x {head_dim} dims, relu"})
+    ix_out = torch.empty((L["T"], wx.top_k), dtype=torch.int32, device=dev)
+    sec = timed(lambda i: ds4a.indexer_topk(L, sc[i % 2], wx.top_k, out=ix_out, stream=stream), 10)
+    by = 4 * n_cand + 4 * L["T"] * wx.top_k
+    out.append({"workload": wx.name + "_topk", "us_per_call": round(sec * 1e6, 2),
+                "gbs": round(by / sec / 1e9, 1), "algorithmic_bytes": by,
+                "note": "exact radix select over each token's candidate scores"})
     for e in out:
         e["peak_kind"] = pk_kind
     return out
@@ -467,7 +487,8 @@ def run_also(torch, ds4a, W, dev, stream, pk, pk_kind):
 
 # ------------------------------------------------------------------ profiling cases
 
-CASES = ("tiny", "decode_r128_32k", "prefill_raw_2048", "indexed_r4_2048", "decode_long_262144")
+CASES = ("tiny", "decode_r128_32k", "prefill_raw_2048", "indexed_r4_2048", "decode_long_262144",
+         "indexer_r4_2048")
 
 
 def run_case(name: str, calls: int) -> None:
@@ -477,6 +498,18 @@ def run_case(name: str, calls: int) -> None:
     from mqa_flash_attention_gb300 import build, ds4a
     from mqa_flash_attention_gb300 import workloads as W
     build.build()
+    if name == "indexer_r4_2048":
+        wx = W.indexer_r4_2048()
+        up = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
+        qx, kx, w = up(wx.q_idx), up(wx.k_idx), up(wx.w)
+        for _ in range(calls):
+            s = ds4a.indexer_scores(wx.layout, qx, kx, w, scale=wx.scale, relu=True)
+            ds4a.indexer_topk(wx.layout, s, wx.top_k)
+        torch.cuda.synchronize()
+        if ds4a.device_status() != ds4a.OK:
+            raise RuntimeError("device wait ran out")
+        print(f"{name}: {calls} calls ok")
+        return
     wl = W.decode_long(262144) if name == "decode_long_262144" else getattr(W, name)()
     L = wl.layout
 

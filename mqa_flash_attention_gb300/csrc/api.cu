@@ -586,6 +586,8 @@ ds4a_status ds4a_indexer_topk(const ds4a_layout *L, const float *scores, int64_t
   // The last token has the most candidates.
   int64_t max_n = ((int64_t)L->q_pos0 + L->T) / ratio;
   if (max_n > L->n_comp) max_n = L->n_comp;
-  p.cached_keys = max_n <= top_k ? 0 : (int)(max_n < ds4a::kTopkMaxCachedKeys ? max_n : ds4a::kTopkMaxCachedKeys);
+  // Keys in shared memory when every token's candidates fit; otherwise every
+  // pass rereads the scores (the kernel variant without the cache).
+  p.cached_keys = (max_n <= top_k || max_n > ds4a::kTopkMaxCachedKeys) ? 0 : (int)max_n;
   return launched(ds4a::launch_indexer_topk(p, p.cached_keys * 4, as_cuda(stream)));
 }

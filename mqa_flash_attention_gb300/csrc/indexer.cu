@@ -41,16 +41,63 @@ __device__ __forceinline__ uint32_t score_key(float x) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// One CTA per token.  Exact radix select (4 passes of 8 bits) finds the key K*
-// of the top_k-th largest candidate and how many keys equal to K* are taken;
-// a final pass in row order writes every row with key > K* and the first such
-// rows with key == K* (lower index first), so the list comes out ascending.
+// One CTA per token.  Exact radix select on the score keys in three digits of
+// 12, 10 and 10 bits (the first spans sign, exponent and 3 mantissa bits, so
+// clustered scores spread over many bins and the shared atomics rarely
+// collide).  After the first digit only the keys in the bin where the count
+// of larger keys reaches top_k matter; they are compacted (warp-aggregated
+// appends) and the two other digits run over them alone.  That gives K* (the
+// top_k-th largest key) and how many keys equal to K* are taken.  Then every
+// row with key > K* is taken, and the first rows with key == K* (lower index
+// first) up to top_k: each warp owns a contiguous chunk of rows, one block
+// scan gives its offset and its share of the ties.
+constexpr int kTopkCompact = 4096;  // keys of the crossing bin kept for the last two digits
+
+// Block-wide: the bin (scanning from the top) where the count of keys in
+// larger bins first reaches `need`; returns it and that count.
+template <int NBINS>
+__device__ __forceinline__ void find_bin(const uint32_t *hist, uint32_t need, uint32_t *sh_out, uint32_t *wsum,
+                                         int tid) {
+  constexpr int PER = NBINS / kTopkThreads;  // bins per thread, descending order
+  const int lane = tid & 31, warp = tid >> 5;
+  const int top = NBINS - 1 - PER * tid;
+  uint32_t s = 0;
+#pragma unroll
+  for (int j = 0; j < PER; ++j) s += hist[top - j];
+  uint32_t incl = s;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t x = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += x;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  uint32_t above = incl - s;
+  for (int w = 0; w < warp; ++w) above += wsum[w];
+  if (above < need && need <= above + s) {
+    uint32_t acc = above;
+    for (int j = 0; j < PER; ++j) {
+      const uint32_t c = hist[top - j];
+      if (acc + c >= need) {
+        sh_out[0] = (uint32_t)(top - j);
+        sh_out[1] = acc;
+        break;
+      }
+      acc += c;
+    }
+  }
+  __syncthreads();
+}
+
+template <bool CACHED>
 __global__ void __launch_bounds__(kTopkThreads) indexer_topk_kernel(const TopkParams p) {
   extern __shared__ uint32_t keys_s[];
-  __shared__ uint32_t hist[kTopkWarps][256];
-  __shared__ uint32_t tot[256];
-  __shared__ uint32_t sh_prefix, sh_need;
+  __shared__ uint32_t hist[4096];
+  __shared__ uint32_t surv[kTopkCompact];
+  __shared__ uint32_t wsum[kTopkWarps];
   __shared__ uint32_t cnt[2][kTopkWarps];
+  __shared__ uint32_t sh_bin[2];
+  __shared__ uint32_t sh_count;
   const int t = blockIdx.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n = n_candidates(p.g, t);
@@ -61,99 +108,100 @@ __global__ void __launch_bounds__(kTopkThreads) indexer_topk_kernel(const TopkPa
     for (int i = tid; i < K; i += kTopkThreads) out[i] = i < n ? i : -1;
     return;
   }
-  const bool cached = n <= p.cached_keys;
-  if (cached) {
-    for (int i = tid; i < n; i += kTopkThreads) keys_s[i] = score_key(__ldg(row + i));
+  auto key_at = [&](int i) -> uint32_t { return CACHED ? keys_s[i] : score_key(__ldg(row + i)); };
+  for (int i = tid; i < 4096; i += kTopkThreads) hist[i] = 0u;
+  if (tid == 0) sh_count = 0;
+  __syncthreads();
+  // digit 1: bits 31..20
+  for (int i = tid; i < n; i += kTopkThreads) {
+    const uint32_t k = score_key(__ldg(row + i));
+    if (CACHED) keys_s[i] = k;
+    atomicAdd(&hist[k >> 20], 1u);
   }
-  uint32_t prefix = 0, need = (uint32_t)K;
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    const uint32_t hi_mask = pass == 0 ? 0u : (0xFFFFFFFFu << (shift + 8));
-    for (int i = tid; i < kTopkWarps * 256; i += kTopkThreads) (&hist[0][0])[i] = 0u;
-    __syncthreads();
-    for (int i = tid; i < n; i += kTopkThreads) {
-      const uint32_t k = cached ? keys_s[i] : score_key(__ldg(row + i));
-      if ((k & hi_mask) == prefix) atomicAdd(&hist[warp][(k >> shift) & 255u], 1u);
-    }
-    __syncthreads();
-    if (tid < 256) {
-      uint32_t s = 0;
-#pragma unroll
-      for (int w = 0; w < kTopkWarps; ++w) s += hist[w][tid];
-      tot[tid] = s;
-    }
-    __syncthreads();
-    if (warp == 0) {
-      // lane l holds bins 255-8l .. 248-8l (descending); find the bin where
-      // the count of larger keys reaches `need`.
-      uint32_t s = 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) s += tot[255 - 8 * lane - j];
-      uint32_t incl = s;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const uint32_t v = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += v;
-      }
-      const uint32_t above = incl - s;
-      if (above < need && need <= incl) {
-        uint32_t acc = above;
-        for (int j = 0; j < 8; ++j) {
-          const int d = 255 - 8 * lane - j;
-          const uint32_t c = tot[d];
-          if (acc + c >= need) {
-            sh_prefix = prefix | ((uint32_t)d << shift);
-            sh_need = need - acc;
-            break;
-          }
-          acc += c;
-        }
-      }
-    }
-    __syncthreads();
-    prefix = sh_prefix;
-    need = sh_need;
-  }
-  // Selection in row order, 512 rows at a time, with ballot scans.
-  const uint32_t kstar = prefix;
+  __syncthreads();
+  find_bin<4096>(hist, (uint32_t)K, sh_bin, wsum, tid);
+  const uint32_t b0 = sh_bin[0];
+  uint32_t need = (uint32_t)K - sh_bin[1];  // keys still to take from bin b0
+  const uint32_t m = hist[b0];              // keys in bin b0
+  const bool compact = m <= (uint32_t)kTopkCompact;
   const uint32_t lt_mask = (1u << lane) - 1u;
-  uint32_t run_eq = 0, run_sel = 0;
-  for (int base = 0; base < n && run_sel < (uint32_t)K; base += kTopkThreads) {
-    const int i = base + tid;
-    const uint32_t k = i < n ? (cached ? keys_s[i] : score_key(__ldg(row + i))) : 0u;
-    const bool gt = i < n && k > kstar, eq = i < n && k == kstar;
+  if (compact) {
+    for (int base = 32 * warp; base < n; base += kTopkThreads) {
+      const int i = base + lane;
+      const uint32_t k = i < n ? key_at(i) : 0u;
+      const bool hit = i < n && (k >> 20) == b0;
+      const uint32_t bal = __ballot_sync(0xffffffffu, hit);
+      if (bal != 0u) {
+        uint32_t off = 0;
+        if (lane == 0) off = atomicAdd(&sh_count, (uint32_t)__popc(bal));
+        off = __shfl_sync(0xffffffffu, off, 0);
+        if (hit) surv[off + __popc(bal & lt_mask)] = k;
+      }
+    }
+  }
+  __syncthreads();  // surv complete; every thread has read hist[b0]
+  // digits 2 and 3: bits 19..10 and 9..0, over bin b0's keys
+  uint32_t prefix = b0, kstar = 0;
+  for (int d = 0; d < 2; ++d) {
+    const int shift = d == 0 ? 10 : 0;
+    for (int i = tid; i < 1024; i += kTopkThreads) hist[i] = 0u;
+    __syncthreads();
+    const int nsrc = compact ? (int)m : n;
+    for (int i = tid; i < nsrc; i += kTopkThreads) {
+      const uint32_t k = compact ? surv[i] : key_at(i);
+      if ((k >> (shift + 10)) == prefix) atomicAdd(&hist[(k >> shift) & 1023u], 1u);
+    }
+    __syncthreads();
+    find_bin<1024>(hist, need, sh_bin, wsum, tid);
+    prefix = (prefix << 10) | sh_bin[0];
+    need -= sh_bin[1];
+  }
+  kstar = prefix;
+  // Selection in row order.
+  const int chunk = ((n + kTopkWarps - 1) / kTopkWarps + 31) & ~31;
+  const int r0 = min(n, warp * chunk), r1 = min(n, r0 + chunk);
+  uint32_t c_gt = 0, c_eq = 0;
+  for (int base = r0; base < r1; base += 32) {
+    const int i = base + lane;
+    const uint32_t k = i < r1 ? key_at(i) : 0u;
+    c_gt += __popc(__ballot_sync(0xffffffffu, i < r1 && k > kstar));
+    c_eq += __popc(__ballot_sync(0xffffffffu, i < r1 && k == kstar));
+  }
+  if (lane == 0) {
+    cnt[0][warp] = c_gt;
+    cnt[1][warp] = c_eq;
+  }
+  __syncthreads();
+  uint32_t eq_run = 0, sel_run = 0;
+  for (int w = 0; w < warp; ++w) {
+    const uint32_t g = cnt[0][w], e = cnt[1][w];
+    const uint32_t taken = eq_run >= need ? 0u : min(e, need - eq_run);
+    sel_run += g + taken;
+    eq_run += e;
+  }
+  for (int base = r0; base < r1; base += 32) {
+    const int i = base + lane;
+    const uint32_t k = i < r1 ? key_at(i) : 0u;
+    const bool gt = i < r1 && k > kstar, eq = i < r1 && k == kstar;
     const uint32_t b_eq = __ballot_sync(0xffffffffu, eq);
-    if (lane == 0) cnt[0][warp] = __popc(b_eq);
-    __syncthreads();
-    uint32_t eq_before = run_eq + __popc(b_eq & lt_mask), eq_tile = 0;
-#pragma unroll
-    for (int w = 0; w < kTopkWarps; ++w) {
-      const uint32_t c = cnt[0][w];
-      eq_before += w < warp ? c : 0u;
-      eq_tile += c;
-    }
-    const bool take = gt || (eq && eq_before < need);
+    const bool take = gt || (eq && eq_run + __popc(b_eq & lt_mask) < need);
     const uint32_t b_sel = __ballot_sync(0xffffffffu, take);
-    if (lane == 0) cnt[1][warp] = __popc(b_sel);
-    __syncthreads();
-    uint32_t pos = run_sel + __popc(b_sel & lt_mask), sel_tile = 0;
-#pragma unroll
-    for (int w = 0; w < kTopkWarps; ++w) {
-      const uint32_t c = cnt[1][w];
-      pos += w < warp ? c : 0u;
-      sel_tile += c;
-    }
+    const uint32_t pos = sel_run + __popc(b_sel & lt_mask);
     if (take && pos < (uint32_t)K) out[pos] = i;
-    run_eq += eq_tile;
-    run_sel += sel_tile;
-    __syncthreads();  // cnt is rewritten by the next tile
+    eq_run += __popc(b_eq);
+    sel_run += __popc(b_sel);
   }
 }
 
 cudaError_t launch_indexer_topk(const TopkParams &p, int dyn_smem, cudaStream_t s) {
-  cudaError_t e = cudaFuncSetAttribute(indexer_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_smem);
-  if (e != cudaSuccess) return e;
-  indexer_topk_kernel<<<p.g.T, kTopkThreads, dyn_smem, s>>>(p);
+  if (p.cached_keys > 0) {
+    cudaError_t e =
+        cudaFuncSetAttribute(indexer_topk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_smem);
+    if (e != cudaSuccess) return e;
+    indexer_topk_kernel<true><<<p.g.T, kTopkThreads, dyn_smem, s>>>(p);
+  } else {
+    indexer_topk_kernel<false><<<p.g.T, kTopkThreads, 0, s>>>(p);
+  }
   return cudaGetLastError();
 }
 
@@ -212,7 +260,55 @@ __device__ __forceinline__ ScoreItem score_item(const ScoreParams &p, int item, 
   return it;
 }
 
-template <int NH>
+// Scores of one tile for the thread's row c and half hf of the 256 columns
+// (tokens G/2*hf ..): w_s holds w[t][h] * |scale| (or * scale without the
+// max), so each TMEM value costs one max and one fma (one fma without max).
+template <int NH, bool RELU, bool NEG>
+__device__ __forceinline__ void score_tile(const ScoreParams &p, const ScoreItem &it, const float *w_s,
+                                           uint32_t tcol, int hf, int c, long long pos1) {
+  constexpr int HW = NH < 32 ? NH : 32;  // heads of one token inside a 32-column chunk
+  constexpr int TPC = 32 / HW;            // tokens per chunk
+  constexpr int CPT = NH < 32 ? 1 : NH / 32;  // chunks per token
+  float acc = 0.f;
+#pragma unroll
+  for (int j2 = 0; j2 < 2; ++j2) {
+    float v[64];
+    tmem_ld64(tcol + 64 * j2, v);
+    tmem_wait_ld();
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj) {
+      const int j = 2 * j2 + jj;
+      const float *ww = w_s + 128 * hf + 32 * j;
+#pragma unroll
+      for (int u = 0; u < TPC; ++u) {
+        float sum = 0.f;
+#pragma unroll
+        for (int h = 0; h < HW; ++h) {
+          float x = v[32 * jj + u * HW + h];
+          if (RELU) x = fmaxf(NEG ? -x : x, 0.f);
+          sum = fmaf(ww[u * HW + h], x, sum);
+        }
+        if (NH >= 32) {
+          acc += sum;
+          if ((j + 1) % CPT == 0) {
+            const int tl = (128 * hf + 32 * j) / NH;  // token of this chunk
+            if (tl < it.nt && c < p.g.n_comp)
+              p.scores[(long long)(it.t0 + tl) * p.score_stride + c] =
+                  (long long)(c + 1) * p.g.ratio <= pos1 + tl ? acc : -INFINITY;
+            acc = 0.f;
+          }
+        } else {
+          const int tl = (128 * hf + 32 * j) / NH + u;
+          if (tl < it.nt && c < p.g.n_comp)
+            p.scores[(long long)(it.t0 + tl) * p.score_stride + c] =
+                (long long)(c + 1) * p.g.ratio <= pos1 + tl ? sum : -INFINITY;
+        }
+      }
+    }
+  }
+}
+
+template <int NH, bool RELU>
 __global__ void __launch_bounds__(kScoreThreads, 1) indexer_scores_kernel(const __grid_constant__ ScoreParams p) {
   constexpr int G = 256 / NH;  // tokens per group
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -354,11 +450,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1) indexer_scores_kernel(const 
     const int q = warp & 3, hf = warp >> 2;
     const int lrow = 32 * q + lane;
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
-    constexpr int HW = NH < 32 ? NH : 32;       // heads of one token inside a 32-column chunk
-    constexpr int TPC = 32 / HW;                 // tokens per chunk
-    constexpr int CPT = NH < 32 ? 1 : NH / 32;   // chunks per token
-    const float scale = p.scale;
-    const bool relu = p.relu != 0;
+    // relu(scale x) = |scale| relu(sign(scale) x): |scale| goes into the weights.
+    const bool neg = RELU && p.scale < 0.f;
+    const float wscale = RELU ? fabsf(p.scale) : p.scale;
     uint32_t tc = 0;
     bool bad = false;
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
@@ -366,7 +460,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1) indexer_scores_kernel(const 
       bar_sync_n(1, kScoreEpiThreads);  // the previous item's epilogue is done with w_s
       {
         const int tl = tid / NH, h = tid % NH;
-        ms.w_s[tid] = tl < it.nt ? __ldg(p.w + (long long)(it.t0 + tl) * NH + h) : 0.f;
+        ms.w_s[tid] = tl < it.nt ? wscale * __ldg(p.w + (long long)(it.t0 + tl) * NH + h) : 0.f;
       }
       bar_sync_n(1, kScoreEpiThreads);
       // Row c is a candidate of token t iff (c+1)*ratio <= q_pos0 + t + 1.
@@ -377,37 +471,11 @@ __global__ void __launch_bounds__(kScoreThreads, 1) indexer_scores_kernel(const 
                                 SITE_IX_ACC_FULL);
         tc_fence_after();
         const int c = 128 * r + lrow;
-        float acc = 0.f;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          float v[32];
-          tmem_ld32(tmem + 256 * buf + 128 * hf + 32 * j + lane_base, v);
-          tmem_wait_ld();
-#pragma unroll
-          for (int u = 0; u < TPC; ++u) {
-            float s = 0.f;
-#pragma unroll
-            for (int h = 0; h < HW; ++h) {
-              const float x = scale * v[u * HW + h];
-              s += ms.w_s[128 * hf + 32 * j + u * HW + h] * (relu ? fmaxf(x, 0.f) : x);
-            }
-            if (NH >= 32) {
-              acc += s;
-              if ((j + 1) % CPT == 0) {
-                const int tl = (128 * hf + 32 * j) / NH;  // token of this chunk
-                if (tl < it.nt && c < p.g.n_comp)
-                  p.scores[(long long)(it.t0 + tl) * p.score_stride + c] =
-                      (long long)(c + 1) * p.g.ratio <= pos1 + tl ? acc : -INFINITY;
-                acc = 0.f;
-              }
-            } else {
-              const int tl = (128 * hf + 32 * j) / NH + u;
-              if (tl < it.nt && c < p.g.n_comp)
-                p.scores[(long long)(it.t0 + tl) * p.score_stride + c] =
-                    (long long)(c + 1) * p.g.ratio <= pos1 + tl ? s : -INFINITY;
-            }
-          }
-        }
+        const uint32_t tcol = tmem + 256 * buf + 128 * hf + lane_base;
+        if (neg)
+          score_tile<NH, RELU, true>(p, it, ms.w_s, tcol, hf, c, pos1);
+        else
+          score_tile<NH, RELU, false>(p, it, ms.w_s, tcol, hf, c, pos1);
         tc_fence_before();
         mbar_arrive(smem_u32(&ms.acc_empty[buf]));
         ++tc;
@@ -431,9 +499,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1) indexer_scores_kernel(const 
   if (warp == kScoreMmaWarp) tmem_dealloc(tmem, 512);
 }
 
-template <int NH>
+template <int NH, bool RELU>
 cudaError_t launch_scores_nh(const ScoreParams &p, int grid, cudaStream_t s) {
-  cudaError_t e = cudaFuncSetAttribute(indexer_scores_kernel<NH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(indexer_scores_kernel<NH, RELU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)kScoreSmemBytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -446,21 +514,26 @@ cudaError_t launch_scores_nh(const ScoreParams &p, int grid, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, indexer_scores_kernel<NH>, p);
+  return cudaLaunchKernelEx(&cfg, indexer_scores_kernel<NH, RELU>, p);
+}
+
+template <bool RELU>
+cudaError_t launch_scores_relu(const ScoreParams &p, int n_heads, int grid, cudaStream_t s) {
+  switch (n_heads) {
+    case 1: return launch_scores_nh<1, RELU>(p, grid, s);
+    case 2: return launch_scores_nh<2, RELU>(p, grid, s);
+    case 4: return launch_scores_nh<4, RELU>(p, grid, s);
+    case 8: return launch_scores_nh<8, RELU>(p, grid, s);
+    case 16: return launch_scores_nh<16, RELU>(p, grid, s);
+    case 32: return launch_scores_nh<32, RELU>(p, grid, s);
+    case 64: return launch_scores_nh<64, RELU>(p, grid, s);
+    case 128: return launch_scores_nh<128, RELU>(p, grid, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t launch_indexer_scores(const ScoreParams &p, int n_heads, int grid, cudaStream_t s) {
-  switch (n_heads) {
-    case 1: return launch_scores_nh<1>(p, grid, s);
-    case 2: return launch_scores_nh<2>(p, grid, s);
-    case 4: return launch_scores_nh<4>(p, grid, s);
-    case 8: return launch_scores_nh<8>(p, grid, s);
-    case 16: return launch_scores_nh<16>(p, grid, s);
-    case 32: return launch_scores_nh<32>(p, grid, s);
-    case 64: return launch_scores_nh<64>(p, grid, s);
-    case 128: return launch_scores_nh<128>(p, grid, s);
-    default: return cudaErrorInvalidValue;
-  }
+  return p.relu ? launch_scores_relu<true>(p, n_heads, grid, s) : launch_scores_relu<false>(p, n_heads, grid, s);
 }
 
 }  // namespace ds4a
