@@ -9,3 +9,4 @@ from .mqa import (  # noqa: F401
     padded_lengths, ceil_to, H, D, BLOCK,
 )
 from . import indexer  # noqa: F401,E402
+from . import fp8  # noqa: F401,E402
