@@ -460,7 +460,18 @@ def run_also(torch, ds4a, W, dev, stream, pk, pk_kind):
     by = decode_bytes(wl.layout)
     out.append({"workload": wl.name, "us_per_call": round(sec * 1e6, 2), "hbm_gbs": round(by / sec / 1e9, 1),
                 "frac_hbm": round(by / sec / 1e9 / pk["hbm_gbs"], 4), "algorithmic_bytes": by})
-    del d, o, ws
+    # the same decode with E4M3 compressed rows (codes + one fp32 scale per row)
+    kc, ks = ds4a.quantize_kv_fp8(d[3], stream=stream)
+    vc, vs = ds4a.quantize_kv_fp8(d[4], stream=stream)
+    torch.cuda.synchronize()
+    sec8 = timed(lambda i: ds4a.attn_decode_fp8(wl.layout, d[0], d[1], d[2], kc, ks, vc, vs, workspace=ws, out=o,
+                                                stream=stream), 10)
+    n_c = wl.layout["n_comp"]
+    by8 = by - n_c * 2048 + n_c * (1024 + 8)
+    out.append({"workload": wl.name + "_fp8kv", "us_per_call": round(sec8 * 1e6, 2), "hbm_gbs": round(by8 / sec8 / 1e9, 1),
+                "frac_hbm": round(by8 / sec8 / 1e9 / pk["hbm_gbs"], 4), "algorithmic_bytes": by8,
+                "speedup_vs_fp16": round(sec / sec8, 2)})
+    del d, o, ws, kc, ks, vc, vs
     # indexer of the ratio-4 layer: scores (64 heads x 128 dims, max(0, x)) and top-512
     wx = W.indexer_r4_2048()
     L = wx.layout

@@ -153,6 +153,24 @@ typedef struct {
 ds4a_status ds4a_pad_kv(const void *src, int64_t src_row_stride, int32_t n_rows,
                         void *dst, int64_t dst_row_stride, ds4a_stream_t stream);
 
+/*
+ * ds4a_quantize_kv_fp8 - [P2] "GPU Backend Architecture" (DS4-specific FP8 KV
+ * quantization) and "Whole-Model Graph Execution" (K/V rows are quantised to
+ * FP8 before they are stored).  The pages do not define the format; this
+ * library's reading: E4M3 codes (bias 7, no infinities, largest finite 448)
+ * with one fp32 scale per row, scale = absmax/448 and
+ * code = E4M3(x * (448/absmax)) (fp32 quotients and product, round to nearest
+ * even, saturating); an all-zero row gets scale 0.  A row's value is
+ * decode(code) * scale.  Exact (bit-for-bit) for the given rows.
+ *   src         fp16 [n_rows][512], row stride src_row_stride bytes (>= 1024,
+ *               multiple of 16), 16-byte aligned.
+ *   dst_codes   uint8 [n_rows][512] out, row stride dst_row_stride bytes
+ *               (>= 512, multiple of 16), 16-byte aligned.
+ *   scales      fp32 [n_rows] out.
+ */
+ds4a_status ds4a_quantize_kv_fp8(const void *src, int64_t src_row_stride, int32_t n_rows, void *dst_codes,
+                                 int64_t dst_row_stride, float *scales, ds4a_stream_t stream);
+
 /* Number of 32-row blocks of the padded logical sequence of L
  * (ceil(n_raw/32) + ceil(n_comp/32)), or -1 if L is NULL. */
 int32_t ds4a_block_count(const ds4a_layout *L);
@@ -229,6 +247,24 @@ ds4a_status ds4a_attn_decode_partials(const ds4a_layout *L, const ds4a_tensors *
                                       void *workspace, size_t workspace_bytes, ds4a_stream_t stream);
 ds4a_status ds4a_attn_decode_merge(const ds4a_layout *L, const ds4a_tensors *X, int32_t n_splits,
                                    const void *workspace, size_t workspace_bytes, ds4a_stream_t stream);
+
+/*
+ * ds4a_attn_decode_fp8 - ds4a_attn_decode with the compressed rows stored as
+ * FP8 ([P2] "GPU Backend Architecture": DS4-specific FP8 KV quantization;
+ * "Whole-Model Graph Execution": K/V rows quantised to FP8 before they are
+ * stored), the format of ds4a_quantize_kv_fp8: E4M3 codes and one fp32 scale
+ * per row.  The result is the attention over the rows' values
+ * decode(code) * scale, within the usual fp16/fp32 tolerance; the compressed
+ * rows cost half the bytes of fp16 rows.  Raw rows, Q and O are fp16 as in
+ * ds4a_attn_decode.
+ *   X->k_comp, X->v_comp  uint8 [n_comp][512] E4M3 codes at X->comp_row_stride
+ *                         bytes (>= 512, multiple of 16), 16-byte aligned.
+ *   k_comp_scale, v_comp_scale  fp32 [n_comp] row scales.
+ *   n_splits, workspace   as for ds4a_attn_decode (same workspace size).
+ */
+ds4a_status ds4a_attn_decode_fp8(const ds4a_layout *L, const ds4a_tensors *X, const float *k_comp_scale,
+                                 const float *v_comp_scale, int32_t n_splits, void *workspace,
+                                 size_t workspace_bytes, ds4a_stream_t stream);
 
 /*
  * ds4a_attn_decode_noalloc - ds4a_attn_decode for callers that cannot

@@ -119,9 +119,10 @@ ds4a_status check_tensors(const ds4a_layout *L, const ds4a_tensors *X) {
 }
 
 ds4a_status encode(CUtensorMap *m, const void *base, int rank, const cuuint64_t *dims, const cuuint64_t *strides,
-                   const cuuint32_t *box, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
+                   const cuuint32_t *box, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B,
+                   CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_FLOAT16) {
   const cuuint32_t es[3] = {1, 1, 1};
-  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, (cuuint32_t)rank, const_cast<void *>(base), dims,
+  const CUresult r = g_encode(m, dtype, (cuuint32_t)rank, const_cast<void *>(base), dims,
                               strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? DS4A_OK : DS4A_ERR_CUDA;
@@ -233,6 +234,22 @@ ds4a_status ds4a_pad_kv(const void *src, int64_t src_row_stride, int32_t n_rows,
   if (st != DS4A_OK) return st;
   return launched(ds4a::launch_pad(src, src_row_stride, n_rows, dst, dst_row_stride, in_place ? n_rows : 0,
                                    as_cuda(stream)));
+}
+
+ds4a_status ds4a_quantize_kv_fp8(const void *src, int64_t src_row_stride, int32_t n_rows, void *dst_codes,
+                                 int64_t dst_row_stride, float *scales, ds4a_stream_t stream) {
+  if (n_rows < 0) return DS4A_ERR_INVALID_ARG;
+  if (n_rows == 0) return DS4A_OK;
+  if (src == nullptr || !aligned(src, 16) || !row_stride_ok(src_row_stride)) return DS4A_ERR_INVALID_ARG;
+  if (dst_codes == nullptr || !aligned(dst_codes, 16) || dst_row_stride < DS4A_HEAD_DIM || dst_row_stride % 16 != 0 ||
+      dst_row_stride >= (1LL << 39))
+    return DS4A_ERR_INVALID_ARG;
+  if (scales == nullptr || !aligned(scales, 4)) return DS4A_ERR_INVALID_ARG;
+  DeviceState *d = nullptr;
+  ds4a_status st = current_device(&d);
+  if (st != DS4A_OK) return st;
+  return launched(ds4a::launch_quantize_fp8(src, src_row_stride, n_rows, dst_codes, dst_row_stride, scales,
+                                            as_cuda(stream)));
 }
 
 int32_t ds4a_block_count(const ds4a_layout *L) {
@@ -399,6 +416,70 @@ ds4a_status ds4a_attn_decode(const ds4a_layout *L, const ds4a_tensors *X, int32_
   ds4a_status st = decode_setup(L, X, n_splits, workspace, workspace_bytes, true, true, &ws_o, &ws_ml);
   if (st != DS4A_OK || L->T == 0) return st;
   st = decode_partials(L, X, n_splits, ws_o, ws_ml, stream);
+  if (st != DS4A_OK) return st;
+  return launched(ds4a::launch_combine(ws_o, ws_ml, n_splits, L->T, static_cast<__half *>(X->o),
+                                       X->o_tok_stride / 2, X->lse, as_cuda(stream)));
+}
+
+ds4a_status ds4a_attn_decode_fp8(const ds4a_layout *L, const ds4a_tensors *X, const float *k_comp_scale,
+                                 const float *v_comp_scale, int32_t n_splits, void *workspace,
+                                 size_t workspace_bytes, ds4a_stream_t stream) {
+  ds4a_status st = check_layout(L);
+  if (st != DS4A_OK) return st;
+  if (L->T == 0) return DS4A_OK;
+  if (X == nullptr) return DS4A_ERR_INVALID_ARG;
+  // Q, O and the fp16 raw rows as usual (checked with the compressed rows left out).
+  ds4a_layout L0 = *L;
+  L0.n_comp = 0;
+  st = check_tensors(&L0, X);
+  if (st != DS4A_OK) return st;
+  if (L->n_comp > 0) {
+    if (X->k_comp == nullptr || X->v_comp == nullptr || !aligned(X->k_comp, 16) || !aligned(X->v_comp, 16) ||
+        X->comp_row_stride < DS4A_HEAD_DIM || X->comp_row_stride % 16 != 0 || X->comp_row_stride >= (1LL << 39))
+      return DS4A_ERR_INVALID_ARG;
+    if (k_comp_scale == nullptr || v_comp_scale == nullptr || !aligned(k_comp_scale, 4) || !aligned(v_comp_scale, 4))
+      return DS4A_ERR_INVALID_ARG;
+  }
+  if (n_splits <= 0) n_splits = ds4a_attn_decode_default_splits(L);
+  if (n_splits > 4096) return DS4A_ERR_INVALID_ARG;
+  const size_t need = ds4a_attn_decode_workspace_size(L, n_splits);
+  if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256)) return DS4A_ERR_WORKSPACE;
+  const size_t n_items = (size_t)L->T * n_splits;
+  if (n_items > (size_t)INT32_MAX) return DS4A_ERR_INVALID_ARG;
+  float *ws_o = static_cast<float *>(workspace);
+  float2 *ws_ml = reinterpret_cast<float2 *>(static_cast<uint8_t *>(workspace) +
+                                             n_items * DS4A_HEADS * DS4A_HEAD_DIM * sizeof(float));
+  DeviceState *d = nullptr;
+  st = current_device(&d);
+  if (st != DS4A_OK) return st;
+  AttnParams p;
+  st = fill_params(p, &L0, X, ds4a::MODE_STRUCT, d);  // no fp16 tensor maps for the compressed rows
+  if (st != DS4A_OK) return st;
+  p.n_comp = L->n_comp;
+  p.ratio = L->n_comp > 0 ? L->ratio : 1;
+  p.n_blocks = p.nbr + ceil_div(L->n_comp, DS4A_BLOCK_ROWS);
+  p.comp_fp8 = L->n_comp > 0 ? 1 : 0;
+  if (p.comp_fp8) {
+    // E4M3 rows as bytes: {512, n_comp}, box {128 codes, 128 rows}, no swizzle.
+    const cuuint64_t dims[2] = {DS4A_HEAD_DIM, (cuuint64_t)L->n_comp};
+    const cuuint64_t strides[1] = {(cuuint64_t)X->comp_row_stride};
+    const cuuint32_t box[2] = {128, 128};
+    st = encode(&p.tm_k8, X->k_comp, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_DATA_TYPE_UINT8);
+    if (st == DS4A_OK)
+      st = encode(&p.tm_v8, X->v_comp, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_DATA_TYPE_UINT8);
+    if (st != DS4A_OK) return st;
+  }
+  p.k_scale = k_comp_scale;
+  p.v_scale = v_comp_scale;
+  p.n_splits = n_splits;
+  p.partial = 1;
+  p.o = nullptr;
+  p.lse = nullptr;
+  p.ws_o = ws_o;
+  p.ws_ml = ws_ml;
+  const int grid = (int)(n_items < (size_t)d->sm_count ? n_items : (size_t)d->sm_count);
+  st = launched(ds4a::launch_attn(p, grid, as_cuda(stream)));
   if (st != DS4A_OK) return st;
   return launched(ds4a::launch_combine(ws_o, ws_ml, n_splits, L->T, static_cast<__half *>(X->o),
                                        X->o_tok_stride / 2, X->lse, as_cuda(stream)));

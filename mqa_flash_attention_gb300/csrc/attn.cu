@@ -5,7 +5,10 @@
 namespace ds4a {
 
 cudaError_t prepare_attn_kernel() {
-  return cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)kSmemBytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(attn_fwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
 }
 
 // Launched with programmatic stream serialization: the kernel's prologue may
@@ -22,7 +25,7 @@ cudaError_t launch_attn(const AttnParams &p, int grid, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, attn_fwd_kernel, p);
+  return p.comp_fp8 ? cudaLaunchKernelEx(&cfg, attn_fwd_kernel<true>, p) : cudaLaunchKernelEx(&cfg, attn_fwd_kernel<false>, p);
 }
 
 }  // namespace ds4a

@@ -251,6 +251,7 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
 // copies and stages stay in flight up to the ring depth.  In this mode a
 // stage barrier expects one arrival per loader thread (TMA stages: thread 0's
 // arrive.expect_tx plus a plain arrival from every other thread).
+template <bool FP8>
 __device__ __forceinline__ void loader_role(const AttnParams &p, uint32_t sbase, Misc &ms, int ltid) {
   volatile int *abrt = &ms.abort_flag;
   const bool group = p.mode == MODE_INDEXED && p.n_comp > 0;  // all loader threads needed
@@ -259,6 +260,7 @@ __device__ __forceinline__ void loader_role(const AttnParams &p, uint32_t sbase,
   Ring ring;
   uint32_t n_item = 0;
   uint32_t filled = 0, last_par = 0;  // TMA stages issued (thread 0), for draining on abort
+  uint32_t code_ph = 0, cfilled = 0, clast_par = 0;  // E4M3 code copies: per-stage phase bits
   bool q_issued = false;
   uint32_t q_par = 0;
   bool ok = true;
@@ -312,7 +314,19 @@ __device__ __forceinline__ void loader_role(const AttnParams &p, uint32_t sbase,
         }
         const uint32_t stage = sbase + kOffKV + ring.st * kStageBytes;
         const uint32_t b_full = smem_u32(&ms.kv_full[ring.st]);
-        if (tl.seg != 2) {
+        if (FP8 && tl.seg == 1) {
+          // E4M3 rows: the codes of this part (128 rows x 128 bytes) land in
+          // the stage's upper half; the converter warps turn them into the
+          // fp16 stage and arrive on kv_full.
+          if (ltid == 0) {
+            const uint32_t b_code = smem_u32(&ms.code_full[ring.st]);
+            mbar_arrive_expect_tx(b_code, kBoxBytes);
+            tma_load_2d(stage + kBoxBytes, part >= 4 ? &p.tm_v8 : &p.tm_k8, b_code, 128 * (part & 3), tl.start);
+            cfilled |= 1u << ring.st;
+            clast_par = (clast_par & ~(1u << ring.st)) | (((code_ph >> ring.st) & 1u) << ring.st);
+            code_ph ^= 1u << ring.st;
+          }
+        } else if (tl.seg != 2) {
           if (ltid == 0) {
             const int dim0 = 128 * (part & 3);
             const CUtensorMap *m = part >= 4 ? &p.tm_v[tl.seg] : &p.tm_k[tl.seg];
@@ -350,6 +364,82 @@ __device__ __forceinline__ void loader_role(const AttnParams &p, uint32_t sbase,
       if (filled & (1u << s))
         mbar_wait(smem_u32(&ms.kv_full[s]), (last_par >> s) & 1, &never, 100000000ull, p.err, SITE_DRAIN);
     if (q_issued) mbar_wait(b_q_full, q_par, &never, 100000000ull, p.err, SITE_DRAIN);
+    for (int st = 0; st < kStages; ++st)
+      if (cfilled & (1u << st))
+        mbar_wait(smem_u32(&ms.code_full[st]), (clast_par >> st) & 1, &never, 100000000ull, p.err, SITE_DRAIN);
+  }
+}
+
+// ------------------------------------------------------------------ E4M3 converters
+
+// Warps 9..11 when the compressed rows are E4M3: for each such K/V part,
+// wait for its codes (upper half of the stage), then convert them (exactly)
+// into the fp16 stage in the swizzled layout the TMA would have produced, and
+// arrive on kv_full.  A thread converts whole rows: row r's fp16 values in the
+// upper box overwrite only row r's own codes, which the thread has read
+// first; chunks are visited in a per-thread rotated order (no bank
+// conflicts).  The same walk of items, tiles and parts as the loader, so both
+// agree on stage and phase.
+constexpr int kConvThreads = kLoaderThreads - 32;
+
+__device__ __forceinline__ void converter_role(const AttnParams &p, uint32_t sbase, Misc &ms, int ctid) {
+  volatile int *abrt = &ms.abort_flag;
+  Ring ring;
+  uint32_t code_ph = 0;
+  bool ok = true;
+  const int n_items = p.T * p.n_splits;
+  for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+    ItemPlan ip = plan_item(p, item);
+    if (ip.j1 == ip.j0) continue;
+    for (int j = ip.j0; j < ip.j1 && ok; ++j) {
+      const Tile tl = ip.cur.next(p);
+#pragma unroll 1
+      for (int part = 0; part < 8; ++part) {
+        if (tl.seg == 1) {
+          const uint32_t st = ring.st;
+          ok = mbar_wait(smem_u32(&ms.code_full[st]), (code_ph >> st) & 1u, abrt, p.timeout_ns, p.err,
+                         SITE_KV_FULL);
+          code_ph ^= 1u << st;
+          if (bar_red_or(3, kConvThreads, !ok)) {
+            ok = false;
+            break;
+          }
+          const uint32_t stage = sbase + kOffKV + st * kStageBytes;
+#pragma unroll 1
+          for (int row = ctid; row < kTile; row += kConvThreads) {
+            uint4 raw[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const int c = (k + row) & 7;
+              const uint32_t a = stage + kBoxBytes + row * 128 + 16 * c;
+              asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                           : "=r"(raw[k].x), "=r"(raw[k].y), "=r"(raw[k].z), "=r"(raw[k].w)
+                           : "r"(a));
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const int c = (k + row) & 7;
+              const uint32_t w[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
+              uint32_t h[8];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                h[2 * i] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[i] & 0xFFFFu));
+                h[2 * i + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[i] >> 16));
+              }
+              // dims 16c .. 16c+15 of the part: box c/4, 16-byte chunks 2(c%4), 2(c%4)+1
+              const uint32_t drow = stage + (c >> 2) * kBoxBytes + row * 128;
+              const int col = 2 * (c & 3);
+              sts_v4(drow + ((col ^ (row & 7)) << 4), h[0], h[1], h[2], h[3]);
+              sts_v4(drow + (((col + 1) ^ (row & 7)) << 4), h[4], h[5], h[6], h[7]);
+            }
+          }
+          fence_proxy_async_smem();  // generic stores -> visible to the tensor core
+          named_bar_sync(3, kConvThreads);
+          if (ctid == 0) mbar_arrive(smem_u32(&ms.kv_full[st]));
+        }
+        ring.advance();
+      }
+    }
   }
 }
 
@@ -489,6 +579,7 @@ __device__ __forceinline__ void load32(const float *src, float (&v)[32]) {
   }
 }
 
+template <bool FP8>
 __device__ __forceinline__ void compute_role(const AttnParams &p, uint8_t *smem, uint32_t tmem, Misc &ms, int tid) {
   volatile int *abrt = &ms.abort_flag;
   const int w = tid >> 5, l = tid & 31;
@@ -527,8 +618,13 @@ __device__ __forceinline__ void compute_role(const AttnParams &p, uint8_t *smem,
       bool vis;
       float bias;
       row_visibility(p, t, tl, r, vis, bias);
+      // E4M3 compressed rows: the MMA saw the codes; the row scales come in here
+      // (K's on the scores, V's on P below).
+      const bool f8 = FP8 && tl.seg == 1;
+      const float sl2 = f8 && vis ? p.scale_log2 * __ldg(p.k_scale + tl.start + r) : p.scale_log2;
+      const float vsc = f8 && vis ? __ldg(p.v_scale + tl.start + r) : 1.f;
 #pragma unroll
-      for (int h = 0; h < 32; ++h) s[h] = vis ? fmaf(s[h], p.scale_log2, bias) : -INFINITY;
+      for (int h = 0; h < 32; ++h) s[h] = vis ? fmaf(s[h], sl2, bias) : -INFINITY;
 
       ms.red[q][col0 + l] = warp_reduce_scatter32<true>(s, l);
       if (bar_red_or(1, kComputeThreads, bad)) {
@@ -573,11 +669,17 @@ __device__ __forceinline__ void compute_role(const AttnParams &p, uint8_t *smem,
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int h = 8 * c + 2 * i;
-            const __half2 hp = __floats2half2_rn(exp2f(s[h] - mu[2 * i]), exp2f(s[h + 1] - mu[2 * i + 1]));
+            const float e0 = exp2f(s[h] - mu[2 * i]), e1 = exp2f(s[h + 1] - mu[2 * i + 1]);
+            const __half2 hp = __floats2half2_rn(e0, e1);
             const float2 f = __half22float2(hp);
             lpart[h] += f.x;
             lpart[h + 1] += f.y;
-            w4[i] = *reinterpret_cast<const uint32_t *>(&hp);
+            if (f8) {  // P times the row's V scale feeds the MMA; the sums keep P
+              const __half2 hv = __floats2half2_rn(e0 * vsc, e1 * vsc);
+              w4[i] = *reinterpret_cast<const uint32_t *>(&hv);
+            } else {
+              w4[i] = *reinterpret_cast<const uint32_t *>(&hp);
+            }
           }
           const int chunk = 4 * hh + c;
           *reinterpret_cast<uint4 *>(prow + ((chunk ^ (r & 7)) << 4)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
@@ -675,6 +777,7 @@ __device__ __forceinline__ void compute_role(const AttnParams &p, uint8_t *smem,
 
 // ------------------------------------------------------------------ kernel
 
+template <bool FP8>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ AttnParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // Align by pointer arithmetic on the __shared__ array (not through an
@@ -691,6 +794,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&ms.kv_full[s]), fill_count);
       mbar_init(smem_u32(&ms.kv_empty[s]), 1);
+      mbar_init(smem_u32(&ms.code_full[s]), 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&ms.s_full[s]), 1);
@@ -735,11 +839,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   grid_launch_dependents();
 
   if (warp < kComputeWarps) {
-    compute_role(p, smem, tmem, ms, threadIdx.x);
+    compute_role<FP8>(p, smem, tmem, ms, threadIdx.x);
   } else if (warp == kMmaWarp) {
     mma_role(p, sbase, tmem, ms, lane);
   } else {
-    loader_role(p, sbase, ms, threadIdx.x - 32 * kLoaderWarp0);
+    const int ltid = threadIdx.x - 32 * kLoaderWarp0;
+    if (FP8 && ltid >= 32)
+      converter_role(p, sbase, ms, ltid - 32);
+    else
+      loader_role<FP8>(p, sbase, ms, ltid);
   }
 
   tc_fence_before();

@@ -56,6 +56,7 @@ struct Misc {
   alignas(16) int idx_s[128];     // compressed rows of the tile being gathered
   alignas(8) uint64_t q_full, q_empty;
   uint64_t kv_full[kStages], kv_empty[kStages];
+  uint64_t code_full[kStages];    // E4M3 codes of a part landed (upper half of the stage)
   uint64_t s_full[2], s_empty[2];
   uint64_t o_full[4];              // O^T block m (dims 128m ..) final for the item
   uint64_t p_full, p_empty, o_empty, mma_done;
@@ -75,6 +76,7 @@ struct AttnParams {
   CUtensorMap tm_v[2];
   CUtensorMap tm_kg, tm_vg;  // compressed rows, box {64, 1} (gather4)
   CUtensorMap tm_o;        // 3-D {512, 64, T}, box {128, 64, 1}, no swizzle (epilogue stores)
+  CUtensorMap tm_k8, tm_v8;  // E4M3 compressed rows: bytes {512, rows}, box {128, 128}, no swizzle
   int T, q_pos0, n_raw, raw_pos0, n_comp, ratio, window;
   float scale_log2;
   int mode;
@@ -82,6 +84,7 @@ struct AttnParams {
   int partial;             // 1: unnormalised partials to the workspace
   int top_k;
   const void *k_comp, *v_comp;  // compressed rows (read directly by the gather warps)
+  const float *k_scale, *v_scale;  // per-row scales of E4M3 compressed rows
   long long comp_row_stride;    // bytes
   const int32_t *idx;
   long long idx_stride;    // elements
@@ -89,7 +92,7 @@ struct AttnParams {
   long long mask_stride;   // elements
   const uint8_t *status;
   int q_tile, n_blocks, nbr;  // nbr = raw blocks (ceil(n_raw / 32))
-  int pad_;
+  int comp_fp8;            // 1: compressed rows are E4M3 codes with per-row scales (k_scale, v_scale)
   __half *o;
   long long o_tok_stride;  // elements
   float *lse;

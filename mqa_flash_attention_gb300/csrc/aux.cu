@@ -244,4 +244,60 @@ cudaError_t launch_selftest_wait(unsigned long long timeout_ns, unsigned int *er
   return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------ FP8 K/V rows
+
+// Per-row E4M3 quantisation ("DwarfStar 4 (DS4) - DeepSeek V4 Flash Inference
+// Engine", sections "GPU Backend Architecture" and "Whole-Model Graph
+// Execution": K/V rows are quantised to FP8 before they are stored; the
+// format is this library's reading): scale = absmax / 448 and
+// code = E4M3(x * (448 / absmax)), quotients and product in fp32 with round to
+// nearest even, the code rounded to nearest even and saturated; an all-zero
+// row gets scale 0 and codes 0.  One warp per row, 16 values per lane.
+__global__ void quantize_fp8_kernel(const uint8_t *__restrict__ src, long long src_stride, int n_rows,
+                                    uint8_t *__restrict__ dst, long long dst_stride, float *__restrict__ scales) {
+  const int lane = threadIdx.x & 31;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < n_rows; r += warps) {
+    const uint4 *s4 = reinterpret_cast<const uint4 *>(src + (long long)r * src_stride) + 2 * lane;
+    const uint4 a = __ldg(s4), b = __ldg(s4 + 1);
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    float x[16];
+    float m = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[i]));
+      x[2 * i] = f.x;
+      x[2 * i + 1] = f.y;
+      m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
+    }
+    // non-negative floats order like their bit patterns
+    const float amax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(m)));
+    uint32_t out[4] = {0u, 0u, 0u, 0u};
+    if (amax > 0.f) {
+      const float inv = __fdiv_rn(448.f, amax);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        uint16_t h;
+        // upper byte <- second operand's element 2i+1, lower byte <- element 2i
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;"
+            : "=h"(h)
+            : "f"(__fmul_rn(x[2 * i + 1], inv)), "f"(__fmul_rn(x[2 * i], inv)));
+        out[i >> 1] |= static_cast<uint32_t>(h) << (16 * (i & 1));
+      }
+    }
+    reinterpret_cast<uint4 *>(dst + (long long)r * dst_stride)[lane] = make_uint4(out[0], out[1], out[2], out[3]);
+    if (lane == 0) scales[r] = amax > 0.f ? __fdiv_rn(amax, 448.f) : 0.f;
+  }
+}
+
+cudaError_t launch_quantize_fp8(const void *src, long long src_stride, int n_rows, void *dst, long long dst_stride,
+                                float *scales, cudaStream_t s) {
+  const int threads = 256, rows_per_block = threads / 32;
+  long long blocks = (n_rows + rows_per_block - 1) / rows_per_block;
+  if (blocks > 65535) blocks = 65535;
+  quantize_fp8_kernel<<<(unsigned)blocks, threads, 0, s>>>(static_cast<const uint8_t *>(src), src_stride, n_rows,
+                                                          static_cast<uint8_t *>(dst), dst_stride, scales);
+  return cudaGetLastError();
+}
+
 }  // namespace ds4a

@@ -26,6 +26,8 @@ cudaError_t launch_block_mask_dense(const GeomScalars &g, const __half *mask, lo
 cudaError_t launch_combine(const float *ws_o, const float2 *ws_ml, int n_splits, int T, __half *o,
                            long long o_tok_stride, float *lse, cudaStream_t s);
 cudaError_t launch_selftest_wait(unsigned long long timeout_ns, unsigned int *err, cudaStream_t s);
+cudaError_t launch_quantize_fp8(const void *src, long long src_stride, int n_rows, void *dst, long long dst_stride,
+                                float *scales, cudaStream_t s);
 
 // indexer.cu
 constexpr int kTopkMaxCachedKeys = 32768;  // candidate keys a top-k CTA keeps in shared memory

@@ -86,6 +86,10 @@ def lib() -> ctypes.CDLL:
         L.ds4a_attn_indexed.argtypes = [PL, PT, vp, i64, i32, vp]
         L.ds4a_indexer_scores.restype = st
         L.ds4a_indexer_scores.argtypes = [PL, vp, i64, i32, i32, vp, i64, vp, ctypes.c_float, i32, vp, i64, vp]
+        L.ds4a_attn_decode_fp8.restype = st
+        L.ds4a_attn_decode_fp8.argtypes = [PL, PT, vp, vp, i32, vp, ctypes.c_size_t, vp]
+        L.ds4a_quantize_kv_fp8.restype = st
+        L.ds4a_quantize_kv_fp8.argtypes = [vp, i64, i32, vp, i64, vp, vp]
         L.ds4a_indexer_topk.restype = st
         L.ds4a_indexer_topk.argtypes = [PL, vp, i64, i32, vp, i64, vp]
         L.ds4a_device_status.restype = st
@@ -236,6 +240,29 @@ def attn_decode(layout, q, k_raw, v_raw, k_comp=None, v_comp=None, *, n_splits=0
     return (out, lse) if (want_lse or lse is not None) else out
 
 
+def attn_decode_fp8(layout, q, k_raw, v_raw, k_codes, k_scale, v_codes, v_scale, *, n_splits=0, workspace=None,
+                    out=None, lse=None, want_lse=False, stream=None):
+    """:func:`attn_decode` with E4M3 compressed rows (codes uint8 [n, 512] and
+    fp32 row scales [n], as made by :func:`quantize_kv_fp8`)."""
+    import torch
+    L = make_layout(layout)
+    out, lse = _outputs(q, out, lse, want_lse)
+    X = _tensors(q, k_raw, v_raw, None, None, out, lse)
+    for c, nm in ((k_codes, "k_codes"), (v_codes, "v_codes")):
+        if c.dtype != torch.uint8 or c.dim() != 2 or c.shape[1] != D or c.stride(1) != 1:
+            raise ValueError(f"{nm} must be uint8 [n, 512] with contiguous rows")
+    if k_codes.stride(0) != v_codes.stride(0):
+        raise ValueError("k_codes and v_codes must share the row stride")
+    X.k_comp, X.v_comp, X.comp_row_stride = k_codes.data_ptr(), v_codes.data_ptr(), k_codes.stride(0)
+    need = decode_workspace_bytes(L, n_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _check(lib().ds4a_attn_decode_fp8(ctypes.byref(L), ctypes.byref(X), _ptr(k_scale), _ptr(v_scale), int(n_splits),
+                                      _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                      _stream(stream)), "ds4a_attn_decode_fp8")
+    return (out, lse) if (want_lse or lse is not None) else out
+
+
 def attn_decode_partials(layout, q, k_raw, v_raw, k_comp=None, v_comp=None, *, n_splits=0, workspace=None,
                          stream=None):
     """First half of :func:`attn_decode`: per-split partials into ``workspace``."""
@@ -325,6 +352,22 @@ def indexer_topk(layout, scores, top_k, *, out=None, stream=None):
     _check(lib().ds4a_indexer_topk(ctypes.byref(L), _ptr(scores), scores.stride(0) * 4, int(top_k), _ptr(out),
                                    out.stride(0) * 4, _stream(stream)), "ds4a_indexer_topk")
     return out
+
+
+def quantize_kv_fp8(rows, *, codes=None, scales=None, stream=None):
+    """E4M3 codes (uint8 [n, 512]) and per-row fp32 scales of fp16 rows [n, 512]."""
+    import torch
+    ptr, stride = _rows(rows, "rows")
+    n = rows.shape[0]
+    if codes is None:
+        codes = torch.empty((n, 512), dtype=torch.uint8, device=rows.device)
+    if scales is None:
+        scales = torch.empty((n,), dtype=torch.float32, device=rows.device)
+    if codes.dtype != torch.uint8 or codes.dim() != 2 or codes.stride(1) != 1 or codes.shape[1] != 512:
+        raise ValueError("codes must be uint8 [n, 512] with contiguous rows")
+    _check(lib().ds4a_quantize_kv_fp8(ptr, stride, n, _ptr(codes), codes.stride(0), _ptr(scales), _stream(stream)),
+           "ds4a_quantize_kv_fp8")
+    return codes, scales
 
 
 def device_status(clear: bool = True, stream=None) -> int:
