@@ -16,6 +16,7 @@ independent replicas (the path has no exchange step).
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import math
@@ -472,6 +473,31 @@ def run_also(torch, ds4a, W, dev, stream, pk, pk_kind):
                 "frac_hbm": round(by8 / sec8 / 1e9 / pk["hbm_gbs"], 4), "algorithmic_bytes": by8,
                 "speedup_vs_fp16": round(sec / sec8, 2)})
     del d, o, ws, kc, ks, vc, vs
+    # batched decode: 64 sequences, each the ratio-128 32K geometry (128 raw + 256 compressed
+    # rows) with its own K/V rows; three input sets rotate (3 x 58.7 MB > L2)
+    wl = W.decode_r128_32k()
+    B, G = 64, 3
+    L = wl.layout
+    geo = torch.tensor([[L["q_pos0"], L["n_raw"], L["raw_pos0"], L["n_comp"]]] * B, dtype=torch.int32, device=dev)
+    bsets = []
+    for gi in range(G):
+        gen = torch.Generator(device=dev).manual_seed(90 + gi)
+        mk = lambda n: torch.randn((B, n, 512), generator=gen, device=dev).to(torch.float16)  # noqa: E731
+        bsets.append([torch.randn((B, 64, 512), generator=gen, device=dev).to(torch.float16),
+                      mk(L["n_raw"]), mk(L["n_raw"]), mk(L["n_comp"]), mk(L["n_comp"]),
+                      torch.empty((B, 64, 512), dtype=torch.float16, device=dev)])
+    b_splits = ds4a.lib().ds4a_attn_decode_batch_default_splits(B, ctypes.byref(ds4a.make_layout(L)), L["n_raw"],
+                                                               L["n_comp"])
+    bws = torch.empty(max(256, ds4a.lib().ds4a_attn_decode_batch_workspace_size(B, b_splits)), dtype=torch.uint8,
+                      device=dev)
+    sec = timed(lambda i: ds4a.attn_decode_batch(L, geo, *bsets[i % G][:5], n_splits=b_splits, workspace=bws,
+                                                 out=bsets[i % G][5], stream=stream), 30)
+    by = B * decode_bytes(L)
+    out.append({"workload": "decode_batch64_ratio128_ctx32768", "us_per_call": round(sec * 1e6, 2),
+                "hbm_gbs": round(by / sec / 1e9, 1), "frac_hbm": round(by / sec / 1e9 / pk["hbm_gbs"], 4),
+                "algorithmic_bytes": by, "n_splits": b_splits,
+                "note": "64 sequences, each 128 raw + 256 compressed rows of its own"})
+    del bsets, bws, geo
     # indexer of the ratio-4 layer: scores (64 heads x 128 dims, max(0, x)) and top-512
     wx = W.indexer_r4_2048()
     L = wx.layout

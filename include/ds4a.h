@@ -267,6 +267,45 @@ ds4a_status ds4a_attn_decode_fp8(const ds4a_layout *L, const ds4a_tensors *X, co
                                  size_t workspace_bytes, ds4a_stream_t stream);
 
 /*
+ * ds4a_attn_decode_batch - one decode step for n_seq independent sequences in
+ * one launch (the pages' "serving many requests in parallel", page 4): each
+ * sequence has one query token, its own position and row counts, and its own
+ * K/V rows.  Sequence b's results equal ds4a_attn_decode on its own layout.
+ *   shape      ratio, window and scale shared by the batch (other fields are
+ *              ignored).
+ *   seq_geom   device int32 [n_seq][4], 16-byte aligned: per sequence
+ *              (q_pos, n_raw, raw_pos0, n_comp) with the meaning of the
+ *              ds4a_layout fields; the row counts are clamped to raw_rows and
+ *              comp_rows.  Read on the device (not validated on the host).
+ *   X          batch tensors: sequence b's K/V row i at base + b*seq_stride +
+ *              i*row_stride (bytes); Q and O fp16 [n_seq][64][512] at their
+ *              sequence strides; lse fp32 [n_seq][64] or NULL.
+ *   n_splits   row ranges per sequence (<= 0: the library's choice);
+ *              workspace as in ds4a_attn_decode, of at least
+ *              ds4a_attn_decode_batch_workspace_size() bytes.
+ */
+typedef struct {
+  const void *q;       /* fp16 [n_seq][64][512] */
+  int64_t q_seq_stride;
+  const void *k_raw, *v_raw;
+  int64_t raw_row_stride, raw_seq_stride;
+  int32_t raw_rows;    /* rows each sequence's raw K/V tensors hold */
+  const void *k_comp, *v_comp;
+  int64_t comp_row_stride, comp_seq_stride;
+  int32_t comp_rows;
+  void *o;             /* fp16 [n_seq][64][512] */
+  int64_t o_seq_stride;
+  float *lse;
+} ds4a_batch_tensors;
+
+int32_t ds4a_attn_decode_batch_default_splits(int32_t n_seq, const ds4a_layout *shape, int32_t raw_rows,
+                                              int32_t comp_rows);
+size_t ds4a_attn_decode_batch_workspace_size(int32_t n_seq, int32_t n_splits);
+ds4a_status ds4a_attn_decode_batch(int32_t n_seq, const ds4a_layout *shape, const int32_t *seq_geom,
+                                   const ds4a_batch_tensors *X, int32_t n_splits, void *workspace,
+                                   size_t workspace_bytes, ds4a_stream_t stream);
+
+/*
  * ds4a_attn_decode_noalloc - ds4a_attn_decode for callers that cannot
  * allocate device memory: code living inside a host framework whose memory
  * pool owns the device, or a serving loop that forbids allocations once it is

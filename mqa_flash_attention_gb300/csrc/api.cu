@@ -485,6 +485,118 @@ ds4a_status ds4a_attn_decode_fp8(const ds4a_layout *L, const ds4a_tensors *X, co
                                        X->o_tok_stride / 2, X->lse, as_cuda(stream)));
 }
 
+// ------------------------------------------------------------------ batched decode
+
+namespace {
+
+// K/V rows of a batch: {512 dims, rows, sequences}, box {64, 128, 1}, 128-byte swizzle.
+ds4a_status encode_batch_rows(CUtensorMap *m, const void *base, int rows, int64_t row_stride, int n_seq,
+                              int64_t seq_stride) {
+  const cuuint64_t dims[3] = {DS4A_HEAD_DIM, (cuuint64_t)rows, (cuuint64_t)n_seq};
+  const cuuint64_t strides[2] = {(cuuint64_t)row_stride, (cuuint64_t)seq_stride};
+  const cuuint32_t box[3] = {64, 128, 1};
+  return encode(m, base, 3, dims, strides, box);
+}
+
+bool batch_rows_ok(const void *k, const void *v, int32_t rows, int64_t row_stride, int64_t seq_stride) {
+  if (rows == 0) return true;
+  return k != nullptr && v != nullptr && aligned(k, 16) && aligned(v, 16) && row_stride_ok(row_stride) &&
+         seq_stride % 16 == 0 && seq_stride >= (int64_t)rows * row_stride && seq_stride < (1LL << 39);
+}
+
+}  // namespace
+
+int32_t ds4a_attn_decode_batch_default_splits(int32_t n_seq, const ds4a_layout *shape, int32_t raw_rows,
+                                              int32_t comp_rows) {
+  if (n_seq <= 0 || shape == nullptr || raw_rows < 0 || comp_rows < 0 || shape->window < 1) return 1;
+  int sms = 148, dev = -1;
+  if (cudaGetDevice(&dev) == cudaSuccess) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0) sms = v;
+  }
+  const int64_t raw = raw_rows < shape->window ? raw_rows : shape->window;
+  const int32_t mt = ceil_div(raw, 128) + (raw > 0 ? 1 : 0) + ceil_div(comp_rows, 128);
+  // Whole SMs per sequence (rounded down): with many sequences, extra splits
+  // cost more (another wave of short items, a wider merge) than they gain.
+  int32_t s = sms / n_seq;
+  if (s > mt) s = mt;
+  return s < 1 ? 1 : s;
+}
+
+size_t ds4a_attn_decode_batch_workspace_size(int32_t n_seq, int32_t n_splits) {
+  if (n_seq <= 0 || n_splits <= 0) return 0;
+  return (size_t)n_seq * (size_t)n_splits * DS4A_HEADS * (DS4A_HEAD_DIM * sizeof(float) + 2 * sizeof(float));
+}
+
+ds4a_status ds4a_attn_decode_batch(int32_t n_seq, const ds4a_layout *shape, const int32_t *seq_geom,
+                                   const ds4a_batch_tensors *X, int32_t n_splits, void *workspace,
+                                   size_t workspace_bytes, ds4a_stream_t stream) {
+  if (n_seq < 0 || shape == nullptr || X == nullptr) return DS4A_ERR_INVALID_ARG;
+  if (n_seq == 0) return DS4A_OK;
+  if (shape->window < 1 || !std::isfinite(shape->scale) || X->raw_rows < 0 || X->comp_rows < 0 ||
+      X->raw_rows > (1 << 30) || X->comp_rows > (1 << 30) || (X->comp_rows > 0 && shape->ratio < 1))
+    return DS4A_ERR_INVALID_ARG;
+  if (seq_geom == nullptr || !aligned(seq_geom, 16)) return DS4A_ERR_INVALID_ARG;
+  if (X->q == nullptr || !aligned(X->q, 16) || !tok_stride_ok(X->q_seq_stride)) return DS4A_ERR_INVALID_ARG;
+  if (X->o == nullptr || !aligned(X->o, 16) || !tok_stride_ok(X->o_seq_stride)) return DS4A_ERR_INVALID_ARG;
+  if (X->lse != nullptr && !aligned(X->lse, 4)) return DS4A_ERR_INVALID_ARG;
+  if (!batch_rows_ok(X->k_raw, X->v_raw, X->raw_rows, X->raw_row_stride, X->raw_seq_stride) ||
+      !batch_rows_ok(X->k_comp, X->v_comp, X->comp_rows, X->comp_row_stride, X->comp_seq_stride))
+    return DS4A_ERR_INVALID_ARG;
+  if (n_splits <= 0) n_splits = ds4a_attn_decode_batch_default_splits(n_seq, shape, X->raw_rows, X->comp_rows);
+  if (n_splits > 4096) return DS4A_ERR_INVALID_ARG;
+  const size_t n_items = (size_t)n_seq * n_splits;
+  if (n_items > (size_t)INT32_MAX) return DS4A_ERR_INVALID_ARG;
+  const size_t need = ds4a_attn_decode_batch_workspace_size(n_seq, n_splits);
+  if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256)) return DS4A_ERR_WORKSPACE;
+  DeviceState *d = nullptr;
+  ds4a_status st = current_device(&d);
+  if (st != DS4A_OK) return st;
+  AttnParams p;
+  std::memset(&p, 0, sizeof(p));
+  {
+    const cuuint64_t dims[3] = {DS4A_HEAD_DIM, DS4A_HEADS, (cuuint64_t)n_seq};
+    const cuuint64_t strides[2] = {DS4A_ROW_BYTES, (cuuint64_t)X->q_seq_stride};
+    const cuuint32_t box[3] = {64, 64, 1};
+    if ((st = encode(&p.tm_q, X->q, 3, dims, strides, box)) != DS4A_OK) return st;
+  }
+  if (X->raw_rows > 0) {
+    st = encode_batch_rows(&p.tm_k[0], X->k_raw, X->raw_rows, X->raw_row_stride, n_seq, X->raw_seq_stride);
+    if (st == DS4A_OK)
+      st = encode_batch_rows(&p.tm_v[0], X->v_raw, X->raw_rows, X->raw_row_stride, n_seq, X->raw_seq_stride);
+    if (st != DS4A_OK) return st;
+  }
+  if (X->comp_rows > 0) {
+    st = encode_batch_rows(&p.tm_k[1], X->k_comp, X->comp_rows, X->comp_row_stride, n_seq, X->comp_seq_stride);
+    if (st == DS4A_OK)
+      st = encode_batch_rows(&p.tm_v[1], X->v_comp, X->comp_rows, X->comp_row_stride, n_seq, X->comp_seq_stride);
+    if (st != DS4A_OK) return st;
+  }
+  p.T = n_seq;
+  p.n_raw = X->raw_rows;
+  p.n_comp = X->comp_rows;
+  p.ratio = X->comp_rows > 0 ? shape->ratio : 1;
+  p.window = shape->window;
+  p.scale_log2 = shape->scale * 1.4426950408889634f;
+  p.mode = ds4a::MODE_STRUCT;
+  p.n_splits = n_splits;
+  p.q_tile = 1;
+  p.batch_geom = reinterpret_cast<const int4 *>(seq_geom);
+  p.partial = 1;
+  float *ws_o = static_cast<float *>(workspace);
+  float2 *ws_ml = reinterpret_cast<float2 *>(static_cast<uint8_t *>(workspace) +
+                                             n_items * DS4A_HEADS * DS4A_HEAD_DIM * sizeof(float));
+  p.ws_o = ws_o;
+  p.ws_ml = ws_ml;
+  p.timeout_ns = kDefaultTimeoutNs;
+  p.err = d->err;
+  const int grid = (int)(n_items < (size_t)d->sm_count ? n_items : (size_t)d->sm_count);
+  st = launched(ds4a::launch_attn(p, grid, as_cuda(stream)));
+  if (st != DS4A_OK) return st;
+  return launched(ds4a::launch_combine(ws_o, ws_ml, n_splits, n_seq, static_cast<__half *>(X->o),
+                                       X->o_seq_stride / 2, X->lse, as_cuda(stream)));
+}
+
 ds4a_status ds4a_attn_decode_noalloc(const ds4a_layout *L, const ds4a_tensors *X, int32_t n_splits,
                                      ds4a_stream_t stream) {
   ds4a_status st = check_layout(L);

@@ -65,26 +65,36 @@ struct TokenTiles {
 __device__ __forceinline__ TokenTiles token_tiles(const AttnParams &p, int t) {
   TokenTiles z;
   z.t = t;
-  z.pos = p.q_pos0 + t;
+  int pos = p.q_pos0 + t, n_raw = p.n_raw, raw_pos0 = p.raw_pos0, n_comp = p.n_comp;
+  if (p.batch_geom != nullptr) {
+    // Batched decode: token t is sequence t, with its own position and row
+    // counts (clamped to the rows its K/V tensors hold).
+    const int4 g = __ldg(p.batch_geom + t);
+    pos = max(g.x, 0);
+    n_raw = min(max(g.y, 0), p.n_raw);
+    raw_pos0 = max(g.z, 0);
+    n_comp = min(max(g.w, 0), p.n_comp);
+  }
+  z.pos = pos;
   if (p.mode == MODE_MASK) {
     z.raw_lo = 0;
-    z.raw_hi = p.n_raw;
-    z.comp_rows = p.n_comp;
+    z.raw_hi = n_raw;
+    z.comp_rows = n_comp;
   } else {
     // Raw row i sits at raw_pos0 + i; the window is pos - window + 1 .. pos.
-    const long long a = (long long)z.pos - p.window + 1 - p.raw_pos0;
-    const long long b = (long long)z.pos + 1 - p.raw_pos0;
+    const long long a = (long long)pos - p.window + 1 - raw_pos0;
+    const long long b = (long long)pos + 1 - raw_pos0;
     long long lo = a < 0 ? 0 : a;
-    long long hi = b > p.n_raw ? p.n_raw : b;
+    long long hi = b > n_raw ? n_raw : b;
     if (hi < lo) hi = lo;
     z.raw_lo = (int)lo;
     z.raw_hi = (int)hi;
     if (p.mode == MODE_INDEXED) {
-      z.comp_rows = p.n_comp > 0 ? p.top_k : 0;
+      z.comp_rows = n_comp > 0 ? p.top_k : 0;
     } else {
       // Compressed row c is pooled from positions c*ratio .. (c+1)*ratio-1.
-      const long long c = p.n_comp > 0 ? ((long long)z.pos + 1) / p.ratio : 0;
-      z.comp_rows = (int)(c < p.n_comp ? c : p.n_comp);
+      const long long c = n_comp > 0 ? ((long long)pos + 1) / p.ratio : 0;
+      z.comp_rows = (int)(c < n_comp ? c : n_comp);
     }
   }
   z.n_rt = (z.raw_hi - z.raw_lo + kTile - 1) / kTile;
@@ -331,8 +341,13 @@ __device__ __forceinline__ void loader_role(const AttnParams &p, uint32_t sbase,
             const int dim0 = 128 * (part & 3);
             const CUtensorMap *m = part >= 4 ? &p.tm_v[tl.seg] : &p.tm_k[tl.seg];
             mbar_arrive_expect_tx(b_full, kStageBytes);
-            tma_load_2d(stage, m, b_full, dim0, tl.start);
-            tma_load_2d(stage + kBoxBytes, m, b_full, dim0 + 64, tl.start);
+            if (p.batch_geom != nullptr) {  // [sequences][rows][512]: the sequence is the third coordinate
+              tma_load_3d(stage, m, b_full, dim0, tl.start, ip.t);
+              tma_load_3d(stage + kBoxBytes, m, b_full, dim0 + 64, tl.start, ip.t);
+            } else {
+              tma_load_2d(stage, m, b_full, dim0, tl.start);
+              tma_load_2d(stage + kBoxBytes, m, b_full, dim0 + 64, tl.start);
+            }
             filled |= 1u << ring.st;
             last_par = (last_par & ~(1u << ring.st)) | (ring.ph << ring.st);
           } else {

@@ -42,6 +42,15 @@ class Tensors(ctypes.Structure):
                 ("lse", ctypes.c_void_p)]
 
 
+class BatchTensors(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("q_seq_stride", ctypes.c_int64),
+                ("k_raw", ctypes.c_void_p), ("v_raw", ctypes.c_void_p), ("raw_row_stride", ctypes.c_int64),
+                ("raw_seq_stride", ctypes.c_int64), ("raw_rows", ctypes.c_int32),
+                ("k_comp", ctypes.c_void_p), ("v_comp", ctypes.c_void_p), ("comp_row_stride", ctypes.c_int64),
+                ("comp_seq_stride", ctypes.c_int64), ("comp_rows", ctypes.c_int32),
+                ("o", ctypes.c_void_p), ("o_seq_stride", ctypes.c_int64), ("lse", ctypes.c_void_p)]
+
+
 _lib = None
 
 
@@ -86,6 +95,12 @@ def lib() -> ctypes.CDLL:
         L.ds4a_attn_indexed.argtypes = [PL, PT, vp, i64, i32, vp]
         L.ds4a_indexer_scores.restype = st
         L.ds4a_indexer_scores.argtypes = [PL, vp, i64, i32, i32, vp, i64, vp, ctypes.c_float, i32, vp, i64, vp]
+        L.ds4a_attn_decode_batch.restype = st
+        L.ds4a_attn_decode_batch.argtypes = [i32, PL, vp, ctypes.POINTER(BatchTensors), i32, vp, ctypes.c_size_t, vp]
+        L.ds4a_attn_decode_batch_workspace_size.restype = ctypes.c_size_t
+        L.ds4a_attn_decode_batch_workspace_size.argtypes = [i32, i32]
+        L.ds4a_attn_decode_batch_default_splits.restype = i32
+        L.ds4a_attn_decode_batch_default_splits.argtypes = [i32, PL, i32, i32]
         L.ds4a_attn_decode_fp8.restype = st
         L.ds4a_attn_decode_fp8.argtypes = [PL, PT, vp, vp, i32, vp, ctypes.c_size_t, vp]
         L.ds4a_quantize_kv_fp8.restype = st
@@ -260,6 +275,44 @@ def attn_decode_fp8(layout, q, k_raw, v_raw, k_codes, k_scale, v_codes, v_scale,
     _check(lib().ds4a_attn_decode_fp8(ctypes.byref(L), ctypes.byref(X), _ptr(k_scale), _ptr(v_scale), int(n_splits),
                                       _ptr(workspace), workspace.numel() * workspace.element_size(),
                                       _stream(stream)), "ds4a_attn_decode_fp8")
+    return (out, lse) if (want_lse or lse is not None) else out
+
+
+def attn_decode_batch(shape, seq_geom, q, k_raw, v_raw, k_comp=None, v_comp=None, *, n_splits=0, workspace=None,
+                      out=None, lse=None, want_lse=False, stream=None):
+    """One decode step for B sequences: q fp16 [B, 64, 512]; k/v_raw fp16
+    [B, raw_rows, 512]; k/v_comp fp16 [B, comp_rows, 512] (rows contiguous);
+    seq_geom int32 [B, 4] on the device: (q_pos, n_raw, raw_pos0, n_comp)."""
+    import torch
+    S = make_layout(shape)
+    B = q.shape[0]
+    if seq_geom.dtype != torch.int32 or tuple(seq_geom.shape) != (B, 4) or not seq_geom.is_contiguous():
+        raise ValueError("seq_geom must be contiguous int32 [B, 4]")
+    out, lse = _outputs(q, out, lse, want_lse)
+    qp, qs = _tokens(q, "q")
+    op, os_ = _tokens(out, "out")
+
+    def seg(k, v):
+        if k is None:
+            return None, None, ROW_BYTES, ROW_BYTES, 0
+        for t, nm in ((k, "k"), (v, "v")):
+            if t.dtype != torch.float16 or t.dim() != 3 or t.shape[0] != B or t.shape[2] != D or t.stride(2) != 1:
+                raise ValueError(f"{nm} must be fp16 [B, rows, 512] with contiguous rows")
+        if k.stride() != v.stride() or k.shape != v.shape:
+            raise ValueError("K and V of a segment must share shape and strides")
+        return k.data_ptr(), v.data_ptr(), k.stride(1) * 2, k.stride(0) * 2, k.shape[1]
+
+    kr, vr, rrs, rss, rr = seg(k_raw, v_raw)
+    kc, vc, crs, css, cr = seg(k_comp, v_comp)
+    X = BatchTensors(qp, qs, kr, vr, rrs, rss, rr, kc, vc, crs, css, cr, op, os_, _ptr(lse))
+    if n_splits <= 0:
+        n_splits = lib().ds4a_attn_decode_batch_default_splits(B, ctypes.byref(S), rr, cr)
+    need = lib().ds4a_attn_decode_batch_workspace_size(B, int(n_splits))
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _check(lib().ds4a_attn_decode_batch(B, ctypes.byref(S), _ptr(seq_geom), ctypes.byref(X), int(n_splits),
+                                        _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                        _stream(stream)), "ds4a_attn_decode_batch")
     return (out, lse) if (want_lse or lse is not None) else out
 
 

@@ -341,6 +341,33 @@ def test_decode_several_tokens(torch, ds4a):
         assert_close(host(o), want, f"decode T=3 splits={s}")
 
 
+def test_decode_batch_matches_oracle(torch, ds4a):
+    """Seven sequences, each with its own position, row counts and K/V rows, in
+    one batched launch; each equals the oracle on its own layout."""
+    from mqa_flash_attention_gb300 import synth
+    R, C, ratio = 200, 300, 128
+    geo = [  # q_pos, n_raw, raw_pos0, n_comp
+        (32767, 128, 32640, 256), (5000, 200, 4801, 39), (130, 131, 0, 1), (70, 71, 0, 0),
+        (38399, 150, 38250, 299), (38400, 128, 38273, 300), (1000, 60, 941, 7)]
+    B = len(geo)
+    q = synth.normal_f16(40, synth.STREAM_Q, (B, 64, 512))
+    kr = synth.normal_f16(40, synth.STREAM_K_RAW, (B, R, 512))
+    vr = synth.normal_f16(40, synth.STREAM_V_RAW, (B, R, 512))
+    kc = synth.normal_f16(40, synth.STREAM_K_COMP, (B, C, 512))
+    vc = synth.normal_f16(40, synth.STREAM_V_COMP, (B, C, 512))
+    g = dev(torch, np.array(geo, dtype=np.int32))
+    shape = make_layout(T=1, q_pos0=0, n_raw=0, raw_pos0=0, n_comp=0, ratio=ratio)
+    for splits in (0, 1, 3):
+        o, lse = ds4a.attn_decode_batch(shape, g, dev(torch, q), dev(torch, kr), dev(torch, vr), dev(torch, kc),
+                                        dev(torch, vc), n_splits=splits, want_lse=True)
+        o, lse = host(o), host(lse)
+        for b, (qp, nr, rp, nc) in enumerate(geo):
+            L = make_layout(T=1, q_pos0=qp, n_raw=nr, raw_pos0=rp, n_comp=nc, ratio=ratio)
+            want, wlse = oracle.attention(L, q[b:b + 1], kr[b, :nr], vr[b, :nr], kc[b, :nc], vc[b, :nc])
+            assert_close(o[b:b + 1], want, f"batch seq {b} splits={splits}")
+            assert_lse_close(lse[b:b + 1], wlse, f"batch seq {b} lse")
+
+
 # ------------------------------------------------------------------ indexed
 
 def test_indexed_ratio4_sampled(torch, ds4a):
