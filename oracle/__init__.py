@@ -10,3 +10,4 @@ from .mqa import (  # noqa: F401
 )
 from . import indexer  # noqa: F401,E402
 from . import fp8  # noqa: F401,E402
+from . import compressor  # noqa: F401,E402
