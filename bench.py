@@ -517,6 +517,35 @@ def run_also(torch, ds4a, W, dev, stream, pk, pk_kind):
     out.append({"workload": wx.name + "_topk", "us_per_call": round(sec * 1e6, 2),
                 "gbs": round(by / sec / 1e9, 1), "algorithmic_bytes": by,
                 "note": "exact radix select over each token's candidate scores"})
+    # compressor, one 2048-token prefill chunk of 512-dim rows (fresh state) on a ratio-4 and a
+    # ratio-128 layer; 20 input sets rotate (20 x 8 MB > L2)
+    for ratio in (4, 128):
+        wc = W.compressor_prefill(ratio)
+        n, width = wc.kv.shape
+        G = 20
+        gen = torch.Generator(device=dev).manual_seed(95 + ratio)
+        csets = [(torch.randn((n, width), generator=gen, device=dev),
+                  2 * torch.randn((n, width), generator=gen, device=dev)) for _ in range(G)]
+        st_kv = torch.empty((ratio - 1, width), dtype=torch.float32, device=dev)
+        st_s = torch.empty((ratio - 1, width), dtype=torch.float32, device=dev)
+        c_out = torch.empty((n // ratio, width), dtype=torch.float16, device=dev)
+        sec = timed(lambda i: ds4a.compress_append(csets[i % G][0], csets[i % G][1], st_kv, st_s, 0, ratio,
+                                                   out=c_out, stream=stream), 40)
+        by = 8 * n * width + 2 * (n // ratio) * width
+        out.append({"workload": wc.name, "us_per_call": round(sec * 1e6, 2), "hbm_gbs": round(by / sec / 1e9, 1),
+                    "frac_hbm": round(by / sec / 1e9 / pk["hbm_gbs"], 4), "algorithmic_bytes": by,
+                    "note": "per-dimension softmax pooling of each ratio span, fp32 in, fp16 out"})
+        del csets
+    # compressor decode step at a ratio-128 boundary: 127 positions in the state, one new
+    st_kv = torch.randn((127, 512), device=dev)
+    st_s = torch.randn((127, 512), device=dev)
+    one = [(torch.randn((1, 512), device=dev), torch.randn((1, 512), device=dev)) for _ in range(2)]
+    c_out = torch.empty((1, 512), dtype=torch.float16, device=dev)
+    sec = timed(lambda i: ds4a.compress_append(one[i % 2][0], one[i % 2][1], st_kv, st_s, 127, 128, out=c_out,
+                                               stream=stream), 40)
+    out.append({"workload": "compressor_ratio128_decode_boundary_w512", "us_per_call": round(sec * 1e6, 2),
+                "note": "one token completes a 128-position span (state in L2): latency"})
+    del st_kv, st_s, one
     for e in out:
         e["peak_kind"] = pk_kind
     return out
@@ -525,7 +554,7 @@ def run_also(torch, ds4a, W, dev, stream, pk, pk_kind):
 # ------------------------------------------------------------------ profiling cases
 
 CASES = ("tiny", "decode_r128_32k", "prefill_raw_2048", "indexed_r4_2048", "decode_long_262144",
-         "indexer_r4_2048")
+         "indexer_r4_2048", "compressor_r4_2048", "compressor_r128_2048")
 
 
 def run_case(name: str, calls: int) -> None:
@@ -545,6 +574,18 @@ def run_case(name: str, calls: int) -> None:
         torch.cuda.synchronize()
         if ds4a.device_status() != ds4a.OK:
             raise RuntimeError("device wait ran out")
+        print(f"{name}: {calls} calls ok")
+        return
+    if name.startswith("compressor_r"):
+        ratio = int(name[len("compressor_r"):].split("_")[0])
+        wc = W.compressor_prefill(ratio)
+        up = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
+        kv, sc = up(wc.kv), up(wc.score)
+        st_kv = torch.empty((ratio - 1, kv.shape[1]), dtype=torch.float32, device="cuda")
+        st_s = torch.empty_like(st_kv)
+        for _ in range(calls):
+            ds4a.compress_append(kv, sc, st_kv, st_s, 0, ratio)
+        torch.cuda.synchronize()
         print(f"{name}: {calls} calls ok")
         return
     wl = W.decode_long(262144) if name == "decode_long_262144" else getattr(W, name)()

@@ -390,6 +390,43 @@ ds4a_status ds4a_indexer_topk(const ds4a_layout *L, const float *scores, int64_t
                               int32_t *idx, int64_t idx_row_stride, ds4a_stream_t stream);
 
 /*
+ * ds4a_compress_append - the compressor ([P2] "Layer Compression": a rolling
+ * K/V and score state, a pooled row appended at each ratio boundary; "KV Cache
+ * Design": attn_state_kv / attn_state_score; "GPU Backend Architecture":
+ * compressor update, prefill and replay).  One call covers all three: it
+ * appends n_new positions (one token in decode, a chunk in prefill, stored
+ * rows after a restore) to a state that holds the n_state positions of the
+ * span in progress.  The pages give no pooling formula; this library's
+ * reading: each position brings a row kv[i] and a score row s[i] of the same
+ * width, and a completed span of `ratio` positions becomes one row
+ *     row[d] = sum_i exp(s[i][d] - m[d]) * kv[i][d] / sum_i exp(s[i][d] - m[d]),
+ * m[d] = max_i s[i][d], a softmax over the span taken per dimension.  With
+ * N = n_state + n_new, the call writes n_out = N / ratio pooled rows (span 0
+ * starts with the state's rows) and leaves the last N % ratio positions, in
+ * order, in the state's rows 0 .. (N % ratio) - 1.  The learned initial states
+ * of ratio-4 layers are not modelled: a fresh state has n_state = 0.
+ * fp32 loads and arithmetic; pooled rows are rounded to fp16.
+ *   width        elements per row, a multiple of 4, 4 .. 65536.
+ *   ratio        span length, 1 .. 65536.   n_state: 0 .. ratio - 1.
+ *   kv, score    fp32 [n_new][width] at new_row_stride bytes; scores finite.
+ *   state_kv, state_score
+ *                fp32 [ratio - 1][width] at state_row_stride bytes, read and
+ *                updated in place (unused, may be NULL, when ratio == 1).
+ *   out          fp16 [n_out][width] at out_row_stride bytes: the pooled rows,
+ *                for instance the next free rows of the compressed K or V
+ *                rows.  May be NULL when n_out == 0.
+ * Strides are at least one row and multiples of 16 bytes (of 8 bytes for the
+ * output); pointers are device pointers owned by the caller, 16-byte aligned.  kv and score may be the
+ * same rows; otherwise no two of the ranges (new rows, the two state tensors,
+ * the output) may overlap (DS4A_ERR_INVALID_ARG).  n_new == 0 does nothing.
+ * ds4a_compress_rows returns n_out for the arguments (-1 if they are invalid).
+ */
+int32_t ds4a_compress_rows(int32_t n_state, int32_t n_new, int32_t ratio);
+ds4a_status ds4a_compress_append(int32_t width, int32_t ratio, int32_t n_state, const float *kv, const float *score,
+                                 int64_t new_row_stride, int32_t n_new, float *state_kv, float *state_score,
+                                 int64_t state_row_stride, void *out, int64_t out_row_stride, ds4a_stream_t stream);
+
+/*
  * ds4a_device_status - synchronises `stream`, then reports the device error
  * word the kernels set when a bounded wait runs out (DS4A_ERR_TIMEOUT) or
  * DS4A_OK.  clear != 0 resets the word.  A CUDA error from the

@@ -252,6 +252,70 @@ ds4a_status ds4a_quantize_kv_fp8(const void *src, int64_t src_row_stride, int32_
                                             as_cuda(stream)));
 }
 
+int32_t ds4a_compress_rows(int32_t n_state, int32_t n_new, int32_t ratio) {
+  if (ratio < 1 || ratio > 65536 || n_state < 0 || n_state >= ratio || n_new < 0) return -1;
+  return (int32_t)(((int64_t)n_state + n_new) / ratio);
+}
+
+ds4a_status ds4a_compress_append(int32_t width, int32_t ratio, int32_t n_state, const float *kv, const float *score,
+                                 int64_t new_row_stride, int32_t n_new, float *state_kv, float *state_score,
+                                 int64_t state_row_stride, void *out, int64_t out_row_stride, ds4a_stream_t stream) {
+  const int32_t n_out = ds4a_compress_rows(n_state, n_new, ratio);
+  if (n_out < 0 || width < 4 || width > 65536 || width % 4 != 0) return DS4A_ERR_INVALID_ARG;
+  if (n_new == 0) return DS4A_OK;
+  auto stride_ok = [](int64_t s, int64_t row) { return s >= row && s % 16 == 0 && s < (1LL << 39); };
+  if (kv == nullptr || score == nullptr || !aligned(kv, 16) || !aligned(score, 16) ||
+      !stride_ok(new_row_stride, 4LL * width))
+    return DS4A_ERR_INVALID_ARG;
+  if (ratio > 1 && (state_kv == nullptr || state_score == nullptr || !aligned(state_kv, 16) ||
+                    !aligned(state_score, 16) || !stride_ok(state_row_stride, 4LL * width)))
+    return DS4A_ERR_INVALID_ARG;
+  if (n_out > 0 && (out == nullptr || !aligned(out, 16) || out_row_stride < 2LL * width || out_row_stride % 8 != 0 ||
+                    out_row_stride >= (1LL << 39)))
+    return DS4A_ERR_INVALID_ARG;
+  // Byte ranges: the new rows are read while the state and the output are
+  // written, so none of the written ranges may meet a read one or each other.
+  struct Span {
+    uintptr_t lo, hi;
+  };
+  auto span = [](const void *ptr, int64_t rows, int64_t stride, int64_t row_bytes) {
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(ptr);
+    return Span{lo, rows > 0 ? lo + (uintptr_t)((rows - 1) * stride + row_bytes) : lo};
+  };
+  auto meet = [](Span a, Span b) { return a.lo < b.hi && b.lo < a.hi; };
+  const Span rd[2] = {span(kv, n_new, new_row_stride, 4LL * width), span(score, n_new, new_row_stride, 4LL * width)};
+  const Span wr[3] = {span(state_kv, ratio > 1 ? ratio - 1 : 0, state_row_stride, 4LL * width),
+                      span(state_score, ratio > 1 ? ratio - 1 : 0, state_row_stride, 4LL * width),
+                      span(out, n_out, out_row_stride, 2LL * width)};
+  for (int i = 0; i < 3; ++i) {
+    for (int j = 0; j < 2; ++j)
+      if (meet(wr[i], rd[j])) return DS4A_ERR_INVALID_ARG;
+    for (int j = i + 1; j < 3; ++j)
+      if (meet(wr[i], wr[j])) return DS4A_ERR_INVALID_ARG;
+  }
+  DeviceState *d = nullptr;
+  ds4a_status st = current_device(&d);
+  if (st != DS4A_OK) return st;
+  ds4a::CompressParams p;
+  p.kv = kv;
+  p.score = score;
+  p.new_stride = new_row_stride / 4;
+  p.state_kv = state_kv;
+  p.state_score = state_score;
+  p.state_stride = ratio > 1 ? state_row_stride / 4 : 0;
+  p.out = static_cast<__half *>(out);
+  p.out_stride = n_out > 0 ? out_row_stride / 2 : 0;
+  p.width = width;
+  p.ratio = ratio;
+  p.n_state = n_state;
+  p.n_new = n_new;
+  p.n_out = n_out;
+  p.tail = (int32_t)(((int64_t)n_state + n_new) % ratio);
+  p.splits = ds4a::compress_splits(ratio);
+  p.chunks = (width + 127) / 128;
+  return launched(ds4a::launch_compress(p, as_cuda(stream)));
+}
+
 int32_t ds4a_block_count(const ds4a_layout *L) {
   if (L == nullptr || L->n_raw < 0 || L->n_comp < 0) return -1;
   return ceil_div(L->n_raw, DS4A_BLOCK_ROWS) + ceil_div(L->n_comp, DS4A_BLOCK_ROWS);

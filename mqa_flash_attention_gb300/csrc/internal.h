@@ -34,4 +34,22 @@ constexpr int kTopkMaxCachedKeys = 32768;  // candidate keys a top-k CTA keeps i
 cudaError_t launch_indexer_topk(const TopkParams &p, int dyn_smem, cudaStream_t s);
 cudaError_t launch_indexer_scores(const ScoreParams &p, int n_heads, int grid, cudaStream_t s);
 
+// compressor.cu
+// One append of n_new rows to a compressor state holding n_state rows
+// (strides in elements).  n_out = (n_state + n_new) / ratio pooled rows are
+// written; tail = (n_state + n_new) % ratio rows remain in the state.
+struct CompressParams {
+  const float *kv, *score;
+  long long new_stride;
+  float *state_kv, *state_score;
+  long long state_stride;
+  __half *out;
+  long long out_stride;
+  int width, ratio, n_state, n_new, n_out, tail;
+  int splits;  // warps that share one span: 1, 2, 4 or 8
+  int chunks;  // ceil(width / 128)
+};
+int compress_splits(int ratio);
+cudaError_t launch_compress(const CompressParams &p, cudaStream_t s);
+
 }  // namespace ds4a

@@ -105,6 +105,10 @@ def lib() -> ctypes.CDLL:
         L.ds4a_attn_decode_fp8.argtypes = [PL, PT, vp, vp, i32, vp, ctypes.c_size_t, vp]
         L.ds4a_quantize_kv_fp8.restype = st
         L.ds4a_quantize_kv_fp8.argtypes = [vp, i64, i32, vp, i64, vp, vp]
+        L.ds4a_compress_rows.restype = i32
+        L.ds4a_compress_rows.argtypes = [i32, i32, i32]
+        L.ds4a_compress_append.restype = st
+        L.ds4a_compress_append.argtypes = [i32, i32, i32, vp, vp, i64, i32, vp, vp, i64, vp, i64, vp]
         L.ds4a_indexer_topk.restype = st
         L.ds4a_indexer_topk.argtypes = [PL, vp, i64, i32, vp, i64, vp]
         L.ds4a_device_status.restype = st
@@ -421,6 +425,45 @@ def quantize_kv_fp8(rows, *, codes=None, scales=None, stream=None):
     _check(lib().ds4a_quantize_kv_fp8(ptr, stride, n, _ptr(codes), codes.stride(0), _ptr(scales), _stream(stream)),
            "ds4a_quantize_kv_fp8")
     return codes, scales
+
+
+def _f32_rows(t, name, width):
+    import torch
+    if t.dtype != torch.float32 or t.dim() != 2 or t.shape[1] != width or t.stride(1) != 1:
+        raise ValueError(f"{name} must be fp32 [rows, {width}] with contiguous rows")
+    return _ptr(t), t.stride(0) * 4
+
+
+def compress_rows(n_state: int, n_new: int, ratio: int) -> int:
+    """Pooled rows one compressor append writes (-1 for invalid arguments)."""
+    return lib().ds4a_compress_rows(n_state, n_new, ratio)
+
+
+def compress_append(kv, score, state_kv, state_score, n_state, ratio, *, out=None, stream=None):
+    """Appends fp32 rows kv / score [n_new, width] to a compressor state
+    (fp32 [>= ratio - 1, width] each, updated in place, holding n_state rows).
+    Returns (pooled fp16 rows [n_out, width], rows left in the state)."""
+    import torch
+    n_new, width = kv.shape
+    kp, ks = _f32_rows(kv, "kv", width)
+    sp, ss = _f32_rows(score, "score", width)
+    if ks != ss or score.shape[0] != n_new:
+        raise ValueError("kv and score must have the same shape and row stride")
+    n_out = compress_rows(n_state, n_new, ratio)
+    if n_out < 0:
+        raise ValueError("invalid n_state / ratio")
+    stp, sts = _f32_rows(state_kv, "state_kv", width)
+    scp, scs = _f32_rows(state_score, "state_score", width)
+    if sts != scs or state_kv.shape[0] < ratio - 1 or state_score.shape[0] < ratio - 1:
+        raise ValueError("the state tensors must hold ratio - 1 rows at one row stride")
+    if out is None:
+        out = torch.empty((n_out, width), dtype=torch.float16, device=kv.device)
+    if out.dtype != torch.float16 or out.dim() != 2 or out.shape[0] < n_out or out.shape[1] != width or \
+            out.stride(1) != 1:
+        raise ValueError("out must be fp16 [>= n_out, width] with contiguous rows")
+    _check(lib().ds4a_compress_append(width, ratio, n_state, kp, sp, ks, n_new, stp, scp, sts, _ptr(out),
+                                      out.stride(0) * 2, _stream(stream)), "ds4a_compress_append")
+    return out[:n_out], (n_state + n_new) % ratio
 
 
 def device_status(clear: bool = True, stream=None) -> int:

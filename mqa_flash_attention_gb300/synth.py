@@ -36,6 +36,8 @@ STREAM_MASK = 7
 STREAM_IDX_Q = 8      # indexer query vectors
 STREAM_IDX_K = 9      # indexer compressed rows
 STREAM_IDX_W = 10     # indexer head weights
+STREAM_CMP_KV = 11    # compressor input rows
+STREAM_CMP_S = 12     # compressor score rows
 
 
 def _mix64(z: np.ndarray) -> np.ndarray:

@@ -153,3 +153,24 @@ def indexer_r4_2048(n_heads: int = 64, head_dim: int = 128) -> IndexerWorkload:
     return draw_indexer("indexer_ratio4_T2048_ctx32768", 12,
                         make_layout(T=2048, q_pos0=30720, n_raw=2175, raw_pos0=30593, n_comp=8192, ratio=4),
                         n_heads, head_dim, 512)
+
+
+@dataclasses.dataclass
+class CompressorWorkload:
+    name: str
+    seed: int
+    ratio: int
+    kv: np.ndarray      # fp32 [n, width]
+    score: np.ndarray   # fp32 [n, width]
+
+
+def draw_compressor(name: str, seed: int, n: int, width: int, ratio: int, score_std: float = 2.0) -> CompressorWorkload:
+    """Rows entering a compressor: kv ~ N(0, 1), scores ~ N(0, score_std^2), fp32."""
+    return CompressorWorkload(name, seed, ratio, synth.normal_f32(seed, synth.STREAM_CMP_KV, (n, width)),
+                              (synth.normal_f32(seed, synth.STREAM_CMP_S, (n, width)) * np.float32(score_std)))
+
+
+def compressor_prefill(ratio: int, width: int = D) -> CompressorWorkload:
+    """One 2048-token prefill chunk entering a compressor of 512-dim K/V rows
+    (a fresh state), on a ratio-4 or a ratio-128 layer."""
+    return draw_compressor(f"compressor_ratio{ratio}_T2048_w{width}", 13, 2048, width, ratio)

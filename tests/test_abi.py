@@ -151,3 +151,31 @@ def test_pad_arguments_are_checked(lib):
 def test_selftest_bound_is_checked(lib):
     assert lib.ds4a_selftest_wait_timeout(10, None) == ds4a.ERR_INVALID_ARG
     assert lib.ds4a_selftest_wait_timeout(10**11, None) == ds4a.ERR_INVALID_ARG
+
+
+def test_compress_arguments_are_checked(lib):
+    A = lambda x: ctypes.c_void_p(x)  # noqa: E731
+    assert lib.ds4a_compress_rows(3, 6, 4) == 2
+    assert lib.ds4a_compress_rows(0, 2048, 128) == 16
+    for bad in [(4, 1, 4), (-1, 1, 4), (0, -1, 4), (0, 1, 0), (0, 1, 65537)]:
+        assert lib.ds4a_compress_rows(*bad) == -1
+    kv, sc, skv, ssc, out = A(1 << 30), A(2 << 30), A(3 << 30), A(4 << 30), A(5 << 30)
+
+    def call(width=512, ratio=4, n_state=0, kv=kv, sc=sc, ns=2048, n_new=8, skv=skv, ssc=ssc, ss=2048, out=out,
+             os_=1024):
+        return lib.ds4a_compress_append(width, ratio, n_state, kv, sc, ns, n_new, skv, ssc, ss, out, os_, None)
+
+    assert call(n_new=0) == ds4a.OK
+    assert call(width=510) == ds4a.ERR_INVALID_ARG           # width % 4
+    assert call(n_state=4) == ds4a.ERR_INVALID_ARG           # n_state >= ratio
+    assert call(ns=2040) == ds4a.ERR_INVALID_ARG             # row shorter than width
+    assert call(ns=2056) == ds4a.ERR_INVALID_ARG             # not a multiple of 16
+    assert call(kv=None) == ds4a.ERR_INVALID_ARG
+    assert call(kv=A((1 << 30) + 8)) == ds4a.ERR_INVALID_ARG  # 16-byte alignment
+    assert call(skv=None) == ds4a.ERR_INVALID_ARG             # ratio > 1 needs a state
+    assert call(out=None) == ds4a.ERR_INVALID_ARG             # two rows are pooled
+    assert call(os_=1000) == ds4a.ERR_INVALID_ARG            # shorter than a row
+    assert call(os_=1028) == ds4a.ERR_INVALID_ARG            # not a multiple of 8
+    assert call(width=132, ns=528, ss=528, os_=264, out=None) == ds4a.ERR_INVALID_ARG   # only the output missing
+    assert call(out=A((1 << 30) + 4096)) == ds4a.ERR_INVALID_ARG   # output inside the new rows
+    assert call(ssc=A((3 << 30) + 2048)) == ds4a.ERR_INVALID_ARG   # the two states overlap
