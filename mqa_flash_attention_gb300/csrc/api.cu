@@ -311,8 +311,9 @@ ds4a_status ds4a_compress_append(int32_t width, int32_t ratio, int32_t n_state, 
   p.n_new = n_new;
   p.n_out = n_out;
   p.tail = (int32_t)(((int64_t)n_state + n_new) % ratio);
-  p.splits = ds4a::compress_splits(ratio);
-  p.chunks = (width + 127) / 128;
+  ds4a::compress_shape(ratio, &p.splits, &p.slots);
+  const int chunk = 128 / p.slots;
+  p.chunks = (width + chunk - 1) / chunk;
   return launched(ds4a::launch_compress(p, as_cuda(stream)));
 }
 

@@ -10,12 +10,13 @@
 // span wait in the state (oldest first) for the next call.
 //
 // The work is HBM-bound (8 bytes read per element, 2 written per pooled
-// element), so it runs on the CUDA cores: a warp owns one span and 128
-// dimensions (a float4 per lane, so every row read is one coalesced 512-byte
-// line), keeps a running (max, sum, weighted sum) per dimension, and loads up
-// to eight rows before it folds them in, so eight pairs of 16-byte loads per
-// lane are in flight.  Long spans are cut across the warps of a block and the
-// partial sums merged through shared memory.
+// element), so it runs on the CUDA cores.  A lane owns 4 dimensions (one
+// float4) of a run of consecutive rows of one span, keeps a running (max,
+// sum, weighted sum) per dimension, and loads up to eight rows before it folds
+// them in.  The rows of a span are cut over up to 4 row slots of a warp (the
+// slot's lanes read one contiguous 128..512-byte piece of a row) and up to 8
+// warps of a block, so that a lane holds about four rows and all its loads are
+// in flight at once; the parts merge through shuffles and shared memory.
 #include <cuda_fp16.h>
 
 #include "internal.h"
@@ -46,23 +47,38 @@ __device__ __forceinline__ void fold_batch(RunSum &r, const float *sc, const flo
   r = RunSum{bm, l, a};
 }
 
+// Combines two running sums of disjoint row sets (either may be empty).
+__device__ __forceinline__ RunSum merge(RunSum x, RunSum y) {
+  const float M = fmaxf(x.m, y.m);
+  const float fx = x.m == -INFINITY ? 0.f : expf(x.m - M);
+  const float fy = y.m == -INFINITY ? 0.f : expf(y.m - M);
+  return RunSum{M, x.l * fx + y.l * fy, x.a * fx + y.a * fy};
+}
+
+// Work: (span c, chunk q of 128/R dimensions) pairs; each pair is cut into
+// S*R parts of consecutive rows: S warps of the block, R row slots per warp
+// (lane = slot * 32/R + g, g owning 4 dimensions).  A part keeps a running
+// sum; parts merge through shuffles (slots) and shared memory (warps).
 __global__ void __launch_bounds__(kCompWarps * 32) compress_pool_kernel(CompressParams p) {
   __shared__ float4 sh_m[kCompWarps][32], sh_l[kCompWarps][32], sh_a[kCompWarps][32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int S = p.splits;
+  const int S = p.splits, R = p.slots;
+  const int G = 32 / R;  // lanes per row slot
+  const int slot = lane / G, g = lane % G;
   const int s = warp & (S - 1);
   const long long pair = (long long)blockIdx.x * (kCompWarps / S) + warp / S;
   const bool active = pair < (long long)p.n_out * p.chunks;
   const int c = active ? (int)(pair / p.chunks) : 0;
   const int q = active ? (int)(pair % p.chunks) : 0;
-  const int d = q * 128 + lane * 4;
+  const int d = q * (128 / R) + g * 4;
   const bool on = active && d < p.width;
 
   RunSum r[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) r[k] = RunSum{-INFINITY, 0.f, 0.f};
-  const int rpw = (p.ratio + S - 1) / S;
-  const int r0 = min(s * rpw, p.ratio), r1 = min(r0 + rpw, p.ratio);
+  const int parts = S * R, part = s * R + slot;
+  const int rpp = (p.ratio + parts - 1) / parts;
+  const int r0 = min(part * rpp, p.ratio), r1 = min(r0 + rpp, p.ratio);
   if (on) {
     for (int rb = r0; rb < r1; rb += kCompBatch) {
       const int nb = min(kCompBatch, r1 - rb);
@@ -92,43 +108,35 @@ __global__ void __launch_bounds__(kCompWarps * 32) compress_pool_kernel(Compress
       for (int k = 0; k < 4; ++k) fold_batch(r[k], sc[k], kv[k], nb);
     }
   }
+  // row slots of the warp -> slot 0 (every lane takes part: the shuffles are warp-wide)
+  for (int off = G; off < 32; off <<= 1) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const RunSum o{__shfl_xor_sync(0xffffffffu, r[k].m, off), __shfl_xor_sync(0xffffffffu, r[k].l, off),
+                     __shfl_xor_sync(0xffffffffu, r[k].a, off)};
+      r[k] = merge(r[k], o);
+    }
+  }
 
-  float out[4];
-  if (S > 1) {
-    sh_m[warp][lane] = make_float4(r[0].m, r[1].m, r[2].m, r[3].m);
-    sh_l[warp][lane] = make_float4(r[0].l, r[1].l, r[2].l, r[3].l);
-    sh_a[warp][lane] = make_float4(r[0].a, r[1].a, r[2].a, r[3].a);
+  if (S > 1 && slot == 0) {
+    sh_m[warp][g] = make_float4(r[0].m, r[1].m, r[2].m, r[3].m);
+    sh_l[warp][g] = make_float4(r[0].l, r[1].l, r[2].l, r[3].l);
+    sh_a[warp][g] = make_float4(r[0].a, r[1].a, r[2].a, r[3].a);
   }
   __syncthreads();  // every read of the state rows of this block is done
-  if (S > 1) {
-    if (s == 0 && on) {
-      const int w0 = warp;
-      float M[4], L[4] = {0.f, 0.f, 0.f, 0.f}, A[4] = {0.f, 0.f, 0.f, 0.f};
-      {
-        const float4 m0 = sh_m[w0][lane];
-        M[0] = m0.x; M[1] = m0.y; M[2] = m0.z; M[3] = m0.w;
-      }
-      for (int t = 1; t < S; ++t) {
-        const float4 mt = sh_m[w0 + t][lane];
-        M[0] = fmaxf(M[0], mt.x); M[1] = fmaxf(M[1], mt.y); M[2] = fmaxf(M[2], mt.z); M[3] = fmaxf(M[3], mt.w);
-      }
-      for (int t = 0; t < S; ++t) {
-        const float4 mt = sh_m[w0 + t][lane], lt = sh_l[w0 + t][lane], at = sh_a[w0 + t][lane];
-        const float f0 = expf(mt.x - M[0]), f1 = expf(mt.y - M[1]), f2 = expf(mt.z - M[2]), f3 = expf(mt.w - M[3]);
-        L[0] = fmaf(lt.x, f0, L[0]); A[0] = fmaf(at.x, f0, A[0]);
-        L[1] = fmaf(lt.y, f1, L[1]); A[1] = fmaf(at.y, f1, A[1]);
-        L[2] = fmaf(lt.z, f2, L[2]); A[2] = fmaf(at.z, f2, A[2]);
-        L[3] = fmaf(lt.w, f3, L[3]); A[3] = fmaf(at.w, f3, A[3]);
-      }
-#pragma unroll
-      for (int k = 0; k < 4; ++k) out[k] = A[k] / L[k];
+  const bool writer = s == 0 && slot == 0 && on;
+  if (S > 1 && writer) {
+    for (int t = 1; t < S; ++t) {
+      const float4 mt = sh_m[warp + t][g], lt = sh_l[warp + t][g], at = sh_a[warp + t][g];
+      r[0] = merge(r[0], RunSum{mt.x, lt.x, at.x});
+      r[1] = merge(r[1], RunSum{mt.y, lt.y, at.y});
+      r[2] = merge(r[2], RunSum{mt.z, lt.z, at.z});
+      r[3] = merge(r[3], RunSum{mt.w, lt.w, at.w});
     }
-  } else if (on) {
-#pragma unroll
-    for (int k = 0; k < 4; ++k) out[k] = r[k].a / r[k].l;
   }
-  if (s == 0 && on) {
-    const __half2 lo = __floats2half2_rn(out[0], out[1]), hi = __floats2half2_rn(out[2], out[3]);
+  if (writer) {
+    const __half2 lo = __floats2half2_rn(r[0].a / r[0].l, r[1].a / r[1].l);
+    const __half2 hi = __floats2half2_rn(r[2].a / r[2].l, r[3].a / r[3].l);
     uint2 v;
     v.x = *reinterpret_cast<const uint32_t *>(&lo);
     v.y = *reinterpret_cast<const uint32_t *>(&hi);
@@ -140,7 +148,7 @@ __global__ void __launch_bounds__(kCompWarps * 32) compress_pool_kernel(Compress
   // block that read the old state's rows of these dimensions (span 0) writes
   // them, after the barrier above.
   if (c == 0 && on && p.tail > 0) {
-    for (int t = s; t < p.tail; t += S) {
+    for (int t = part; t < p.tail; t += parts) {
       const long long src = (long long)(p.n_new - p.tail + t) * p.new_stride + d;
       const long long dst = (long long)t * p.state_stride + d;
       st4(p.state_kv + dst, ldg4(p.kv + src));
@@ -164,10 +172,13 @@ __global__ void compress_append_kernel(CompressParams p) {
   }
 }
 
-int compress_splits(int ratio) {
-  int s = 1;
-  while (s < kCompWarps && s * 16 <= ratio) s *= 2;
-  return s;
+// About four rows per part (one round of loads), at most 32 parts: row
+// slots first (narrower chunks, more blocks), then warps.
+void compress_shape(int ratio, int *splits, int *slots) {
+  int parts = 1;
+  while (parts < 32 && parts * 4 < ratio) parts *= 2;
+  *slots = parts < 4 ? parts : 4;
+  *splits = parts / *slots;
 }
 
 cudaError_t launch_compress(const CompressParams &p, cudaStream_t st) {

@@ -47,9 +47,10 @@ struct CompressParams {
   long long out_stride;
   int width, ratio, n_state, n_new, n_out, tail;
   int splits;  // warps that share one span: 1, 2, 4 or 8
-  int chunks;  // ceil(width / 128)
+  int slots;   // row slots per warp: 1, 2 or 4 (a chunk is 128 / slots dimensions)
+  int chunks;  // ceil(width / (128 / slots))
 };
-int compress_splits(int ratio);
+void compress_shape(int ratio, int *splits, int *slots);
 cudaError_t launch_compress(const CompressParams &p, cudaStream_t s);
 
 }  // namespace ds4a
