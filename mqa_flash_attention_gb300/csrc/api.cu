@@ -167,6 +167,8 @@ ds4a_status fill_params(AttnParams &p, const ds4a_layout *L, const ds4a_tensors 
   p.k_comp = X->k_comp;
   p.v_comp = X->v_comp;
   p.comp_row_stride = X->comp_row_stride;
+  p.q_ptr = static_cast<const uint8_t *>(X->q);
+  p.q_tok_bytes = X->q_tok_stride;
   p.T = L->T;
   p.q_pos0 = L->q_pos0;
   p.n_raw = L->n_raw;
@@ -637,6 +639,8 @@ ds4a_status ds4a_attn_decode_batch(int32_t n_seq, const ds4a_layout *shape, cons
       st = encode_batch_rows(&p.tm_v[1], X->v_comp, X->comp_rows, X->comp_row_stride, n_seq, X->comp_seq_stride);
     if (st != DS4A_OK) return st;
   }
+  p.q_ptr = static_cast<const uint8_t *>(X->q);
+  p.q_tok_bytes = X->q_seq_stride;
   p.T = n_seq;
   p.n_raw = X->raw_rows;
   p.n_comp = X->comp_rows;

@@ -245,6 +245,47 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
+// Q through the load/store path, for a CTA with a single work item (a short
+// decode: Q's latency is then paid once, at the head of the chain).  Loader
+// warps 9-11 copy the item's Q while thread 0 issues the K/V tiles, so Q does
+// not queue in front of them on the SM's TMA engine: 8.8 -> 8.5 us for a
+// 384-row decode split over 3 CTAs.  (In a long prefill, where each CTA runs
+// many items, it made no difference: there every TMA load takes ~2.7 us under
+// load whatever is queued with it.)  4096 chunks of 16 bytes: chunk (head h,
+// 16-byte column c of the 1024-byte head row) lands in box c/8 at row h,
+// column (c%8) ^ (h%8) (the 128-byte swizzle TMA applies).  Each thread's
+// copies arrive on q_full by themselves when they land.
+constexpr int kQCopyThreads = kLoaderThreads - 32;
+
+__device__ __forceinline__ bool q_by_lsu(const AttnParams &p, bool fp8) {
+  return !fp8 && !(p.mode == MODE_INDEXED && p.n_comp > 0) && p.q_ptr != nullptr &&
+         (long long)p.T * p.n_splits <= (long long)gridDim.x;
+}
+
+__device__ __noinline__ void q_copy_role(const AttnParams &p, uint32_t sbase, Misc &ms, int qtid) {
+  volatile int *abrt = &ms.abort_flag;
+  const uint32_t b_q_full = smem_u32(&ms.q_full), b_q_empty = smem_u32(&ms.q_empty);
+  const int n_items = p.T * p.n_splits;
+  const bool plan_reads_status = p.mode == MODE_MASK && p.status != nullptr;
+  if (plan_reads_status) grid_dependency_wait();
+  uint32_t n_item = 0;
+  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+    const ItemPlan ip = plan_item(p, item);
+    if (ip.j1 == ip.j0) continue;
+    if (n_item == 0 && !plan_reads_status) grid_dependency_wait();
+    if (!mbar_wait(b_q_empty, (n_item & 1) ^ 1, abrt, p.timeout_ns, p.err, SITE_Q_EMPTY)) break;
+    const uint8_t *q = p.q_ptr + (long long)ip.t * p.q_tok_bytes;
+#pragma unroll 4
+    for (int i = qtid; i < 4096; i += kQCopyThreads) {
+      const int h = i >> 6, c = i & 63;
+      cp_async16(sbase + kOffQ + (c >> 3) * kQBoxBytes + h * 128 + (((c & 7) ^ (h & 7)) << 4), q + 16 * i);
+    }
+    cp_async_arrive_noinc(b_q_full);
+    ++n_item;
+  }
+  cp_async_wait<0>();  // no copy may still be landing at exit
+}
+
 // The loader warps fill Q (once per work item) and every K/V ring stage, in
 // ring order.  Only fillers wait on a "stage free" barrier: a parity wait is
 // unambiguous only for a waiter at most one phase behind, and a filler cannot
@@ -265,7 +306,11 @@ template <bool FP8>
 __device__ __forceinline__ void loader_role(const AttnParams &p, uint32_t sbase, Misc &ms, int ltid) {
   volatile int *abrt = &ms.abort_flag;
   const bool group = p.mode == MODE_INDEXED && p.n_comp > 0;  // all loader threads needed
-  if (!group && ltid != 0) return;
+  const bool q_lsu = q_by_lsu(p, FP8);
+  if (!group && ltid != 0) {
+    if (q_lsu && ltid >= 32) q_copy_role(p, sbase, ms, ltid - 32);
+    return;
+  }
   const uint32_t b_q_full = smem_u32(&ms.q_full), b_q_empty = smem_u32(&ms.q_empty);
   Ring ring;
   uint32_t n_item = 0;
@@ -288,19 +333,19 @@ __device__ __forceinline__ void loader_role(const AttnParams &p, uint32_t sbase,
     if (ip.j1 == ip.j0) continue;
     if (n_item == 0 && !plan_reads_status) grid_dependency_wait();  // first global read follows
     bool bad = false;
-    if (ltid == 0) bad = !mbar_wait(b_q_empty, (n_item & 1) ^ 1, abrt, p.timeout_ns, p.err, SITE_Q_EMPTY);
+    if (ltid == 0 && !q_lsu) bad = !mbar_wait(b_q_empty, (n_item & 1) ^ 1, abrt, p.timeout_ns, p.err, SITE_Q_EMPTY);
     if (group) bad = bar_red_or(2, kLoaderThreads, bad);
     if (bad) {
       ok = false;
       break;
     }
-    if (ltid == 0) {
+    if (ltid == 0 && !q_lsu) {
       mbar_arrive_expect_tx(b_q_full, kQBytes);
 #pragma unroll 1
       for (int b = 0; b < 8; ++b)
         tma_load_3d(sbase + kOffQ + b * kQBoxBytes, &p.tm_q, b_q_full, 64 * b, 0, ip.t);
     }
-    q_issued = true;
+    q_issued = !q_lsu;
     q_par = n_item & 1;
     for (int j = ip.j0; j < ip.j1 && ok; ++j) {
       const Tile tl = ip.cur.next(p);
@@ -803,7 +848,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    mbar_init(smem_u32(&ms.q_full), 1);
+    mbar_init(smem_u32(&ms.q_full), q_by_lsu(p, FP8) ? kQCopyThreads : 1);
     mbar_init(smem_u32(&ms.q_empty), 1);
     const uint32_t fill_count = (p.mode == MODE_INDEXED && p.n_comp > 0) ? kLoaderThreads : 1;
     for (int s = 0; s < kStages; ++s) {

@@ -101,6 +101,8 @@ struct AttnParams {
   float2 *ws_ml;           // [T * n_splits][64] (m in log2 units, l)
   unsigned long long timeout_ns;
   unsigned int *err;       // device error word
+  const uint8_t *q_ptr;    // Q [T][64][512] fp16 (copied with cp.async when TMA is left to K/V)
+  long long q_tok_bytes;
 };
 
 }  // namespace ds4a
