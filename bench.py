@@ -352,40 +352,54 @@ def run_ours(args) -> None:
                 "peak_kind": f"{pk_kind} hbm_gbs (copy bandwidth)",
                 "algorithmic_bytes_per_launch": step_bytes}
 
-    # End to end through the API with host buffers: H2D inputs, call, D2H output, every step.
-    host_in = [torch.from_numpy(np.ascontiguousarray(a)).pin_memory() for a in (wl.q, wl.k_raw, wl.v_raw,
-                                                                                wl.k_comp, wl.v_comp)]
+    # End to end through the API with host buffers: every step copies its inputs from pinned host
+    # memory (Q, K/V raw, K/V compressed packed in one buffer, one transfer), calls the API on
+    # device views of that buffer and copies the output back.
+    arrays = [np.ascontiguousarray(a) for a in (wl.q, wl.k_raw, wl.v_raw, wl.k_comp, wl.v_comp)]
+    offs, total = [], 0
+    for a in arrays:
+        offs.append(total)
+        total += (a.nbytes + 255) // 256 * 256
+    host_pack = torch.empty(total, dtype=torch.uint8).pin_memory()
+    for a, o in zip(arrays, offs):
+        host_pack[o:o + a.nbytes].copy_(torch.from_numpy(a.view(np.uint8).reshape(-1)))
+    dev_pack = torch.empty(total, dtype=torch.uint8, device=dev)
+    views = [dev_pack[o:o + a.nbytes].view(torch.float16).view(a.shape) for a, o in zip(arrays, offs)]
     host_out = torch.empty(tuple(wl.q.shape), dtype=torch.float16).pin_memory()
-    dq, dkr, dvr, dkc, dvc, do = sets[0]
-    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    do = torch.empty_like(sets[0][5])
+    h2d = total
     d2h = host_out.numel() * host_out.element_size()
     Ke = min(K, 2000)
     with torch.cuda.stream(stream):
         for _ in range(3):
-            for d, h in zip((dq, dkr, dvr, dkc, dvc), host_in):
-                d.copy_(h, non_blocking=True)
-            ds4a.attn_decode(L, dq, dkr, dvr, dkc, dvc, n_splits=n_splits, workspace=ws, out=do, stream=stream)
+            dev_pack.copy_(host_pack, non_blocking=True)
+            ds4a.attn_decode(L, *views, n_splits=n_splits, workspace=ws, out=do, stream=stream)
             host_out.copy_(do, non_blocking=True)
     barrier()
     x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         x0.record(stream)
         for _ in range(Ke):
-            for d, h in zip((dq, dkr, dvr, dkc, dvc), host_in):
-                d.copy_(h, non_blocking=True)
-            ds4a.attn_decode(L, dq, dkr, dvr, dkc, dvc, n_splits=n_splits, workspace=ws, out=do, stream=stream)
+            dev_pack.copy_(host_pack, non_blocking=True)
+            ds4a.attn_decode(L, *views, n_splits=n_splits, workspace=ws, out=do, stream=stream)
             host_out.copy_(do, non_blocking=True)
         x1.record(stream)
     barrier()
+    e2e_check = host_out.clone()
     e2e_ms = max_over_ranks(x0.elapsed_time(x1), dev) / Ke
     e2e = {"value": round(step_bytes * world / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": Ke, "ms_per_step": round(e2e_ms, 5)}
 
-    # Correctness guard on the timed outputs (decode of set 0 vs the kernel's own eager result).
+    # Correctness guard on the timed outputs (decode of set 0 vs the kernel's own eager result), and
+    # the end-to-end output against the same call on the workload's own inputs.
     ref = torch.empty_like(sets[0][5])
     ds4a.attn_decode(L, *sets[0][:5], n_splits=n_splits, workspace=ws, out=ref, stream=stream)
+    ref_w = torch.empty_like(sets[0][5])
+    ds4a.attn_decode(L, *[torch.from_numpy(a).to(dev) for a in arrays], n_splits=n_splits, workspace=ws,
+                     out=ref_w, stream=stream)
     torch.cuda.synchronize()
-    if not torch.equal(ref, sets[0][5]) or ds4a.device_status() != ds4a.OK:
+    if not torch.equal(ref, sets[0][5]) or not torch.equal(ref_w.cpu(), e2e_check) or \
+            ds4a.device_status() != ds4a.OK:
         raise RuntimeError("timed outputs differ from an eager call or a device wait ran out")
 
     also = None
