@@ -92,8 +92,12 @@ __device__ __forceinline__ void find_bin(const uint32_t *hist, uint32_t need, ui
 template <bool CACHED>
 __global__ void __launch_bounds__(kTopkThreads) indexer_topk_kernel(const TopkParams p) {
   extern __shared__ uint32_t keys_s[];
+  // The first digit's histogram, then (once bin b0 is known) the compacted keys
+  // of that bin: one array, so that four CTAs fit on an SM.
   __shared__ uint32_t hist[4096];
-  __shared__ uint32_t surv[kTopkCompact];
+  __shared__ uint32_t hist2[1024];  // digits 2 and 3
+  static_assert(kTopkCompact <= 4096, "the survivors reuse the first histogram");
+  uint32_t *surv = hist;
   __shared__ uint32_t wsum[kTopkWarps];
   __shared__ uint32_t cnt[2][kTopkWarps];
   __shared__ uint32_t sh_bin[2];
@@ -124,6 +128,7 @@ __global__ void __launch_bounds__(kTopkThreads) indexer_topk_kernel(const TopkPa
   uint32_t need = (uint32_t)K - sh_bin[1];  // keys still to take from bin b0
   const uint32_t m = hist[b0];              // keys in bin b0
   const bool compact = m <= (uint32_t)kTopkCompact;
+  __syncthreads();  // every thread has read hist[b0] before the survivors overwrite it
   const uint32_t lt_mask = (1u << lane) - 1u;
   if (compact) {
     for (int base = 32 * warp; base < n; base += kTopkThreads) {
@@ -139,20 +144,20 @@ __global__ void __launch_bounds__(kTopkThreads) indexer_topk_kernel(const TopkPa
       }
     }
   }
-  __syncthreads();  // surv complete; every thread has read hist[b0]
+  __syncthreads();  // surv complete
   // digits 2 and 3: bits 19..10 and 9..0, over bin b0's keys
   uint32_t prefix = b0, kstar = 0;
   for (int d = 0; d < 2; ++d) {
     const int shift = d == 0 ? 10 : 0;
-    for (int i = tid; i < 1024; i += kTopkThreads) hist[i] = 0u;
+    for (int i = tid; i < 1024; i += kTopkThreads) hist2[i] = 0u;
     __syncthreads();
     const int nsrc = compact ? (int)m : n;
     for (int i = tid; i < nsrc; i += kTopkThreads) {
       const uint32_t k = compact ? surv[i] : key_at(i);
-      if ((k >> (shift + 10)) == prefix) atomicAdd(&hist[(k >> shift) & 1023u], 1u);
+      if ((k >> (shift + 10)) == prefix) atomicAdd(&hist2[(k >> shift) & 1023u], 1u);
     }
     __syncthreads();
-    find_bin<1024>(hist, need, sh_bin, wsum, tid);
+    find_bin<1024>(hist2, need, sh_bin, wsum, tid);
     prefix = (prefix << 10) | sh_bin[0];
     need -= sh_bin[1];
   }
