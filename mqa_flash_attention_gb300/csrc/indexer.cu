@@ -44,14 +44,18 @@ __device__ __forceinline__ uint32_t score_key(float x) {
 // One CTA per token.  Exact radix select on the score keys in three digits of
 // 12, 10 and 10 bits (the first spans sign, exponent and 3 mantissa bits, so
 // clustered scores spread over many bins and the shared atomics rarely
-// collide).  After the first digit only the keys in the bin where the count
-// of larger keys reaches top_k matter; they are compacted (warp-aggregated
-// appends) and the two other digits run over them alone.  That gives K* (the
-// top_k-th largest key) and how many keys equal to K* are taken.  Then every
-// row with key > K* is taken, and the first rows with key == K* (lower index
-// first) up to top_k: each warp owns a contiguous chunk of rows, one block
-// scan gives its offset and its share of the ties.
-constexpr int kTopkCompact = 4096;  // keys of the crossing bin kept for the last two digits
+// collide).  The first pass histograms the first digit; it names the bin b0
+// where the count of larger keys reaches top_k.  The second pass walks each
+// warp's contiguous chunk of rows, counts the keys of larger bins (all of
+// them are taken) and compacts bin b0's keys with their row numbers.  The
+// other two digits run over those survivors alone and give K* (the top_k-th
+// largest key) and how many keys equal to K* are taken; the survivors' own
+// K* comparisons finish each chunk's counts.  A last pass in row order takes
+// every row with key > K* and the first rows with key == K* (lower index
+// first) up to top_k, from each chunk's offset and share of the ties.  When
+// bin b0 is too large to compact, the last two digits and the counts run over
+// all keys instead.
+constexpr int kTopkCompact = 2048;  // (key, row) pairs of the crossing bin kept for the last two digits
 
 // Block-wide: the bin (scanning from the top) where the count of keys in
 // larger bins first reaches `need`; returns it and that count.
@@ -92,12 +96,12 @@ __device__ __forceinline__ void find_bin(const uint32_t *hist, uint32_t need, ui
 template <bool CACHED>
 __global__ void __launch_bounds__(kTopkThreads) indexer_topk_kernel(const TopkParams p) {
   extern __shared__ uint32_t keys_s[];
-  // The first digit's histogram, then (once bin b0 is known) the compacted keys
-  // of that bin: one array, so that four CTAs fit on an SM.
-  __shared__ uint32_t hist[4096];
+  // The first digit's histogram, then (once bin b0 is known) the compacted
+  // (key, row) pairs of that bin: one array, so that four CTAs fit on an SM.
+  __shared__ __align__(16) uint32_t hist[4096];
   __shared__ uint32_t hist2[1024];  // digits 2 and 3
-  static_assert(kTopkCompact <= 4096, "the survivors reuse the first histogram");
-  uint32_t *surv = hist;
+  static_assert(2 * kTopkCompact <= 4096, "the survivors reuse the first histogram");
+  uint2 *surv = reinterpret_cast<uint2 *>(hist);
   __shared__ uint32_t wsum[kTopkWarps];
   __shared__ uint32_t cnt[2][kTopkWarps];
   __shared__ uint32_t sh_bin[2];
@@ -114,9 +118,13 @@ __global__ void __launch_bounds__(kTopkThreads) indexer_topk_kernel(const TopkPa
   }
   auto key_at = [&](int i) -> uint32_t { return CACHED ? keys_s[i] : score_key(__ldg(row + i)); };
   for (int i = tid; i < 4096; i += kTopkThreads) hist[i] = 0u;
+  if (tid < kTopkWarps) {
+    cnt[0][tid] = 0u;
+    cnt[1][tid] = 0u;
+  }
   if (tid == 0) sh_count = 0;
   __syncthreads();
-  // digit 1: bits 31..20
+  // pass 1, digit 1: bits 31..20
   for (int i = tid; i < n; i += kTopkThreads) {
     const uint32_t k = score_key(__ldg(row + i));
     if (CACHED) keys_s[i] = k;
@@ -130,30 +138,38 @@ __global__ void __launch_bounds__(kTopkThreads) indexer_topk_kernel(const TopkPa
   const bool compact = m <= (uint32_t)kTopkCompact;
   __syncthreads();  // every thread has read hist[b0] before the survivors overwrite it
   const uint32_t lt_mask = (1u << lane) - 1u;
+  // Each warp owns rows [r0, r1), a multiple of 32 long.
+  const int chunk = ((n + kTopkWarps - 1) / kTopkWarps + 31) & ~31;
+  const int r0 = min(n, warp * chunk), r1 = min(n, r0 + chunk);
+  // pass 2: keys of larger bins counted per chunk, bin b0 compacted with its rows
   if (compact) {
-    for (int base = 32 * warp; base < n; base += kTopkThreads) {
+    uint32_t c_hi = 0;
+    for (int base = r0; base < r1; base += 32) {
       const int i = base + lane;
-      const uint32_t k = i < n ? key_at(i) : 0u;
-      const bool hit = i < n && (k >> 20) == b0;
+      const uint32_t k = i < r1 ? key_at(i) : 0u;
+      const uint32_t bin = k >> 20;
+      c_hi += __popc(__ballot_sync(0xffffffffu, i < r1 && bin > b0));
+      const bool hit = i < r1 && bin == b0;
       const uint32_t bal = __ballot_sync(0xffffffffu, hit);
       if (bal != 0u) {
         uint32_t off = 0;
         if (lane == 0) off = atomicAdd(&sh_count, (uint32_t)__popc(bal));
         off = __shfl_sync(0xffffffffu, off, 0);
-        if (hit) surv[off + __popc(bal & lt_mask)] = k;
+        if (hit) surv[off + __popc(bal & lt_mask)] = make_uint2(k, (uint32_t)i);
       }
     }
+    if (lane == 0) cnt[0][warp] = c_hi;
   }
-  __syncthreads();  // surv complete
+  __syncthreads();  // surv and the larger-bin counts complete
   // digits 2 and 3: bits 19..10 and 9..0, over bin b0's keys
-  uint32_t prefix = b0, kstar = 0;
+  uint32_t prefix = b0;
   for (int d = 0; d < 2; ++d) {
     const int shift = d == 0 ? 10 : 0;
     for (int i = tid; i < 1024; i += kTopkThreads) hist2[i] = 0u;
     __syncthreads();
     const int nsrc = compact ? (int)m : n;
     for (int i = tid; i < nsrc; i += kTopkThreads) {
-      const uint32_t k = compact ? surv[i] : key_at(i);
+      const uint32_t k = compact ? surv[i].x : key_at(i);
       if ((k >> (shift + 10)) == prefix) atomicAdd(&hist2[(k >> shift) & 1023u], 1u);
     }
     __syncthreads();
@@ -161,22 +177,30 @@ __global__ void __launch_bounds__(kTopkThreads) indexer_topk_kernel(const TopkPa
     prefix = (prefix << 10) | sh_bin[0];
     need -= sh_bin[1];
   }
-  kstar = prefix;
-  // Selection in row order.
-  const int chunk = ((n + kTopkWarps - 1) / kTopkWarps + 31) & ~31;
-  const int r0 = min(n, warp * chunk), r1 = min(n, r0 + chunk);
-  uint32_t c_gt = 0, c_eq = 0;
-  for (int base = r0; base < r1; base += 32) {
-    const int i = base + lane;
-    const uint32_t k = i < r1 ? key_at(i) : 0u;
-    c_gt += __popc(__ballot_sync(0xffffffffu, i < r1 && k > kstar));
-    c_eq += __popc(__ballot_sync(0xffffffffu, i < r1 && k == kstar));
-  }
-  if (lane == 0) {
-    cnt[0][warp] = c_gt;
-    cnt[1][warp] = c_eq;
+  const uint32_t kstar = prefix;
+  // Per chunk: keys > K* (cnt[0]) and keys == K* (cnt[1]).
+  if (compact) {
+    for (int i = tid; i < (int)m; i += kTopkThreads) {
+      const uint2 e = surv[i];
+      const int w = (int)e.y / chunk;
+      if (e.x > kstar) atomicAdd(&cnt[0][w], 1u);
+      else if (e.x == kstar) atomicAdd(&cnt[1][w], 1u);
+    }
+  } else {
+    uint32_t c_gt = 0, c_eq = 0;
+    for (int base = r0; base < r1; base += 32) {
+      const int i = base + lane;
+      const uint32_t k = i < r1 ? key_at(i) : 0u;
+      c_gt += __popc(__ballot_sync(0xffffffffu, i < r1 && k > kstar));
+      c_eq += __popc(__ballot_sync(0xffffffffu, i < r1 && k == kstar));
+    }
+    if (lane == 0) {
+      cnt[0][warp] = c_gt;
+      cnt[1][warp] = c_eq;
+    }
   }
   __syncthreads();
+  // pass 3: selection in row order
   uint32_t eq_run = 0, sel_run = 0;
   for (int w = 0; w < warp; ++w) {
     const uint32_t g = cnt[0][w], e = cnt[1][w];
