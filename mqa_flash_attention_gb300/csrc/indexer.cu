@@ -292,6 +292,23 @@ __device__ __forceinline__ ScoreItem score_item(const ScoreParams &p, int item, 
 // Scores of one tile for the thread's row c and half hf of the 256 columns
 // (tokens G/2*hf ..): w_s holds w[t][h] * |scale| (or * scale without the
 // max), so each TMEM value costs one max and one fma (one fma without max).
+// Packed pair of fp32 lanes (fma.rn.f32x2: two fmas per instruction).
+__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ float f2_sum(uint64_t r) {
+  float a, b;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+  return a + b;
+}
+
 template <int NH, bool RELU, bool NEG>
 __device__ __forceinline__ void score_tile(const ScoreParams &p, const ScoreItem &it, const float *w_s,
                                            uint32_t tcol, int hf, int c, long long pos1) {
@@ -311,11 +328,24 @@ __device__ __forceinline__ void score_tile(const ScoreParams &p, const ScoreItem
 #pragma unroll
       for (int u = 0; u < TPC; ++u) {
         float sum = 0.f;
-#pragma unroll
-        for (int h = 0; h < HW; ++h) {
-          float x = v[32 * jj + u * HW + h];
+        if (HW == 1) {
+          float x = v[32 * jj + u];
           if (RELU) x = fmaxf(NEG ? -x : x, 0.f);
-          sum = fmaf(ww[u * HW + h], x, sum);
+          sum = ww[u] * x;
+        } else {
+          // two heads per packed fma: even and odd heads in separate partial sums
+          uint64_t s2 = 0;
+#pragma unroll
+          for (int h = 0; h < HW; h += 2) {
+            float x0 = v[32 * jj + u * HW + h], x1 = v[32 * jj + u * HW + h + 1];
+            if (RELU) {
+              x0 = fmaxf(NEG ? -x0 : x0, 0.f);
+              x1 = fmaxf(NEG ? -x1 : x1, 0.f);
+            }
+            const float2 w2 = *reinterpret_cast<const float2 *>(ww + u * HW + h);
+            s2 = f2_fma(f2_pack(w2.x, w2.y), f2_pack(x0, x1), s2);
+          }
+          sum = f2_sum(s2);
         }
         if (NH >= 32) {
           acc += sum;
