@@ -259,6 +259,36 @@ def attn_decode(layout, q, k_raw, v_raw, k_comp=None, v_comp=None, *, n_splits=0
     return (out, lse) if (want_lse or lse is not None) else out
 
 
+class PreparedCall:
+    """A library call whose ctypes arguments were built once.  Each ``call()``
+    goes through the C ABI with the same tensors, layout and stream; the
+    tensors are kept alive by the object.  For loops that call the library
+    every step on fixed buffers, where building the arguments again would cost
+    more host time than the call itself."""
+
+    def __init__(self, fn, name, args, keep):
+        self._fn, self._name, self._args, self._keep = fn, name, args, keep
+
+    def __call__(self) -> None:
+        st = self._fn(*self._args)
+        if st != OK:
+            raise Ds4aError(st, self._name)
+
+
+def prepare_decode(layout, q, k_raw, v_raw, k_comp=None, v_comp=None, *, n_splits=0, workspace, out, lse=None,
+                   stream=None) -> PreparedCall:
+    """:func:`attn_decode` on fixed buffers, as a :class:`PreparedCall`."""
+    L = make_layout(layout)
+    X = _tensors(q, k_raw, v_raw, k_comp, v_comp, out, lse)
+    need = decode_workspace_bytes(L, n_splits)
+    nbytes = workspace.numel() * workspace.element_size()
+    if nbytes < need:
+        raise ValueError(f"workspace of {nbytes} bytes, {need} needed")
+    args = (ctypes.byref(L), ctypes.byref(X), int(n_splits), _ptr(workspace), nbytes, _stream(stream))
+    return PreparedCall(lib().ds4a_attn_decode, "ds4a_attn_decode", args,
+                        (L, X, q, k_raw, v_raw, k_comp, v_comp, workspace, out, lse, stream))
+
+
 def attn_decode_fp8(layout, q, k_raw, v_raw, k_codes, k_scale, v_codes, v_scale, *, n_splits=0, workspace=None,
                     out=None, lse=None, want_lse=False, stream=None):
     """:func:`attn_decode` with E4M3 compressed rows (codes uint8 [n, 512] and

@@ -440,3 +440,20 @@ def test_decode_partials_then_merge(torch, ds4a):
     want, wlse = oracle_out(wl)
     assert_close(host(out), want, "partials + merge")
     assert_lse_close(host(lse), wlse, "partials + merge lse")
+
+
+def test_prepared_decode_equals_call(torch, ds4a):
+    """The prepared call (arguments built once, the C entry point called each
+    time) gives the same bits as the regular binding, call after call."""
+    wl = W.decode_r128_32k()
+    d = {k: dev(torch, getattr(wl, k)) for k in ("q", "k_raw", "v_raw", "k_comp", "v_comp")}
+    ref = ds4a.attn_decode(wl.layout, d["q"], d["k_raw"], d["v_raw"], d["k_comp"], d["v_comp"])
+    ws = torch.empty(ds4a.decode_workspace_bytes(wl.layout), dtype=torch.uint8, device="cuda")
+    out = torch.full_like(ref, 7.0)
+    call = ds4a.prepare_decode(wl.layout, d["q"], d["k_raw"], d["v_raw"], d["k_comp"], d["v_comp"], workspace=ws,
+                               out=out)
+    for _ in range(3):
+        out.fill_(7.0)
+        call()
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref)
