@@ -786,10 +786,10 @@ def run_reference(args) -> None:
     step_bytes = decode_bytes(L)
     probe = oracle_leg("decode_r128_32k", 0.5)
     per_call = probe["seconds_per_call"]
-    budget = 90.0
+    max_seconds = 90.0  # the whole reference run stays within a few minutes
     heads = None
-    if (args.steps + args.warmup) * per_call > budget:
-        heads = max(1, min(64, int(64 * budget / ((args.steps + args.warmup) * per_call))))
+    if (args.steps + args.warmup) * per_call > max_seconds:
+        heads = max(1, min(64, int(64 * max_seconds / ((args.steps + args.warmup) * per_call))))
     import numpy as np  # noqa: F401
     import oracle
     q = wl.q if heads is None else np.ascontiguousarray(wl.q[:, :heads])

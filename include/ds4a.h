@@ -83,7 +83,7 @@ typedef struct CUstream_st *ds4a_stream_t;
 typedef enum {
   DS4A_OK = 0,
   DS4A_ERR_INVALID_ARG = 1, /* an argument breaks the contract; nothing launched */
-  DS4A_ERR_UNSUPPORTED = 2, /* valid request this build does not serve (e.g. no sm_103a device) */
+  DS4A_ERR_UNSUPPORTED = 2, /* valid request the library does not serve (e.g. no sm_103a device) */
   DS4A_ERR_WORKSPACE = 3,   /* workspace missing or smaller than ds4a_attn_decode_workspace_size() */
   DS4A_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed (launch, tensor-map encode, ...) */
   DS4A_ERR_TIMEOUT = 5      /* a bounded device wait ran out (reported by ds4a_device_status) */
