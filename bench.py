@@ -617,6 +617,22 @@ def run_also(torch, ds4a, W, dev, stream, pk, pk_kind):
                 "tflops": round(fl / sec / 1e12, 1), "frac_tensor": round(fl / sec / 1e12 / pk["bf16_tflops"], 4),
                 "algorithmic_flops": fl})
     del sets
+    # long-decode sweep (config 5 at N = 1K, 8K, 64K): input sets rotate so every call reads HBM
+    for n_c in (1024, 8192, 65536):
+        wl = W.decode_long(n_c)
+        base = [up(a) for a in (wl.q, wl.k_raw, wl.v_raw, wl.k_comp, wl.v_comp)]
+        sb = sum(t.numel() * t.element_size() for t in base)
+        R = min(256, max(2, math.ceil(4 * L2_BYTES / sb)))
+        dsets = [[t.clone() for t in base] for _ in range(R)]
+        del base
+        o = torch.empty(wl.q.shape, dtype=torch.float16, device=dev)
+        ws = torch.empty(ds4a.decode_workspace_bytes(wl.layout), dtype=torch.uint8, device=dev)
+        sec = timed(lambda i: ds4a.attn_decode(wl.layout, *dsets[i % R], workspace=ws, out=o, stream=stream), R)
+        by = decode_bytes(wl.layout)
+        out.append({"workload": wl.name, "us_per_call": round(sec * 1e6, 2), "hbm_gbs": round(by / sec / 1e9, 1),
+                    "frac_hbm": round(by / sec / 1e9 / pk["hbm_gbs"], 4), "algorithmic_bytes": by,
+                    "rotating_input_sets": R})
+        del dsets, o, ws
     # long decode, 262144 compressed rows (537 MB of K/V > L2)
     wl = W.decode_long(262144)
     d = [up(a) for a in (wl.q, wl.k_raw, wl.v_raw, wl.k_comp, wl.v_comp)]
