@@ -204,6 +204,80 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float *_
     lse[(long long)t * 64 + h] = L > 0.f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
 }
 
+// Many splits (a long decode): one block per (token, head, 64-dim chunk), 512
+// blocks per token.  Warp w sums the splits w, w+8, w+16, ... over the chunk's
+// 64 dims (a float2 per lane, four loads in flight), and the eight warp sums
+// are added in shared memory: the per-thread chains are 1/8 as long and four
+// times as many blocks load at once as in combine_kernel.
+constexpr int kWideChunks = 8;        // 64-dim chunks per head
+constexpr int kWideMinSplits = 17;    // below this the one-dim-per-thread merge is as fast
+
+__global__ void __launch_bounds__(kCombineThreads) combine_wide_kernel(const float *__restrict__ ws_o,
+                                                                       const float2 *__restrict__ ws_ml,
+                                                                       int n_splits, __half *__restrict__ o,
+                                                                       long long o_tok_stride,
+                                                                       float *__restrict__ lse) {
+  __shared__ float w_s[kCombineMaxSplits];
+  __shared__ float red[kCombineThreads / 32];
+  __shared__ float2 part[kCombineThreads / 32][32];
+  grid_dependency_wait();  // the partials come from the previous kernel
+  grid_launch_dependents();
+  const int chunk = blockIdx.x, h = blockIdx.y, t = blockIdx.z;
+  const long long base = (long long)t * n_splits;
+  float mx = -INFINITY;
+  for (int s = threadIdx.x; s < n_splits; s += kCombineThreads) mx = fmaxf(mx, ws_ml[(base + s) * 64 + h].x);
+  const float M = block_reduce(mx, true, red);
+  float lsum = 0.f;
+  for (int s = threadIdx.x; s < n_splits; s += kCombineThreads) {
+    const float2 ml = ws_ml[(base + s) * 64 + h];
+    const float wgt = (ml.x == -INFINITY || M == -INFINITY) ? 0.f : exp2f(ml.x - M);
+    w_s[s] = wgt;
+    lsum += wgt * ml.y;
+  }
+  const float L = block_reduce(lsum, false, red);  // also orders the w_s writes before the reads below
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int kW = kCombineThreads / 32;
+  const int d = 64 * chunk + 2 * lane;
+  const float *src = ws_o + (base * 64 + h) * 512 + d;
+  const long long step = 64LL * 512;
+  // A split without visible rows left its partial unwritten (any bits): its
+  // weight is 0 and the select drops the value.
+  float2 acc = make_float2(0.f, 0.f);
+  int s = warp;
+  for (; s + 3 * kW < n_splits; s += 4 * kW) {
+    float2 x[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) x[i] = __ldg(reinterpret_cast<const float2 *>(src + (long long)(s + i * kW) * step));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float wgt = w_s[s + i * kW];
+      acc.x += wgt != 0.f ? wgt * x[i].x : 0.f;
+      acc.y += wgt != 0.f ? wgt * x[i].y : 0.f;
+    }
+  }
+  for (; s < n_splits; s += kW) {
+    const float2 x = __ldg(reinterpret_cast<const float2 *>(src + (long long)s * step));
+    const float wgt = w_s[s];
+    acc.x += wgt != 0.f ? wgt * x.x : 0.f;
+    acc.y += wgt != 0.f ? wgt * x.y : 0.f;
+  }
+  part[warp][lane] = acc;
+  __syncthreads();
+  if (warp == 0) {
+    float2 sum = part[0][lane];
+#pragma unroll
+    for (int w = 1; w < kW; ++w) {
+      sum.x += part[w][lane].x;
+      sum.y += part[w][lane].y;
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    *reinterpret_cast<__half2 *>(o + (long long)t * o_tok_stride + h * 512 + d) =
+        __floats2half2_rn(sum.x * inv, sum.y * inv);
+  }
+  if (lse != nullptr && chunk == 0 && threadIdx.x == 0)
+    lse[(long long)t * 64 + h] = L > 0.f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
+}
+
 cudaError_t launch_combine(const float *ws_o, const float2 *ws_ml, int n_splits, int T, __half *o,
                            long long o_tok_stride, float *lse, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
@@ -211,7 +285,8 @@ cudaError_t launch_combine(const float *ws_o, const float2 *ws_ml, int n_splits,
   // Programmatic dependent launch: the merge is scheduled while the partial
   // kernel runs and waits for it inside (griddepcontrol.wait).
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2, 64, T);
+  const bool wide = n_splits >= kWideMinSplits;
+  cfg.gridDim = dim3(wide ? kWideChunks : 2, 64, T);
   cfg.blockDim = dim3(kCombineThreads);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -219,6 +294,7 @@ cudaError_t launch_combine(const float *ws_o, const float2 *ws_ml, int n_splits,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (wide) return cudaLaunchKernelEx(&cfg, combine_wide_kernel, ws_o, ws_ml, n_splits, o, o_tok_stride, lse);
   return cudaLaunchKernelEx(&cfg, combine_kernel, ws_o, ws_ml, n_splits, o, o_tok_stride, lse);
 }
 
