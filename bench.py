@@ -213,12 +213,17 @@ def run_oracle_all_cores(workload: str, seconds: float) -> dict:
 # ------------------------------------------------------------------ host copies
 
 def cuda_runtime():
-    """The toolkit's CUDA runtime library through ctypes, or None."""
+    """The toolkit's CUDA runtime library through ctypes, or None.  Its current
+    device is set to torch's (this copy of the runtime keeps its own)."""
+    import torch
     for name in ("libcudart.so.13", "/usr/local/cuda/lib64/libcudart.so.13", "/usr/local/cuda/lib64/libcudart.so"):
         try:
-            return ctypes.CDLL(name)
+            rt = ctypes.CDLL(name)
         except OSError:
-            pass
+            continue
+        if rt.cudaSetDevice(ctypes.c_int(torch.cuda.current_device())) != 0:
+            return None
+        return rt
     return None
 
 
