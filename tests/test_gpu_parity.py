@@ -341,6 +341,24 @@ def test_decode_several_tokens(torch, ds4a):
         assert_close(host(o), want, f"decode T=3 splits={s}")
 
 
+@pytest.mark.parametrize("splits", [5, 17, 40])
+def test_decode_empty_splits_ignore_workspace_contents(torch, ds4a, splits):
+    """More splits than tiles (two per token here): the extra splits see no
+    row and never write their partials, and the merge (the one-dim-per-thread
+    form below 17 splits, the warp-split form from 17) must ignore whatever the
+    workspace holds there, NaN in this test."""
+    L = make_layout(T=3, q_pos0=5000, n_raw=200, raw_pos0=4850, n_comp=39, ratio=128)
+    wl = W.draw("dec_empty", 68, L)
+    d = upload(torch, wl)
+    want, wlse = oracle_out(wl)
+    ws = torch.full((ds4a.decode_workspace_bytes(L, splits) // 4,), float("nan"), dtype=torch.float32,
+                    device="cuda")
+    o, lse = ds4a.attn_decode(L, d["q"], d["k_raw"], d["v_raw"], d["k_comp"], d["v_comp"], n_splits=splits,
+                              workspace=ws, want_lse=True)
+    assert_close(host(o), want, f"decode T=3 splits={splits}")
+    assert_lse_close(host(lse), wlse, f"decode T=3 splits={splits} lse")
+
+
 def test_decode_batch_matches_oracle(torch, ds4a):
     """Seven sequences, each with its own position, row counts and K/V rows, in
     one batched launch; each equals the oracle on its own layout."""
