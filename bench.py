@@ -598,140 +598,166 @@ def run_also(torch, ds4a, W, dev, stream, pk, pk_kind):
     def up(a):
         return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
 
-    # prefill, raw-only, T = 2048 (two input sets alternate: each is ~270 MB > L2)
-    wl = W.prefill_raw_2048()
-    sets = [[up(wl.q), up(wl.k_raw), up(wl.v_raw), torch.empty(wl.q.shape, dtype=torch.float16, device=dev)]
-            for _ in range(2)]
-    sec = timed(lambda i: ds4a.attn_prefill(wl.layout, sets[i % 2][0], sets[i % 2][1], sets[i % 2][2],
-                                            out=sets[i % 2][3], stream=stream), 10)
-    fl = attn_flops(wl.layout)
-    by = 2 * wl.q.nbytes + wl.k_raw.nbytes + wl.v_raw.nbytes
-    out.append({"workload": wl.name, "us_per_call": round(sec * 1e6, 2),
-                "tflops": round(fl / sec / 1e12, 1), "frac_tensor": round(fl / sec / 1e12 / pk["bf16_tflops"], 4),
-                "hbm_gbs": round(by / sec / 1e9, 1), "frac_hbm": round(by / sec / 1e9 / pk["hbm_gbs"], 4),
-                "algorithmic_flops": fl, "algorithmic_bytes": by})
-    del sets
-    # indexed ratio-4, T = 2048, top-512
-    wl = W.indexed_r4_2048()
-    sets = [[up(wl.q), up(wl.k_raw), up(wl.v_raw), up(wl.k_comp), up(wl.v_comp), up(wl.idx),
-             torch.empty(wl.q.shape, dtype=torch.float16, device=dev)] for _ in range(2)]
-    sec = timed(lambda i: ds4a.attn_indexed(wl.layout, *sets[i % 2][:6], out=sets[i % 2][6], stream=stream), 6)
-    rows = sum(min(wl.layout["n_raw"], 128) + int((wl.idx[t] >= 0).sum()) for t in range(wl.layout["T"]))
-    fl = attn_flops(wl.layout, rows)
-    out.append({"workload": wl.name, "us_per_call": round(sec * 1e6, 2),
-                "tflops": round(fl / sec / 1e12, 1), "frac_tensor": round(fl / sec / 1e12 / pk["bf16_tflops"], 4),
-                "algorithmic_flops": fl})
-    del sets
-    # long-decode sweep (config 5 at N = 1K, 8K, 64K): input sets rotate so every call reads HBM
-    for n_c in (1024, 8192, 65536):
-        wl = W.decode_long(n_c)
-        base = [up(a) for a in (wl.q, wl.k_raw, wl.v_raw, wl.k_comp, wl.v_comp)]
-        sb = sum(t.numel() * t.element_size() for t in base)
-        R = min(256, max(2, math.ceil(4 * L2_BYTES / sb)))
-        dsets = [[t.clone() for t in base] for _ in range(R)]
-        del base
+    def sec_prefill():
+        # prefill, raw-only, T = 2048 (two input sets alternate: each is ~270 MB > L2)
+        wl = W.prefill_raw_2048()
+        sets = [[up(wl.q), up(wl.k_raw), up(wl.v_raw), torch.empty(wl.q.shape, dtype=torch.float16, device=dev)]
+                for _ in range(2)]
+        sec = timed(lambda i: ds4a.attn_prefill(wl.layout, sets[i % 2][0], sets[i % 2][1], sets[i % 2][2],
+                                                out=sets[i % 2][3], stream=stream), 10)
+        fl = attn_flops(wl.layout)
+        by = 2 * wl.q.nbytes + wl.k_raw.nbytes + wl.v_raw.nbytes
+        out.append({"workload": wl.name, "us_per_call": round(sec * 1e6, 2),
+                    "tflops": round(fl / sec / 1e12, 1), "frac_tensor": round(fl / sec / 1e12 / pk["bf16_tflops"], 4),
+                    "hbm_gbs": round(by / sec / 1e9, 1), "frac_hbm": round(by / sec / 1e9 / pk["hbm_gbs"], 4),
+                    "algorithmic_flops": fl, "algorithmic_bytes": by})
+        del sets
+
+    def sec_indexed():
+        # indexed ratio-4, T = 2048, top-512
+        wl = W.indexed_r4_2048()
+        sets = [[up(wl.q), up(wl.k_raw), up(wl.v_raw), up(wl.k_comp), up(wl.v_comp), up(wl.idx),
+                 torch.empty(wl.q.shape, dtype=torch.float16, device=dev)] for _ in range(2)]
+        sec = timed(lambda i: ds4a.attn_indexed(wl.layout, *sets[i % 2][:6], out=sets[i % 2][6], stream=stream), 6)
+        rows = sum(min(wl.layout["n_raw"], 128) + int((wl.idx[t] >= 0).sum()) for t in range(wl.layout["T"]))
+        fl = attn_flops(wl.layout, rows)
+        out.append({"workload": wl.name, "us_per_call": round(sec * 1e6, 2),
+                    "tflops": round(fl / sec / 1e12, 1), "frac_tensor": round(fl / sec / 1e12 / pk["bf16_tflops"], 4),
+                    "algorithmic_flops": fl})
+        del sets
+
+    def sec_decode_sweep():
+        # long-decode sweep (config 5 at N = 1K, 8K, 64K): input sets rotate so every call reads HBM
+        for n_c in (1024, 8192, 65536):
+            wl = W.decode_long(n_c)
+            base = [up(a) for a in (wl.q, wl.k_raw, wl.v_raw, wl.k_comp, wl.v_comp)]
+            sb = sum(t.numel() * t.element_size() for t in base)
+            R = min(256, max(2, math.ceil(4 * L2_BYTES / sb)))
+            dsets = [[t.clone() for t in base] for _ in range(R)]
+            del base
+            o = torch.empty(wl.q.shape, dtype=torch.float16, device=dev)
+            ws = torch.empty(ds4a.decode_workspace_bytes(wl.layout), dtype=torch.uint8, device=dev)
+            sec = timed(lambda i: ds4a.attn_decode(wl.layout, *dsets[i % R], workspace=ws, out=o, stream=stream), R)
+            by = decode_bytes(wl.layout)
+            out.append({"workload": wl.name, "us_per_call": round(sec * 1e6, 2), "hbm_gbs": round(by / sec / 1e9, 1),
+                        "frac_hbm": round(by / sec / 1e9 / pk["hbm_gbs"], 4), "algorithmic_bytes": by,
+                        "rotating_input_sets": R})
+            del dsets, o, ws
+
+    def sec_decode_256k_fp16_and_fp8():
+        # long decode, 262144 compressed rows (537 MB of K/V > L2)
+        wl = W.decode_long(262144)
+        d = [up(a) for a in (wl.q, wl.k_raw, wl.v_raw, wl.k_comp, wl.v_comp)]
         o = torch.empty(wl.q.shape, dtype=torch.float16, device=dev)
         ws = torch.empty(ds4a.decode_workspace_bytes(wl.layout), dtype=torch.uint8, device=dev)
-        sec = timed(lambda i: ds4a.attn_decode(wl.layout, *dsets[i % R], workspace=ws, out=o, stream=stream), R)
+        sec = timed(lambda i: ds4a.attn_decode(wl.layout, *d, workspace=ws, out=o, stream=stream), 10)
         by = decode_bytes(wl.layout)
         out.append({"workload": wl.name, "us_per_call": round(sec * 1e6, 2), "hbm_gbs": round(by / sec / 1e9, 1),
-                    "frac_hbm": round(by / sec / 1e9 / pk["hbm_gbs"], 4), "algorithmic_bytes": by,
-                    "rotating_input_sets": R})
-        del dsets, o, ws
-    # long decode, 262144 compressed rows (537 MB of K/V > L2)
-    wl = W.decode_long(262144)
-    d = [up(a) for a in (wl.q, wl.k_raw, wl.v_raw, wl.k_comp, wl.v_comp)]
-    o = torch.empty(wl.q.shape, dtype=torch.float16, device=dev)
-    ws = torch.empty(ds4a.decode_workspace_bytes(wl.layout), dtype=torch.uint8, device=dev)
-    sec = timed(lambda i: ds4a.attn_decode(wl.layout, *d, workspace=ws, out=o, stream=stream), 10)
-    by = decode_bytes(wl.layout)
-    out.append({"workload": wl.name, "us_per_call": round(sec * 1e6, 2), "hbm_gbs": round(by / sec / 1e9, 1),
-                "frac_hbm": round(by / sec / 1e9 / pk["hbm_gbs"], 4), "algorithmic_bytes": by})
-    # the same decode with E4M3 compressed rows (codes + one fp32 scale per row)
-    kc, ks = ds4a.quantize_kv_fp8(d[3], stream=stream)
-    vc, vs = ds4a.quantize_kv_fp8(d[4], stream=stream)
-    torch.cuda.synchronize()
-    sec8 = timed(lambda i: ds4a.attn_decode_fp8(wl.layout, d[0], d[1], d[2], kc, ks, vc, vs, workspace=ws, out=o,
-                                                stream=stream), 10)
-    n_c = wl.layout["n_comp"]
-    by8 = by - n_c * 2048 + n_c * (1024 + 8)
-    out.append({"workload": wl.name + "_fp8kv", "us_per_call": round(sec8 * 1e6, 2), "hbm_gbs": round(by8 / sec8 / 1e9, 1),
-                "frac_hbm": round(by8 / sec8 / 1e9 / pk["hbm_gbs"], 4), "algorithmic_bytes": by8,
-                "speedup_vs_fp16": round(sec / sec8, 2)})
-    del d, o, ws, kc, ks, vc, vs
-    # batched decode: 64 sequences, each the ratio-128 32K geometry (128 raw + 256 compressed
-    # rows) with its own K/V rows; three input sets rotate (3 x 58.7 MB > L2)
-    wl = W.decode_r128_32k()
-    B, G = 64, 3
-    L = wl.layout
-    geo = torch.tensor([[L["q_pos0"], L["n_raw"], L["raw_pos0"], L["n_comp"]]] * B, dtype=torch.int32, device=dev)
-    bsets = []
-    for gi in range(G):
-        gen = torch.Generator(device=dev).manual_seed(90 + gi)
-        mk = lambda n: torch.randn((B, n, 512), generator=gen, device=dev).to(torch.float16)  # noqa: E731
-        bsets.append([torch.randn((B, 64, 512), generator=gen, device=dev).to(torch.float16),
-                      mk(L["n_raw"]), mk(L["n_raw"]), mk(L["n_comp"]), mk(L["n_comp"]),
-                      torch.empty((B, 64, 512), dtype=torch.float16, device=dev)])
-    b_splits = ds4a.lib().ds4a_attn_decode_batch_default_splits(B, ctypes.byref(ds4a.make_layout(L)), L["n_raw"],
-                                                               L["n_comp"])
-    bws = torch.empty(max(256, ds4a.lib().ds4a_attn_decode_batch_workspace_size(B, b_splits)), dtype=torch.uint8,
-                      device=dev)
-    sec = timed(lambda i: ds4a.attn_decode_batch(L, geo, *bsets[i % G][:5], n_splits=b_splits, workspace=bws,
-                                                 out=bsets[i % G][5], stream=stream), 30)
-    by = B * decode_bytes(L)
-    out.append({"workload": "decode_batch64_ratio128_ctx32768", "us_per_call": round(sec * 1e6, 2),
-                "hbm_gbs": round(by / sec / 1e9, 1), "frac_hbm": round(by / sec / 1e9 / pk["hbm_gbs"], 4),
-                "algorithmic_bytes": by, "n_splits": b_splits,
-                "note": "64 sequences, each 128 raw + 256 compressed rows of its own"})
-    del bsets, bws, geo
-    # indexer of the ratio-4 layer: scores (64 heads x 128 dims, max(0, x)) and top-512
-    wx = W.indexer_r4_2048()
-    L = wx.layout
-    qx, kx, wx_w = up(wx.q_idx), up(wx.k_idx), up(wx.w)
-    sc = [torch.empty((L["T"], L["n_comp"]), dtype=torch.float32, device=dev) for _ in range(2)]
-    sec = timed(lambda i: ds4a.indexer_scores(L, qx, kx, wx_w, scale=wx.scale, relu=True, out=sc[i % 2],
-                                              stream=stream), 10)
-    n_cand = sum(min(L["n_comp"], (L["q_pos0"] + t + 1) // L["ratio"]) for t in range(L["T"]))
-    n_heads, head_dim = wx.q_idx.shape[1], wx.q_idx.shape[2]
-    fl = 2.0 * n_cand * n_heads * head_dim
-    out.append({"workload": wx.name + "_scores", "us_per_call": round(sec * 1e6, 2),
-                "tflops": round(fl / sec / 1e12, 1), "frac_tensor": round(fl / sec / 1e12 / pk["bf16_tflops"], 4),
-                "algorithmic_flops": fl, "shape": f"{n_heads} heads x {head_dim} dims, relu"})
-    ix_out = torch.empty((L["T"], wx.top_k), dtype=torch.int32, device=dev)
-    sec = timed(lambda i: ds4a.indexer_topk(L, sc[i % 2], wx.top_k, out=ix_out, stream=stream), 10)
-    by = 4 * n_cand + 4 * L["T"] * wx.top_k
-    out.append({"workload": wx.name + "_topk", "us_per_call": round(sec * 1e6, 2),
-                "gbs": round(by / sec / 1e9, 1), "algorithmic_bytes": by,
-                "note": "exact radix select over each token's candidate scores"})
-    # compressor, one 2048-token prefill chunk of 512-dim rows (fresh state) on a ratio-4 and a
-    # ratio-128 layer; 20 input sets rotate (20 x 8 MB > L2)
-    for ratio in (4, 128):
-        wc = W.compressor_prefill(ratio)
-        n, width = wc.kv.shape
-        G = 20
-        gen = torch.Generator(device=dev).manual_seed(95 + ratio)
-        csets = [(torch.randn((n, width), generator=gen, device=dev),
-                  2 * torch.randn((n, width), generator=gen, device=dev)) for _ in range(G)]
-        st_kv = torch.empty((ratio - 1, width), dtype=torch.float32, device=dev)
-        st_s = torch.empty((ratio - 1, width), dtype=torch.float32, device=dev)
-        c_out = torch.empty((n // ratio, width), dtype=torch.float16, device=dev)
-        sec = timed(lambda i: ds4a.compress_append(csets[i % G][0], csets[i % G][1], st_kv, st_s, 0, ratio,
-                                                   out=c_out, stream=stream), 40)
-        by = 8 * n * width + 2 * (n // ratio) * width
-        out.append({"workload": wc.name, "us_per_call": round(sec * 1e6, 2), "hbm_gbs": round(by / sec / 1e9, 1),
-                    "frac_hbm": round(by / sec / 1e9 / pk["hbm_gbs"], 4), "algorithmic_bytes": by,
-                    "note": "per-dimension softmax pooling of each ratio span, fp32 in, fp16 out"})
-        del csets
-    # compressor decode step at a ratio-128 boundary: 127 positions in the state, one new
-    st_kv = torch.randn((127, 512), device=dev)
-    st_s = torch.randn((127, 512), device=dev)
-    one = [(torch.randn((1, 512), device=dev), torch.randn((1, 512), device=dev)) for _ in range(2)]
-    c_out = torch.empty((1, 512), dtype=torch.float16, device=dev)
-    sec = timed(lambda i: ds4a.compress_append(one[i % 2][0], one[i % 2][1], st_kv, st_s, 127, 128, out=c_out,
-                                               stream=stream), 40)
-    out.append({"workload": "compressor_ratio128_decode_boundary_w512", "us_per_call": round(sec * 1e6, 2),
-                "note": "one token completes a 128-position span (state in L2): latency"})
-    del st_kv, st_s, one
+                    "frac_hbm": round(by / sec / 1e9 / pk["hbm_gbs"], 4), "algorithmic_bytes": by})
+        # the same decode with E4M3 compressed rows (codes + one fp32 scale per row)
+        kc, ks = ds4a.quantize_kv_fp8(d[3], stream=stream)
+        vc, vs = ds4a.quantize_kv_fp8(d[4], stream=stream)
+        torch.cuda.synchronize()
+        sec8 = timed(lambda i: ds4a.attn_decode_fp8(wl.layout, d[0], d[1], d[2], kc, ks, vc, vs, workspace=ws, out=o,
+                                                    stream=stream), 10)
+        n_c = wl.layout["n_comp"]
+        by8 = by - n_c * 2048 + n_c * (1024 + 8)
+        out.append({"workload": wl.name + "_fp8kv", "us_per_call": round(sec8 * 1e6, 2), "hbm_gbs": round(by8 / sec8 / 1e9, 1),
+                    "frac_hbm": round(by8 / sec8 / 1e9 / pk["hbm_gbs"], 4), "algorithmic_bytes": by8,
+                    "speedup_vs_fp16": round(sec / sec8, 2)})
+        del d, o, ws, kc, ks, vc, vs
+
+    def sec_decode_batch64():
+        # batched decode: 64 sequences, each the ratio-128 32K geometry (128 raw + 256 compressed
+        # rows) with its own K/V rows; three input sets rotate (3 x 58.7 MB > L2)
+        wl = W.decode_r128_32k()
+        B, G = 64, 3
+        L = wl.layout
+        geo = torch.tensor([[L["q_pos0"], L["n_raw"], L["raw_pos0"], L["n_comp"]]] * B, dtype=torch.int32, device=dev)
+        bsets = []
+        for gi in range(G):
+            gen = torch.Generator(device=dev).manual_seed(90 + gi)
+            mk = lambda n: torch.randn((B, n, 512), generator=gen, device=dev).to(torch.float16)  # noqa: E731
+            bsets.append([torch.randn((B, 64, 512), generator=gen, device=dev).to(torch.float16),
+                          mk(L["n_raw"]), mk(L["n_raw"]), mk(L["n_comp"]), mk(L["n_comp"]),
+                          torch.empty((B, 64, 512), dtype=torch.float16, device=dev)])
+        b_splits = ds4a.lib().ds4a_attn_decode_batch_default_splits(B, ctypes.byref(ds4a.make_layout(L)), L["n_raw"],
+                                                                   L["n_comp"])
+        bws = torch.empty(max(256, ds4a.lib().ds4a_attn_decode_batch_workspace_size(B, b_splits)), dtype=torch.uint8,
+                          device=dev)
+        sec = timed(lambda i: ds4a.attn_decode_batch(L, geo, *bsets[i % G][:5], n_splits=b_splits, workspace=bws,
+                                                     out=bsets[i % G][5], stream=stream), 30)
+        by = B * decode_bytes(L)
+        out.append({"workload": "decode_batch64_ratio128_ctx32768", "us_per_call": round(sec * 1e6, 2),
+                    "hbm_gbs": round(by / sec / 1e9, 1), "frac_hbm": round(by / sec / 1e9 / pk["hbm_gbs"], 4),
+                    "algorithmic_bytes": by, "n_splits": b_splits,
+                    "note": "64 sequences, each 128 raw + 256 compressed rows of its own"})
+        del bsets, bws, geo
+
+    def sec_indexer():
+        # indexer of the ratio-4 layer: scores (64 heads x 128 dims, max(0, x)) and top-512
+        wx = W.indexer_r4_2048()
+        L = wx.layout
+        qx, kx, wx_w = up(wx.q_idx), up(wx.k_idx), up(wx.w)
+        sc = [torch.empty((L["T"], L["n_comp"]), dtype=torch.float32, device=dev) for _ in range(2)]
+        sec = timed(lambda i: ds4a.indexer_scores(L, qx, kx, wx_w, scale=wx.scale, relu=True, out=sc[i % 2],
+                                                  stream=stream), 10)
+        n_cand = sum(min(L["n_comp"], (L["q_pos0"] + t + 1) // L["ratio"]) for t in range(L["T"]))
+        n_heads, head_dim = wx.q_idx.shape[1], wx.q_idx.shape[2]
+        fl = 2.0 * n_cand * n_heads * head_dim
+        out.append({"workload": wx.name + "_scores", "us_per_call": round(sec * 1e6, 2),
+                    "tflops": round(fl / sec / 1e12, 1), "frac_tensor": round(fl / sec / 1e12 / pk["bf16_tflops"], 4),
+                    "algorithmic_flops": fl, "shape": f"{n_heads} heads x {head_dim} dims, relu"})
+        ix_out = torch.empty((L["T"], wx.top_k), dtype=torch.int32, device=dev)
+        sec = timed(lambda i: ds4a.indexer_topk(L, sc[i % 2], wx.top_k, out=ix_out, stream=stream), 10)
+        by = 4 * n_cand + 4 * L["T"] * wx.top_k
+        out.append({"workload": wx.name + "_topk", "us_per_call": round(sec * 1e6, 2),
+                    "gbs": round(by / sec / 1e9, 1), "algorithmic_bytes": by,
+                    "note": "exact radix select over each token's candidate scores"})
+
+    def sec_compressor_prefill():
+        # compressor, one 2048-token prefill chunk of 512-dim rows (fresh state) on a ratio-4 and a
+        # ratio-128 layer; 20 input sets rotate (20 x 8 MB > L2)
+        for ratio in (4, 128):
+            wc = W.compressor_prefill(ratio)
+            n, width = wc.kv.shape
+            G = 20
+            gen = torch.Generator(device=dev).manual_seed(95 + ratio)
+            csets = [(torch.randn((n, width), generator=gen, device=dev),
+                      2 * torch.randn((n, width), generator=gen, device=dev)) for _ in range(G)]
+            st_kv = torch.empty((ratio - 1, width), dtype=torch.float32, device=dev)
+            st_s = torch.empty((ratio - 1, width), dtype=torch.float32, device=dev)
+            c_out = torch.empty((n // ratio, width), dtype=torch.float16, device=dev)
+            sec = timed(lambda i: ds4a.compress_append(csets[i % G][0], csets[i % G][1], st_kv, st_s, 0, ratio,
+                                                       out=c_out, stream=stream), 40)
+            by = 8 * n * width + 2 * (n // ratio) * width
+            out.append({"workload": wc.name, "us_per_call": round(sec * 1e6, 2), "hbm_gbs": round(by / sec / 1e9, 1),
+                        "frac_hbm": round(by / sec / 1e9 / pk["hbm_gbs"], 4), "algorithmic_bytes": by,
+                        "note": "per-dimension softmax pooling of each ratio span, fp32 in, fp16 out"})
+            del csets
+
+    def sec_compressor_decode():
+        # compressor decode step at a ratio-128 boundary: 127 positions in the state, one new
+        st_kv = torch.randn((127, 512), device=dev)
+        st_s = torch.randn((127, 512), device=dev)
+        one = [(torch.randn((1, 512), device=dev), torch.randn((1, 512), device=dev)) for _ in range(2)]
+        c_out = torch.empty((1, 512), dtype=torch.float16, device=dev)
+        sec = timed(lambda i: ds4a.compress_append(one[i % 2][0], one[i % 2][1], st_kv, st_s, 127, 128, out=c_out,
+                                                   stream=stream), 40)
+        out.append({"workload": "compressor_ratio128_decode_boundary_w512", "us_per_call": round(sec * 1e6, 2),
+                    "note": "one token completes a 128-position span (state in L2): latency"})
+        del st_kv, st_s, one
+
+    # Each line is measured on its own: a failure (for instance too little memory on a smaller
+    # device) becomes an entry with the error instead of losing the benchmark line.
+    for sec_fn in (sec_prefill, sec_indexed, sec_decode_sweep, sec_decode_256k_fp16_and_fp8, sec_decode_batch64,
+                   sec_indexer, sec_compressor_prefill, sec_compressor_decode):
+        try:
+            sec_fn()
+        except Exception as e:  # noqa: BLE001 - reported in the line
+            out.append({"workload": sec_fn.__name__[4:], "error": repr(e)[:300]})
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
     for e in out:
         e["peak_kind"] = pk_kind
     return out
