@@ -9,6 +9,8 @@
   -inf exactly.
 """
 
+import dataclasses
+
 import numpy as np
 import pytest
 
@@ -115,7 +117,7 @@ def test_topk_strided_rows(torch, ds4a):
 def _check_scores(got, wl, tokens=None):
     L = wl.layout
     want = ix.scores(L, wl.q_idx, wl.k_idx, wl.w, wl.scale, wl.relu, tokens=tokens)
-    bound = ix.scores(L, np.abs(wl.q_idx), np.abs(wl.k_idx), np.abs(wl.w), wl.scale, False, tokens=tokens)
+    bound = ix.scores(L, np.abs(wl.q_idx), np.abs(wl.k_idx), np.abs(wl.w), abs(wl.scale), False, tokens=tokens)
     g = np.asarray(got, np.float64)
     fin = np.isfinite(want)
     assert np.array_equal(np.isfinite(g), fin), "-inf pattern differs"
@@ -150,6 +152,15 @@ def test_scores_every_head_count(torch, ds4a, n_heads):
 def test_scores_head_dims(torch, ds4a, head_dim, relu):
     wl = _indexer_case(T=19, q_pos0=1200, n_comp=700, ratio=4, n_heads=64, head_dim=head_dim, relu=relu,
                        seed=40 + head_dim)
+    _check_scores(_run_scores(torch, ds4a, wl), wl)
+
+
+@pytest.mark.parametrize("relu", [False, True])
+@pytest.mark.parametrize("n_heads", [8, 64])
+def test_scores_negative_scale(torch, ds4a, relu, n_heads):
+    # max(0, scale x) with scale < 0: the kernel folds |scale| into the weights and negates x
+    wl = _indexer_case(T=9, q_pos0=800, n_comp=300, ratio=4, n_heads=n_heads, head_dim=128, relu=relu, seed=55)
+    wl = dataclasses.replace(wl, scale=-0.3)
     _check_scores(_run_scores(torch, ds4a, wl), wl)
 
 
