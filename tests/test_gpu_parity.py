@@ -297,6 +297,38 @@ def test_dense_mask_of_the_window_equals_structural(torch, ds4a):
     assert_close(b.astype(np.float64), a.astype(np.float64), "mask == window")
 
 
+def _random_layout(rng):
+    ratio = int(rng.choice([4, 128]))
+    T = int(rng.integers(1, 25))
+    q_pos0 = int(rng.integers(0, 3000))
+    n_raw = int(rng.integers(0, 400))
+    # raw rows mostly end around the tokens (the window), sometimes before or after them
+    raw_pos0 = max(0, q_pos0 + T - n_raw + int(rng.integers(-160, 161)))
+    n_comp = int(rng.integers(0, min(600, (q_pos0 + T) // ratio + 3) + 1))
+    return make_layout(T=T, q_pos0=q_pos0, n_raw=n_raw, raw_pos0=raw_pos0, n_comp=n_comp, ratio=ratio)
+
+
+def test_random_layouts_against_oracle(torch, ds4a):
+    """Seeded random geometries (token counts, row counts, offsets, both ratios;
+    rows past a token's position, empty segments, tokens that see nothing):
+    prefill, and decode with a random split count for the short ones."""
+    rng = np.random.default_rng(2024)
+    for case in range(32):
+        L = _random_layout(rng)
+        wl = W.draw(f"rand{case}", 300 + case, L)
+        d = upload(torch, wl)
+        want, wlse = oracle_out(wl)
+        o, lse = ds4a.attn_prefill(L, d["q"], d["k_raw"], d["v_raw"], d["k_comp"], d["v_comp"], want_lse=True)
+        assert_close(host(o), want, f"random prefill {case} {L}")
+        assert_lse_close(host(lse), wlse, f"random prefill lse {case} {L}")
+        if L["T"] <= 4:
+            splits = int(rng.integers(1, 9))
+            o, lse = ds4a.attn_decode(L, d["q"], d["k_raw"], d["v_raw"], d["k_comp"], d["v_comp"], n_splits=splits,
+                                      want_lse=True)
+            assert_close(host(o), want, f"random decode {case} splits={splits} {L}")
+            assert_lse_close(host(lse), wlse, f"random decode lse {case} {L}")
+
+
 # ------------------------------------------------------------------ decode
 
 def test_decode_r128_32k(torch, ds4a):
