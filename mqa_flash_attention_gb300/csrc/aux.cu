@@ -278,6 +278,55 @@ __global__ void __launch_bounds__(kCombineThreads) combine_wide_kernel(const flo
     lse[(long long)t * 64 + h] = L > 0.f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
 }
 
+// Few splits (a short decode): one block per (token, head), warp w owning dims
+// 64w .. 64w+63 (a float2 per lane).  Each warp reads the (m, l) pairs (one per
+// lane) and every partial value of its dims at once, and reduces with shuffles:
+// one round of memory latency, no shared memory and no block barrier.
+constexpr int kSmallMaxSplits = 8;
+
+__global__ void __launch_bounds__(kCombineThreads) combine_small_kernel(const float *__restrict__ ws_o,
+                                                                        const float2 *__restrict__ ws_ml,
+                                                                        int n_splits, __half *__restrict__ o,
+                                                                        long long o_tok_stride,
+                                                                        float *__restrict__ lse) {
+  grid_dependency_wait();  // the partials come from the previous kernel
+  grid_launch_dependents();
+  const int h = blockIdx.x, t = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long base = (long long)t * n_splits;
+  const int d = 64 * warp + 2 * lane;
+  const float *src = ws_o + (base * 64 + h) * 512 + d;
+  const long long step = 64LL * 512;
+  const float2 ml = lane < n_splits ? ws_ml[(base + lane) * 64 + h] : make_float2(-INFINITY, 0.f);
+  float2 x[kSmallMaxSplits];
+#pragma unroll
+  for (int i = 0; i < kSmallMaxSplits; ++i)
+    x[i] = i < n_splits ? __ldg(reinterpret_cast<const float2 *>(src + (long long)i * step)) : make_float2(0.f, 0.f);
+  float M = ml.x;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  const float w = (ml.x == -INFINITY || M == -INFINITY) ? 0.f : exp2f(ml.x - M);
+  float L = w * ml.y;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+  // A split without visible rows left its partial unwritten (any bits): its
+  // weight is 0 and the select drops the value.
+  float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int i = 0; i < kSmallMaxSplits; ++i) {
+    const float wi = __shfl_sync(0xffffffffu, w, i);
+    if (i < n_splits) {
+      acc.x += wi != 0.f ? wi * x[i].x : 0.f;
+      acc.y += wi != 0.f ? wi * x[i].y : 0.f;
+    }
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  *reinterpret_cast<__half2 *>(o + (long long)t * o_tok_stride + h * 512 + d) =
+      __floats2half2_rn(acc.x * inv, acc.y * inv);
+  if (lse != nullptr && threadIdx.x == 0)
+    lse[(long long)t * 64 + h] = L > 0.f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
+}
+
 cudaError_t launch_combine(const float *ws_o, const float2 *ws_ml, int n_splits, int T, __half *o,
                            long long o_tok_stride, float *lse, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
@@ -285,8 +334,8 @@ cudaError_t launch_combine(const float *ws_o, const float2 *ws_ml, int n_splits,
   // Programmatic dependent launch: the merge is scheduled while the partial
   // kernel runs and waits for it inside (griddepcontrol.wait).
   cudaLaunchConfig_t cfg = {};
-  const bool wide = n_splits >= kWideMinSplits;
-  cfg.gridDim = dim3(wide ? kWideChunks : 2, 64, T);
+  const bool wide = n_splits >= kWideMinSplits, small = n_splits <= kSmallMaxSplits;
+  cfg.gridDim = small ? dim3(64, T, 1) : dim3(wide ? kWideChunks : 2, 64, T);
   cfg.blockDim = dim3(kCombineThreads);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -294,6 +343,7 @@ cudaError_t launch_combine(const float *ws_o, const float2 *ws_ml, int n_splits,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (small) return cudaLaunchKernelEx(&cfg, combine_small_kernel, ws_o, ws_ml, n_splits, o, o_tok_stride, lse);
   if (wide) return cudaLaunchKernelEx(&cfg, combine_wide_kernel, ws_o, ws_ml, n_splits, o, o_tok_stride, lse);
   return cudaLaunchKernelEx(&cfg, combine_kernel, ws_o, ws_ml, n_splits, o, o_tok_stride, lse);
 }
