@@ -234,12 +234,13 @@ ds4a_status ds4a_attn_decode(const ds4a_layout *L, const ds4a_tensors *X, int32_
  * ds4a_attn_decode, for callers that merge partial results themselves (for
  * instance across devices that each hold part of the compressed rows).
  * Workspace layout, with I = T * n_splits items (item = t * n_splits + s):
- *   float O_part[I][64][512]   unnormalised sum_j p_j v_j of split s of token t
+ *   fp16 o_part[I][64][512]    the split's own attention output
+ *                              sum_j p_j v_j / l, rounded to fp16
  *   float2 ml[I][64]           (m, l): p_j = 2^(log2(e) * (scale q.k_j + bias_j) - m),
  *                              l = sum_j p_j; m = -inf and l = 0 for a split with
- *                              no visible row (its O_part is then not written)
- * The merge computes o = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s with
- * M = max_s m_s, and lse = (M + log2 L) * ln 2.  decode_partials ignores X->o
+ *                              no visible row (its o_part is then not written)
+ * The merge computes o = sum_s W_s o_s / L with W_s = 2^(m_s - M) l_s,
+ * L = sum_s W_s, M = max_s m_s, and lse = (M + log2 L) * ln 2.  decode_partials ignores X->o
  * and X->lse; decode_merge reads only the workspace and writes X->o / X->lse
  * (X->q and the K/V pointers are not used and may be NULL).
  */
@@ -313,8 +314,8 @@ ds4a_status ds4a_attn_decode_batch(int32_t n_seq, const ds4a_layout *shape, cons
  * counterpart of this call; it exists for those callers.
  *   The split-KV partials go to an 8 MiB array inside the library (a
  *   file-scope device array that every device loading the library holds until
- *   the process exits), so T * n_splits * 131584 bytes must fit in 8 MiB
- *   (T * n_splits <= 63).  n_splits <= 0 picks the usual split count, capped to
+ *   the process exits), so T * n_splits * 66048 bytes must fit in 8 MiB
+ *   (T * n_splits <= 127).  n_splits <= 0 picks the usual split count, capped to
  *   fit; a T or n_splits that cannot fit returns DS4A_ERR_WORKSPACE before any
  *   launch.  Nothing is allocated: no cudaMalloc, no cudaFree.
  *   The array needs no clearing: every byte a call reads was written earlier

@@ -390,14 +390,14 @@ int32_t ds4a_attn_decode_default_splits(const ds4a_layout *L) {
 size_t ds4a_attn_decode_workspace_size(const ds4a_layout *L, int32_t n_splits) {
   if (check_layout(L) != DS4A_OK) return 0;
   if (n_splits <= 0) n_splits = ds4a_attn_decode_default_splits(L);
-  return (size_t)L->T * (size_t)n_splits * DS4A_HEADS * (DS4A_HEAD_DIM * sizeof(float) + 2 * sizeof(float));
+  return (size_t)L->T * (size_t)n_splits * DS4A_HEADS * (DS4A_HEAD_DIM * sizeof(__half) + 2 * sizeof(float));
 }
 
 namespace {
 
 // Shared checks of the decode calls; fills the partial-output pointers.
 ds4a_status decode_setup(const ds4a_layout *L, const ds4a_tensors *X, int32_t &n_splits, const void *workspace,
-                         size_t workspace_bytes, bool need_inputs, bool need_outputs, float **ws_o,
+                         size_t workspace_bytes, bool need_inputs, bool need_outputs, __half **ws_o,
                          float2 **ws_ml) {
   ds4a_status st = check_layout(L);
   if (st != DS4A_OK) return st;
@@ -422,13 +422,13 @@ ds4a_status decode_setup(const ds4a_layout *L, const ds4a_tensors *X, int32_t &n
   if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256)) return DS4A_ERR_WORKSPACE;
   const size_t n_items = (size_t)L->T * n_splits;
   if (n_items > (size_t)INT32_MAX) return DS4A_ERR_INVALID_ARG;
-  *ws_o = static_cast<float *>(const_cast<void *>(workspace));
+  *ws_o = static_cast<__half *>(const_cast<void *>(workspace));
   *ws_ml = reinterpret_cast<float2 *>(static_cast<uint8_t *>(const_cast<void *>(workspace)) +
-                                      n_items * DS4A_HEADS * DS4A_HEAD_DIM * sizeof(float));
+                                      n_items * DS4A_HEADS * DS4A_HEAD_DIM * sizeof(__half));
   return DS4A_OK;
 }
 
-ds4a_status decode_partials(const ds4a_layout *L, const ds4a_tensors *X, int32_t n_splits, float *ws_o,
+ds4a_status decode_partials(const ds4a_layout *L, const ds4a_tensors *X, int32_t n_splits, __half *ws_o,
                             float2 *ws_ml, ds4a_stream_t stream) {
   DeviceState *d = nullptr;
   ds4a_status st = current_device(&d);
@@ -456,7 +456,7 @@ ds4a_status decode_partials(const ds4a_layout *L, const ds4a_tensors *X, int32_t
 
 ds4a_status ds4a_attn_decode_partials(const ds4a_layout *L, const ds4a_tensors *X, int32_t n_splits,
                                       void *workspace, size_t workspace_bytes, ds4a_stream_t stream) {
-  float *ws_o = nullptr;
+  __half *ws_o = nullptr;
   float2 *ws_ml = nullptr;
   ds4a_status st = decode_setup(L, X, n_splits, workspace, workspace_bytes, true, false, &ws_o, &ws_ml);
   if (st != DS4A_OK || L->T == 0) return st;
@@ -465,7 +465,7 @@ ds4a_status ds4a_attn_decode_partials(const ds4a_layout *L, const ds4a_tensors *
 
 ds4a_status ds4a_attn_decode_merge(const ds4a_layout *L, const ds4a_tensors *X, int32_t n_splits,
                                    const void *workspace, size_t workspace_bytes, ds4a_stream_t stream) {
-  float *ws_o = nullptr;
+  __half *ws_o = nullptr;
   float2 *ws_ml = nullptr;
   ds4a_status st = decode_setup(L, X, n_splits, workspace, workspace_bytes, false, true, &ws_o, &ws_ml);
   if (st != DS4A_OK || L->T == 0) return st;
@@ -478,7 +478,7 @@ ds4a_status ds4a_attn_decode_merge(const ds4a_layout *L, const ds4a_tensors *X, 
 
 ds4a_status ds4a_attn_decode(const ds4a_layout *L, const ds4a_tensors *X, int32_t n_splits, void *workspace,
                              size_t workspace_bytes, ds4a_stream_t stream) {
-  float *ws_o = nullptr;
+  __half *ws_o = nullptr;
   float2 *ws_ml = nullptr;
   ds4a_status st = decode_setup(L, X, n_splits, workspace, workspace_bytes, true, true, &ws_o, &ws_ml);
   if (st != DS4A_OK || L->T == 0) return st;
@@ -513,9 +513,9 @@ ds4a_status ds4a_attn_decode_fp8(const ds4a_layout *L, const ds4a_tensors *X, co
   if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256)) return DS4A_ERR_WORKSPACE;
   const size_t n_items = (size_t)L->T * n_splits;
   if (n_items > (size_t)INT32_MAX) return DS4A_ERR_INVALID_ARG;
-  float *ws_o = static_cast<float *>(workspace);
+  __half *ws_o = static_cast<__half *>(workspace);
   float2 *ws_ml = reinterpret_cast<float2 *>(static_cast<uint8_t *>(workspace) +
-                                             n_items * DS4A_HEADS * DS4A_HEAD_DIM * sizeof(float));
+                                             n_items * DS4A_HEADS * DS4A_HEAD_DIM * sizeof(__half));
   DeviceState *d = nullptr;
   st = current_device(&d);
   if (st != DS4A_OK) return st;
@@ -592,7 +592,7 @@ int32_t ds4a_attn_decode_batch_default_splits(int32_t n_seq, const ds4a_layout *
 
 size_t ds4a_attn_decode_batch_workspace_size(int32_t n_seq, int32_t n_splits) {
   if (n_seq <= 0 || n_splits <= 0) return 0;
-  return (size_t)n_seq * (size_t)n_splits * DS4A_HEADS * (DS4A_HEAD_DIM * sizeof(float) + 2 * sizeof(float));
+  return (size_t)n_seq * (size_t)n_splits * DS4A_HEADS * (DS4A_HEAD_DIM * sizeof(__half) + 2 * sizeof(float));
 }
 
 ds4a_status ds4a_attn_decode_batch(int32_t n_seq, const ds4a_layout *shape, const int32_t *seq_geom,
@@ -652,9 +652,9 @@ ds4a_status ds4a_attn_decode_batch(int32_t n_seq, const ds4a_layout *shape, cons
   p.q_tile = 1;
   p.batch_geom = reinterpret_cast<const int4 *>(seq_geom);
   p.partial = 1;
-  float *ws_o = static_cast<float *>(workspace);
+  __half *ws_o = static_cast<__half *>(workspace);
   float2 *ws_ml = reinterpret_cast<float2 *>(static_cast<uint8_t *>(workspace) +
-                                             n_items * DS4A_HEADS * DS4A_HEAD_DIM * sizeof(float));
+                                             n_items * DS4A_HEADS * DS4A_HEAD_DIM * sizeof(__half));
   p.ws_o = ws_o;
   p.ws_ml = ws_ml;
   p.timeout_ns = kDefaultTimeoutNs;
@@ -685,7 +685,7 @@ ds4a_status ds4a_attn_decode_noalloc(const ds4a_layout *L, const ds4a_tensors *X
   DeviceState *d = nullptr;
   st = current_device(&d);  // the first call on a device looks up the scratch address
   if (st != DS4A_OK) return st;
-  float *ws_o = nullptr;
+  __half *ws_o = nullptr;
   float2 *ws_ml = nullptr;
   st = decode_setup(L, X, n_splits, d->scratch, kNoAllocScratchBytes, true, true, &ws_o, &ws_ml);
   if (st != DS4A_OK) return st;

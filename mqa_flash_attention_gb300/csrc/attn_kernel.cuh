@@ -769,8 +769,9 @@ __device__ __forceinline__ void compute_role(const AttnParams &p, uint8_t *smem,
     if (aborted) break;
 
     // Epilogue: sum the row partials per head (they do not depend on O), then
-    // normalise (or hand out partials) one O^T block at a time as each block
-    // of the last PV completes.
+    // normalise one O^T block at a time as each block of the last PV
+    // completes.  A split-KV item hands out its own normalised o (fp16) and
+    // (m, l); a whole token writes o and the log-sum-exp.
     ms.red[q][col0 + l] = warp_reduce_scatter32<false>(lpart, l);
     if (bar_red_or(1, kComputeThreads, bad)) {
       aborted = true;
@@ -778,36 +779,24 @@ __device__ __forceinline__ void compute_role(const AttnParams &p, uint8_t *smem,
     }
     if (tid < kH) {
       const float lsum = ms.red[0][tid] + ms.red[1][tid] + ms.red[2][tid] + ms.red[3][tid];
+      ms.inv_l[tid] = lsum > 0.f ? 1.f / lsum : 0.f;
       if (p.partial) {
         p.ws_ml[(long long)item * kH + tid] = make_float2(lsum > 0.f ? m_ref : -INFINITY, lsum);
-      } else {
-        ms.inv_l[tid] = lsum > 0.f ? 1.f / lsum : 0.f;
-        if (p.lse != nullptr)
-          p.lse[(long long)t * kH + tid] = lsum > 0.f ? (m_ref + log2f(lsum)) * kLn2 : -INFINITY;
+      } else if (p.lse != nullptr) {
+        p.lse[(long long)t * kH + tid] = lsum > 0.f ? (m_ref + log2f(lsum)) * kLn2 : -INFINITY;
       }
     }
     named_bar_sync(1, kComputeThreads);
-    if (p.partial) {
-#pragma unroll 1
-      for (int m = 0; m < 4; ++m) {
-        bad = bad || !mbar_wait(smem_u32(&ms.o_full[m]), n_item & 1, abrt, p.timeout_ns, p.err, SITE_O_FULL);
-        tc_fence_after();
-        float o[32];
-        tmem_ld32(tmem + 64 * m + col0 + lane_base, o);
-        tmem_wait_ld();
-        float *dst = p.ws_o + ((long long)item * kH + col0) * kD + 128 * m + r;
-#pragma unroll
-        for (int h = 0; h < 32; ++h) dst[h * kD] = o[h];
-      }
-    } else {
-      // O^T[128 dims][64 heads] -> fp16 O.  Lanes 2k and 2k+1 hold adjacent
+    {
+      // O^T[128 dims][64 heads] -> fp16 o.  Lanes 2k and 2k+1 hold adjacent
       // dims: for each pair of heads they swap one value, so the even lane
       // writes both dims of the first head and the odd lane both dims of the
       // second (32-bit stores, 64 contiguous bytes per head per warp).
       float inv[32];
       load32(ms.inv_l + col0, inv);
       const bool odd = l & 1;
-      __half *obase = p.o + (long long)t * p.o_tok_stride + (long long)col0 * kD + (r & ~1);
+      __half *obase = p.partial ? p.ws_o + ((long long)item * kH + col0) * kD + (r & ~1)
+                                : p.o + (long long)t * p.o_tok_stride + (long long)col0 * kD + (r & ~1);
 #pragma unroll 1
       for (int m = 0; m < 4; ++m) {
         bad = bad || !mbar_wait(smem_u32(&ms.o_full[m]), n_item & 1, abrt, p.timeout_ns, p.err, SITE_O_FULL);

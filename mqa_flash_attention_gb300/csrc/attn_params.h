@@ -97,7 +97,7 @@ struct AttnParams {
   __half *o;
   long long o_tok_stride;  // elements
   float *lse;
-  float *ws_o;             // [T * n_splits][64][512]
+  __half *ws_o;            // [T * n_splits][64][512]: the split's o = sum_j p_j v_j / l, fp16
   float2 *ws_ml;           // [T * n_splits][64] (m in log2 units, l)
   unsigned long long timeout_ns;
   unsigned int *err;       // device error word

@@ -132,9 +132,10 @@ cudaError_t launch_block_mask_dense(const GeomScalars &g, const __half *mask, lo
 }
 
 // ------------------------------------------------------------------ split merge
-// Each split s of a token left an unnormalised O_s (fp32, relative to its
-// reference max m_s in log2 units) and l_s.  With M = max_s m_s:
-//   o = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s,  lse = (M + log2 L) ln 2.
+// Each split s of a token left its own normalised o_s (fp16) with its
+// reference max m_s (log2 units) and row sum l_s.  With M = max_s m_s and the
+// split weights W_s = 2^(m_s - M) l_s:
+//   o = sum_s W_s o_s / L,  L = sum_s W_s,  lse = (M + log2 L) ln 2.
 // One block per (token, head, half of the dims), 256 threads, one dim each.
 // The split weights are computed once into shared memory; the partials are
 // then streamed with eight independent loads in flight per thread.
@@ -159,7 +160,7 @@ __device__ __forceinline__ float block_reduce(float v, bool is_max, float *red) 
   return __shfl_sync(0xffffffffu, v, 0);
 }
 
-__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float *__restrict__ ws_o,
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __half *__restrict__ ws_o,
                                                                   const float2 *__restrict__ ws_ml, int n_splits,
                                                                   __half *__restrict__ o, long long o_tok_stride,
                                                                   float *__restrict__ lse) {
@@ -175,13 +176,13 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float *_
   float lsum = 0.f;
   for (int s = threadIdx.x; s < n_splits; s += kCombineThreads) {
     const float2 ml = ws_ml[(base + s) * 64 + h];
-    const float wgt = (ml.x == -INFINITY || M == -INFINITY) ? 0.f : exp2f(ml.x - M);
+    const float wgt = (ml.x == -INFINITY || M == -INFINITY) ? 0.f : exp2f(ml.x - M) * ml.y;
     w_s[s] = wgt;
-    lsum += wgt * ml.y;
+    lsum += wgt;
   }
   const float L = block_reduce(lsum, false, red);  // also orders the w_s writes before the reads below
   const int d = 256 * half + threadIdx.x;
-  const float *src = ws_o + (base * 64 + h) * 512 + d;
+  const __half *src = ws_o + (base * 64 + h) * 512 + d;
   const long long step = 64LL * 512;
   float acc[8];
 #pragma unroll
@@ -191,12 +192,12 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float *_
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const float wgt = w_s[s + i];  // same for every thread: no divergence
-      if (wgt != 0.f) acc[i] += wgt * __ldg(src + (long long)(s + i) * step);
+      if (wgt != 0.f) acc[i] += wgt * __half2float(__ldg(src + (long long)(s + i) * step));
     }
   }
   for (; s < n_splits; ++s) {
     const float wgt = w_s[s];
-    if (wgt != 0.f) acc[0] += wgt * __ldg(src + (long long)s * step);
+    if (wgt != 0.f) acc[0] += wgt * __half2float(__ldg(src + (long long)s * step));
   }
   const float sum = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
   o[(long long)t * o_tok_stride + h * 512 + d] = __float2half_rn(L > 0.f ? sum / L : 0.f);
@@ -206,13 +207,13 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float *_
 
 // Many splits (a long decode): one block per (token, head, 64-dim chunk), 512
 // blocks per token.  Warp w sums the splits w, w+8, w+16, ... over the chunk's
-// 64 dims (a float2 per lane, four loads in flight), and the eight warp sums
+// 64 dims (a half2 per lane, four loads in flight), and the eight warp sums
 // are added in shared memory: the per-thread chains are 1/8 as long and four
 // times as many blocks load at once as in combine_kernel.
 constexpr int kWideChunks = 8;        // 64-dim chunks per head
 constexpr int kWideMinSplits = 17;    // below this the one-dim-per-thread merge is as fast
 
-__global__ void __launch_bounds__(kCombineThreads) combine_wide_kernel(const float *__restrict__ ws_o,
+__global__ void __launch_bounds__(kCombineThreads) combine_wide_kernel(const __half *__restrict__ ws_o,
                                                                        const float2 *__restrict__ ws_ml,
                                                                        int n_splits, __half *__restrict__ o,
                                                                        long long o_tok_stride,
@@ -230,15 +231,15 @@ __global__ void __launch_bounds__(kCombineThreads) combine_wide_kernel(const flo
   float lsum = 0.f;
   for (int s = threadIdx.x; s < n_splits; s += kCombineThreads) {
     const float2 ml = ws_ml[(base + s) * 64 + h];
-    const float wgt = (ml.x == -INFINITY || M == -INFINITY) ? 0.f : exp2f(ml.x - M);
+    const float wgt = (ml.x == -INFINITY || M == -INFINITY) ? 0.f : exp2f(ml.x - M) * ml.y;
     w_s[s] = wgt;
-    lsum += wgt * ml.y;
+    lsum += wgt;
   }
   const float L = block_reduce(lsum, false, red);  // also orders the w_s writes before the reads below
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int kW = kCombineThreads / 32;
   const int d = 64 * chunk + 2 * lane;
-  const float *src = ws_o + (base * 64 + h) * 512 + d;
+  const __half *src = ws_o + (base * 64 + h) * 512 + d;
   const long long step = 64LL * 512;
   // A split without visible rows left its partial unwritten (any bits): its
   // weight is 0 and the select drops the value.
@@ -247,7 +248,8 @@ __global__ void __launch_bounds__(kCombineThreads) combine_wide_kernel(const flo
   for (; s + 3 * kW < n_splits; s += 4 * kW) {
     float2 x[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) x[i] = __ldg(reinterpret_cast<const float2 *>(src + (long long)(s + i * kW) * step));
+    for (int i = 0; i < 4; ++i)
+      x[i] = __half22float2(__ldg(reinterpret_cast<const __half2 *>(src + (long long)(s + i * kW) * step)));
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const float wgt = w_s[s + i * kW];
@@ -256,7 +258,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_wide_kernel(const flo
     }
   }
   for (; s < n_splits; s += kW) {
-    const float2 x = __ldg(reinterpret_cast<const float2 *>(src + (long long)s * step));
+    const float2 x = __half22float2(__ldg(reinterpret_cast<const __half2 *>(src + (long long)s * step)));
     const float wgt = w_s[s];
     acc.x += wgt != 0.f ? wgt * x.x : 0.f;
     acc.y += wgt != 0.f ? wgt * x.y : 0.f;
@@ -279,12 +281,12 @@ __global__ void __launch_bounds__(kCombineThreads) combine_wide_kernel(const flo
 }
 
 // Few splits (a short decode): one block per (token, head), warp w owning dims
-// 64w .. 64w+63 (a float2 per lane).  Each warp reads the (m, l) pairs (one per
+// 64w .. 64w+63 (a half2 per lane).  Each warp reads the (m, l) pairs (one per
 // lane) and every partial value of its dims at once, and reduces with shuffles:
 // one round of memory latency, no shared memory and no block barrier.
 constexpr int kSmallMaxSplits = 8;
 
-__global__ void __launch_bounds__(kCombineThreads) combine_small_kernel(const float *__restrict__ ws_o,
+__global__ void __launch_bounds__(kCombineThreads) combine_small_kernel(const __half *__restrict__ ws_o,
                                                                         const float2 *__restrict__ ws_ml,
                                                                         int n_splits, __half *__restrict__ o,
                                                                         long long o_tok_stride,
@@ -295,18 +297,19 @@ __global__ void __launch_bounds__(kCombineThreads) combine_small_kernel(const fl
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long base = (long long)t * n_splits;
   const int d = 64 * warp + 2 * lane;
-  const float *src = ws_o + (base * 64 + h) * 512 + d;
+  const __half *src = ws_o + (base * 64 + h) * 512 + d;
   const long long step = 64LL * 512;
   const float2 ml = lane < n_splits ? ws_ml[(base + lane) * 64 + h] : make_float2(-INFINITY, 0.f);
   float2 x[kSmallMaxSplits];
 #pragma unroll
   for (int i = 0; i < kSmallMaxSplits; ++i)
-    x[i] = i < n_splits ? __ldg(reinterpret_cast<const float2 *>(src + (long long)i * step)) : make_float2(0.f, 0.f);
+    x[i] = i < n_splits ? __half22float2(__ldg(reinterpret_cast<const __half2 *>(src + (long long)i * step)))
+                        : make_float2(0.f, 0.f);
   float M = ml.x;
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-  const float w = (ml.x == -INFINITY || M == -INFINITY) ? 0.f : exp2f(ml.x - M);
-  float L = w * ml.y;
+  const float w = (ml.x == -INFINITY || M == -INFINITY) ? 0.f : exp2f(ml.x - M) * ml.y;
+  float L = w;
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
   // A split without visible rows left its partial unwritten (any bits): its
@@ -327,7 +330,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_small_kernel(const fl
     lse[(long long)t * 64 + h] = L > 0.f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
 }
 
-cudaError_t launch_combine(const float *ws_o, const float2 *ws_ml, int n_splits, int T, __half *o,
+cudaError_t launch_combine(const __half *ws_o, const float2 *ws_ml, int n_splits, int T, __half *o,
                            long long o_tok_stride, float *lse, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   if (n_splits > kCombineMaxSplits) return cudaErrorInvalidValue;

@@ -23,7 +23,7 @@ cudaError_t launch_pad(const void *src, long long src_stride, int n_rows, void *
 cudaError_t launch_block_mask_struct(const GeomScalars &g, int q_tile, uint8_t *status, cudaStream_t s);
 cudaError_t launch_block_mask_dense(const GeomScalars &g, const __half *mask, long long mask_stride, int q_tile,
                                     uint8_t *status, cudaStream_t s);
-cudaError_t launch_combine(const float *ws_o, const float2 *ws_ml, int n_splits, int T, __half *o,
+cudaError_t launch_combine(const __half *ws_o, const float2 *ws_ml, int n_splits, int T, __half *o,
                            long long o_tok_stride, float *lse, cudaStream_t s);
 cudaError_t launch_selftest_wait(unsigned long long timeout_ns, unsigned int *err, cudaStream_t s);
 cudaError_t launch_quantize_fp8(const void *src, long long src_stride, int n_rows, void *dst, long long dst_stride,

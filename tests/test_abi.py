@@ -60,7 +60,7 @@ def test_block_count(lib):
 
 def test_decode_workspace_size(lib):
     L = _layout(T=3, n_comp=1000, ratio=128)
-    per_split = 64 * (512 * 4 + 8)
+    per_split = 64 * (512 * 2 + 8)
     assert lib.ds4a_attn_decode_workspace_size(ctypes.byref(L), 5) == 3 * 5 * per_split
     assert lib.ds4a_attn_decode_workspace_size(None, 5) == 0
 

@@ -49,8 +49,8 @@ def test_noalloc_decode_matches_decode_on_two_calls():
         assert (lse - ref_lse).abs().max().item() <= 1e-3
         assert lib.ds4a_device_status(stream, 1) == ds4a.OK
 
-    # a request that cannot fit in the 8 MiB array is refused before any launch
-    L = ds4a.make_layout(W.make_layout(T=64, q_pos0=40000, n_raw=128, raw_pos0=39873, n_comp=300, ratio=128))
+    # a request that cannot fit in the 8 MiB array (127 items) is refused before any launch
+    L = ds4a.make_layout(W.make_layout(T=128, q_pos0=40000, n_raw=128, raw_pos0=39873, n_comp=300, ratio=128))
     assert lib.ds4a_attn_decode_noalloc(ctypes.byref(L), ctypes.byref(X), 0, stream) == ds4a.ERR_WORKSPACE
     L1 = ds4a.make_layout(W.decode_r128_32k().layout)
-    assert lib.ds4a_attn_decode_noalloc(ctypes.byref(L1), ctypes.byref(X), 64, stream) == ds4a.ERR_WORKSPACE
+    assert lib.ds4a_attn_decode_noalloc(ctypes.byref(L1), ctypes.byref(X), 128, stream) == ds4a.ERR_WORKSPACE
