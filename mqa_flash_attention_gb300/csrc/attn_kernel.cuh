@@ -35,7 +35,11 @@
 //               KV rows or dims) and heads 32*(w/4) .. +31
 //   warps 8-11  loaders: Q once per item, every K/V stage in ring order (TMA
 //               tiles, or 16-byte cp.async gathers of index-listed rows: a
-//               TMA gather moves only 512 bytes per instruction)
+//               TMA gather moves only 512 bytes per instruction); with E4M3
+//               compressed rows warps 9-11 convert the codes, and in a CTA
+//               with a single item they copy its Q
+//   epilogue    a whole token: o (fp16) and its log-sum-exp; a split of a
+//               token: the split's own normalised o (fp16) and (m, l)
 //   warp  12    TMEM allocator and tcgen05.mma issuer
 // Each mbarrier is waited on only by a role that cannot fall more than one
 // phase behind it, which a parity wait needs.

@@ -81,7 +81,7 @@ struct AttnParams {
   float scale_log2;
   int mode;
   int n_splits;            // row ranges per token
-  int partial;             // 1: unnormalised partials to the workspace
+  int partial;             // 1: per-split outputs and (m, l) to the workspace
   int top_k;
   const void *k_comp, *v_comp;  // compressed rows (read directly by the gather warps)
   const float *k_scale, *v_scale;  // per-row scales of E4M3 compressed rows
