@@ -42,8 +42,9 @@ Readings taken where the pages are silent (each one is pinned by a test):
 * with a dense mask, the mask replaces the structural rule: a real row is
   visible iff its mask entry is not -inf, and the entry is added to the scaled
   score (natural-log units);
-* an index list entry < 0 is an empty slot; every other entry counts once per
-  occurrence (plain gather);
+* an index list entry < 0 is an empty slot, and so is an entry >= n_comp (a
+  list slot that names no stored row: the library's interface declares such
+  entries empty); every other entry counts once per occurrence (plain gather);
 * a token with no visible row gets o = 0 and lse = -inf.
 
 Numbers: every fp16 input is widened exactly to float64 and all arithmetic is
@@ -110,11 +111,14 @@ def pair_visibility(layout: dict, mask: np.ndarray | None = None):
     return vis, bias
 
 
-def listed_rows(lst) -> np.ndarray:
-    """Compressed rows named by one token's index list: every entry >= 0, once
-    per occurrence, in list order (entries < 0 are empty slots)."""
+def listed_rows(lst, n_comp: int) -> np.ndarray:
+    """Compressed rows named by one token's index list: every entry ``c`` with
+    ``0 <= c < n_comp``, once per occurrence, in list order.  Entries < 0 and
+    entries >= n_comp name no stored row and are empty slots (the top-512
+    lists of "DwarfStar 4 (DS4) - DeepSeek V4 Flash Inference Engine",
+    section "Layer Compression", pick among the stored compressed rows)."""
     lst = np.asarray(lst, dtype=np.int64)
-    return lst[lst >= 0]
+    return lst[(lst >= 0) & (lst < n_comp)]
 
 
 # ------------------------------------------------------------------ attention
@@ -171,7 +175,7 @@ def attention(layout: dict, q, k_raw, v_raw, k_comp=None, v_comp=None, *,
             if idx is None:
                 csel = np.nonzero(comp_visible(layout, p))[0]
             else:
-                csel = listed_rows(idx[t])
+                csel = listed_rows(idx[t], n_comp)
             keys = np.concatenate([kr[rsel], kc[csel]])
             vals = np.concatenate([vr[rsel], vc[csel]])
             bias = np.zeros(keys.shape[0])

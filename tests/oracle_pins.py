@@ -277,6 +277,23 @@ def pin_indexed_all_rows_equals_dense(o):
     np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-12)
 
 
+def pin_index_entries_past_the_rows_are_empty(o):
+    """An index entry that names no stored row (>= n_comp, as well as < 0) is
+    an empty slot, as the library's interface declares: a list whose only
+    stored row is 5 gives exactly v_5 (one visible row has weight 1), and a
+    list of out-of-range entries alone gives o = 0, lse = -inf."""
+    L = make_layout(T=2, q_pos0=99, n_raw=0, raw_pos0=0, n_comp=24, ratio=4)
+    q = _normal(27, 1, (2, H, D))
+    kc, vc = _normal(27, 4, (24, D)), _normal(27, 5, (24, D))
+    empty = np.zeros((0, D), np.float16)
+    idx = np.array([[24, 5, 1000, -1, 2 ** 31 - 1],
+                    [24, 25, 2 ** 31 - 1, -7, 47]], np.int32)
+    out, lse = o.attention(L, q, empty, empty, kc, vc, idx=idx)
+    assert np.array_equal(out[0], np.broadcast_to(vc[5].astype(np.float64), (H, D)))
+    assert np.all(np.isfinite(lse[0]))
+    assert np.all(out[1] == 0.0) and np.all(lse[1] == -np.inf)
+
+
 def pin_no_visible_rows(o):
     """A token whose rows are all masked gets o = 0 and lse = -inf."""
     L = _tiny_layout(T=1)

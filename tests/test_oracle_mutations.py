@@ -77,9 +77,19 @@ def _softmax_variant(kind):
     return f
 
 
-def _unique_rows(lst):
+def _unique_rows(lst, n_comp):
     lst = np.asarray(lst, dtype=np.int64)
-    return np.unique(lst[lst >= 0])
+    return np.unique(lst[(lst >= 0) & (lst < n_comp)])
+
+
+def _rows_past_the_end_kept(lst, n_comp):
+    lst = np.asarray(lst, dtype=np.int64)
+    return lst[lst >= 0]
+
+
+def _rows_wrapped(lst, n_comp):
+    lst = np.asarray(lst, dtype=np.int64)
+    return lst[lst >= 0] % max(n_comp, 1)
 
 
 def _pairs_pad_visible(layout, mask=None):
@@ -122,6 +132,8 @@ MUTATIONS = {
     "no_normalisation": ("_softmax_weighted", _softmax_variant("no_normalise")),
     "lse_without_max": ("_softmax_weighted", _softmax_variant("lse_without_max")),
     "index_duplicates_collapsed": ("listed_rows", _unique_rows),
+    "index_entries_past_the_rows_kept": ("listed_rows", _rows_past_the_end_kept),
+    "index_entries_wrapped_modulo_rows": ("listed_rows", _rows_wrapped),
     "status_pad_rows_visible": ("pair_visibility", _pairs_pad_visible),
     "status_bias_ignored": ("pair_visibility", _pairs_bias_ignored_in_status),
     "status_partial_full_swapped": ("block_status", _status_any_all_swapped),
