@@ -92,7 +92,10 @@ typedef enum {
 /* Static message for a status code; never NULL. */
 const char *ds4a_status_string(int status);
 
-/* Library version string, e.g. "ds4a 0.1 sm_103a". */
+/* Library version string, "ds4a 0.2 sm_103a".  The minor number changes
+ * whenever a layout callers can see changes: 0.2 is the first version whose
+ * decode workspace holds fp16 normalised partials with the merge weight
+ * W_s = 2^(m_s - M) l_s (0.1 held fp32 unnormalised sums). */
 const char *ds4a_version(void);
 
 /*
@@ -220,9 +223,13 @@ ds4a_status ds4a_attn_prefill(const ds4a_layout *L, const ds4a_tensors *X,
  *   n_splits   ranges per token, >= 1, or <= 0 for the library's choice
  *              (ds4a_attn_decode_default_splits).
  *   workspace  device scratch of at least ds4a_attn_decode_workspace_size()
- *              bytes, 256-byte aligned, owned by the caller; it is fully
- *              overwritten and need not be initialised.  Two calls in flight
- *              at the same time must not share a workspace.
+ *              bytes, 256-byte aligned, owned by the caller; it need not be
+ *              initialised.  Every (m, l) pair is written by the call; the
+ *              o_part slot of a split with no visible row is not, and the
+ *              merge drops whatever that slot holds (bytes of an earlier
+ *              call, or anything) by selecting on the split's zero weight.
+ *              Two calls in flight at the same time must not share a
+ *              workspace.
  */
 int32_t ds4a_attn_decode_default_splits(const ds4a_layout *L);
 size_t ds4a_attn_decode_workspace_size(const ds4a_layout *L, int32_t n_splits);
@@ -238,7 +245,9 @@ ds4a_status ds4a_attn_decode(const ds4a_layout *L, const ds4a_tensors *X, int32_
  *                              sum_j p_j v_j / l, rounded to fp16
  *   float2 ml[I][64]           (m, l): p_j = 2^(log2(e) * (scale q.k_j + bias_j) - m),
  *                              l = sum_j p_j; m = -inf and l = 0 for a split with
- *                              no visible row (its o_part is then not written)
+ *                              no visible row (its o_part slot is then not
+ *                              written and may hold stale bytes; the merge
+ *                              never uses it, since its weight is 0)
  * The merge computes o = sum_s W_s o_s / L with W_s = 2^(m_s - M) l_s,
  * L = sum_s W_s, M = max_s m_s, and lse = (M + log2 L) * ln 2.  decode_partials ignores X->o
  * and X->lse; decode_merge reads only the workspace and writes X->o / X->lse
@@ -318,10 +327,12 @@ ds4a_status ds4a_attn_decode_batch(int32_t n_seq, const ds4a_layout *shape, cons
  *   (T * n_splits <= 127).  n_splits <= 0 picks the usual split count, capped to
  *   fit; a T or n_splits that cannot fit returns DS4A_ERR_WORKSPACE before any
  *   launch.  Nothing is allocated: no cudaMalloc, no cudaFree.
- *   The array needs no clearing: every byte a call reads was written earlier
- *   in the same call.  All calls share the one array, so calls whose kernels
- *   overlap on the GPU (different streams, or different host threads) race on
- *   it and must be serialised by the caller.
+ *   The array needs no clearing.  A call writes every (m, l) pair it reads;
+ *   the o_part slot of a split with no visible row keeps whatever an earlier
+ *   call left there, and the merge drops it by selecting on that split's zero
+ *   weight.  All calls share the one array, so calls whose kernels overlap on
+ *   the GPU (different streams, or different host threads) race on it and
+ *   must be serialised by the caller.
  *   The first call of the library on a device (any entry point) looks up the
  *   array's device address; make that first call before any stream capture.
  */

@@ -213,7 +213,7 @@ const char *ds4a_status_string(int status) {
   }
 }
 
-const char *ds4a_version(void) { return "ds4a 0.1 sm_103a"; }
+const char *ds4a_version(void) { return "ds4a 0.2 sm_103a"; }
 
 ds4a_status ds4a_pad_kv(const void *src, int64_t src_row_stride, int32_t n_rows, void *dst, int64_t dst_row_stride,
                         ds4a_stream_t stream) {

@@ -188,6 +188,8 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __half *
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.f;
   int s = 0;
+  // A split without visible rows left its o_part slot unwritten (stale bytes,
+  // possibly NaN): its weight is 0 and the branch never reads the slot.
   for (; s + 8 <= n_splits; s += 8) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -241,8 +243,9 @@ __global__ void __launch_bounds__(kCombineThreads) combine_wide_kernel(const __h
   const int d = 64 * chunk + 2 * lane;
   const __half *src = ws_o + (base * 64 + h) * 512 + d;
   const long long step = 64LL * 512;
-  // A split without visible rows left its partial unwritten (any bits): its
-  // weight is 0 and the select drops the value.
+  // A split without visible rows left its o_part slot unwritten (stale bytes,
+  // possibly NaN): the value is loaded, but its weight is 0 and the select
+  // (never a multiply, which would turn 0 * NaN into NaN) drops it.
   float2 acc = make_float2(0.f, 0.f);
   int s = warp;
   for (; s + 3 * kW < n_splits; s += 4 * kW) {
@@ -312,8 +315,9 @@ __global__ void __launch_bounds__(kCombineThreads) combine_small_kernel(const __
   float L = w;
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-  // A split without visible rows left its partial unwritten (any bits): its
-  // weight is 0 and the select drops the value.
+  // A split without visible rows left its o_part slot unwritten (stale bytes,
+  // possibly NaN): the value is loaded, but its weight is 0 and the select
+  // (never a multiply, which would turn 0 * NaN into NaN) drops it.
   float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
   for (int i = 0; i < kSmallMaxSplits; ++i) {

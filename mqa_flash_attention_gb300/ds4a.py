@@ -154,33 +154,93 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-def _rows(t, name):
-    """A [rows, 512] fp16 tensor with contiguous rows -> (pointer, byte stride)."""
+def _on_device(**named):
+    """Every given tensor must live on the current CUDA device: the kernels
+    dereference the pointers there, so a host tensor or one on another device
+    would be read out of bounds on the GPU rather than rejected."""
+    import torch
+    for name, t in named.items():
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor (got {t.device})")
+        if t.device.index != torch.cuda.current_device():
+            raise ValueError(f"{name} is on {t.device}, not on the current device cuda:{torch.cuda.current_device()}")
+
+
+def _n_blocks(L) -> int:
+    return -(-L.n_raw // BLOCK_ROWS) + -(-L.n_comp // BLOCK_ROWS)
+
+
+def _rows(t, name, need=0):
+    """A [rows, 512] fp16 tensor with contiguous rows -> (pointer, byte stride).
+    It must hold at least ``need`` rows (the rows the layout says it has)."""
     import torch
     if t is None:
+        if need > 0:
+            raise ValueError(f"{name} is missing but the layout has {need} rows")
         return None, ROW_BYTES
     if t.dtype != torch.float16 or t.dim() != 2 or t.shape[1] != D or t.stride(1) != 1:
         raise ValueError(f"{name} must be fp16 [rows, 512] with contiguous rows")
+    if t.shape[0] < need:
+        raise ValueError(f"{name} holds {t.shape[0]} rows, the layout needs {need}")
     return _ptr(t), t.stride(0) * 2
 
 
-def _tokens(t, name):
+def _tokens(t, name, T=None):
+    """A [T, 64, 512] fp16 tensor with contiguous heads -> (pointer, byte stride)."""
     import torch
     if t.dtype != torch.float16 or t.dim() != 3 or t.shape[1:] != (H, D) or t.stride(2) != 1 or t.stride(1) != D:
         raise ValueError(f"{name} must be fp16 [T, 64, 512] with contiguous heads")
+    if T is not None and t.shape[0] != T:
+        raise ValueError(f"{name} has {t.shape[0]} tokens, the layout has T = {T}")
     return _ptr(t), t.stride(0) * 2
 
 
-def _tensors(q, k_raw, v_raw, k_comp, v_comp, out, lse) -> Tensors:
-    qp, qs = _tokens(q, "q")
-    op, os_ = _tokens(out, "out")
-    krp, rs = _rows(k_raw, "k_raw")
-    vrp, rs2 = _rows(v_raw, "v_raw")
-    kcp, cs = _rows(k_comp, "k_comp")
-    vcp, cs2 = _rows(v_comp, "v_comp")
+def _lse_ok(lse, T):
+    import torch
+    if lse is None:
+        return
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (T, H) or not lse.is_contiguous():
+        raise ValueError(f"lse must be contiguous fp32 [{T}, 64]")
+
+
+def _tensors(L, q, k_raw, v_raw, k_comp, v_comp, out, lse, check_device=True) -> Tensors:
+    """Operands of one attention call, checked against the layout ``L``: token
+    counts, row counts, dtypes, strides and (unless the caller checks them
+    after its own size checks) devices."""
+    qp, qs = _tokens(q, "q", L.T)
+    op, os_ = _tokens(out, "out", L.T) if out is not None else (None, 0)
+    krp, rs = _rows(k_raw, "k_raw", L.n_raw)
+    vrp, rs2 = _rows(v_raw, "v_raw", L.n_raw)
+    kcp, cs = _rows(k_comp, "k_comp", L.n_comp)
+    vcp, cs2 = _rows(v_comp, "v_comp", L.n_comp)
     if rs != rs2 or cs != cs2:
         raise ValueError("K and V of a segment must share the row stride")
+    _lse_ok(lse, L.T)
+    if check_device:
+        _on_device(q=q, out=out, k_raw=k_raw, v_raw=v_raw, k_comp=k_comp, v_comp=v_comp, lse=lse)
     return Tensors(qp, qs, krp, vrp, rs, kcp, vcp, cs, op, os_, _ptr(lse))
+
+
+def _mask_ok(L, mask):
+    """A dense mask is fp16 [>= T, >= block_count * 32] with contiguous rows."""
+    import torch
+    if mask is None:
+        return
+    cols = _n_blocks(L) * BLOCK_ROWS
+    if mask.dtype != torch.float16 or mask.dim() != 2 or mask.stride(1) != 1:
+        raise ValueError("mask must be fp16 [T, block_count * 32] with contiguous rows")
+    if mask.shape[0] < L.T or mask.shape[1] < cols:
+        raise ValueError(f"mask is {tuple(mask.shape)}, the layout needs at least ({L.T}, {cols})")
+
+
+def _status_ok(L, status, q_tile, name):
+    """Status bytes are contiguous uint8 [ceil(T / q_tile), block_count]."""
+    import torch
+    want = (-(-L.T // int(q_tile)), _n_blocks(L))
+    if status.dtype != torch.uint8 or tuple(status.shape) != want or not status.is_contiguous():
+        raise ValueError(f"{name} must be contiguous uint8 {want}")
 
 
 def _outputs(q, out, lse, want_lse):
@@ -202,8 +262,9 @@ def pad_kv(src, n_rows: int | None = None, dst=None, stream=None):
     n_pad = -(-n // BLOCK_ROWS) * BLOCK_ROWS
     if dst is None:
         dst = torch.empty((n_pad, D), dtype=torch.float16, device=src.device)
-    sp, ss = _rows(src, "src")
-    dp, ds = _rows(dst, "dst")
+    sp, ss = _rows(src, "src", n)
+    dp, ds = _rows(dst, "dst", n_pad)
+    _on_device(src=src, dst=dst)
     _check(lib().ds4a_pad_kv(sp, ss, n, dp, ds, _stream(stream)), "ds4a_pad_kv")
     return dst
 
@@ -216,9 +277,14 @@ def block_mask(layout, q_tile: int, mask=None, out=None, stream=None):
     """Status bytes ``uint8 [ceil(T/q_tile), block_count]``."""
     import torch
     L = make_layout(layout)
-    nb = block_count(L)
+    if int(q_tile) < 1:
+        raise ValueError("q_tile must be >= 1")
+    nb = _n_blocks(L)
+    _mask_ok(L, mask)
     if out is None:
         out = torch.empty((-(-L.T // q_tile), nb), dtype=torch.uint8, device="cuda")
+    _status_ok(L, out, q_tile, "out")
+    _on_device(mask=mask, out=out)
     ms = 0 if mask is None else mask.stride(0) * 2
     _check(lib().ds4a_block_mask(ctypes.byref(L), _ptr(mask), ms, int(q_tile), _ptr(out), _stream(stream)),
            "ds4a_block_mask")
@@ -228,8 +294,14 @@ def block_mask(layout, q_tile: int, mask=None, out=None, stream=None):
 def attn_prefill(layout, q, k_raw, v_raw, k_comp=None, v_comp=None, *, mask=None, status=None, q_tile=1,
                  out=None, lse=None, want_lse=False, stream=None):
     L = make_layout(layout)
+    _mask_ok(L, mask)
+    if status is not None:
+        if mask is None:
+            raise ValueError("status bytes are read only with a dense mask")
+        _status_ok(L, status, q_tile, "status")
     out, lse = _outputs(q, out, lse, want_lse)
-    X = _tensors(q, k_raw, v_raw, k_comp, v_comp, out, lse)
+    X = _tensors(L, q, k_raw, v_raw, k_comp, v_comp, out, lse)
+    _on_device(mask=mask, status=status)
     ms = 0 if mask is None else mask.stride(0) * 2
     _check(lib().ds4a_attn_prefill(ctypes.byref(L), ctypes.byref(X), _ptr(mask), ms, _ptr(status), int(q_tile),
                                    _stream(stream)), "ds4a_attn_prefill")
@@ -249,10 +321,11 @@ def attn_decode(layout, q, k_raw, v_raw, k_comp=None, v_comp=None, *, n_splits=0
     import torch
     L = make_layout(layout)
     out, lse = _outputs(q, out, lse, want_lse)
-    X = _tensors(q, k_raw, v_raw, k_comp, v_comp, out, lse)
+    X = _tensors(L, q, k_raw, v_raw, k_comp, v_comp, out, lse)
     need = decode_workspace_bytes(L, n_splits)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _on_device(workspace=workspace)
     _check(lib().ds4a_attn_decode(ctypes.byref(L), ctypes.byref(X), int(n_splits), _ptr(workspace),
                                   workspace.numel() * workspace.element_size(), _stream(stream)),
            "ds4a_attn_decode")
@@ -279,11 +352,12 @@ def prepare_decode(layout, q, k_raw, v_raw, k_comp=None, v_comp=None, *, n_split
                    stream=None) -> PreparedCall:
     """:func:`attn_decode` on fixed buffers, as a :class:`PreparedCall`."""
     L = make_layout(layout)
-    X = _tensors(q, k_raw, v_raw, k_comp, v_comp, out, lse)
+    X = _tensors(L, q, k_raw, v_raw, k_comp, v_comp, out, lse)
     need = decode_workspace_bytes(L, n_splits)
     nbytes = workspace.numel() * workspace.element_size()
     if nbytes < need:
         raise ValueError(f"workspace of {nbytes} bytes, {need} needed")
+    _on_device(workspace=workspace)
     args = (ctypes.byref(L), ctypes.byref(X), int(n_splits), _ptr(workspace), nbytes, _stream(stream))
     return PreparedCall(lib().ds4a_attn_decode, "ds4a_attn_decode", args,
                         (L, X, q, k_raw, v_raw, k_comp, v_comp, workspace, out, lse, stream))
@@ -296,16 +370,26 @@ def attn_decode_fp8(layout, q, k_raw, v_raw, k_codes, k_scale, v_codes, v_scale,
     import torch
     L = make_layout(layout)
     out, lse = _outputs(q, out, lse, want_lse)
-    X = _tensors(q, k_raw, v_raw, None, None, out, lse)
+    L0 = make_layout(layout)
+    L0.n_comp = 0
+    X = _tensors(L0, q, k_raw, v_raw, None, None, out, lse, check_device=False)
     for c, nm in ((k_codes, "k_codes"), (v_codes, "v_codes")):
         if c.dtype != torch.uint8 or c.dim() != 2 or c.shape[1] != D or c.stride(1) != 1:
             raise ValueError(f"{nm} must be uint8 [n, 512] with contiguous rows")
+        if c.shape[0] < L.n_comp:
+            raise ValueError(f"{nm} holds {c.shape[0]} rows, the layout needs {L.n_comp}")
+    for sc, nm in ((k_scale, "k_scale"), (v_scale, "v_scale")):
+        if sc.dtype != torch.float32 or sc.dim() != 1 or sc.stride(0) != 1 or sc.shape[0] < L.n_comp:
+            raise ValueError(f"{nm} must be contiguous fp32 [>= {L.n_comp}]")
     if k_codes.stride(0) != v_codes.stride(0):
         raise ValueError("k_codes and v_codes must share the row stride")
+    _on_device(q=q, out=out, lse=lse, k_raw=k_raw, v_raw=v_raw, k_codes=k_codes, v_codes=v_codes, k_scale=k_scale,
+               v_scale=v_scale)
     X.k_comp, X.v_comp, X.comp_row_stride = k_codes.data_ptr(), v_codes.data_ptr(), k_codes.stride(0)
     need = decode_workspace_bytes(L, n_splits)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _on_device(workspace=workspace)
     _check(lib().ds4a_attn_decode_fp8(ctypes.byref(L), ctypes.byref(X), _ptr(k_scale), _ptr(v_scale), int(n_splits),
                                       _ptr(workspace), workspace.numel() * workspace.element_size(),
                                       _stream(stream)), "ds4a_attn_decode_fp8")
@@ -324,7 +408,9 @@ def attn_decode_batch(shape, seq_geom, q, k_raw, v_raw, k_comp=None, v_comp=None
         raise ValueError("seq_geom must be contiguous int32 [B, 4]")
     out, lse = _outputs(q, out, lse, want_lse)
     qp, qs = _tokens(q, "q")
-    op, os_ = _tokens(out, "out")
+    op, os_ = _tokens(out, "out", B)
+    _lse_ok(lse, B)
+    _on_device(seq_geom=seq_geom, q=q, out=out, lse=lse, k_raw=k_raw, v_raw=v_raw, k_comp=k_comp, v_comp=v_comp)
 
     def seg(k, v):
         if k is None:
@@ -344,6 +430,7 @@ def attn_decode_batch(shape, seq_geom, q, k_raw, v_raw, k_comp=None, v_comp=None
     need = lib().ds4a_attn_decode_batch_workspace_size(B, int(n_splits))
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _on_device(workspace=workspace)
     _check(lib().ds4a_attn_decode_batch(B, ctypes.byref(S), _ptr(seq_geom), ctypes.byref(X), int(n_splits),
                                         _ptr(workspace), workspace.numel() * workspace.element_size(),
                                         _stream(stream)), "ds4a_attn_decode_batch")
@@ -355,10 +442,10 @@ def attn_decode_partials(layout, q, k_raw, v_raw, k_comp=None, v_comp=None, *, n
     """First half of :func:`attn_decode`: per-split partials into ``workspace``."""
     import torch
     L = make_layout(layout)
-    X = _tensors(q, k_raw, v_raw, k_comp, v_comp, q, None)
-    X.o = None
+    X = _tensors(L, q, k_raw, v_raw, k_comp, v_comp, None, None)
     if workspace is None:
         workspace = torch.empty(max(decode_workspace_bytes(L, n_splits), 256), dtype=torch.uint8, device=q.device)
+    _on_device(workspace=workspace)
     _check(lib().ds4a_attn_decode_partials(ctypes.byref(L), ctypes.byref(X), int(n_splits), _ptr(workspace),
                                            workspace.numel() * workspace.element_size(), _stream(stream)),
            "ds4a_attn_decode_partials")
@@ -368,7 +455,9 @@ def attn_decode_partials(layout, q, k_raw, v_raw, k_comp=None, v_comp=None, *, n
 def attn_decode_merge(layout, workspace, *, n_splits=0, out, lse=None, stream=None):
     """Second half of :func:`attn_decode`: merges the partials into ``out``."""
     L = make_layout(layout)
-    op, os_ = _tokens(out, "out")
+    op, os_ = _tokens(out, "out", L.T)
+    _lse_ok(lse, L.T)
+    _on_device(workspace=workspace, out=out, lse=lse)
     X = Tensors(None, 0, None, None, ROW_BYTES, None, None, ROW_BYTES, op, os_, _ptr(lse))
     _check(lib().ds4a_attn_decode_merge(ctypes.byref(L), ctypes.byref(X), int(n_splits), _ptr(workspace),
                                         workspace.numel() * workspace.element_size(), _stream(stream)),
@@ -382,7 +471,7 @@ def attn_decode_noalloc(layout, q, k_raw, v_raw, k_comp=None, v_comp=None, *, n_
     array holds the split partials (for callers that cannot allocate)."""
     L = make_layout(layout)
     out, lse = _outputs(q, out, lse, want_lse)
-    X = _tensors(q, k_raw, v_raw, k_comp, v_comp, out, lse)
+    X = _tensors(L, q, k_raw, v_raw, k_comp, v_comp, out, lse)
     _check(lib().ds4a_attn_decode_noalloc(ctypes.byref(L), ctypes.byref(X), int(n_splits), _stream(stream)),
            "ds4a_attn_decode_noalloc")
     return (out, lse) if (want_lse or lse is not None) else out
@@ -393,8 +482,11 @@ def attn_indexed(layout, q, k_raw, v_raw, k_comp, v_comp, idx, *, out=None, lse=
     L = make_layout(layout)
     if idx.dtype != torch.int32 or idx.dim() != 2 or idx.stride(1) != 1:
         raise ValueError("idx must be int32 [T, top_k] with contiguous rows")
+    if idx.shape[0] < L.T:
+        raise ValueError(f"idx has {idx.shape[0]} lists, the layout has T = {L.T}")
     out, lse = _outputs(q, out, lse, want_lse)
-    X = _tensors(q, k_raw, v_raw, k_comp, v_comp, out, lse)
+    X = _tensors(L, q, k_raw, v_raw, k_comp, v_comp, out, lse)
+    _on_device(idx=idx)
     _check(lib().ds4a_attn_indexed(ctypes.byref(L), ctypes.byref(X), _ptr(idx), idx.stride(0) * 4, idx.shape[1],
                                    _stream(stream)), "ds4a_attn_indexed")
     return (out, lse) if (want_lse or lse is not None) else out
@@ -417,9 +509,17 @@ def indexer_scores(layout, q_idx, k_idx, head_weights, *, scale, relu=True, out=
     if w.dtype != torch.float32 or not w.is_contiguous() or tuple(w.shape) != (T, n_heads):
         raise ValueError("head_weights must be contiguous fp32 [T, n_heads]")
     n_comp = L.n_comp
+    if T != L.T:
+        raise ValueError(f"q_idx has {T} tokens, the layout has T = {L.T}")
+    if k_idx.shape[0] < n_comp:
+        raise ValueError(f"k_idx holds {k_idx.shape[0]} rows, the layout needs {n_comp}")
     if out is None:
         stride = (n_comp + 3) // 4 * 4
         out = torch.empty((T, stride), dtype=torch.float32, device=q_idx.device)[:, :n_comp]
+    if out.dtype != torch.float32 or out.dim() != 2 or out.stride(1) != 1 or out.shape[0] < T or \
+            out.shape[1] < n_comp:
+        raise ValueError(f"out must be fp32 [>= {T}, >= {n_comp}] with contiguous rows")
+    _on_device(q_idx=q_idx, k_idx=k_idx, head_weights=w, out=out)
     _check(lib().ds4a_indexer_scores(ctypes.byref(L), _ptr(q_idx), q_idx.stride(0) * 2, n_heads, head_dim,
                                      _ptr(k_idx), k_idx.stride(0) * 2, _ptr(w), float(scale), 1 if relu else 0,
                                      _ptr(out), out.stride(0) * 4, _stream(stream)), "ds4a_indexer_scores")
@@ -433,9 +533,15 @@ def indexer_topk(layout, scores, top_k, *, out=None, stream=None):
     if scores.dtype != torch.float32 or scores.dim() != 2 or scores.stride(1) != 1:
         raise ValueError("scores must be fp32 [T, >= n_comp] with contiguous rows")
     T = scores.shape[0]
+    if T < L.T or scores.shape[1] < L.n_comp:
+        raise ValueError(f"scores is {tuple(scores.shape)}, the layout needs at least ({L.T}, {L.n_comp})")
     if out is None:
         stride = (top_k + 3) // 4 * 4
         out = torch.empty((T, stride), dtype=torch.int32, device=scores.device)[:, :top_k]
+    if out.dtype != torch.int32 or out.dim() != 2 or out.stride(1) != 1 or out.shape[0] < L.T or \
+            out.shape[1] < top_k:
+        raise ValueError(f"out must be int32 [>= {L.T}, >= {top_k}] with contiguous rows")
+    _on_device(scores=scores, out=out)
     _check(lib().ds4a_indexer_topk(ctypes.byref(L), _ptr(scores), scores.stride(0) * 4, int(top_k), _ptr(out),
                                    out.stride(0) * 4, _stream(stream)), "ds4a_indexer_topk")
     return out
@@ -450,8 +556,12 @@ def quantize_kv_fp8(rows, *, codes=None, scales=None, stream=None):
         codes = torch.empty((n, 512), dtype=torch.uint8, device=rows.device)
     if scales is None:
         scales = torch.empty((n,), dtype=torch.float32, device=rows.device)
-    if codes.dtype != torch.uint8 or codes.dim() != 2 or codes.stride(1) != 1 or codes.shape[1] != 512:
-        raise ValueError("codes must be uint8 [n, 512] with contiguous rows")
+    if codes.dtype != torch.uint8 or codes.dim() != 2 or codes.stride(1) != 1 or codes.shape[1] != 512 or \
+            codes.shape[0] < n:
+        raise ValueError(f"codes must be uint8 [>= {n}, 512] with contiguous rows")
+    if scales.dtype != torch.float32 or scales.dim() != 1 or scales.stride(0) != 1 or scales.shape[0] < n:
+        raise ValueError(f"scales must be contiguous fp32 [>= {n}]")
+    _on_device(rows=rows, codes=codes, scales=scales)
     _check(lib().ds4a_quantize_kv_fp8(ptr, stride, n, _ptr(codes), codes.stride(0), _ptr(scales), _stream(stream)),
            "ds4a_quantize_kv_fp8")
     return codes, scales
@@ -491,6 +601,7 @@ def compress_append(kv, score, state_kv, state_score, n_state, ratio, *, out=Non
     if out.dtype != torch.float16 or out.dim() != 2 or out.shape[0] < n_out or out.shape[1] != width or \
             out.stride(1) != 1:
         raise ValueError("out must be fp16 [>= n_out, width] with contiguous rows")
+    _on_device(kv=kv, score=score, state_kv=state_kv, state_score=state_score, out=out)
     _check(lib().ds4a_compress_append(width, ratio, n_state, kp, sp, ks, n_new, stp, scp, sts, _ptr(out),
                                       out.stride(0) * 2, _stream(stream)), "ds4a_compress_append")
     return out[:n_out], (n_state + n_new) % ratio

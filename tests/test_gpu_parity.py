@@ -167,15 +167,16 @@ def test_prefill_tiny(torch, ds4a):
     assert_lse_close(host(lse), wlse, "tiny prefill lse")
 
 
-def test_prefill_raw_2048_sampled(torch, ds4a):
-    """Full-size 2048-token raw-only chunk; outputs compared on sampled tokens."""
+def test_prefill_raw_2048_all_tokens(torch, ds4a):
+    """Full-size 2048-token raw-only chunk, every output element of every
+    token against the oracle (output pre-filled with NaN)."""
     wl = W.prefill_raw_2048()
     d = upload(torch, wl)
-    o, lse = ds4a.attn_prefill(wl.layout, d["q"], d["k_raw"], d["v_raw"], want_lse=True)
-    toks = sorted(set([0, 1, 2, 126, 127, 128, 1023, 2046, 2047] + list(range(5, 2048, 97))))
-    want, wlse = oracle_out(wl, tokens=toks)
-    assert_close(host(o)[toks], want, "prefill 2048")
-    assert_lse_close(host(lse)[toks], wlse, "prefill 2048 lse")
+    out = torch.full_like(d["q"], float("nan"))
+    o, lse = ds4a.attn_prefill(wl.layout, d["q"], d["k_raw"], d["v_raw"], out=out, want_lse=True)
+    want, wlse = oracle_out(wl)
+    assert_close(host(o), want, "prefill 2048")
+    assert_lse_close(host(lse), wlse, "prefill 2048 lse")
 
 
 def _ragged_cases():
@@ -420,31 +421,41 @@ def test_decode_batch_matches_oracle(torch, ds4a):
 
 # ------------------------------------------------------------------ indexed
 
-def test_indexed_ratio4_sampled(torch, ds4a):
+def test_indexed_ratio4_all_tokens(torch, ds4a):
+    """Full-size indexed ratio-4 chunk (2048 tokens, top-512 of 8192 rows),
+    every token against the oracle (output pre-filled with NaN)."""
     wl = W.indexed_r4_2048()
     d = upload(torch, wl)
     idx = dev(torch, wl.idx)
-    o, lse = ds4a.attn_indexed(wl.layout, d["q"], d["k_raw"], d["v_raw"], d["k_comp"], d["v_comp"], idx,
+    out = torch.full_like(d["q"], float("nan"))
+    o, lse = ds4a.attn_indexed(wl.layout, d["q"], d["k_raw"], d["v_raw"], d["k_comp"], d["v_comp"], idx, out=out,
                                want_lse=True)
-    toks = sorted(set([0, 1, 127, 128, 1000, 2046, 2047] + list(range(3, 2048, 131))))
-    want, wlse = oracle_out(wl, tokens=toks, idx=wl.idx)
-    assert_close(host(o)[toks], want, "indexed")
-    assert_lse_close(host(lse)[toks], wlse, "indexed lse")
+    want, wlse = oracle_out(wl, idx=wl.idx)
+    assert_close(host(o), want, "indexed")
+    assert_lse_close(host(lse), wlse, "indexed lse")
 
 
 def test_indexed_edge_cases(torch, ds4a):
-    L = make_layout(T=5, q_pos0=700, n_raw=140, raw_pos0=600, n_comp=175, ratio=4)
+    L = make_layout(T=7, q_pos0=700, n_raw=140, raw_pos0=600, n_comp=175, ratio=4)
     wl = W.draw("idx_edge", 68, L)
-    idx = np.full((5, 200), -1, np.int32)
+    idx = np.full((7, 200), -1, np.int32)
     idx[0, :3] = [4, 4, 9]                         # duplicates
     idx[1, 50:60] = np.arange(10)                  # -1 around the entries
     idx[2, :] = np.arange(200) % 175               # every row, some twice
     idx[3, 0] = 174
     idx[4, 199] = 0                                # last slot only
+    idx[5, :6] = [175, 3, 176, 2 ** 31 - 1, 8, 100000]   # entries past the last row are empty slots
+    idx[6, 10:140] = np.arange(175, 305)           # only entries past the last row: raw window alone
     d = upload(torch, wl)
-    o = ds4a.attn_indexed(L, d["q"], d["k_raw"], d["v_raw"], d["k_comp"], d["v_comp"], dev(torch, idx))
-    want, _ = oracle_out(wl, idx=idx)
+    o, lse = ds4a.attn_indexed(L, d["q"], d["k_raw"], d["v_raw"], d["k_comp"], d["v_comp"], dev(torch, idx),
+                               want_lse=True)
+    want, wlse = oracle_out(wl, idx=idx)
     assert_close(host(o), want, "indexed edges")
+    assert_lse_close(host(lse), wlse, "indexed edges lse")
+    # entries past the last row behave exactly like -1 (bit-identical output)
+    idx_m1 = np.where(idx >= 175, -1, idx).astype(np.int32)
+    o2 = ds4a.attn_indexed(L, d["q"], d["k_raw"], d["v_raw"], d["k_comp"], d["v_comp"], dev(torch, idx_m1))
+    assert np.array_equal(host(o2).view(np.uint16), host(o).view(np.uint16))
 
 
 def test_indexed_all_available_equals_dense(torch, ds4a):
