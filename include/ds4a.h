@@ -51,6 +51,9 @@
  *     16-byte aligned.  Q and O are [T][64][512]: heads contiguous (1024 bytes
  *     apart), token stride in bytes (>= 65536, multiple of 16).
  *   - K and V may alias (k == v), as in an engine that stores one KV row.
+ *     Then every row is read once and serves both Q.K and the V weighting
+ *     (fp16 rows; the E4M3 rows of ds4a_attn_decode_fp8 are read as two
+ *     arrays even when they alias).
  *   - Rows that a token cannot see must still hold finite values (pad rows
  *     written by ds4a_pad_kv are +0.0): an invisible row gets weight 0, and
  *     0 * inf or 0 * nan would poison the sum.

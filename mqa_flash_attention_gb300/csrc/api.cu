@@ -167,6 +167,10 @@ ds4a_status fill_params(AttnParams &p, const ds4a_layout *L, const ds4a_tensors 
   p.k_comp = X->k_comp;
   p.v_comp = X->v_comp;
   p.comp_row_stride = X->comp_row_stride;
+  // One row serving as K and V (the pointers are equal; a segment has one row
+  // stride): each tile part is loaded once for both products.
+  p.alias_raw = (L->n_raw > 0 && X->k_raw == X->v_raw) ? 1 : 0;
+  p.alias_comp = (L->n_comp > 0 && X->k_comp == X->v_comp) ? 1 : 0;
   p.q_ptr = static_cast<const uint8_t *>(X->q);
   p.q_tok_bytes = X->q_tok_stride;
   p.T = L->T;
@@ -651,6 +655,8 @@ ds4a_status ds4a_attn_decode_batch(int32_t n_seq, const ds4a_layout *shape, cons
   p.n_splits = n_splits;
   p.q_tile = 1;
   p.batch_geom = reinterpret_cast<const int4 *>(seq_geom);
+  p.alias_raw = (X->raw_rows > 0 && X->k_raw == X->v_raw) ? 1 : 0;
+  p.alias_comp = (X->comp_rows > 0 && X->k_comp == X->v_comp) ? 1 : 0;
   p.partial = 1;
   __half *ws_o = static_cast<__half *>(workspace);
   float2 *ws_ml = reinterpret_cast<float2 *>(static_cast<uint8_t *>(workspace) +

@@ -148,6 +148,15 @@ __device__ __forceinline__ int count_tiles(const AttnParams &p, const TokenTiles
   return c;
 }
 
+// K/V parts of a tile in ring order: 4 K parts then 4 V parts, or only the 4
+// K parts when the segment's K and V are the same rows.  Then each K part
+// stays in the ring after QK^T and serves PV as V^T: a part holds 128 dims of
+// every row of the tile, which is the K-major A operand of QK^T and the
+// MN-major A operand of PV alike, so each row crosses into the SM once.
+__device__ __forceinline__ bool tile_aliased(const AttnParams &p, const Tile &tl) {
+  return (tl.seg == 0 ? p.alias_raw : p.alias_comp) != 0;
+}
+
 struct TileCursor {
   TokenTiles z;
   int cand;
@@ -363,8 +372,9 @@ __device__ __forceinline__ void loader_role(const AttnParams &p, uint32_t sbase,
         }
         named_bar_sync(2, kLoaderThreads);
       }
+      const int n_parts = tile_aliased(p, tl) ? 4 : 8;
 #pragma unroll 1
-      for (int part = 0; part < 8; ++part) {  // parts 0-3: K dims 128*part, parts 4-7: V
+      for (int part = 0; part < n_parts; ++part) {  // parts 0-3: K dims 128*part, parts 4-7: V
         // Every thread waits for the slot itself (bounded); a thread that gives
         // up stops filling, and the group meets at the next tile's barrier.
         if (!mbar_wait(smem_u32(&ms.kv_empty[ring.st]), ring.ph ^ 1, abrt, p.timeout_ns, p.err, SITE_KV_EMPTY)) {
@@ -457,8 +467,9 @@ __device__ __forceinline__ void converter_role(const AttnParams &p, uint32_t sba
     if (ip.j1 == ip.j0) continue;
     for (int j = ip.j0; j < ip.j1 && ok; ++j) {
       const Tile tl = ip.cur.next(p);
+      const int n_parts = tile_aliased(p, tl) ? 4 : 8;  // E4M3 rows are never aliased
 #pragma unroll 1
-      for (int part = 0; part < 8; ++part) {
+      for (int part = 0; part < n_parts; ++part) {
         if (tl.seg == 1) {
           const uint32_t st = ring.st;
           ok = mbar_wait(smem_u32(&ms.code_full[st]), (code_ph >> st) & 1u, abrt, p.timeout_ns, p.err,
@@ -533,6 +544,9 @@ __device__ __forceinline__ void mma_role(const AttnParams &p, uint32_t sbase, ui
       if (!ok) break;
       const int nt = ip.j1 - ip.j0;
       for (int jj = 0; jj < nt && ok; ++jj) {
+        const Tile tl = ip.cur.next(p);
+        const bool alias = tile_aliased(p, tl);
+        const uint32_t k0 = ring.st;  // aliased: K part m sits in stage (k0 + m) % kStages until PV m
         const uint32_t sb = g & 1;
         ok = mbar_wait(smem_u32(&ms.s_empty[sb]), ((g >> 1) & 1) ^ 1, abrt, p.timeout_ns, p.err, SITE_S_EMPTY);
         if (!ok) break;
@@ -557,7 +571,7 @@ __device__ __forceinline__ void mma_role(const AttnParams &p, uint32_t sbase, ui
                 umma_f16_acc(d_s, a, b, kIdescQK);
             }
           }
-          umma_commit(smem_u32(&ms.kv_empty[ring.st]));
+          if (!alias) umma_commit(smem_u32(&ms.kv_empty[ring.st]));  // aliased: held for PV
           ring.advance();
         }
         if (!ok) break;
@@ -572,10 +586,14 @@ __device__ __forceinline__ void mma_role(const AttnParams &p, uint32_t sbase, ui
         tc_fence_after();
         // O^T[m] += V_tile^T[dims 128m..] . P^T, 16 rows per instruction.
         for (int m = 0; m < 4 && ok; ++m) {
-          ok = mbar_wait(smem_u32(&ms.kv_full[ring.st]), ring.ph, abrt, p.timeout_ns, p.err, SITE_KV_FULL);
-          if (!ok) break;
-          tc_fence_after();
-          const uint64_t a0 = sdesc_add(v_desc, ring.st * kStageBytes);
+          uint32_t vst = (k0 + m) % kStages;  // aliased: the K part of the same dims, already landed
+          if (!alias) {
+            ok = mbar_wait(smem_u32(&ms.kv_full[ring.st]), ring.ph, abrt, p.timeout_ns, p.err, SITE_KV_FULL);
+            if (!ok) break;
+            tc_fence_after();
+            vst = ring.st;
+          }
+          const uint64_t a0 = sdesc_add(v_desc, vst * kStageBytes);
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
             const uint64_t a = sdesc_add(a0, ks * 2048);
@@ -585,11 +603,11 @@ __device__ __forceinline__ void mma_role(const AttnParams &p, uint32_t sbase, ui
             else
               umma_f16_acc(tmem + 64 * m, a, b, kIdescPV);
           }
-          umma_commit(smem_u32(&ms.kv_empty[ring.st]));
+          umma_commit(smem_u32(&ms.kv_empty[vst]));
           // After the item's last tile, block m of O^T is final: the epilogue
           // drains it while the remaining blocks are still being computed.
           if (jj == nt - 1) umma_commit(smem_u32(&ms.o_full[m]));
-          ring.advance();
+          if (!alias) ring.advance();
         }
         if (!ok) break;
         umma_commit(smem_u32(&ms.p_empty));

@@ -93,6 +93,7 @@ struct AttnParams {
   const uint8_t *status;
   int q_tile, n_blocks, nbr;  // nbr = raw blocks (ceil(n_raw / 32))
   int comp_fp8;            // 1: compressed rows are E4M3 codes with per-row scales (k_scale, v_scale)
+  int alias_raw, alias_comp;  // 1: K and V of the segment are the same rows (each part loaded once)
   const int4 *batch_geom;  // batched decode: per sequence (q_pos, n_raw, raw_pos0, n_comp); "token" t = sequence t
   __half *o;
   long long o_tok_stride;  // elements

@@ -244,6 +244,67 @@ def test_aliased_k_and_v(torch, ds4a):
     assert_close(got, want, "k == v")
 
 
+@pytest.mark.parametrize("name", ["decode_r128_32k", "prefill_raw_2048", "indexed_r4_2048", "decode_long_65536",
+                                  "mixed_segments"])
+def test_aliased_k_and_v_configs(torch, ds4a, name):
+    """One row serving as K and V (the pointers alias, as in an engine that
+    stores one KV row): each tile part is loaded once and used by both
+    products.  Against the oracle on the same rows used as K and V, on the
+    decode, prefill, indexed and long-decode workloads; "mixed_segments"
+    aliases the raw rows only (compressed K and V stay distinct)."""
+    if name == "decode_r128_32k":
+        wl = W.decode_r128_32k()
+    elif name == "prefill_raw_2048":
+        wl = W.prefill_raw_2048()
+    elif name == "indexed_r4_2048":
+        wl = W.indexed_r4_2048()
+    elif name == "decode_long_65536":
+        wl = W.decode_long(65536)
+    else:
+        wl = W.draw("alias_mixed", 75, make_layout(T=5, q_pos0=40000, n_raw=200, raw_pos0=39873, n_comp=312,
+                                                    ratio=128))
+    wl.v_raw = wl.k_raw
+    if name != "mixed_segments":
+        wl.v_comp = wl.k_comp
+    L = wl.layout
+    kr = dev(torch, wl.k_raw)
+    kc = dev(torch, wl.k_comp) if L["n_comp"] else None
+    vc = kc if name != "mixed_segments" else dev(torch, wl.v_comp)
+    q = dev(torch, wl.q)
+    idx = wl.idx if name == "indexed_r4_2048" else None
+    want, wlse = oracle_out(wl, idx=idx)
+    out = torch.full_like(q, float("nan"))
+    if idx is not None:
+        o, lse = ds4a.attn_indexed(L, q, kr, kr, kc, vc, dev(torch, idx), out=out, want_lse=True)
+    elif L["T"] > 8:
+        o, lse = ds4a.attn_prefill(L, q, kr, kr, kc, vc, out=out, want_lse=True)
+    else:
+        o, lse = ds4a.attn_decode(L, q, kr, kr, kc, vc, out=out, want_lse=True)
+    assert_close(host(o), want, f"aliased {name}")
+    assert_lse_close(host(lse), wlse, f"aliased {name} lse")
+    if L["T"] <= 8:   # the prefill kernel on the same aliased rows
+        o2 = ds4a.attn_prefill(L, q, kr, kr, kc, vc)
+        assert_close(host(o2), want, f"aliased {name} prefill")
+
+
+def test_aliased_decode_batch(torch, ds4a):
+    """Batched decode with K and V of both segments aliased."""
+    from mqa_flash_attention_gb300 import synth
+    geo = [(32767, 128, 32640, 256), (5000, 200, 4801, 39), (1000, 60, 941, 7)]
+    B, R, C = len(geo), 200, 300
+    q = synth.normal_f16(76, synth.STREAM_Q, (B, 64, 512))
+    kr = synth.normal_f16(76, synth.STREAM_K_RAW, (B, R, 512))
+    kc = synth.normal_f16(76, synth.STREAM_K_COMP, (B, C, 512))
+    g = dev(torch, np.array(geo, dtype=np.int32))
+    shape = make_layout(T=1, q_pos0=0, n_raw=0, raw_pos0=0, n_comp=0, ratio=128)
+    dkr, dkc = dev(torch, kr), dev(torch, kc)
+    o = host(ds4a.attn_decode_batch(shape, g, dev(torch, q), dkr, dkr, dkc, dkc))
+    for b, (qp, nr, rp, nc) in enumerate(geo):
+        L = make_layout(T=1, q_pos0=qp, n_raw=nr, raw_pos0=rp, n_comp=nc, ratio=128)
+        want, _ = oracle.attention(L, q[b:b + 1], kr[b, :nr], kr[b, :nr], kc[b, :nc], kc[b, :nc])
+        assert_close(o[b:b + 1], want, f"aliased batch seq {b}")
+
+
 def test_large_score_rescale_path(torch, ds4a):
     """Rows whose scores jump far above the running max in later tiles force
     the lazy reference to move and O to be rescaled (twice for token 0)."""
