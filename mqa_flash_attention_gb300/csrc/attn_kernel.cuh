@@ -172,6 +172,13 @@ struct TileCursor {
   }
 };
 
+// The plan of an item reads memory the caller (or the previous kernel in the
+// stream) wrote: status bytes in dense-mask mode, the per-sequence geometry in
+// batched decode.  Roles then wait for the previous grid before planning.
+__device__ __forceinline__ bool plan_reads_inputs(const AttnParams &p) {
+  return (p.mode == MODE_MASK && p.status != nullptr) || p.batch_geom != nullptr;
+}
+
 // Work item -> token, tile range [j0, j1) and a cursor positioned at j0.
 struct ItemPlan {
   int t, j0, j1;
@@ -279,7 +286,7 @@ __device__ __noinline__ void q_copy_role(const AttnParams &p, uint32_t sbase, Mi
   volatile int *abrt = &ms.abort_flag;
   const uint32_t b_q_full = smem_u32(&ms.q_full), b_q_empty = smem_u32(&ms.q_empty);
   const int n_items = p.T * p.n_splits;
-  const bool plan_reads_status = p.mode == MODE_MASK && p.status != nullptr;
+  const bool plan_reads_status = plan_reads_inputs(p);
   if (plan_reads_status) grid_dependency_wait();
   uint32_t n_item = 0;
   for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
@@ -339,8 +346,8 @@ __device__ __forceinline__ void loader_role(const AttnParams &p, uint32_t sbase,
   const uint8_t *vbase = reinterpret_cast<const uint8_t *>(p.v_comp);
 
   const int n_items = p.T * p.n_splits;
-  const bool plan_reads_status = p.mode == MODE_MASK && p.status != nullptr;
-  if (plan_reads_status) grid_dependency_wait();  // the plan reads the caller's status bytes
+  const bool plan_reads_status = plan_reads_inputs(p);
+  if (plan_reads_status) grid_dependency_wait();  // the plan reads status bytes or sequence geometry
   for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
     ItemPlan ip = plan_item(p, item);
     if (ip.j1 == ip.j0) continue;
@@ -462,6 +469,7 @@ __device__ __forceinline__ void converter_role(const AttnParams &p, uint32_t sba
   uint32_t code_ph = 0;
   bool ok = true;
   const int n_items = p.T * p.n_splits;
+  if (plan_reads_inputs(p)) grid_dependency_wait();
   for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
     ItemPlan ip = plan_item(p, item);
     if (ip.j1 == ip.j0) continue;
@@ -536,7 +544,7 @@ __device__ __forceinline__ void mma_role(const AttnParams &p, uint32_t sbase, ui
     uint32_t g = 0, n_item = 0;
     bool ok = true;
     const int n_items = p.T * p.n_splits;
-    if (p.mode == MODE_MASK && p.status != nullptr) grid_dependency_wait();  // the plan reads status bytes
+    if (plan_reads_inputs(p)) grid_dependency_wait();  // the plan reads status bytes or sequence geometry
     for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
       ItemPlan ip = plan_item(p, item);
       if (ip.j1 == ip.j0) continue;
@@ -905,8 +913,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   // Let the next kernel in the stream start its own prologue.  Inputs may come
   // from the previous kernel: each role waits for it just before its first
   // global access (the loader after planning its first item, so that work
-  // overlaps the previous kernel's tail; the MMA warp touches no global memory
-  // except the status bytes its plan reads in dense-mask mode).
+  // overlaps the previous kernel's tail, unless the plan itself reads inputs:
+  // status bytes in dense-mask mode, the sequences' geometry in batched
+  // decode).
   grid_launch_dependents();
 
   if (warp < kComputeWarps) {
