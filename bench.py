@@ -618,6 +618,29 @@ def run_also(torch, ds4a, W, dev, stream, pk, pk_kind):
                     "algorithmic_flops": fl, "algorithmic_bytes": by})
         del sets
 
+    def sec_prefill_fp8kv():
+        # the same prefill chunk with E4M3 raw rows (codes + one fp32 scale per row)
+        wl = W.prefill_raw_2048()
+        sets = []
+        for _ in range(2):
+            kr, vr = up(wl.k_raw), up(wl.v_raw)
+            kc, ks = ds4a.quantize_kv_fp8(kr, stream=stream)
+            vc, vs = ds4a.quantize_kv_fp8(vr, stream=stream)
+            sets.append([up(wl.q), kc, ks, vc, vs, torch.empty(wl.q.shape, dtype=torch.float16, device=dev)])
+        torch.cuda.synchronize()
+        sec = timed(lambda i: ds4a.attn_prefill_fp8kv(wl.layout, sets[i % 2][0], sets[i % 2][1], sets[i % 2][3],
+                                                      k_raw_scale=sets[i % 2][2], v_raw_scale=sets[i % 2][4],
+                                                      out=sets[i % 2][5], stream=stream), 10)
+        fl = attn_flops(wl.layout)
+        n = wl.layout["n_raw"]
+        by = 2 * wl.q.nbytes + 2 * n * (512 + 4)
+        out.append({"workload": wl.name + "_fp8kv", "us_per_call": round(sec * 1e6, 2),
+                    "tflops": round(fl / sec / 1e12, 1), "frac_tensor": round(fl / sec / 1e12 / pk["bf16_tflops"], 4),
+                    "hbm_gbs": round(by / sec / 1e9, 1), "frac_hbm": round(by / sec / 1e9 / pk["hbm_gbs"], 4),
+                    "algorithmic_flops": fl, "algorithmic_bytes": by,
+                    "note": "raw K/V rows as E4M3 codes with per-row scales"})
+        del sets
+
     def sec_indexed():
         # indexed ratio-4, T = 2048, top-512
         wl = W.indexed_r4_2048()
@@ -763,7 +786,7 @@ def run_also(torch, ds4a, W, dev, stream, pk, pk_kind):
 
     # Each line is measured on its own: a failure (for instance too little memory on a smaller
     # device) becomes an entry with the error instead of losing the benchmark line.
-    for sec_fn in (sec_prefill, sec_indexed, sec_decode_sweep, sec_decode_256k_fp16_and_fp8, sec_decode_batch64,
+    for sec_fn in (sec_prefill, sec_prefill_fp8kv, sec_indexed, sec_decode_sweep, sec_decode_256k_fp16_and_fp8, sec_decode_batch64,
                    sec_indexer, sec_compressor_prefill, sec_compressor_decode):
         try:
             sec_fn()

@@ -51,9 +51,10 @@
  *     16-byte aligned.  Q and O are [T][64][512]: heads contiguous (1024 bytes
  *     apart), token stride in bytes (>= 65536, multiple of 16).
  *   - K and V may alias (k == v), as in an engine that stores one KV row.
- *     Then every row is read once and serves both Q.K and the V weighting
- *     (fp16 rows; the E4M3 rows of ds4a_attn_decode_fp8 are read as two
- *     arrays even when they alias).
+ *     When they alias in every segment that has rows, every row is read once
+ *     and serves both Q.K and the V weighting (fp16 rows; E4M3 rows are read
+ *     as two arrays even when they alias, and so are calls where only one
+ *     segment aliases).
  *   - Rows that a token cannot see must still hold finite values (pad rows
  *     written by ds4a_pad_kv are +0.0): an invisible row gets weight 0, and
  *     0 * inf or 0 * nan would poison the sum.
@@ -274,10 +275,40 @@ ds4a_status ds4a_attn_decode_merge(const ds4a_layout *L, const ds4a_tensors *X, 
  *                         bytes (>= 512, multiple of 16), 16-byte aligned.
  *   k_comp_scale, v_comp_scale  fp32 [n_comp] row scales.
  *   n_splits, workspace   as for ds4a_attn_decode (same workspace size).
+ * Equivalent to ds4a_attn_decode_fp8kv with fp16 raw rows (below).
  */
 ds4a_status ds4a_attn_decode_fp8(const ds4a_layout *L, const ds4a_tensors *X, const float *k_comp_scale,
                                  const float *v_comp_scale, int32_t n_splits, void *workspace,
                                  size_t workspace_bytes, ds4a_stream_t stream);
+
+/*
+ * ds4a_attn_decode_fp8kv / ds4a_attn_prefill_fp8kv - decode (split-KV, as
+ * ds4a_attn_decode) and structural prefill (as ds4a_attn_prefill without a
+ * mask) over E4M3 rows, the raw rows included when their scales are given
+ * ([P2] "Whole-Model Graph Execution": K/V rows are quantised to FP8 before
+ * they are stored, raw rows as well as compressed ones; "GPU Backend
+ * Architecture": DS4-specific FP8 KV quantization).  The format is that of
+ * ds4a_quantize_kv_fp8; a row's value is decode(code) * scale and the result
+ * is the attention over those values, within the usual fp16/fp32 tolerance.
+ *   S->k_comp, S->v_comp  fp32 [n_comp] scales of the E4M3 compressed rows
+ *                         X->k_comp / X->v_comp (uint8 [n_comp][512] at
+ *                         X->comp_row_stride bytes: >= 512, multiple of 16).
+ *   S->k_raw, S->v_raw    fp32 [n_raw] scales of E4M3 raw rows (X->k_raw /
+ *                         X->v_raw then uint8 [n_raw][512] at X->raw_row_stride
+ *                         bytes, >= 512, multiple of 16), or both NULL: the raw
+ *                         rows are fp16 as in ds4a_attn_decode.
+ *   n_splits, workspace   (decode) as for ds4a_attn_decode, same workspace size.
+ * K and V are read as two arrays even when their pointers are equal.
+ */
+typedef struct {
+  const float *k_raw, *v_raw;
+  const float *k_comp, *v_comp;
+} ds4a_fp8_scales;
+
+ds4a_status ds4a_attn_decode_fp8kv(const ds4a_layout *L, const ds4a_tensors *X, const ds4a_fp8_scales *S,
+                                   int32_t n_splits, void *workspace, size_t workspace_bytes, ds4a_stream_t stream);
+ds4a_status ds4a_attn_prefill_fp8kv(const ds4a_layout *L, const ds4a_tensors *X, const ds4a_fp8_scales *S,
+                                    ds4a_stream_t stream);
 
 /*
  * ds4a_attn_decode_batch - one decode step for n_seq independent sequences in

@@ -167,10 +167,11 @@ ds4a_status fill_params(AttnParams &p, const ds4a_layout *L, const ds4a_tensors 
   p.k_comp = X->k_comp;
   p.v_comp = X->v_comp;
   p.comp_row_stride = X->comp_row_stride;
-  // One row serving as K and V (the pointers are equal; a segment has one row
-  // stride): each tile part is loaded once for both products.
-  p.alias_raw = (L->n_raw > 0 && X->k_raw == X->v_raw) ? 1 : 0;
-  p.alias_comp = (L->n_comp > 0 && X->k_comp == X->v_comp) ? 1 : 0;
+  // One row serving as K and V in every segment that has rows (the pointers
+  // are equal; a segment has one row stride): each tile part is loaded once
+  // for both products.  A call whose segments differ reads K and V apart.
+  p.alias_kv = ((L->n_raw == 0 || X->k_raw == X->v_raw) && (L->n_comp == 0 || X->k_comp == X->v_comp) &&
+                L->n_raw + L->n_comp > 0) ? 1 : 0;
   p.q_ptr = static_cast<const uint8_t *>(X->q);
   p.q_tok_bytes = X->q_tok_stride;
   p.T = L->T;
@@ -492,25 +493,83 @@ ds4a_status ds4a_attn_decode(const ds4a_layout *L, const ds4a_tensors *X, int32_
                                        X->o_tok_stride / 2, X->lse, as_cuda(stream)));
 }
 
-ds4a_status ds4a_attn_decode_fp8(const ds4a_layout *L, const ds4a_tensors *X, const float *k_comp_scale,
-                                 const float *v_comp_scale, int32_t n_splits, void *workspace,
-                                 size_t workspace_bytes, ds4a_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+bool e4m3_rows_ok(const void *k, const void *v, int64_t stride) {
+  return k != nullptr && v != nullptr && aligned(k, 16) && aligned(v, 16) && stride >= DS4A_HEAD_DIM &&
+         stride % 16 == 0 && stride < (1LL << 39);
+}
+
+bool scales_ok(const float *k, const float *v) { return k != nullptr && v != nullptr && aligned(k, 4) && aligned(v, 4); }
+
+// E4M3 rows as bytes: {512, rows}, box {128 codes, 128 rows}, no swizzle.
+ds4a_status encode_codes(CUtensorMap *m, const void *codes, int rows, int64_t stride) {
+  const cuuint64_t dims[2] = {DS4A_HEAD_DIM, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)stride};
+  const cuuint32_t box[2] = {128, 128};
+  return encode(m, codes, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_DATA_TYPE_UINT8);
+}
+
+// Checks and kernel parameters of an attention call whose compressed rows (and
+// raw rows, when S->k_raw is given) are E4M3 codes with per-row scales.
+ds4a_status e4m3_params(AttnParams &p, const ds4a_layout *L, const ds4a_tensors *X, const ds4a_fp8_scales *S,
+                        DeviceState **dev) {
+  ds4a_status st = check_layout(L);
+  if (st != DS4A_OK) return st;
+  if (X == nullptr || S == nullptr) return DS4A_ERR_INVALID_ARG;
+  const bool raw_fp8 = S->k_raw != nullptr || S->v_raw != nullptr;
+  // Q, O and the fp16 rows as usual (checked with the E4M3 segments left out).
+  ds4a_layout L0 = *L;
+  L0.n_comp = 0;
+  if (raw_fp8) L0.n_raw = 0;
+  st = check_tensors(&L0, X);
+  if (st != DS4A_OK) return st;
+  if (L->n_comp > 0 && (!e4m3_rows_ok(X->k_comp, X->v_comp, X->comp_row_stride) || !scales_ok(S->k_comp, S->v_comp)))
+    return DS4A_ERR_INVALID_ARG;
+  if (raw_fp8 && L->n_raw > 0 && (!e4m3_rows_ok(X->k_raw, X->v_raw, X->raw_row_stride) || !scales_ok(S->k_raw, S->v_raw)))
+    return DS4A_ERR_INVALID_ARG;
+  st = current_device(dev);
+  if (st != DS4A_OK) return st;
+  st = fill_params(p, &L0, X, ds4a::MODE_STRUCT, *dev);  // fp16 tensor maps only for fp16 segments
+  if (st != DS4A_OK) return st;
+  p.n_raw = L->n_raw;
+  p.n_comp = L->n_comp;
+  p.ratio = L->n_comp > 0 ? L->ratio : 1;
+  p.nbr = ceil_div(L->n_raw, DS4A_BLOCK_ROWS);
+  p.n_blocks = p.nbr + ceil_div(L->n_comp, DS4A_BLOCK_ROWS);
+  p.comp_fp8 = 1;  // selects the E4M3 instantiation of the kernel
+  p.raw_fp8 = raw_fp8 ? 1 : 0;
+  p.alias_kv = 0;  // the E4M3 path reads K and V as two arrays
+  if (L->n_comp > 0) {
+    if ((st = encode_codes(&p.tm_k8[1], X->k_comp, L->n_comp, X->comp_row_stride)) != DS4A_OK) return st;
+    if ((st = encode_codes(&p.tm_v8[1], X->v_comp, L->n_comp, X->comp_row_stride)) != DS4A_OK) return st;
+  }
+  if (raw_fp8 && L->n_raw > 0) {
+    if ((st = encode_codes(&p.tm_k8[0], X->k_raw, L->n_raw, X->raw_row_stride)) != DS4A_OK) return st;
+    if ((st = encode_codes(&p.tm_v8[0], X->v_raw, L->n_raw, X->raw_row_stride)) != DS4A_OK) return st;
+  }
+  p.k_scale[0] = S->k_raw;
+  p.v_scale[0] = S->v_raw;
+  p.k_scale[1] = S->k_comp;
+  p.v_scale[1] = S->v_comp;
+  return DS4A_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+ds4a_status ds4a_attn_decode_fp8kv(const ds4a_layout *L, const ds4a_tensors *X, const ds4a_fp8_scales *S,
+                                   int32_t n_splits, void *workspace, size_t workspace_bytes, ds4a_stream_t stream) {
   ds4a_status st = check_layout(L);
   if (st != DS4A_OK) return st;
   if (L->T == 0) return DS4A_OK;
-  if (X == nullptr) return DS4A_ERR_INVALID_ARG;
-  // Q, O and the fp16 raw rows as usual (checked with the compressed rows left out).
-  ds4a_layout L0 = *L;
-  L0.n_comp = 0;
-  st = check_tensors(&L0, X);
+  AttnParams p;
+  DeviceState *d = nullptr;
+  st = e4m3_params(p, L, X, S, &d);
   if (st != DS4A_OK) return st;
-  if (L->n_comp > 0) {
-    if (X->k_comp == nullptr || X->v_comp == nullptr || !aligned(X->k_comp, 16) || !aligned(X->v_comp, 16) ||
-        X->comp_row_stride < DS4A_HEAD_DIM || X->comp_row_stride % 16 != 0 || X->comp_row_stride >= (1LL << 39))
-      return DS4A_ERR_INVALID_ARG;
-    if (k_comp_scale == nullptr || v_comp_scale == nullptr || !aligned(k_comp_scale, 4) || !aligned(v_comp_scale, 4))
-      return DS4A_ERR_INVALID_ARG;
-  }
   if (n_splits <= 0) n_splits = ds4a_attn_decode_default_splits(L);
   if (n_splits > 4096) return DS4A_ERR_INVALID_ARG;
   const size_t need = ds4a_attn_decode_workspace_size(L, n_splits);
@@ -520,29 +579,6 @@ ds4a_status ds4a_attn_decode_fp8(const ds4a_layout *L, const ds4a_tensors *X, co
   __half *ws_o = static_cast<__half *>(workspace);
   float2 *ws_ml = reinterpret_cast<float2 *>(static_cast<uint8_t *>(workspace) +
                                              n_items * DS4A_HEADS * DS4A_HEAD_DIM * sizeof(__half));
-  DeviceState *d = nullptr;
-  st = current_device(&d);
-  if (st != DS4A_OK) return st;
-  AttnParams p;
-  st = fill_params(p, &L0, X, ds4a::MODE_STRUCT, d);  // no fp16 tensor maps for the compressed rows
-  if (st != DS4A_OK) return st;
-  p.n_comp = L->n_comp;
-  p.ratio = L->n_comp > 0 ? L->ratio : 1;
-  p.n_blocks = p.nbr + ceil_div(L->n_comp, DS4A_BLOCK_ROWS);
-  p.comp_fp8 = L->n_comp > 0 ? 1 : 0;
-  if (p.comp_fp8) {
-    // E4M3 rows as bytes: {512, n_comp}, box {128 codes, 128 rows}, no swizzle.
-    const cuuint64_t dims[2] = {DS4A_HEAD_DIM, (cuuint64_t)L->n_comp};
-    const cuuint64_t strides[1] = {(cuuint64_t)X->comp_row_stride};
-    const cuuint32_t box[2] = {128, 128};
-    st = encode(&p.tm_k8, X->k_comp, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_DATA_TYPE_UINT8);
-    if (st == DS4A_OK)
-      st = encode(&p.tm_v8, X->v_comp, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE,
-                  CU_TENSOR_MAP_DATA_TYPE_UINT8);
-    if (st != DS4A_OK) return st;
-  }
-  p.k_scale = k_comp_scale;
-  p.v_scale = v_comp_scale;
   p.n_splits = n_splits;
   p.partial = 1;
   p.o = nullptr;
@@ -554,6 +590,26 @@ ds4a_status ds4a_attn_decode_fp8(const ds4a_layout *L, const ds4a_tensors *X, co
   if (st != DS4A_OK) return st;
   return launched(ds4a::launch_combine(ws_o, ws_ml, n_splits, L->T, static_cast<__half *>(X->o),
                                        X->o_tok_stride / 2, X->lse, as_cuda(stream)));
+}
+
+ds4a_status ds4a_attn_decode_fp8(const ds4a_layout *L, const ds4a_tensors *X, const float *k_comp_scale,
+                                 const float *v_comp_scale, int32_t n_splits, void *workspace,
+                                 size_t workspace_bytes, ds4a_stream_t stream) {
+  const ds4a_fp8_scales S = {nullptr, nullptr, k_comp_scale, v_comp_scale};
+  return ds4a_attn_decode_fp8kv(L, X, &S, n_splits, workspace, workspace_bytes, stream);
+}
+
+ds4a_status ds4a_attn_prefill_fp8kv(const ds4a_layout *L, const ds4a_tensors *X, const ds4a_fp8_scales *S,
+                                    ds4a_stream_t stream) {
+  ds4a_status st = check_layout(L);
+  if (st != DS4A_OK) return st;
+  if (L->T == 0) return DS4A_OK;
+  AttnParams p;
+  DeviceState *d = nullptr;
+  st = e4m3_params(p, L, X, S, &d);
+  if (st != DS4A_OK) return st;
+  const int grid = L->T < d->sm_count ? L->T : d->sm_count;
+  return launched(ds4a::launch_attn(p, grid, as_cuda(stream)));
 }
 
 // ------------------------------------------------------------------ batched decode
@@ -655,8 +711,8 @@ ds4a_status ds4a_attn_decode_batch(int32_t n_seq, const ds4a_layout *shape, cons
   p.n_splits = n_splits;
   p.q_tile = 1;
   p.batch_geom = reinterpret_cast<const int4 *>(seq_geom);
-  p.alias_raw = (X->raw_rows > 0 && X->k_raw == X->v_raw) ? 1 : 0;
-  p.alias_comp = (X->comp_rows > 0 && X->k_comp == X->v_comp) ? 1 : 0;
+  p.alias_kv = ((X->raw_rows == 0 || X->k_raw == X->v_raw) && (X->comp_rows == 0 || X->k_comp == X->v_comp) &&
+                X->raw_rows + X->comp_rows > 0) ? 1 : 0;
   p.partial = 1;
   __half *ws_o = static_cast<__half *>(workspace);
   float2 *ws_ml = reinterpret_cast<float2 *>(static_cast<uint8_t *>(workspace) +

@@ -35,9 +35,10 @@
 //               KV rows or dims) and heads 32*(w/4) .. +31
 //   warps 8-11  loaders: Q once per item, every K/V stage in ring order (TMA
 //               tiles, or 16-byte cp.async gathers of index-listed rows: a
-//               TMA gather moves only 512 bytes per instruction); with E4M3
-//               compressed rows warps 9-11 convert the codes, and in a CTA
-//               with a single item they copy its Q
+//               TMA gather moves only 512 bytes per instruction); in a CTA
+//               with a single item warps 9-11 copy its Q.  With E4M3 rows
+//               (the FP8 instantiation) the codes of each part land in the
+//               upper half of its stage and warps 9-11 convert them in place
 //   epilogue    a whole token: o (fp16) and its log-sum-exp; a split of a
 //               token: the split's own normalised o (fp16) and (m, l)
 //   warp  12    TMEM allocator and tcgen05.mma issuer
@@ -148,13 +149,11 @@ __device__ __forceinline__ int count_tiles(const AttnParams &p, const TokenTiles
   return c;
 }
 
-// K/V parts of a tile in ring order: 4 K parts then 4 V parts, or only the 4
-// K parts when the segment's K and V are the same rows.  Then each K part
-// stays in the ring after QK^T and serves PV as V^T: a part holds 128 dims of
-// every row of the tile, which is the K-major A operand of QK^T and the
-// MN-major A operand of PV alike, so each row crosses into the SM once.
-__device__ __forceinline__ bool tile_aliased(const AttnParams &p, const Tile &tl) {
-  return (tl.seg == 0 ? p.alias_raw : p.alias_comp) != 0;
+
+// A tile's parts arrive as E4M3 codes (compressed rows; raw rows too when
+// they are E4M3) or as fp16 boxes.  Used by the FP8 instantiation only.
+__device__ __forceinline__ bool tile_codes(const AttnParams &p, const Tile &tl) {
+  return tl.seg == 0 ? p.raw_fp8 != 0 : true;
 }
 
 struct TileCursor {
@@ -379,7 +378,9 @@ __device__ __forceinline__ void loader_role(const AttnParams &p, uint32_t sbase,
         }
         named_bar_sync(2, kLoaderThreads);
       }
-      const int n_parts = tile_aliased(p, tl) ? 4 : 8;
+      // K/V parts of a tile in ring order: 4 K parts then 4 V parts, or only
+      // the 4 K parts when K and V are the same rows (see mma_role).
+      const int n_parts = p.alias_kv ? 4 : 8;
 #pragma unroll 1
       for (int part = 0; part < n_parts; ++part) {  // parts 0-3: K dims 128*part, parts 4-7: V
         // Every thread waits for the slot itself (bounded); a thread that gives
@@ -390,14 +391,15 @@ __device__ __forceinline__ void loader_role(const AttnParams &p, uint32_t sbase,
         }
         const uint32_t stage = sbase + kOffKV + ring.st * kStageBytes;
         const uint32_t b_full = smem_u32(&ms.kv_full[ring.st]);
-        if (FP8 && tl.seg == 1) {
+        if (FP8 && tile_codes(p, tl)) {
           // E4M3 rows: the codes of this part (128 rows x 128 bytes) land in
           // the stage's upper half; the converter warps turn them into the
           // fp16 stage and arrive on kv_full.
           if (ltid == 0) {
             const uint32_t b_code = smem_u32(&ms.code_full[ring.st]);
             mbar_arrive_expect_tx(b_code, kBoxBytes);
-            tma_load_2d(stage + kBoxBytes, part >= 4 ? &p.tm_v8 : &p.tm_k8, b_code, 128 * (part & 3), tl.start);
+            tma_load_2d(stage + kBoxBytes, part >= 4 ? &p.tm_v8[tl.seg] : &p.tm_k8[tl.seg], b_code, 128 * (part & 3),
+                        tl.start);
             cfilled |= 1u << ring.st;
             clast_par = (clast_par & ~(1u << ring.st)) | (((code_ph >> ring.st) & 1u) << ring.st);
             code_ph ^= 1u << ring.st;
@@ -453,7 +455,8 @@ __device__ __forceinline__ void loader_role(const AttnParams &p, uint32_t sbase,
 
 // ------------------------------------------------------------------ E4M3 converters
 
-// Warps 9..11 when the compressed rows are E4M3: for each such K/V part,
+
+// Warps 9..11 when K/V rows are E4M3: for each such K/V part,
 // wait for its codes (upper half of the stage), then convert them (exactly)
 // into the fp16 stage in the swizzled layout the TMA would have produced, and
 // arrive on kv_full.  A thread converts whole rows: row r's fp16 values in the
@@ -475,10 +478,10 @@ __device__ __forceinline__ void converter_role(const AttnParams &p, uint32_t sba
     if (ip.j1 == ip.j0) continue;
     for (int j = ip.j0; j < ip.j1 && ok; ++j) {
       const Tile tl = ip.cur.next(p);
-      const int n_parts = tile_aliased(p, tl) ? 4 : 8;  // E4M3 rows are never aliased
+      const int n_parts = p.alias_kv ? 4 : 8;  // the E4M3 path never aliases
 #pragma unroll 1
       for (int part = 0; part < n_parts; ++part) {
-        if (tl.seg == 1) {
+        if (tile_codes(p, tl)) {
           const uint32_t st = ring.st;
           ok = mbar_wait(smem_u32(&ms.code_full[st]), (code_ph >> st) & 1u, abrt, p.timeout_ns, p.err,
                          SITE_KV_FULL);
@@ -552,8 +555,11 @@ __device__ __forceinline__ void mma_role(const AttnParams &p, uint32_t sbase, ui
       if (!ok) break;
       const int nt = ip.j1 - ip.j0;
       for (int jj = 0; jj < nt && ok; ++jj) {
-        const Tile tl = ip.cur.next(p);
-        const bool alias = tile_aliased(p, tl);
+        // K and V the same rows: each K part stays in the ring after QK^T and
+        // serves PV as V^T.  A part holds 128 dims of every row of the tile,
+        // the K-major A operand of QK^T and the MN-major A operand of PV alike,
+        // so each row crosses into the SM once.
+        const bool alias = p.alias_kv != 0;
         const uint32_t k0 = ring.st;  // aliased: K part m sits in stage (k0 + m) % kStages until PV m
         const uint32_t sb = g & 1;
         ok = mbar_wait(smem_u32(&ms.s_empty[sb]), ((g >> 1) & 1) ^ 1, abrt, p.timeout_ns, p.err, SITE_S_EMPTY);
@@ -708,11 +714,13 @@ __device__ __forceinline__ void compute_role(const AttnParams &p, uint8_t *smem,
       bool vis;
       float bias;
       row_visibility(p, t, tl, r, vis, bias);
-      // E4M3 compressed rows: the MMA saw the codes; the row scales come in here
+      // E4M3 rows: the MMA saw the unscaled codes; the row scales come in here
       // (K's on the scores, V's on P below).
-      const bool f8 = FP8 && tl.seg == 1;
-      const float sl2 = f8 && vis ? p.scale_log2 * __ldg(p.k_scale + tl.start + r) : p.scale_log2;
-      const float vsc = f8 && vis ? __ldg(p.v_scale + tl.start + r) : 1.f;
+      const bool f8 = FP8 && tile_codes(p, tl);
+      const float *ksc = tl.seg == 0 ? p.k_scale[0] : p.k_scale[1];
+      const float *vsp = tl.seg == 0 ? p.v_scale[0] : p.v_scale[1];
+      const float sl2 = f8 && vis ? p.scale_log2 * __ldg(ksc + tl.start + r) : p.scale_log2;
+      const float vsc = f8 && vis ? __ldg(vsp + tl.start + r) : 1.f;
 #pragma unroll
       for (int h = 0; h < 32; ++h) s[h] = vis ? fmaf(s[h], sl2, bias) : -INFINITY;
 
@@ -901,8 +909,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       tma_prefetch_desc(&p.tm_v[0]);
     }
     if (p.n_comp > 0 && p.mode != MODE_INDEXED) {
-      tma_prefetch_desc(&p.tm_k[1]);
-      tma_prefetch_desc(&p.tm_v[1]);
+      tma_prefetch_desc(FP8 ? &p.tm_k8[1] : &p.tm_k[1]);
+      tma_prefetch_desc(FP8 ? &p.tm_v8[1] : &p.tm_v[1]);
+    }
+    if (FP8 && p.raw_fp8) {
+      tma_prefetch_desc(&p.tm_k8[0]);
+      tma_prefetch_desc(&p.tm_v8[0]);
     }
     if (!p.partial) tma_prefetch_desc(&p.tm_o);
   }

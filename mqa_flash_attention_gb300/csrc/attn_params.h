@@ -76,7 +76,7 @@ struct AttnParams {
   CUtensorMap tm_v[2];
   CUtensorMap tm_kg, tm_vg;  // compressed rows, box {64, 1} (gather4)
   CUtensorMap tm_o;        // 3-D {512, 64, T}, box {128, 64, 1}, no swizzle (epilogue stores)
-  CUtensorMap tm_k8, tm_v8;  // E4M3 compressed rows: bytes {512, rows}, box {128, 128}, no swizzle
+  CUtensorMap tm_k8[2], tm_v8[2];  // E4M3 rows [raw, comp]: bytes {512, rows}, box {128, 128}, no swizzle
   int T, q_pos0, n_raw, raw_pos0, n_comp, ratio, window;
   float scale_log2;
   int mode;
@@ -84,7 +84,7 @@ struct AttnParams {
   int partial;             // 1: per-split outputs and (m, l) to the workspace
   int top_k;
   const void *k_comp, *v_comp;  // compressed rows (read directly by the gather warps)
-  const float *k_scale, *v_scale;  // per-row scales of E4M3 compressed rows
+  const float *k_scale[2], *v_scale[2];  // per-row scales of E4M3 rows [raw, comp]
   long long comp_row_stride;    // bytes
   const int32_t *idx;
   long long idx_stride;    // elements
@@ -92,8 +92,9 @@ struct AttnParams {
   long long mask_stride;   // elements
   const uint8_t *status;
   int q_tile, n_blocks, nbr;  // nbr = raw blocks (ceil(n_raw / 32))
-  int comp_fp8;            // 1: compressed rows are E4M3 codes with per-row scales (k_scale, v_scale)
-  int alias_raw, alias_comp;  // 1: K and V of the segment are the same rows (each part loaded once)
+  int comp_fp8;            // 1: compressed rows are E4M3 codes with per-row scales (k_scale[1], v_scale[1])
+  int raw_fp8;             // 1: raw rows are E4M3 codes too (k_scale[0], v_scale[0])
+  int alias_kv;            // 1: K and V are the same rows in every segment (each part loaded once)
   const int4 *batch_geom;  // batched decode: per sequence (q_pos, n_raw, raw_pos0, n_comp); "token" t = sequence t
   __half *o;
   long long o_tok_stride;  // elements

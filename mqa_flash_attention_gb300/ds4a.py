@@ -42,6 +42,11 @@ class Tensors(ctypes.Structure):
                 ("lse", ctypes.c_void_p)]
 
 
+class Fp8Scales(ctypes.Structure):
+    _fields_ = [("k_raw", ctypes.c_void_p), ("v_raw", ctypes.c_void_p),
+                ("k_comp", ctypes.c_void_p), ("v_comp", ctypes.c_void_p)]
+
+
 class BatchTensors(ctypes.Structure):
     _fields_ = [("q", ctypes.c_void_p), ("q_seq_stride", ctypes.c_int64),
                 ("k_raw", ctypes.c_void_p), ("v_raw", ctypes.c_void_p), ("raw_row_stride", ctypes.c_int64),
@@ -103,6 +108,10 @@ def lib() -> ctypes.CDLL:
         L.ds4a_attn_decode_batch_default_splits.argtypes = [i32, PL, i32, i32]
         L.ds4a_attn_decode_fp8.restype = st
         L.ds4a_attn_decode_fp8.argtypes = [PL, PT, vp, vp, i32, vp, ctypes.c_size_t, vp]
+        L.ds4a_attn_decode_fp8kv.restype = st
+        L.ds4a_attn_decode_fp8kv.argtypes = [PL, PT, ctypes.POINTER(Fp8Scales), i32, vp, ctypes.c_size_t, vp]
+        L.ds4a_attn_prefill_fp8kv.restype = st
+        L.ds4a_attn_prefill_fp8kv.argtypes = [PL, PT, ctypes.POINTER(Fp8Scales), vp]
         L.ds4a_quantize_kv_fp8.restype = st
         L.ds4a_quantize_kv_fp8.argtypes = [vp, i64, i32, vp, i64, vp, vp]
         L.ds4a_compress_rows.restype = i32
@@ -393,6 +402,84 @@ def attn_decode_fp8(layout, q, k_raw, v_raw, k_codes, k_scale, v_codes, v_scale,
     _check(lib().ds4a_attn_decode_fp8(ctypes.byref(L), ctypes.byref(X), _ptr(k_scale), _ptr(v_scale), int(n_splits),
                                       _ptr(workspace), workspace.numel() * workspace.element_size(),
                                       _stream(stream)), "ds4a_attn_decode_fp8")
+    return (out, lse) if (want_lse or lse is not None) else out
+
+
+def _codes(t, name, need):
+    """E4M3 rows: uint8 [>= need, 512] with contiguous rows -> (pointer, byte stride)."""
+    import torch
+    if t.dtype != torch.uint8 or t.dim() != 2 or t.shape[1] != D or t.stride(1) != 1:
+        raise ValueError(f"{name} must be uint8 [rows, 512] with contiguous rows")
+    if t.shape[0] < need:
+        raise ValueError(f"{name} holds {t.shape[0]} rows, the layout needs {need}")
+    return t.data_ptr(), t.stride(0)
+
+
+def _scales(t, name, need):
+    import torch
+    if t.dtype != torch.float32 or t.dim() != 1 or t.stride(0) != 1 or t.shape[0] < need:
+        raise ValueError(f"{name} must be contiguous fp32 [>= {need}]")
+    return t.data_ptr()
+
+
+def _fp8kv(L, q, k_raw, v_raw, k_comp, v_comp, out, lse, k_raw_scale, v_raw_scale, k_comp_scale, v_comp_scale):
+    """Operands of an E4M3 call: compressed rows (and raw rows when their scales
+    are given) as codes with per-row scales."""
+    raw_fp8 = k_raw_scale is not None or v_raw_scale is not None
+    L0 = Layout(L.T, L.q_pos0, 0 if raw_fp8 else L.n_raw, L.raw_pos0, 0, L.ratio, L.window, L.scale)
+    X = _tensors(L0, q, None if raw_fp8 else k_raw, None if raw_fp8 else v_raw, None, None, out, lse,
+                 check_device=False)
+    S = Fp8Scales(None, None, None, None)
+    if raw_fp8 and L.n_raw > 0:
+        kp, ks = _codes(k_raw, "k_raw", L.n_raw)
+        vp, vs = _codes(v_raw, "v_raw", L.n_raw)
+        if ks != vs:
+            raise ValueError("k_raw and v_raw codes must share the row stride")
+        X.k_raw, X.v_raw, X.raw_row_stride = kp, vp, ks
+        S.k_raw, S.v_raw = _scales(k_raw_scale, "k_raw_scale", L.n_raw), _scales(v_raw_scale, "v_raw_scale", L.n_raw)
+    if L.n_comp > 0:
+        kp, ks = _codes(k_comp, "k_comp", L.n_comp)
+        vp, vs = _codes(v_comp, "v_comp", L.n_comp)
+        if ks != vs:
+            raise ValueError("k_comp and v_comp codes must share the row stride")
+        X.k_comp, X.v_comp, X.comp_row_stride = kp, vp, ks
+        S.k_comp = _scales(k_comp_scale, "k_comp_scale", L.n_comp)
+        S.v_comp = _scales(v_comp_scale, "v_comp_scale", L.n_comp)
+    _on_device(q=q, out=out, lse=lse, k_raw=k_raw, v_raw=v_raw, k_comp=k_comp, v_comp=v_comp,
+               k_raw_scale=k_raw_scale, v_raw_scale=v_raw_scale, k_comp_scale=k_comp_scale,
+               v_comp_scale=v_comp_scale)
+    return X, S
+
+
+def attn_decode_fp8kv(layout, q, k_raw, v_raw, k_comp, v_comp, *, k_comp_scale, v_comp_scale, k_raw_scale=None,
+                      v_raw_scale=None, n_splits=0, workspace=None, out=None, lse=None, want_lse=False, stream=None):
+    """Split-KV decode over E4M3 rows: compressed rows k/v_comp as uint8 codes
+    [n_comp, 512] with fp32 row scales; raw rows as codes too when their
+    scales are given, else fp16 [n_raw, 512]."""
+    import torch
+    L = make_layout(layout)
+    out, lse = _outputs(q, out, lse, want_lse)
+    X, S = _fp8kv(L, q, k_raw, v_raw, k_comp, v_comp, out, lse, k_raw_scale, v_raw_scale, k_comp_scale,
+                  v_comp_scale)
+    need = decode_workspace_bytes(L, n_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _on_device(workspace=workspace)
+    _check(lib().ds4a_attn_decode_fp8kv(ctypes.byref(L), ctypes.byref(X), ctypes.byref(S), int(n_splits),
+                                        _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                        _stream(stream)), "ds4a_attn_decode_fp8kv")
+    return (out, lse) if (want_lse or lse is not None) else out
+
+
+def attn_prefill_fp8kv(layout, q, k_raw, v_raw, k_comp=None, v_comp=None, *, k_comp_scale=None, v_comp_scale=None,
+                       k_raw_scale=None, v_raw_scale=None, out=None, lse=None, want_lse=False, stream=None):
+    """Structural prefill over E4M3 rows (operands as in :func:`attn_decode_fp8kv`)."""
+    L = make_layout(layout)
+    out, lse = _outputs(q, out, lse, want_lse)
+    X, S = _fp8kv(L, q, k_raw, v_raw, k_comp, v_comp, out, lse, k_raw_scale, v_raw_scale, k_comp_scale,
+                  v_comp_scale)
+    _check(lib().ds4a_attn_prefill_fp8kv(ctypes.byref(L), ctypes.byref(X), ctypes.byref(S), _stream(stream)),
+           "ds4a_attn_prefill_fp8kv")
     return (out, lse) if (want_lse or lse is not None) else out
 
 

@@ -2,8 +2,11 @@
 
 * ds4a_quantize_kv_fp8: codes and scales bit for bit against the oracle (the
   fp32 quotients, product and E4M3 rounding are the same operations).
-* ds4a_attn_decode_fp8: against the fp64 attention oracle run on the rows'
-  values decode(code) * scale, within max abs 5e-3 and mean abs 5e-4.
+* ds4a_attn_decode_fp8 / _fp8kv and ds4a_attn_prefill_fp8kv: against the
+  fp64 attention oracle run on the rows' values decode(code) * scale, within
+  max abs 5e-3 and mean abs 5e-4.  The codes and scales the GPU reads are the
+  oracle's own quantisation of the rows (uploaded), so no expected value
+  comes from the CUDA path.
 """
 
 import numpy as np
@@ -76,11 +79,16 @@ def test_quantize_strided(torch, ds4a):
     assert (c[:, 512:] == 9).all()
 
 
+def _quantized(torch, rows):
+    """The oracle's E4M3 codes and scales of fp16 rows, on the device, and the
+    rows' values decode(code) * scale (float64) for the oracle."""
+    codes, scales = f8.quantize_rows(rows)
+    return dev(torch, codes), dev(torch, scales), f8.dequantize_rows(codes, scales)
+
+
 def _fp8_case(torch, ds4a, wl):
-    kc, ks = ds4a.quantize_kv_fp8(dev(torch, wl.k_comp))
-    vc, vs = ds4a.quantize_kv_fp8(dev(torch, wl.v_comp))
-    kd = f8.dequantize_rows(host(kc), host(ks))
-    vd = f8.dequantize_rows(host(vc), host(vs))
+    kc, ks, kd = _quantized(torch, wl.k_comp)
+    vc, vs, vd = _quantized(torch, wl.v_comp)
     want, wlse = oracle.attention(wl.layout, wl.q, wl.k_raw, wl.v_raw, kd, vd)
     return (kc, ks, vc, vs), want, wlse
 
@@ -114,3 +122,87 @@ def test_decode_fp8_full_size(torch, ds4a):
     (kc, ks, vc, vs), want, _ = _fp8_case(torch, ds4a, wl)
     o = ds4a.attn_decode_fp8(wl.layout, dev(torch, wl.q), dev(torch, wl.k_raw), dev(torch, wl.v_raw), kc, ks, vc, vs)
     _check(host(o), want, "fp8 decode N=262144")
+
+
+# ------------------------------------------------------------------ E4M3 raw rows too
+
+def _fp8kv_case(torch, wl, raw_fp8=True):
+    """Codes and scales of the compressed rows and, with raw_fp8, of the raw
+    rows; the oracle's result over the rows' decoded values."""
+    L = wl.layout
+    ops = {}
+    kr, vr = wl.k_raw, wl.v_raw
+    if raw_fp8 and L["n_raw"]:
+        ops["k_raw"], ops["k_raw_scale"], kr = _quantized(torch, wl.k_raw)
+        ops["v_raw"], ops["v_raw_scale"], vr = _quantized(torch, wl.v_raw)
+    else:
+        ops["k_raw"], ops["v_raw"] = dev(torch, wl.k_raw), dev(torch, wl.v_raw)
+    kc = vc = None
+    if L["n_comp"]:
+        ops["k_comp"], ops["k_comp_scale"], kc = _quantized(torch, wl.k_comp)
+        ops["v_comp"], ops["v_comp_scale"], vc = _quantized(torch, wl.v_comp)
+    else:
+        ops["k_comp"] = ops["v_comp"] = None
+    want, wlse = oracle.attention(L, wl.q, kr, vr, kc, vc)
+    return ops, want, wlse
+
+
+def _call(ds4a, fn, wl, q, ops, **kw):
+    return fn(wl.layout, q, ops["k_raw"], ops["v_raw"], ops["k_comp"], ops["v_comp"],
+              k_comp_scale=ops.get("k_comp_scale"), v_comp_scale=ops.get("v_comp_scale"),
+              k_raw_scale=ops.get("k_raw_scale"), v_raw_scale=ops.get("v_raw_scale"), **kw)
+
+
+@pytest.mark.parametrize("name", ["decode_r128_32k", "long_8192", "ragged_t3", "raw_only"])
+def test_decode_fp8kv_raw_rows_too(torch, ds4a, name):
+    """Decode with every K/V row in E4M3 (raw and compressed), several split
+    counts, against the oracle over the decoded rows; outputs start as NaN."""
+    if name == "decode_r128_32k":
+        wl = W.decode_r128_32k()
+    elif name == "long_8192":
+        wl = W.decode_long(8192)
+    elif name == "ragged_t3":
+        wl = W.draw("fp8kv_ragged", 33, make_layout(T=3, q_pos0=40000, n_raw=150, raw_pos0=39853, n_comp=311,
+                                                     ratio=128))
+    else:
+        wl = W.draw("fp8kv_raw", 34, make_layout(T=2, q_pos0=600, n_raw=300, raw_pos0=400))
+    ops, want, wlse = _fp8kv_case(torch, wl)
+    q = dev(torch, wl.q)
+    for splits in (0, 1, 3):
+        out = torch.full_like(q, float("nan"))
+        o, lse = _call(ds4a, ds4a.attn_decode_fp8kv, wl, q, ops, n_splits=splits, out=out, want_lse=True)
+        _check(host(o), want, f"{name} splits={splits}")
+        fin = np.isfinite(wlse)
+        assert np.abs(host(lse)[fin] - wlse[fin]).max() <= 1e-3
+
+
+def test_decode_fp8kv_full_size_raw_fp16(torch, ds4a):
+    """256K compressed E4M3 rows with fp16 raw rows, through the fp8kv entry."""
+    wl = W.decode_long(262144)
+    ops, want, _ = _fp8kv_case(torch, wl, raw_fp8=False)
+    o = _call(ds4a, ds4a.attn_decode_fp8kv, wl, dev(torch, wl.q), ops)
+    _check(host(o), want, "fp8kv decode N=262144")
+
+
+@pytest.mark.parametrize("name", ["tiny", "prefill_raw_2048", "ragged_mixed", "comp_fp8_raw_fp16"])
+def test_prefill_fp8kv(torch, ds4a, name):
+    """Structural prefill over E4M3 rows against the oracle over the decoded
+    rows, every token (the 2048-token chunk included)."""
+    raw_fp8 = True
+    if name == "tiny":
+        wl = W.tiny()
+    elif name == "prefill_raw_2048":
+        wl = W.prefill_raw_2048()
+    elif name == "ragged_mixed":
+        wl = W.draw("fp8kv_pre", 35, make_layout(T=37, q_pos0=999, n_raw=170, raw_pos0=862, n_comp=250, ratio=4))
+    else:
+        wl = W.draw("fp8kv_pre2", 36, make_layout(T=9, q_pos0=5000, n_raw=200, raw_pos0=4850, n_comp=39,
+                                                   ratio=128))
+        raw_fp8 = False
+    ops, want, wlse = _fp8kv_case(torch, wl, raw_fp8=raw_fp8)
+    q = dev(torch, wl.q)
+    out = torch.full_like(q, float("nan"))
+    o, lse = _call(ds4a, ds4a.attn_prefill_fp8kv, wl, q, ops, out=out, want_lse=True)
+    _check(host(o), want, f"prefill fp8kv {name}")
+    fin = np.isfinite(wlse)
+    assert np.abs(host(lse)[fin] - wlse[fin]).max() <= 1e-3
