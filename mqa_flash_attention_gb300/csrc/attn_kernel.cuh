@@ -102,8 +102,8 @@ __device__ __forceinline__ TokenTiles token_tiles(const AttnParams &p, int t) {
       z.comp_rows = (int)(c < n_comp ? c : n_comp);
     }
   }
-  z.n_rt = (z.raw_hi - z.raw_lo + kTile - 1) / kTile;
-  z.n_ct = (z.comp_rows + kTile - 1) / kTile;
+  z.n_rt = (z.raw_hi - z.raw_lo + p.tile_rows - 1) / p.tile_rows;
+  z.n_ct = (z.comp_rows + p.tile_rows - 1) / p.tile_rows;
   return z;
 }
 
@@ -113,12 +113,12 @@ __device__ __forceinline__ Tile tile_candidate(const AttnParams &p, const TokenT
   tl.open = 0;
   if (i < z.n_rt) {
     tl.seg = 0;
-    tl.start = z.raw_lo + i * kTile;
-    tl.count = min(kTile, z.raw_hi - tl.start);
+    tl.start = z.raw_lo + i * p.tile_rows;
+    tl.count = min(p.tile_rows, z.raw_hi - tl.start);
   } else {
     tl.seg = p.mode == MODE_INDEXED ? 2 : 1;
-    tl.start = (i - z.n_rt) * kTile;
-    tl.count = min(kTile, z.comp_rows - tl.start);
+    tl.start = (i - z.n_rt) * p.tile_rows;
+    tl.count = min(p.tile_rows, z.comp_rows - tl.start);
   }
   if (p.mode == MODE_MASK && p.status != nullptr) {
     const int base = tl.seg == 0 ? 0 : p.nbr;
@@ -380,7 +380,7 @@ __device__ __forceinline__ void loader_role(const AttnParams &p, uint32_t sbase,
       }
       // K/V parts of a tile in ring order: 4 K parts then 4 V parts, or only
       // the 4 K parts when K and V are the same rows (see mma_role).
-      const int n_parts = p.alias_kv ? 4 : 8;
+      const int n_parts = (p.alias_kv | p.kv_pair) ? 4 : 8;
 #pragma unroll 1
       for (int part = 0; part < n_parts; ++part) {  // parts 0-3: K dims 128*part, parts 4-7: V
         // Every thread waits for the slot itself (bounded); a thread that gives
@@ -409,7 +409,15 @@ __device__ __forceinline__ void loader_role(const AttnParams &p, uint32_t sbase,
             const int dim0 = 128 * (part & 3);
             const CUtensorMap *m = part >= 4 ? &p.tm_v[tl.seg] : &p.tm_k[tl.seg];
             mbar_arrive_expect_tx(b_full, kStageBytes);
-            if (p.batch_geom != nullptr) {  // [sequences][rows][512]: the sequence is the third coordinate
+            if (p.kv_pair) {
+              // 64-row tile: the K and the V slice of dims dim0 .. dim0+127 in
+              // one stage, four [64 rows][64 dims] boxes of 8 KB.
+              constexpr uint32_t hb = kBoxBytes / 2;
+              tma_load_2d(stage, &p.tm_k[tl.seg], b_full, dim0, tl.start);
+              tma_load_2d(stage + hb, &p.tm_k[tl.seg], b_full, dim0 + 64, tl.start);
+              tma_load_2d(stage + 2 * hb, &p.tm_v[tl.seg], b_full, dim0, tl.start);
+              tma_load_2d(stage + 3 * hb, &p.tm_v[tl.seg], b_full, dim0 + 64, tl.start);
+            } else if (p.batch_geom != nullptr) {  // [sequences][rows][512]: the sequence is the third coordinate
               tma_load_3d(stage, m, b_full, dim0, tl.start, ip.t);
               tma_load_3d(stage + kBoxBytes, m, b_full, dim0 + 64, tl.start, ip.t);
             } else {
@@ -541,6 +549,11 @@ __device__ __forceinline__ void mma_role(const AttnParams &p, uint32_t sbase, ui
     // P^T: one 64-head MN atom, LBO unused.
     const uint64_t k_desc = sdesc_sw128(sbase + kOffKV, 16, 1024);
     const uint64_t v_desc = sdesc_sw128(sbase + kOffKV, kBoxBytes, 1024);
+    static_assert(kBoxBytes == (1u << 14), "K box distances are taken as shifts");
+    // Paired stages (64-row tiles): K boxes at +0 and +8 KB, V boxes at +16 KB
+    // and +24 KB of the stage, so V^T's two 64-dim atoms are 8 KB apart.
+    const uint64_t pv_desc = p.kv_pair ? sdesc_sw128(sbase + kOffKV + kBoxBytes, kBoxBytes / 2, 1024) : v_desc;
+    const uint32_t kbox_shift = p.kv_pair ? 13 : 14;  // log2 of the distance of a part's two K boxes
     const uint64_t q_desc = sdesc_sw128(sbase + kOffQ, 16, 1024);
     const uint64_t p_desc = sdesc_sw128(sbase + kOffP, 16, 1024);
     Ring ring;
@@ -558,9 +571,14 @@ __device__ __forceinline__ void mma_role(const AttnParams &p, uint32_t sbase, ui
         // K and V the same rows: each K part stays in the ring after QK^T and
         // serves PV as V^T.  A part holds 128 dims of every row of the tile,
         // the K-major A operand of QK^T and the MN-major A operand of PV alike,
-        // so each row crosses into the SM once.
+        // so each row crosses into the SM once.  Paired stages hold the K and
+        // the V slice of a 64-row tile: they too stay from QK^T until PV.  With
+        // 64 rows the M = 128 QK^T reads 64 more rows (the next boxes of the
+        // stage): their scores are dropped by the mask, and PV only takes the
+        // tile's own rows.
         const bool alias = p.alias_kv != 0;
-        const uint32_t k0 = ring.st;  // aliased: K part m sits in stage (k0 + m) % kStages until PV m
+        const bool hold = alias || p.kv_pair != 0;
+        const uint32_t k0 = ring.st;  // held: part m sits in stage (k0 + m) % kStages until PV m
         const uint32_t sb = g & 1;
         ok = mbar_wait(smem_u32(&ms.s_empty[sb]), ((g >> 1) & 1) ^ 1, abrt, p.timeout_ns, p.err, SITE_S_EMPTY);
         if (!ok) break;
@@ -577,7 +595,7 @@ __device__ __forceinline__ void mma_role(const AttnParams &p, uint32_t sbase, ui
           for (int b2 = 0; b2 < 2; ++b2) {
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
-              const uint64_t a = sdesc_add(a0, b2 * kBoxBytes + ks * 32);
+              const uint64_t a = sdesc_add(a0, (b2 << kbox_shift) + ks * 32);
               const uint64_t b = sdesc_add(b0, b2 * kQBoxBytes + ks * 32);
               if (b2 == 0 && ks == 0)
                 umma_f16(d_s, a, b, kIdescQK, c != 0 ? 1u : 0u);
@@ -585,7 +603,7 @@ __device__ __forceinline__ void mma_role(const AttnParams &p, uint32_t sbase, ui
                 umma_f16_acc(d_s, a, b, kIdescQK);
             }
           }
-          if (!alias) umma_commit(smem_u32(&ms.kv_empty[ring.st]));  // aliased: held for PV
+          if (!hold) umma_commit(smem_u32(&ms.kv_empty[ring.st]));  // held for PV otherwise
           ring.advance();
         }
         if (!ok) break;
@@ -600,16 +618,17 @@ __device__ __forceinline__ void mma_role(const AttnParams &p, uint32_t sbase, ui
         tc_fence_after();
         // O^T[m] += V_tile^T[dims 128m..] . P^T, 16 rows per instruction.
         for (int m = 0; m < 4 && ok; ++m) {
-          uint32_t vst = (k0 + m) % kStages;  // aliased: the K part of the same dims, already landed
-          if (!alias) {
+          uint32_t vst = (k0 + m) % kStages;  // held: the part of the same dims, already landed
+          if (!hold) {
             ok = mbar_wait(smem_u32(&ms.kv_full[ring.st]), ring.ph, abrt, p.timeout_ns, p.err, SITE_KV_FULL);
             if (!ok) break;
             tc_fence_after();
             vst = ring.st;
           }
-          const uint64_t a0 = sdesc_add(v_desc, vst * kStageBytes);
+          const uint64_t a0 = sdesc_add(pv_desc, vst * kStageBytes);
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
+            if (ks == 4 && p.kv_pair) break;  // a 64-row tile: its rows only
             const uint64_t a = sdesc_add(a0, ks * 2048);
             const uint64_t b = sdesc_add(p_desc, ks * 2048);
             if (ks == 0)
@@ -621,7 +640,7 @@ __device__ __forceinline__ void mma_role(const AttnParams &p, uint32_t sbase, ui
           // After the item's last tile, block m of O^T is final: the epilogue
           // drains it while the remaining blocks are still being computed.
           if (jj == nt - 1) umma_commit(smem_u32(&ms.o_full[m]));
-          if (!alias) ring.advance();
+          if (!hold) ring.advance();
         }
         if (!ok) break;
         umma_commit(smem_u32(&ms.p_empty));

@@ -95,6 +95,8 @@ struct AttnParams {
   int comp_fp8;            // 1: compressed rows are E4M3 codes with per-row scales (k_scale[1], v_scale[1])
   int raw_fp8;             // 1: raw rows are E4M3 codes too (k_scale[0], v_scale[0])
   int alias_kv;            // 1: K and V are the same rows in every segment (each part loaded once)
+  int kv_pair;             // 1: 64-row tiles, each stage holds the K and the V part of one 128-dim slice
+  int tile_rows;           // rows per tile: 128, or 64 with kv_pair
   const int4 *batch_geom;  // batched decode: per sequence (q_pos, n_raw, raw_pos0, n_comp); "token" t = sequence t
   __half *o;
   long long o_tok_stride;  // elements

@@ -44,8 +44,8 @@ def test_noalloc_decode_against_the_oracle_call_after_call():
         return torch.from_numpy(np.ascontiguousarray(a)).cuda()
 
     mk = W.make_layout
-    cases = [  # (workload, n_splits requested, items the call must run)
-        (W.decode_r128_32k(), 0, 3),
+    cases = [  # (workload, n_splits requested (0: the library's choice, capped to 127 items), items required)
+        (W.decode_r128_32k(), 0, None),
         # 129 tiles: the default split count is capped to the array's 127 items
         (W.draw("noalloc_cap1", 71, mk(T=1, q_pos0=128 * 16384 - 1, n_raw=128, raw_pos0=128 * 16384 - 128,
                                        n_comp=16384, ratio=128)), 0, 127),
@@ -61,6 +61,9 @@ def test_noalloc_decode_against_the_oracle_call_after_call():
     for wl, n_splits, items in cases:
         Lp = ds4a.make_layout(wl.layout)
         T = Lp.T
+        splits_used = n_splits if n_splits > 0 else min(ds4a.decode_default_splits(Lp), 127 // T)
+        if items is not None:
+            assert T * splits_used == items, (wl.name, T * splits_used)
         q, kr, vr, kc, vc = (up(a) for a in (wl.q, wl.k_raw, wl.v_raw, wl.k_comp, wl.v_comp))
         out = torch.full_like(q, float("nan"))
         lse = torch.full((T, 64), float("nan"), dtype=torch.float32, device="cuda")
@@ -81,7 +84,6 @@ def test_noalloc_decode_against_the_oracle_call_after_call():
         assert np.abs(gl - wlse).max() <= LSE_ABS, wl.name
 
         # the same kernels on a caller workspace, at the split count the call used
-        splits_used = items // T
         ref = ds4a.attn_decode(wl.layout, q, kr, vr, kc, vc, n_splits=splits_used)
         torch.cuda.synchronize()
         assert torch.equal(out, ref), wl.name
