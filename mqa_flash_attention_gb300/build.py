@@ -21,7 +21,7 @@ OUT_DIR = os.path.join(PKG, "_lib")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libds4a.so")
 
-SOURCES = ["attn.cu", "aux.cu", "indexer.cu", "compressor.cu", "api.cu"]
+SOURCES = ["attn.cu", "attn_pair.cu", "aux.cu", "indexer.cu", "compressor.cu", "api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "--use_fast_math", "-Xcompiler", "-fPIC,-O2",
          "-Xptxas", "-v", f"-I{INCLUDE}", f"-I{CSRC}"]

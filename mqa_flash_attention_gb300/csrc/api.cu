@@ -59,7 +59,8 @@ ds4a_status current_device(DeviceState **out) {
     d.sm_count = sms;
     d.supported = (major == 10 && minor == 3);
     if (d.supported) {
-      if (ds4a::prepare_attn_kernel() != cudaSuccess) return DS4A_ERR_CUDA;
+      if (ds4a::prepare_attn_kernel() != cudaSuccess || ds4a::prepare_pair_kernel() != cudaSuccess)
+        return DS4A_ERR_CUDA;
       if (cudaGetSymbolAddress(reinterpret_cast<void **>(&d.err), g_ds4a_device_error) != cudaSuccess)
         return DS4A_ERR_CUDA;
       if (cudaGetSymbolAddress(&d.scratch, g_decode_scratch) != cudaSuccess) return DS4A_ERR_CUDA;
@@ -214,6 +215,40 @@ int32_t max_tiles_per_token(const ds4a_layout *L, int rows = 128) {
 bool short_decode(const ds4a_layout *L, int sm_count) {
   const int64_t half_tiles = (int64_t)2 * max_tiles_per_token(L);
   return half_tiles <= 32 && half_tiles * L->T <= sm_count;
+}
+
+// Raw rows only, window <= 128, T >= 2: pairs of consecutive tokens share one
+// 128-row tile (attn_pair.cu); the result is the structural attention.
+ds4a_status prefill_pairs(const ds4a_layout *L, const ds4a_tensors *X, DeviceState *d, ds4a_stream_t stream) {
+  ds4a::PairParams p;
+  std::memset(&p, 0, sizeof(p));
+  {
+    const cuuint64_t dims[3] = {DS4A_HEAD_DIM, DS4A_HEADS, (cuuint64_t)L->T};
+    const cuuint64_t strides[2] = {DS4A_ROW_BYTES, (cuuint64_t)X->q_tok_stride};
+    const cuuint32_t box[3] = {64, 64, 2};
+    ds4a_status st = encode(&p.tm_q2, X->q, 3, dims, strides, box);
+    if (st != DS4A_OK) return st;
+  }
+  ds4a_status st = encode_rows(&p.tm_k, X->k_raw, L->n_raw, X->raw_row_stride, 128);
+  if (st == DS4A_OK) st = encode_rows(&p.tm_v, X->v_raw, L->n_raw, X->raw_row_stride, 128);
+  if (st != DS4A_OK) return st;
+  p.T = L->T;
+  p.q_pos0 = L->q_pos0;
+  p.n_raw = L->n_raw;
+  p.raw_pos0 = L->raw_pos0;
+  p.window = L->window;
+  p.scale_log2 = L->scale * 1.4426950408889634f;
+  p.k_raw = static_cast<const uint8_t *>(X->k_raw);
+  p.v_raw = static_cast<const uint8_t *>(X->v_raw);
+  p.raw_row_stride = X->raw_row_stride;
+  p.o = static_cast<__half *>(X->o);
+  p.o_tok_stride = X->o_tok_stride / 2;
+  p.lse = X->lse;
+  p.timeout_ns = kDefaultTimeoutNs;
+  p.err = d->err;
+  const int pairs = (L->T + 1) / 2;
+  const int grid = pairs < d->sm_count ? pairs : d->sm_count;
+  return launched(ds4a::launch_pair(p, grid, as_cuda(stream)));
 }
 
 }  // namespace
@@ -379,6 +414,8 @@ ds4a_status ds4a_attn_prefill(const ds4a_layout *L, const ds4a_tensors *X, const
   DeviceState *d = nullptr;
   st = current_device(&d);
   if (st != DS4A_OK) return st;
+  if (dense_mask == nullptr && L->n_comp == 0 && L->n_raw > 0 && L->window <= 128 && L->T >= 2)
+    return prefill_pairs(L, X, d, stream);
   AttnParams p;
   st = fill_params(p, L, X, dense_mask != nullptr ? ds4a::MODE_MASK : ds4a::MODE_STRUCT, d);
   if (st != DS4A_OK) return st;

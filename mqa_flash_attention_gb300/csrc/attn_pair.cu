@@ -1,0 +1,554 @@
+// Fused attention forward for pairs of consecutive query tokens over raw rows
+// (structural rule, no compressed rows, window <= 128): the raw-only layers
+// and the raw part of a prefill chunk ("DwarfStar 4 (DS4) - DeepSeek V4 Flash
+// Inference Engine", sections "Layer Compression" and "Whole-Model Graph
+// Execution"; fused as in "How DeepSeek V4 Flash Model Inference Works on
+// Apple Silicon with Metal Backend", section "FlashAttention Kernel
+// Architecture").  The result is the same attention as attn_fwd_kernel's.
+//
+// Why pairs.  Two consecutive tokens see windows that differ by one row, so
+// one 128-row K/V tile serves both: the tile is the later token's window and
+// the earlier token's one remaining row (below the tile) is folded in on the
+// CUDA cores.  Every K/V row then enters the SM once per two tokens (Q 64 KB
+// + K 64 KB + V 64 KB per token instead of 64 + 128 + 128), and both
+// products run as N = 128 MMAs (two tokens x 64 heads), at the tensor core's
+// full rate where a single token's N = 64 runs near half of it:
+//   S^T[128 rows][128]      = K_tile[128][512] . Q_pair[128][512]^T   (K-major A, K-major B)
+//   O^T_m[128 dims][128]    = V_tile^T[dims 128m..][128] . P^T          (MN-major A, MN-major B)
+// TMEM: S^T at columns 0-127; O^T is produced one 128-dim block at a time
+// into two alternating 128-column buffers that the epilogue drains as they
+// complete (no block accumulates across tiles: the pair has one tile).
+//
+// Shared memory: a ring of 10 slots of 16 KB through which every box of a
+// pair streams in a fixed order (Q box b, K box b for b = 0..7, then V boxes
+// 0..7; a PV block takes two adjacent V slots), P^T of the pair (32 KB), the
+// extra row's K and V (two 2 KB buffers, by pair parity) and bookkeeping.
+// Warp roles (352 threads):
+//   warps 0-7  softmax + epilogue; thread (TMEM lane quarter w % 4, token w / 4)
+//              handles one row (or dim) and that token's 64 heads in two halves
+//   warp  8    loader (one thread issues every TMA copy)
+//   warp  9    TMEM allocator and tcgen05.mma issuer
+//   warp 10    extra row: loads its K and V rows and takes token a's scores
+//              against it from the Q boxes as they pass through the ring
+// A Q slot is released by the MMA's commit and by the extra-row warp (it reads
+// it), a K or V slot by the commit and a plain arrival of the MMA thread:
+// every slot's "free" barrier counts two arrivals.  The extra-row warp learns
+// that Q box b landed from the MMA thread (qx[b]), which waits on every slot
+// in order: a parity wait must not fall more than one phase behind, and a
+// ring position passes through K and V uses the extra-row warp never sees.
+// Every wait is bounded as in attn_fwd_kernel.
+#include <cuda_fp16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace ds4a {
+namespace {
+
+constexpr int kPWarps = 8;
+constexpr int kPThreadsC = 32 * kPWarps;
+constexpr int kPLoaderWarp = 8;
+constexpr int kPMmaWarp = 9;
+constexpr int kPXWarp = 10;
+constexpr int kPThreads = 32 * (kPXWarp + 1);
+constexpr int kPSlots = 10;
+constexpr uint32_t kPSlot = 16384;
+constexpr int kPSlotsPerPair = 24;  // 8 Q + 8 K + 8 V boxes
+constexpr uint32_t kPOffRing = 0;
+constexpr uint32_t kPOffP = kPSlots * kPSlot;      // P^T: token a's box, then token b's
+constexpr uint32_t kPOffX = kPOffP + 2 * kPSlot;   // extra rows by pair parity: K [512] fp16, then V [512]
+constexpr uint32_t kPOffMisc = kPOffX + 2 * 2048;
+static_assert(kPSlots % 2 == 0 && kPSlotsPerPair % 2 == 0, "V slot pairs must stay adjacent in the ring");
+
+struct PairMisc {
+  alignas(16) float red[4][128];  // per lane quarter: partial max, then partial sum, of each column
+  alignas(16) float m_use[128];   // reference max of each column (log2 units), 0 when nothing is visible
+  alignas(16) float m_true[128];  // the max itself (-inf when nothing is visible)
+  alignas(16) float inv_l[128];
+  alignas(16) float sx[2][64];    // extra row, by pair parity: scaled score of token a per head (log2 units)
+  alignas(16) float px[64];       // extra row: its weight
+  alignas(8) uint64_t full[kPSlots], empty[kPSlots];
+  uint64_t s_full, s_empty, p_full, p_empty, o_full[2], o_empty[2], mma_done;
+  uint64_t x_full, x_empty[2];    // extra-row scores of a pair ready; a parity's row buffer free again
+  uint64_t qx[8];                 // Q box b of the current pair has landed (passed on by the MMA thread)
+  uint32_t tmem_base;
+  int abort_flag;
+};
+constexpr uint32_t kPSmemBytes = kPOffMisc + ((sizeof(PairMisc) + 127) / 128) * 128 + 1024;
+static_assert(kPSmemBytes <= 232448, "pair kernel shared memory");
+
+enum : unsigned int {
+  SITE_PR_EMPTY = 0x20, SITE_PR_FULL, SITE_PR_S_EMPTY, SITE_PR_S_FULL, SITE_PR_P_FULL, SITE_PR_P_EMPTY,
+  SITE_PR_O_EMPTY, SITE_PR_O_FULL, SITE_PR_DRAIN, SITE_PR_X_FULL, SITE_PR_X_EMPTY
+};
+
+// The pair's tokens and rows.  Token a = 2 * pair, token b = a + 1 (absent for
+// an odd last token).  Token t sees raw rows [lo, hi) (its window clipped to
+// the rows given); the tile is the 128 rows ending at the later token's last
+// row (it may start below row 0: the TMA fills those rows with zeros and the
+// mask drops them); with a window of at most 128, token a reaches at most one
+// row below the tile.
+struct PairGeom {
+  int ta;
+  bool has_b;
+  int lo[2], hi[2];
+  int tile_lo;
+  bool extra;
+};
+
+__device__ __forceinline__ PairGeom pair_geom(const PairParams &p, int pr) {
+  PairGeom g;
+  g.ta = 2 * pr;
+  g.has_b = g.ta + 1 < p.T;
+  int hi_max = 0;
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    int lo = 0, hi = 0;
+    if (u == 0 || g.has_b) {
+      const long long pos = (long long)p.q_pos0 + g.ta + u;
+      const long long a = pos - p.window + 1 - p.raw_pos0, b = pos + 1 - p.raw_pos0;
+      lo = (int)(a < 0 ? 0 : a);
+      hi = (int)(b > p.n_raw ? p.n_raw : b);
+      if (hi < lo) hi = lo;
+    }
+    g.lo[u] = lo;
+    g.hi[u] = hi;
+    hi_max = max(hi_max, hi);
+  }
+  g.tile_lo = hi_max - 128;
+  g.extra = g.lo[0] < g.hi[0] && g.lo[0] < g.tile_lo;
+  return g;
+}
+
+__device__ __forceinline__ uint32_t slot_addr(uint32_t sbase, uint32_t sl) {
+  return sbase + kPOffRing + (sl % kPSlots) * kPSlot;
+}
+__device__ __forceinline__ uint32_t slot_phase(uint32_t sl) { return (sl / kPSlots) & 1u; }
+
+// ------------------------------------------------------------------ loader
+
+__device__ __forceinline__ void pair_loader(const PairParams &p, uint32_t sbase, PairMisc &ms) {
+  volatile int *abrt = &ms.abort_flag;
+  const int n_pairs = (p.T + 1) / 2;
+  uint32_t sl = 0, filled = 0, last_par = 0;
+  bool ok = true;
+  grid_dependency_wait();  // Q, K and V may come from the previous kernel
+  for (int pr = blockIdx.x; pr < n_pairs && ok; pr += gridDim.x) {
+    const PairGeom g = pair_geom(p, pr);
+#pragma unroll 1
+    for (int i = 0; i < kPSlotsPerPair && ok; ++i, ++sl) {
+      const uint32_t pos = sl % kPSlots, ph = slot_phase(sl);
+      ok = mbar_wait(smem_u32(&ms.empty[pos]), ph ^ 1, abrt, p.timeout_ns, p.err, SITE_PR_EMPTY);
+      if (!ok) break;
+      const uint32_t dst = slot_addr(sbase, sl), bar = smem_u32(&ms.full[pos]);
+      mbar_arrive_expect_tx(bar, kPSlot);
+      if (i < 16) {
+        const int b = i >> 1;
+        if ((i & 1) == 0)
+          tma_load_3d(dst, &p.tm_q2, bar, 64 * b, 0, g.ta);  // both tokens' heads, dims 64b ..
+        else
+          tma_load_2d(dst, &p.tm_k, bar, 64 * b, g.tile_lo);
+      } else {
+        tma_load_2d(dst, &p.tm_v, bar, 64 * (i - 16), g.tile_lo);
+      }
+      filled |= 1u << pos;
+      last_par = (last_par & ~(1u << pos)) | (ph << pos);
+    }
+  }
+  if (!ok) {
+    // Let every copy already issued land before the shared memory goes away.
+    volatile int never = 0;
+    for (int s = 0; s < kPSlots; ++s)
+      if (filled & (1u << s))
+        mbar_wait(smem_u32(&ms.full[s]), (last_par >> s) & 1, &never, 100000000ull, p.err, SITE_PR_DRAIN);
+  }
+}
+
+// ------------------------------------------------------------------ MMA issuer
+
+__device__ __forceinline__ void pair_mma(const PairParams &p, uint32_t sbase, uint32_t tmem, PairMisc &ms) {
+  volatile int *abrt = &ms.abort_flag;
+  constexpr uint32_t kIdescQK = idesc_f16_f32(128, 128, false, false);
+  constexpr uint32_t kIdescPV = idesc_f16_f32(128, 128, true, true);
+  // K and Q boxes: K-major, SBO = one 8-row group.  V^T: MN-major, its two
+  // 64-dim atoms in adjacent slots (LBO = one slot).  P^T: MN-major, token a's
+  // heads then token b's (LBO = one box).
+  const uint64_t kq_desc = sdesc_sw128(sbase + kPOffRing, 16, 1024);
+  const uint64_t v_desc = sdesc_sw128(sbase + kPOffRing, kPSlot, 1024);
+  const uint64_t p_desc = sdesc_sw128(sbase + kPOffP, kPSlot, 1024);
+  const int n_pairs = (p.T + 1) / 2;
+  uint32_t sl = 0, n = 0;
+  bool ok = true;
+  for (int pr = blockIdx.x; pr < n_pairs && ok; pr += gridDim.x, ++n) {
+    ok = mbar_wait(smem_u32(&ms.s_empty), (n & 1) ^ 1, abrt, p.timeout_ns, p.err, SITE_PR_S_EMPTY);
+    if (!ok) break;
+    tc_fence_after();
+    for (int b = 0; b < 8 && ok; ++b, sl += 2) {
+      const uint32_t pq = sl % kPSlots, pk = (sl + 1) % kPSlots;
+      ok = mbar_wait(smem_u32(&ms.full[pq]), slot_phase(sl), abrt, p.timeout_ns, p.err, SITE_PR_FULL) &&
+           mbar_wait(smem_u32(&ms.full[pk]), slot_phase(sl + 1), abrt, p.timeout_ns, p.err, SITE_PR_FULL);
+      if (!ok) break;
+      tc_fence_after();
+      const uint64_t a0 = sdesc_add(kq_desc, pk * kPSlot), b0 = sdesc_add(kq_desc, pq * kPSlot);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        if (b == 0 && ks == 0)
+          umma_f16(tmem, sdesc_add(a0, ks * 32), sdesc_add(b0, ks * 32), kIdescQK, 0u);
+        else
+          umma_f16_acc(tmem, sdesc_add(a0, ks * 32), sdesc_add(b0, ks * 32), kIdescQK);
+      }
+      mbar_arrive(smem_u32(&ms.qx[b]));      // the extra-row warp may read Q box b
+      umma_commit(smem_u32(&ms.empty[pq]));  // the extra-row warp gives the Q slot's second arrival
+      umma_commit(smem_u32(&ms.empty[pk]));
+      mbar_arrive(smem_u32(&ms.empty[pk]));
+    }
+    if (!ok) break;
+    umma_commit(smem_u32(&ms.s_full));
+    ok = mbar_wait(smem_u32(&ms.p_full), n & 1, abrt, p.timeout_ns, p.err, SITE_PR_P_FULL);
+    if (!ok) break;
+    tc_fence_after();
+    for (int m = 0; m < 4 && ok; ++m, sl += 2) {
+      const uint32_t gb = 4 * n + m, buf = gb & 1;
+      const uint32_t pa = sl % kPSlots, pb = (sl + 1) % kPSlots;  // pa even: pb = pa + 1
+      ok = mbar_wait(smem_u32(&ms.o_empty[buf]), ((gb >> 1) & 1) ^ 1, abrt, p.timeout_ns, p.err, SITE_PR_O_EMPTY) &&
+           mbar_wait(smem_u32(&ms.full[pa]), slot_phase(sl), abrt, p.timeout_ns, p.err, SITE_PR_FULL) &&
+           mbar_wait(smem_u32(&ms.full[pb]), slot_phase(sl + 1), abrt, p.timeout_ns, p.err, SITE_PR_FULL);
+      if (!ok) break;
+      tc_fence_after();
+      const uint64_t a0 = sdesc_add(v_desc, pa * kPSlot);
+      const uint32_t d = tmem + 128 + 128 * buf;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        if (ks == 0)
+          umma_f16(d, a0, p_desc, kIdescPV, 0u);
+        else
+          umma_f16_acc(d, sdesc_add(a0, ks * 2048), sdesc_add(p_desc, ks * 2048), kIdescPV);
+      }
+      umma_commit(smem_u32(&ms.empty[pa]));
+      umma_commit(smem_u32(&ms.empty[pb]));
+      mbar_arrive(smem_u32(&ms.empty[pa]));
+      mbar_arrive(smem_u32(&ms.empty[pb]));
+      umma_commit(smem_u32(&ms.o_full[buf]));
+    }
+    if (!ok) break;
+    umma_commit(smem_u32(&ms.p_empty));
+  }
+  // Every MMA issued so far must finish before TMEM is released.
+  umma_commit(smem_u32(&ms.mma_done));
+  volatile int never = 0;
+  mbar_wait(smem_u32(&ms.mma_done), 0, &never, 100000000ull, p.err, SITE_PR_DRAIN);
+}
+
+// ------------------------------------------------------------------ softmax and epilogue
+
+// Lane l ends with the max (or sum) over the warp's 32 rows of column l of the
+// 32 columns held in s[0..31].
+template <bool kMax>
+__device__ __forceinline__ float reduce_scatter32(const float (&s)[32], int lane) {
+  float a[16];
+  {
+    const bool up = lane & 16;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float send = up ? s[i] : s[i + 16];
+      const float keep = up ? s[i + 16] : s[i];
+      const float got = __shfl_xor_sync(0xffffffffu, send, 16);
+      a[i] = kMax ? fmaxf(keep, got) : keep + got;
+    }
+  }
+#pragma unroll
+  for (int c = 16; c >= 2; c >>= 1) {
+    const int half = c / 2;
+    const bool up = lane & half;
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const float send = up ? a[i] : a[i + half];
+      const float keep = up ? a[i + half] : a[i];
+      const float got = __shfl_xor_sync(0xffffffffu, send, half);
+      a[i] = kMax ? fmaxf(keep, got) : keep + got;
+    }
+  }
+  return a[0];
+}
+
+__device__ __forceinline__ void csync() { asm volatile("bar.sync 1, %0;" ::"n"(kPThreadsC) : "memory"); }
+
+__device__ __forceinline__ void pair_compute(const PairParams &p, uint8_t *smem, uint32_t tmem, PairMisc &ms,
+                                             int tid) {
+  volatile int *abrt = &ms.abort_flag;
+  const int w = tid >> 5, l = tid & 31;
+  const int q = w & 3;       // TMEM lane quarter: rows (or dims) 32q .. 32q+31
+  const int tau = w >> 2;    // token of the pair whose columns this thread takes
+  const int r = 32 * q + l;  // this thread's TMEM lane
+  const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+  const int n_pairs = (p.T + 1) / 2;
+  uint32_t n = 0;
+  bool bad = false;
+  grid_dependency_wait();  // the outputs may still be read by the previous kernel
+  for (int pr = blockIdx.x; pr < n_pairs; pr += gridDim.x, ++n) {
+    const PairGeom g = pair_geom(p, pr);
+    const bool has_tok = tau == 0 || g.has_b;
+    const float *sx = ms.sx[n & 1];
+    const __half *vx = reinterpret_cast<const __half *>(smem + kPOffX + 2048 * (n & 1)) + 512;
+    // The extra-row warp's scores of this pair (every pair, so the phases
+    // stay in step).
+    bad = bad || !mbar_wait(smem_u32(&ms.x_full), n & 1, abrt, p.timeout_ns, p.err, SITE_PR_X_FULL);
+
+    // Softmax of the pair's tile.  Pass 1: column maxima.
+    bad = bad || !mbar_wait(smem_u32(&ms.s_full), n & 1, abrt, p.timeout_ns, p.err, SITE_PR_S_FULL);
+    tc_fence_after();
+    const int row = g.tile_lo + r;
+    const bool vis = has_tok && row >= g.lo[tau] && row < g.hi[tau];
+#pragma unroll 1
+    for (int u = 0; u < 2; ++u) {
+      float s[32];
+      tmem_ld32(tmem + 64 * tau + 32 * u + lane_base, s);
+      tmem_wait_ld();
+#pragma unroll
+      for (int h = 0; h < 32; ++h) s[h] = vis ? s[h] * p.scale_log2 : -INFINITY;
+      ms.red[q][64 * tau + 32 * u + l] = reduce_scatter32<true>(s, l);
+    }
+    if (bar_red_or(1, kPThreadsC, bad)) break;
+    if (tid < 128) {
+      const int tt = tid >> 6, h = tid & 63;
+      float mx = fmaxf(fmaxf(ms.red[0][tid], ms.red[1][tid]), fmaxf(ms.red[2][tid], ms.red[3][tid]));
+      if (tt == 0 && g.extra) mx = fmaxf(mx, sx[h]);
+      ms.m_true[tid] = mx;
+      ms.m_use[tid] = mx == -INFINITY ? 0.f : mx;
+    }
+    csync();
+    // Pass 2: P = 2^(s - m) in fp16 (P^T row r of token tau's box, 16-byte
+    // chunk c at c ^ (r & 7): the 128-byte swizzle) and the row sums of the
+    // same fp16 values.  P may be rewritten once the previous pair's PV is done.
+    bad = bad || !mbar_wait(smem_u32(&ms.p_empty), (n & 1) ^ 1, abrt, p.timeout_ns, p.err, SITE_PR_P_EMPTY);
+    uint8_t *prow = smem + kPOffP + tau * kPSlot + r * 128;
+#pragma unroll 1
+    for (int u = 0; u < 2; ++u) {
+      float s[32];
+      tmem_ld32(tmem + 64 * tau + 32 * u + lane_base, s);
+      tmem_wait_ld();
+      const float *mu = ms.m_use + 64 * tau + 32 * u;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t w4[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int h = 8 * c + 2 * i;
+          const float e0 = vis ? exp2f(s[h] * p.scale_log2 - mu[h]) : 0.f;
+          const float e1 = vis ? exp2f(s[h + 1] * p.scale_log2 - mu[h + 1]) : 0.f;
+          const __half2 hp = __floats2half2_rn(e0, e1);
+          const float2 f = __half22float2(hp);
+          s[h] = f.x;
+          s[h + 1] = f.y;
+          w4[i] = *reinterpret_cast<const uint32_t *>(&hp);
+        }
+        const int chunk = 4 * u + c;
+        *reinterpret_cast<uint4 *>(prow + ((chunk ^ (r & 7)) << 4)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+      }
+      ms.red[q][64 * tau + 32 * u + l] = reduce_scatter32<false>(s, l);
+    }
+    tc_fence_before();
+    mbar_arrive(smem_u32(&ms.s_empty));  // S^T read for the last time
+    fence_proxy_async_smem();
+    mbar_arrive(smem_u32(&ms.p_full));
+    if (bar_red_or(1, kPThreadsC, bad)) break;
+    if (tid < 128) {
+      const int tt = tid >> 6, h = tid & 63;
+      float lsum = ms.red[0][tid] + ms.red[1][tid] + ms.red[2][tid] + ms.red[3][tid];
+      if (tt == 0 && g.extra) {
+        const float px = exp2f(sx[h] - ms.m_use[tid]);
+        ms.px[h] = px;
+        lsum += px;
+      }
+      ms.inv_l[tid] = lsum > 0.f ? 1.f / lsum : 0.f;
+      if (p.lse != nullptr && (tt == 0 || g.has_b))
+        p.lse[(long long)(g.ta + tt) * kH + h] = lsum > 0.f ? (ms.m_true[tid] + log2f(lsum)) * kLn2 : -INFINITY;
+    }
+    csync();
+
+    // Epilogue: O^T block m [128 dims][128] -> o of both tokens.  Lanes 2k
+    // and 2k+1 hold adjacent dims: for each pair of heads they swap one value,
+    // so the even lane writes both dims of the first head and the odd lane
+    // both dims of the second (32-bit stores).
+    const bool odd = l & 1;
+    __half *obase = p.o + (long long)(g.ta + tau) * p.o_tok_stride + (r & ~1);
+#pragma unroll 1
+    for (int m = 0; m < 4; ++m) {
+      const uint32_t gb = 4 * n + m, buf = gb & 1;
+      bad = bad || !mbar_wait(smem_u32(&ms.o_full[buf]), (gb >> 1) & 1, abrt, p.timeout_ns, p.err, SITE_PR_O_FULL);
+      tc_fence_after();
+      const float xv = (tau == 0 && g.extra) ? __half2float(vx[128 * m + r]) : 0.f;
+#pragma unroll 1
+      for (int u = 0; u < 2; ++u) {
+        float o[32];
+        tmem_ld32(tmem + 128 + 128 * buf + 64 * tau + 32 * u + lane_base, o);
+        tmem_wait_ld();
+        if (u == 1) {
+          tc_fence_before();
+          mbar_arrive(smem_u32(&ms.o_empty[buf]));
+        }
+        if (has_tok) {
+          const float *iv = ms.inv_l + 64 * tau + 32 * u;
+          const float *pxu = ms.px + 32 * u;
+#pragma unroll
+          for (int h = 0; h < 32; h += 2) {
+            const float a = (o[h] + pxu[h] * xv) * iv[h], b = (o[h + 1] + pxu[h + 1] * xv) * iv[h + 1];
+            const float got = __shfl_xor_sync(0xffffffffu, odd ? a : b, 1);
+            const __half2 v = odd ? __floats2half2_rn(got, b) : __floats2half2_rn(a, got);
+            *reinterpret_cast<__half2 *>(obase + (32 * u + h + (odd ? 1 : 0)) * kD + 128 * m) = v;
+          }
+        }
+      }
+    }
+    if (bar_red_or(1, kPThreadsC, bad)) break;
+    if (tid == 0) mbar_arrive(smem_u32(&ms.x_empty[n & 1]));  // every thread is done with this parity's rows
+  }
+}
+
+// Warp 10: for each pair, token a's row below the tile (when there is one):
+// its K and V rows into this parity's buffer (once the softmax warps are done
+// with the pair two back), then token a's scores against it, taken from the Q
+// boxes as they pass through the ring (lane l: heads 2l and 2l+1), and the
+// second release of every Q slot.
+__device__ __forceinline__ void pair_extra_row(const PairParams &p, uint8_t *smem, PairMisc &ms, int lane) {
+  volatile int *abrt = &ms.abort_flag;
+  const int n_pairs = (p.T + 1) / 2;
+  uint32_t sl = 0, n = 0;
+  bool ok = true;
+  grid_dependency_wait();  // the extra rows are read from global memory
+  for (int pr = blockIdx.x; pr < n_pairs && ok; pr += gridDim.x, ++n) {
+    const PairGeom g = pair_geom(p, pr);
+    uint8_t *xb = smem + kPOffX + 2048 * (n & 1);
+    if (g.extra) {
+      ok = mbar_wait(smem_u32(&ms.x_empty[n & 1]), ((n >> 1) & 1) ^ 1, abrt, p.timeout_ns, p.err, SITE_PR_X_EMPTY);
+      if (!ok) break;
+      const long long off = (long long)(g.tile_lo - 1) * p.raw_row_stride;
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int c = lane + 32 * i;  // 16-byte chunk of the 1024-byte row
+        *reinterpret_cast<uint4 *>(xb + 16 * c) = *reinterpret_cast<const uint4 *>(p.k_raw + off + 16 * c);
+        *reinterpret_cast<uint4 *>(xb + 1024 + 16 * c) = *reinterpret_cast<const uint4 *>(p.v_raw + off + 16 * c);
+      }
+      __syncwarp();
+    }
+    const __half *kx = reinterpret_cast<const __half *>(xb);
+    float acc0 = 0.f, acc1 = 0.f;
+    for (int b = 0; b < 8; ++b, sl += 2) {
+      const uint32_t pq = sl % kPSlots;
+      ok = mbar_wait(smem_u32(&ms.qx[b]), n & 1, abrt, p.timeout_ns, p.err, SITE_PR_FULL);
+      if (!ok) break;
+      if (g.extra) {
+        // Q box b: row (token a, head h) at h * 128, 16-byte chunk c (dims
+        // 64b + 8c ..) at column c ^ (h & 7).
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 kv = *reinterpret_cast<const uint4 *>(kx + 64 * b + 8 * c);
+          const __half2 *k2 = reinterpret_cast<const __half2 *>(&kv);
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const int h = 2 * lane + j;
+            const uint4 qv = *reinterpret_cast<const uint4 *>(smem + kPOffRing + pq * kPSlot + h * 128 +
+                                                              ((c ^ (h & 7)) << 4));
+            const __half2 *q2 = reinterpret_cast<const __half2 *>(&qv);
+            float a = 0.f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 x = __half22float2(q2[e]), y = __half22float2(k2[e]);
+              a = fmaf(x.x, y.x, fmaf(x.y, y.y, a));
+            }
+            if (j == 0) acc0 += a; else acc1 += a;
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&ms.empty[pq]));
+    }
+    if (!ok) break;
+    sl += 8;  // the V slots
+    ms.sx[n & 1][2 * lane] = acc0 * p.scale_log2;
+    ms.sx[n & 1][2 * lane + 1] = acc1 * p.scale_log2;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&ms.x_full));
+  }
+}
+
+__global__ void __launch_bounds__(kPThreads, 1) attn_pair_kernel(const __grid_constant__ PairParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const uint32_t sbase = smem_u32(smem);
+  PairMisc &ms = *reinterpret_cast<PairMisc *>(smem + kPOffMisc);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPSlots; ++s) {
+      mbar_init(smem_u32(&ms.full[s]), 1);
+      mbar_init(smem_u32(&ms.empty[s]), 2);
+    }
+    mbar_init(smem_u32(&ms.s_full), 1);
+    mbar_init(smem_u32(&ms.s_empty), kPThreadsC);
+    mbar_init(smem_u32(&ms.p_full), kPThreadsC);
+    mbar_init(smem_u32(&ms.p_empty), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&ms.o_full[b]), 1);
+      mbar_init(smem_u32(&ms.o_empty[b]), kPThreadsC);
+    }
+    mbar_init(smem_u32(&ms.mma_done), 1);
+    mbar_init(smem_u32(&ms.x_full), 1);
+    mbar_init(smem_u32(&ms.x_empty[0]), 1);
+    mbar_init(smem_u32(&ms.x_empty[1]), 1);
+    for (int b = 0; b < 8; ++b) mbar_init(smem_u32(&ms.qx[b]), 1);
+    ms.abort_flag = 0;
+    for (int i = 0; i < 64; ++i) ms.px[i] = 0.f;
+    fence_barrier_init();
+  }
+  if (warp == kPMmaWarp) {
+    tmem_alloc(smem_u32(&ms.tmem_base), 512);
+    tmem_relinquish();
+  }
+  if (warp == kPLoaderWarp && lane == 0) {
+    tma_prefetch_desc(&p.tm_q2);
+    tma_prefetch_desc(&p.tm_k);
+    tma_prefetch_desc(&p.tm_v);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ms.tmem_base;
+  grid_launch_dependents();
+  if (warp < kPWarps) {
+    pair_compute(p, smem, tmem, ms, threadIdx.x);
+  } else if (warp == kPLoaderWarp) {
+    if (lane == 0) pair_loader(p, sbase, ms);
+    __syncwarp();
+  } else if (warp == kPMmaWarp) {
+    if (lane == 0) pair_mma(p, sbase, tmem, ms);
+    __syncwarp();
+  } else {
+    pair_extra_row(p, smem, ms, lane);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kPMmaWarp) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace
+
+cudaError_t prepare_pair_kernel() {
+  return cudaFuncSetAttribute(attn_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPSmemBytes);
+}
+
+cudaError_t launch_pair(const PairParams &p, int grid, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kPThreads);
+  cfg.dynamicSmemBytes = kPSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attn_pair_kernel, p);
+}
+
+}  // namespace ds4a

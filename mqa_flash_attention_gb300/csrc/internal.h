@@ -17,6 +17,24 @@ struct GeomScalars {
 cudaError_t prepare_attn_kernel();
 cudaError_t launch_attn(const AttnParams &p, int grid, cudaStream_t s);
 
+// attn_pair.cu: pairs of consecutive tokens over raw rows (structural rule,
+// no compressed rows, window <= 128).
+struct PairParams {
+  CUtensorMap tm_q2;          // 3-D {512, 64, T}, box {64, 64, 2}: both tokens of a pair, 128-byte swizzle
+  CUtensorMap tm_k, tm_v;     // 2-D {512, n_raw}, box {64, 128}, 128-byte swizzle
+  int T, q_pos0, n_raw, raw_pos0, window;
+  float scale_log2;
+  const uint8_t *k_raw, *v_raw;  // the row below a pair's tile is read directly
+  long long raw_row_stride;      // bytes
+  __half *o;
+  long long o_tok_stride;        // elements
+  float *lse;
+  unsigned long long timeout_ns;
+  unsigned int *err;
+};
+cudaError_t prepare_pair_kernel();
+cudaError_t launch_pair(const PairParams &p, int grid, cudaStream_t s);
+
 // aux.cu
 cudaError_t launch_pad(const void *src, long long src_stride, int n_rows, void *dst, long long dst_stride,
                        int first_row, cudaStream_t s);
