@@ -96,6 +96,12 @@ typedef enum {
 /* Static message for a status code; never NULL. */
 const char *ds4a_status_string(int status);
 
+/* The CUDA call and error code behind the latest DS4A_ERR_CUDA returned on the
+ * calling thread (e.g. "kernel launch: error 1 invalid argument"); "" when
+ * there was none.  The string belongs to the library and stays valid until the
+ * thread's next failing call. */
+const char *ds4a_last_cuda_error(void);
+
 /* Library version string, "ds4a 0.2 sm_103a".  The minor number changes
  * whenever a layout callers can see changes: 0.2 is the first version whose
  * decode workspace holds fp16 normalised partials with the merge weight

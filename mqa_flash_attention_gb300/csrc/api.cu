@@ -6,6 +6,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <cstdio>
 #include <cstring>
 #include <mutex>
 
@@ -39,6 +40,22 @@ struct DeviceState {
 };
 
 std::mutex g_mu;
+
+// What the latest DS4A_ERR_CUDA of this thread came from (empty when none).
+thread_local char g_cuda_detail[192] = "";
+
+ds4a_status cuda_failed(const char *call, int code, const char *text) {
+  std::snprintf(g_cuda_detail, sizeof(g_cuda_detail), "%s: error %d%s%s", call, code, text ? " " : "",
+                text ? text : "");
+  return DS4A_ERR_CUDA;
+}
+ds4a_status cuda_failed(const char *call, cudaError_t e) { return cuda_failed(call, (int)e, cudaGetErrorString(e)); }
+#define DS4A_CUDA_TRY(call)                              \
+  do {                                                   \
+    const cudaError_t e_ = (call);                       \
+    if (e_ != cudaSuccess) return cuda_failed(#call, e_); \
+  } while (0)
+
 DeviceState g_dev[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
@@ -46,31 +63,28 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 // word's address, the kernel's shared-memory opt-in and the tensor-map encoder.
 ds4a_status current_device(DeviceState **out) {
   int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) return DS4A_ERR_CUDA;
+  DS4A_CUDA_TRY(cudaGetDevice(&dev));
   if (dev < 0 || dev >= kMaxDevices) return DS4A_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_mu);
   DeviceState &d = g_dev[dev];
   if (!d.ready) {
     int major = 0, minor = 0, sms = 0;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      return DS4A_ERR_CUDA;
+    DS4A_CUDA_TRY(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev));
+    DS4A_CUDA_TRY(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev));
+    DS4A_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
     d.sm_count = sms;
     d.supported = (major == 10 && minor == 3);
     if (d.supported) {
-      if (ds4a::prepare_attn_kernel() != cudaSuccess || ds4a::prepare_pair_kernel() != cudaSuccess)
-        return DS4A_ERR_CUDA;
-      if (cudaGetSymbolAddress(reinterpret_cast<void **>(&d.err), g_ds4a_device_error) != cudaSuccess)
-        return DS4A_ERR_CUDA;
-      if (cudaGetSymbolAddress(&d.scratch, g_decode_scratch) != cudaSuccess) return DS4A_ERR_CUDA;
+      DS4A_CUDA_TRY(ds4a::prepare_attn_kernel());
+      DS4A_CUDA_TRY(ds4a::prepare_pair_kernel());
+      DS4A_CUDA_TRY(cudaGetSymbolAddress(reinterpret_cast<void **>(&d.err), g_ds4a_device_error));
+      DS4A_CUDA_TRY(cudaGetSymbolAddress(&d.scratch, g_decode_scratch));
       if (g_encode == nullptr) {
         cudaDriverEntryPointQueryResult q;
         void *fn = nullptr;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
-                cudaSuccess ||
-            q != cudaDriverEntryPointSuccess || fn == nullptr)
-          return DS4A_ERR_CUDA;
+        DS4A_CUDA_TRY(cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q));
+        if (q != cudaDriverEntryPointSuccess || fn == nullptr)
+          return cuda_failed("cudaGetDriverEntryPointByVersion(cuTensorMapEncodeTiled)", (int)q, nullptr);
         g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
       }
     }
@@ -122,11 +136,21 @@ ds4a_status check_tensors(const ds4a_layout *L, const ds4a_tensors *X) {
 ds4a_status encode(CUtensorMap *m, const void *base, int rank, const cuuint64_t *dims, const cuuint64_t *strides,
                    const cuuint32_t *box, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B,
                    CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_FLOAT16) {
-  const cuuint32_t es[3] = {1, 1, 1};
+  const cuuint32_t es[5] = {1, 1, 1, 1, 1};  // element strides, up to rank 5
   const CUresult r = g_encode(m, dtype, (cuuint32_t)rank, const_cast<void *>(base), dims,
                               strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? DS4A_OK : DS4A_ERR_CUDA;
+  if (r == CUDA_SUCCESS) return DS4A_OK;
+  char what[160];
+  int n = std::snprintf(what, sizeof(what), "cuTensorMapEncodeTiled(rank %d, dims", rank);
+  for (int i = 0; i < rank && n < (int)sizeof(what); ++i)
+    n += std::snprintf(what + n, sizeof(what) - n, " %llu", (unsigned long long)dims[i]);
+  for (int i = 0; i + 1 < rank && n < (int)sizeof(what); ++i)
+    n += std::snprintf(what + n, sizeof(what) - n, "%s%llu", i == 0 ? ", strides " : " ", (unsigned long long)strides[i]);
+  for (int i = 0; i < rank && n < (int)sizeof(what); ++i)
+    n += std::snprintf(what + n, sizeof(what) - n, "%s%u", i == 0 ? ", box " : " ", box[i]);
+  if (n < (int)sizeof(what)) std::snprintf(what + n, sizeof(what) - n, ")");
+  return cuda_failed(what, (int)r, nullptr);
 }
 
 // K/V rows: {512 dims, rows}, box {64 dims, box_rows rows}, 128-byte swizzle.
@@ -137,14 +161,32 @@ ds4a_status encode_rows(CUtensorMap *m, const void *base, int rows, int64_t stri
   return encode(m, base, 2, dims, strides, box);
 }
 
+// K/V rows as 64-dim column blocks: {64 dims, rows, 8 blocks} (block stride
+// 128 bytes), box {64, box_rows, 2}: one copy brings a 128-dim part of a tile
+// as two [box_rows][64] swizzled boxes, one after the other.  A thread's bulk
+// copies start one after another, some 650 cycles apart whatever their size,
+// so fewer, larger copies load a tile sooner.
+ds4a_status encode_row_parts(CUtensorMap *m, const void *base, int rows, int64_t stride, unsigned box_rows) {
+  const cuuint64_t dims[3] = {64, (cuuint64_t)rows, DS4A_HEAD_DIM / 64};
+  const cuuint64_t strides[2] = {(cuuint64_t)stride, 128};
+  const cuuint32_t box[3] = {64, box_rows, 2};
+  return encode(m, base, 3, dims, strides, box);
+}
+
+// Q of every token (or sequence) at once per copy: {64 dims, 64 heads, n,
+// 8 blocks}, box {64, 64, 1, 8}: the eight [64 heads][64 dims] boxes of a token.
+ds4a_status encode_q_blocks(CUtensorMap *m, const void *base, int n, int64_t stride) {
+  const cuuint64_t dims[4] = {64, DS4A_HEADS, (cuuint64_t)n, DS4A_HEAD_DIM / 64};
+  const cuuint64_t strides[3] = {DS4A_ROW_BYTES, (cuuint64_t)stride, 128};
+  const cuuint32_t box[4] = {64, 64, 1, DS4A_HEAD_DIM / 64};
+  return encode(m, base, 4, dims, strides, box);
+}
+
 // Fills the parts of the kernel parameters every attention mode shares.
 ds4a_status fill_params(AttnParams &p, const ds4a_layout *L, const ds4a_tensors *X, int mode, DeviceState *d) {
   std::memset(&p, 0, sizeof(p));
   {
-    const cuuint64_t dims[3] = {DS4A_HEAD_DIM, DS4A_HEADS, (cuuint64_t)L->T};
-    const cuuint64_t strides[2] = {DS4A_ROW_BYTES, (cuuint64_t)X->q_tok_stride};
-    const cuuint32_t box[3] = {64, 64, 1};
-    ds4a_status st = encode(&p.tm_q, X->q, 3, dims, strides, box);
+    ds4a_status st = encode_q_blocks(&p.tm_q, X->q, L->T, X->q_tok_stride);
     if (st != DS4A_OK) return st;
   }
   if (X->o != nullptr) {
@@ -156,13 +198,13 @@ ds4a_status fill_params(AttnParams &p, const ds4a_layout *L, const ds4a_tensors 
     if (st != DS4A_OK) return st;
   }
   if (L->n_raw > 0) {
-    ds4a_status st = encode_rows(&p.tm_k[0], X->k_raw, L->n_raw, X->raw_row_stride, 128);
-    if (st == DS4A_OK) st = encode_rows(&p.tm_v[0], X->v_raw, L->n_raw, X->raw_row_stride, 128);
+    ds4a_status st = encode_row_parts(&p.tm_k[0], X->k_raw, L->n_raw, X->raw_row_stride, 128);
+    if (st == DS4A_OK) st = encode_row_parts(&p.tm_v[0], X->v_raw, L->n_raw, X->raw_row_stride, 128);
     if (st != DS4A_OK) return st;
   }
   if (L->n_comp > 0) {
-    ds4a_status st = encode_rows(&p.tm_k[1], X->k_comp, L->n_comp, X->comp_row_stride, 128);
-    if (st == DS4A_OK) st = encode_rows(&p.tm_v[1], X->v_comp, L->n_comp, X->comp_row_stride, 128);
+    ds4a_status st = encode_row_parts(&p.tm_k[1], X->k_comp, L->n_comp, X->comp_row_stride, 128);
+    if (st == DS4A_OK) st = encode_row_parts(&p.tm_v[1], X->v_comp, L->n_comp, X->comp_row_stride, 128);
     if (st != DS4A_OK) return st;
   }
   p.k_comp = X->k_comp;
@@ -197,7 +239,7 @@ ds4a_status fill_params(AttnParams &p, const ds4a_layout *L, const ds4a_tensors 
   return DS4A_OK;
 }
 
-ds4a_status launched(cudaError_t e) { return e == cudaSuccess ? DS4A_OK : DS4A_ERR_CUDA; }
+ds4a_status launched(cudaError_t e) { return e == cudaSuccess ? DS4A_OK : cuda_failed("kernel launch", e); }
 
 int32_t max_tiles_per_token(const ds4a_layout *L, int rows = 128) {
   const int64_t raw = L->window < L->n_raw ? L->window : L->n_raw;
@@ -268,6 +310,8 @@ const char *ds4a_status_string(int status) {
 }
 
 const char *ds4a_version(void) { return "ds4a 0.2 sm_103a"; }
+
+const char *ds4a_last_cuda_error(void) { return g_cuda_detail; }
 
 ds4a_status ds4a_pad_kv(const void *src, int64_t src_row_stride, int32_t n_rows, void *dst, int64_t dst_row_stride,
                         ds4a_stream_t stream) {
@@ -503,12 +547,12 @@ ds4a_status decode_partials(const ds4a_layout *L, const ds4a_tensors *X, int32_t
     p.tile_rows = 64;
     // K/V rows in 64-row boxes for the paired stages.
     if (L->n_raw > 0) {
-      if ((st = encode_rows(&p.tm_k[0], X->k_raw, L->n_raw, X->raw_row_stride, 64)) != DS4A_OK) return st;
-      if ((st = encode_rows(&p.tm_v[0], X->v_raw, L->n_raw, X->raw_row_stride, 64)) != DS4A_OK) return st;
+      if ((st = encode_row_parts(&p.tm_k[0], X->k_raw, L->n_raw, X->raw_row_stride, 64)) != DS4A_OK) return st;
+      if ((st = encode_row_parts(&p.tm_v[0], X->v_raw, L->n_raw, X->raw_row_stride, 64)) != DS4A_OK) return st;
     }
     if (L->n_comp > 0) {
-      if ((st = encode_rows(&p.tm_k[1], X->k_comp, L->n_comp, X->comp_row_stride, 64)) != DS4A_OK) return st;
-      if ((st = encode_rows(&p.tm_v[1], X->v_comp, L->n_comp, X->comp_row_stride, 64)) != DS4A_OK) return st;
+      if ((st = encode_row_parts(&p.tm_k[1], X->k_comp, L->n_comp, X->comp_row_stride, 64)) != DS4A_OK) return st;
+      if ((st = encode_row_parts(&p.tm_v[1], X->v_comp, L->n_comp, X->comp_row_stride, 64)) != DS4A_OK) return st;
     }
   }
   p.n_splits = n_splits;
@@ -745,12 +789,7 @@ ds4a_status ds4a_attn_decode_batch(int32_t n_seq, const ds4a_layout *shape, cons
   if (st != DS4A_OK) return st;
   AttnParams p;
   std::memset(&p, 0, sizeof(p));
-  {
-    const cuuint64_t dims[3] = {DS4A_HEAD_DIM, DS4A_HEADS, (cuuint64_t)n_seq};
-    const cuuint64_t strides[2] = {DS4A_ROW_BYTES, (cuuint64_t)X->q_seq_stride};
-    const cuuint32_t box[3] = {64, 64, 1};
-    if ((st = encode(&p.tm_q, X->q, 3, dims, strides, box)) != DS4A_OK) return st;
-  }
+  if ((st = encode_q_blocks(&p.tm_q, X->q, n_seq, X->q_seq_stride)) != DS4A_OK) return st;
   if (X->raw_rows > 0) {
     st = encode_batch_rows(&p.tm_k[0], X->k_raw, X->raw_rows, X->raw_row_stride, n_seq, X->raw_seq_stride);
     if (st == DS4A_OK)
@@ -851,12 +890,12 @@ ds4a_status ds4a_device_error_word(ds4a_stream_t stream, uint32_t *word, int cle
   DeviceState *d = nullptr;
   ds4a_status st = current_device(&d);
   if (st != DS4A_OK) return st;
-  if (cudaStreamSynchronize(as_cuda(stream)) != cudaSuccess) return DS4A_ERR_CUDA;
+  DS4A_CUDA_TRY(cudaStreamSynchronize(as_cuda(stream)));
   unsigned int v = 0;
-  if (cudaMemcpy(&v, d->err, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return DS4A_ERR_CUDA;
+  DS4A_CUDA_TRY(cudaMemcpy(&v, d->err, sizeof(v), cudaMemcpyDeviceToHost));
   if (clear && v != 0) {
     const unsigned int zero = 0;
-    if (cudaMemcpy(d->err, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return DS4A_ERR_CUDA;
+    DS4A_CUDA_TRY(cudaMemcpy(d->err, &zero, sizeof(zero), cudaMemcpyHostToDevice));
   }
   *word = v;
   return DS4A_OK;

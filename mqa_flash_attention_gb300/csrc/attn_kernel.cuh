@@ -310,7 +310,8 @@ __device__ __noinline__ void q_copy_role(const AttnParams &p, uint32_t sbase, Mi
 // unambiguous only for a waiter at most one phase behind, and a filler cannot
 // fall behind a barrier that only advances after its own fills.
 //
-// TMA tiles: thread 0 issues two 16 KB box loads per 32 KB stage.
+// TMA tiles: thread 0 issues one copy per 32 KB stage (the row maps' boxes
+// span two 64-dim blocks), Q in one 64 KB copy.
 // Gathered tiles (index-listed compressed rows): per stage (128 rows x 128
 // dims) the loader threads copy 2048 chunks of 16 bytes; a warp instruction
 // covers two rows x 256 contiguous bytes.  Chunk (row r, 16-byte column c of a
@@ -360,9 +361,7 @@ __device__ __forceinline__ void loader_role(const AttnParams &p, uint32_t sbase,
     }
     if (ltid == 0 && !q_lsu) {
       mbar_arrive_expect_tx(b_q_full, kQBytes);
-#pragma unroll 1
-      for (int b = 0; b < 8; ++b)
-        tma_load_3d(sbase + kOffQ + b * kQBoxBytes, &p.tm_q, b_q_full, 64 * b, 0, ip.t);
+      tma_load_4d(sbase + kOffQ, &p.tm_q, b_q_full, 0, 0, ip.t, 0);  // the eight boxes in one copy
     }
     q_issued = !q_lsu;
     q_par = n_item & 1;
@@ -411,18 +410,15 @@ __device__ __forceinline__ void loader_role(const AttnParams &p, uint32_t sbase,
             mbar_arrive_expect_tx(b_full, kStageBytes);
             if (p.kv_pair) {
               // 64-row tile: the K and the V slice of dims dim0 .. dim0+127 in
-              // one stage, four [64 rows][64 dims] boxes of 8 KB.
-              constexpr uint32_t hb = kBoxBytes / 2;
-              tma_load_2d(stage, &p.tm_k[tl.seg], b_full, dim0, tl.start);
-              tma_load_2d(stage + hb, &p.tm_k[tl.seg], b_full, dim0 + 64, tl.start);
-              tma_load_2d(stage + 2 * hb, &p.tm_v[tl.seg], b_full, dim0, tl.start);
-              tma_load_2d(stage + 3 * hb, &p.tm_v[tl.seg], b_full, dim0 + 64, tl.start);
+              // one stage, four [64 rows][64 dims] boxes of 8 KB (two copies:
+              // the maps' boxes span two 64-dim blocks).
+              tma_load_3d(stage, &p.tm_k[tl.seg], b_full, 0, tl.start, dim0 / 64);
+              tma_load_3d(stage + kBoxBytes, &p.tm_v[tl.seg], b_full, 0, tl.start, dim0 / 64);
             } else if (p.batch_geom != nullptr) {  // [sequences][rows][512]: the sequence is the third coordinate
               tma_load_3d(stage, m, b_full, dim0, tl.start, ip.t);
               tma_load_3d(stage + kBoxBytes, m, b_full, dim0 + 64, tl.start, ip.t);
             } else {
-              tma_load_2d(stage, m, b_full, dim0, tl.start);
-              tma_load_2d(stage + kBoxBytes, m, b_full, dim0 + 64, tl.start);
+              tma_load_3d(stage, m, b_full, 0, tl.start, dim0 / 64);  // both 64-dim boxes of the part
             }
             filled |= 1u << ring.st;
             last_par = (last_par & ~(1u << ring.st)) | (ring.ph << ring.st);

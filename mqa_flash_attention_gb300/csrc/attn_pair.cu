@@ -15,9 +15,10 @@
 // full rate where a single token's N = 64 runs near half of it:
 //   S^T[128 rows][128]      = K_tile[128][512] . Q_pair[128][512]^T   (K-major A, K-major B)
 //   O^T_m[128 dims][128]    = V_tile^T[dims 128m..][128] . P^T          (MN-major A, MN-major B)
-// TMEM: S^T at columns 0-127; O^T is produced one 128-dim block at a time
-// into two alternating 128-column buffers that the epilogue drains as they
-// complete (no block accumulates across tiles: the pair has one tile).
+// TMEM: S^T at columns 0-127; the four 128-dim blocks of O^T at columns
+// 128-511 (blocks 0-2) and 0-127 (block 3, once S^T has been read), so all of
+// a pair's PV products go out as soon as P^T is written and free their V
+// boxes at once; no block accumulates across tiles (the pair has one tile).
 //
 // Shared memory: a ring of 10 slots of 16 KB through which every box of a
 // pair streams in a fixed order (Q box b, K box b for b = 0..7, then V boxes
@@ -68,7 +69,7 @@ struct PairMisc {
   alignas(16) float sx[2][64];    // extra row, by pair parity: scaled score of token a per head (log2 units)
   alignas(16) float px[64];       // extra row: its weight
   alignas(8) uint64_t full[kPSlots], empty[kPSlots];
-  uint64_t s_full, s_empty, p_full, p_empty, o_full[2], o_empty[2], mma_done;
+  uint64_t s_full, s_empty, p_full, p_empty, o_full[4], mma_done;
   uint64_t x_full, x_empty[2];    // extra-row scores of a pair ready; a parity's row buffer free again
   uint64_t qx[8];                 // Q box b of the current pair has landed (passed on by the MMA thread)
   uint32_t tmem_base;
@@ -124,6 +125,8 @@ __device__ __forceinline__ uint32_t slot_addr(uint32_t sbase, uint32_t sl) {
   return sbase + kPOffRing + (sl % kPSlots) * kPSlot;
 }
 __device__ __forceinline__ uint32_t slot_phase(uint32_t sl) { return (sl / kPSlots) & 1u; }
+// TMEM column of O^T block m: blocks 0-2 after S^T, block 3 in S^T's columns.
+__device__ __forceinline__ uint32_t o_column(int m) { return m == 3 ? 0u : 128u + 128u * m; }
 
 // ------------------------------------------------------------------ loader
 
@@ -204,19 +207,22 @@ __device__ __forceinline__ void pair_mma(const PairParams &p, uint32_t sbase, ui
     }
     if (!ok) break;
     umma_commit(smem_u32(&ms.s_full));
+    // P^T written means S^T has been read and every O^T block of the previous
+    // pair drained: all four blocks go out at once, block 3 (the last V boxes)
+    // first into S^T's columns, which the epilogue drains first.
     ok = mbar_wait(smem_u32(&ms.p_full), n & 1, abrt, p.timeout_ns, p.err, SITE_PR_P_FULL);
     if (!ok) break;
     tc_fence_after();
-    for (int m = 0; m < 4 && ok; ++m, sl += 2) {
-      const uint32_t gb = 4 * n + m, buf = gb & 1;
-      const uint32_t pa = sl % kPSlots, pb = (sl + 1) % kPSlots;  // pa even: pb = pa + 1
-      ok = mbar_wait(smem_u32(&ms.o_empty[buf]), ((gb >> 1) & 1) ^ 1, abrt, p.timeout_ns, p.err, SITE_PR_O_EMPTY) &&
-           mbar_wait(smem_u32(&ms.full[pa]), slot_phase(sl), abrt, p.timeout_ns, p.err, SITE_PR_FULL) &&
-           mbar_wait(smem_u32(&ms.full[pb]), slot_phase(sl + 1), abrt, p.timeout_ns, p.err, SITE_PR_FULL);
+    for (int k = 0; k < 4 && ok; ++k) {
+      const int m = (k + 3) & 3;
+      const uint32_t sv = sl + 2 * m;
+      const uint32_t pa = sv % kPSlots, pb = (sv + 1) % kPSlots;  // pa even: pb = pa + 1
+      ok = mbar_wait(smem_u32(&ms.full[pa]), slot_phase(sv), abrt, p.timeout_ns, p.err, SITE_PR_FULL) &&
+           mbar_wait(smem_u32(&ms.full[pb]), slot_phase(sv + 1), abrt, p.timeout_ns, p.err, SITE_PR_FULL);
       if (!ok) break;
       tc_fence_after();
       const uint64_t a0 = sdesc_add(v_desc, pa * kPSlot);
-      const uint32_t d = tmem + 128 + 128 * buf;
+      const uint32_t d = tmem + o_column(m);
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
         if (ks == 0)
@@ -228,9 +234,10 @@ __device__ __forceinline__ void pair_mma(const PairParams &p, uint32_t sbase, ui
       umma_commit(smem_u32(&ms.empty[pb]));
       mbar_arrive(smem_u32(&ms.empty[pa]));
       mbar_arrive(smem_u32(&ms.empty[pb]));
-      umma_commit(smem_u32(&ms.o_full[buf]));
+      umma_commit(smem_u32(&ms.o_full[m]));
     }
     if (!ok) break;
+    sl += 8;
     umma_commit(smem_u32(&ms.p_empty));
   }
   // Every MMA issued so far must finish before TMEM is released.
@@ -347,8 +354,7 @@ __device__ __forceinline__ void pair_compute(const PairParams &p, uint8_t *smem,
       }
       ms.red[q][64 * tau + 32 * u + l] = reduce_scatter32<false>(s, l);
     }
-    tc_fence_before();
-    mbar_arrive(smem_u32(&ms.s_empty));  // S^T read for the last time
+    tc_fence_before();  // S^T read for the last time
     fence_proxy_async_smem();
     mbar_arrive(smem_u32(&ms.p_full));
     if (bar_red_or(1, kPThreadsC, bad)) break;
@@ -366,35 +372,55 @@ __device__ __forceinline__ void pair_compute(const PairParams &p, uint8_t *smem,
     }
     csync();
 
-    // Epilogue: O^T block m [128 dims][128] -> o of both tokens.  Lanes 2k
-    // and 2k+1 hold adjacent dims: for each pair of heads they swap one value,
-    // so the even lane writes both dims of the first head and the odd lane
-    // both dims of the second (32-bit stores).
+    // Epilogue: O^T block m [128 dims][128] -> o of both tokens, block 3
+    // first (it frees S^T's columns for the next pair).  Lanes 2k and 2k+1
+    // hold adjacent dims: for each pair of heads they swap one value, so the
+    // even lane writes both dims of the first head and the odd lane both dims
+    // of the second (32-bit stores).
     const bool odd = l & 1;
+    const bool with_x = tau == 0 && g.extra;  // token a folds in its extra row
     __half *obase = p.o + (long long)(g.ta + tau) * p.o_tok_stride + (r & ~1);
 #pragma unroll 1
-    for (int m = 0; m < 4; ++m) {
-      const uint32_t gb = 4 * n + m, buf = gb & 1;
-      bad = bad || !mbar_wait(smem_u32(&ms.o_full[buf]), (gb >> 1) & 1, abrt, p.timeout_ns, p.err, SITE_PR_O_FULL);
+    for (int k = 0; k < 4; ++k) {
+      const int m = (k + 3) & 3;
+      bad = bad || !mbar_wait(smem_u32(&ms.o_full[m]), n & 1, abrt, p.timeout_ns, p.err, SITE_PR_O_FULL);
       tc_fence_after();
-      const float xv = (tau == 0 && g.extra) ? __half2float(vx[128 * m + r]) : 0.f;
+      const float xv = with_x ? __half2float(vx[128 * m + r]) : 0.f;
 #pragma unroll 1
       for (int u = 0; u < 2; ++u) {
         float o[32];
-        tmem_ld32(tmem + 128 + 128 * buf + 64 * tau + 32 * u + lane_base, o);
+        tmem_ld32(tmem + o_column(m) + 64 * tau + 32 * u + lane_base, o);
         tmem_wait_ld();
-        if (u == 1) {
+        if (k == 0 && u == 1) {
           tc_fence_before();
-          mbar_arrive(smem_u32(&ms.o_empty[buf]));
+          mbar_arrive(smem_u32(&ms.s_empty));  // S^T's columns may take the next pair's scores
         }
         if (has_tok) {
-          const float *iv = ms.inv_l + 64 * tau + 32 * u;
-          const float *pxu = ms.px + 32 * u;
+          const float4 *iv4 = reinterpret_cast<const float4 *>(ms.inv_l + 64 * tau + 32 * u);
+          if (with_x) {
+            const float4 *px4 = reinterpret_cast<const float4 *>(ms.px + 32 * u);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const float4 iv = iv4[j], px = px4[j];
+              o[4 * j] = fmaf(px.x, xv, o[4 * j]) * iv.x;
+              o[4 * j + 1] = fmaf(px.y, xv, o[4 * j + 1]) * iv.y;
+              o[4 * j + 2] = fmaf(px.z, xv, o[4 * j + 2]) * iv.z;
+              o[4 * j + 3] = fmaf(px.w, xv, o[4 * j + 3]) * iv.w;
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const float4 iv = iv4[j];
+              o[4 * j] *= iv.x;
+              o[4 * j + 1] *= iv.y;
+              o[4 * j + 2] *= iv.z;
+              o[4 * j + 3] *= iv.w;
+            }
+          }
 #pragma unroll
           for (int h = 0; h < 32; h += 2) {
-            const float a = (o[h] + pxu[h] * xv) * iv[h], b = (o[h + 1] + pxu[h + 1] * xv) * iv[h + 1];
-            const float got = __shfl_xor_sync(0xffffffffu, odd ? a : b, 1);
-            const __half2 v = odd ? __floats2half2_rn(got, b) : __floats2half2_rn(a, got);
+            const float got = __shfl_xor_sync(0xffffffffu, odd ? o[h] : o[h + 1], 1);
+            const __half2 v = odd ? __floats2half2_rn(got, o[h + 1]) : __floats2half2_rn(o[h], got);
             *reinterpret_cast<__half2 *>(obase + (32 * u + h + (odd ? 1 : 0)) * kD + 128 * m) = v;
           }
         }
@@ -487,10 +513,7 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_pair_kernel(const __grid_co
     mbar_init(smem_u32(&ms.s_empty), kPThreadsC);
     mbar_init(smem_u32(&ms.p_full), kPThreadsC);
     mbar_init(smem_u32(&ms.p_empty), 1);
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(smem_u32(&ms.o_full[b]), 1);
-      mbar_init(smem_u32(&ms.o_empty[b]), kPThreadsC);
-    }
+    for (int b = 0; b < 4; ++b) mbar_init(smem_u32(&ms.o_full[b]), 1);
     mbar_init(smem_u32(&ms.mma_done), 1);
     mbar_init(smem_u32(&ms.x_full), 1);
     mbar_init(smem_u32(&ms.x_empty[0]), 1);

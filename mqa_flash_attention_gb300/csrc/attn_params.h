@@ -71,8 +71,9 @@ static_assert(offsetof(Misc, red) % 16 == 0 && offsetof(Misc, m_use) % 16 == 0 &
 constexpr uint32_t kSmemBytes = kOffMisc + ((sizeof(Misc) + 127) / 128) * 128 + 1024;
 
 struct AttnParams {
-  CUtensorMap tm_q;        // 3-D {512, 64, T}, box {64, 64, 1}
-  CUtensorMap tm_k[2];     // [raw, comp] 2-D {512, rows}, box {64, 128}
+  CUtensorMap tm_q;        // 4-D {64, 64 heads, T, 8 dim blocks}, box {64, 64, 1, 8}
+  CUtensorMap tm_k[2];     // [raw, comp] 3-D {64, rows, 8 dim blocks}, box {64, tile rows, 2}
+                           // (batched decode: 3-D {512, rows, sequences}, box {64, 128, 1})
   CUtensorMap tm_v[2];
   CUtensorMap tm_kg, tm_vg;  // compressed rows, box {64, 1} (gather4)
   CUtensorMap tm_o;        // 3-D {512, 64, T}, box {128, 64, 1}, no swizzle (epilogue stores)

@@ -76,6 +76,8 @@ def lib() -> ctypes.CDLL:
         L.ds4a_status_string.argtypes = [ctypes.c_int]
         L.ds4a_version.restype = ctypes.c_char_p
         L.ds4a_version.argtypes = []
+        L.ds4a_last_cuda_error.restype = ctypes.c_char_p
+        L.ds4a_last_cuda_error.argtypes = []
         L.ds4a_pad_kv.restype = st
         L.ds4a_pad_kv.argtypes = [vp, i64, i32, vp, i64, vp]
         L.ds4a_block_count.restype = i32
@@ -138,9 +140,14 @@ def version() -> str:
     return lib().ds4a_version().decode()
 
 
+def last_cuda_error() -> str:
+    """The CUDA call and code behind the latest ERR_CUDA on this thread ("" if none)."""
+    return lib().ds4a_last_cuda_error().decode()
+
+
 def _check(status: int, what: str) -> None:
     if status != OK:
-        raise Ds4aError(status, what)
+        raise Ds4aError(status, what + (" [" + last_cuda_error() + "]" if status == ERR_CUDA else ""))
 
 
 def make_layout(layout) -> Layout:

@@ -43,6 +43,7 @@ def test_status_strings(lib):
     assert ds4a.status_string(99) == "unknown status"
     # 0.2: the decode workspace holds fp16 normalised partials (0.1 held fp32 sums)
     assert ds4a.version() == "ds4a 0.2 sm_103a"
+    assert ds4a.last_cuda_error() == ""  # no CUDA call has failed on this thread
 
 
 def _layout(**kw):
