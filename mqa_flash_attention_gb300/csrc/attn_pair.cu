@@ -15,15 +15,19 @@
 // full rate where a single token's N = 64 runs near half of it:
 //   S^T[128 rows][128]      = K_tile[128][512] . Q_pair[128][512]^T   (K-major A, K-major B)
 //   O^T_m[128 dims][128]    = V_tile^T[dims 128m..][128] . P^T          (MN-major A, MN-major B)
-// TMEM: S^T at columns 0-127; the four 128-dim blocks of O^T at columns
-// 128-511 (blocks 0-2) and 0-127 (block 3, once S^T has been read), so all of
-// a pair's PV products go out as soon as P^T is written and free their V
-// boxes at once; no block accumulates across tiles (the pair has one tile).
+// TMEM: two S^T buffers (columns 0-127 and 128-255, by pair parity) and two
+// 128-column O^T buffers (256-383 and 384-511) through which the four 128-dim
+// blocks of a pair's O^T pass, drained by the epilogue as they complete; no
+// block accumulates across tiles (the pair has one tile).  With two S^T
+// buffers the QK^T of the next pair runs while the softmax reads this one.
 //
-// Shared memory: a ring of 10 slots of 16 KB through which every box of a
-// pair streams in a fixed order (Q box b, K box b for b = 0..7, then V boxes
-// 0..7; a PV block takes two adjacent V slots), P^T of the pair (32 KB), the
-// extra row's K and V (two 2 KB buffers, by pair parity) and bookkeeping.
+// Shared memory: a ring of 10 slots of 16 KB through which every box streams
+// in the order the MMAs take them: the Q and K boxes of pair 0, then for each
+// pair n the Q and K boxes of pair n+1 (Q box b, K box b for b = 0..7) before
+// the V boxes of pair n (0..7; a PV block takes two adjacent V slots), so the
+// next pair's loads are not queued behind V boxes that wait for this pair's
+// softmax.  Also P^T of a pair (32 KB), the extra row's K and V (two 2 KB
+// buffers, by pair parity) and bookkeeping.
 // Warp roles (352 threads):
 //   warps 0-7  softmax + epilogue; thread (TMEM lane quarter w % 4, token w / 4)
 //              handles one row (or dim) and that token's 64 heads in two halves
@@ -37,6 +41,9 @@
 // that Q box b landed from the MMA thread (qx[b]), which waits on every slot
 // in order: a parity wait must not fall more than one phase behind, and a
 // ring position passes through K and V uses the extra-row warp never sees.
+// For the same reason the MMA thread passes on Q box b of a pair only after
+// the extra-row warp has finished box b of the previous pair (xdone[b]), and
+// the extra-row scores are handed over through one barrier per pair parity.
 // Every wait is bounded as in attn_fwd_kernel.
 #include <cuda_fp16.h>
 
@@ -69,9 +76,10 @@ struct PairMisc {
   alignas(16) float sx[2][64];    // extra row, by pair parity: scaled score of token a per head (log2 units)
   alignas(16) float px[64];       // extra row: its weight
   alignas(8) uint64_t full[kPSlots], empty[kPSlots];
-  uint64_t s_full, s_empty, p_full, p_empty, o_full[4], mma_done;
-  uint64_t x_full, x_empty[2];    // extra-row scores of a pair ready; a parity's row buffer free again
+  uint64_t s_full[2], s_empty[2], p_full, p_empty, o_full[2], o_empty[2], mma_done;
+  uint64_t x_full[2], x_empty[2]; // by pair parity: extra-row scores ready; the row buffer free again
   uint64_t qx[8];                 // Q box b of the current pair has landed (passed on by the MMA thread)
+  uint64_t xdone[8];              // the extra-row warp is done with Q box b of its current pair
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -125,10 +133,38 @@ __device__ __forceinline__ uint32_t slot_addr(uint32_t sbase, uint32_t sl) {
   return sbase + kPOffRing + (sl % kPSlots) * kPSlot;
 }
 __device__ __forceinline__ uint32_t slot_phase(uint32_t sl) { return (sl / kPSlots) & 1u; }
-// TMEM column of O^T block m: blocks 0-2 after S^T, block 3 in S^T's columns.
-__device__ __forceinline__ uint32_t o_column(int m) { return m == 3 ? 0u : 128u + 128u * m; }
+// TMEM columns: S^T of pair parity i at 128 i; O^T block m in buffer m & 1 at 256 + 128 (m & 1).
+__device__ __forceinline__ uint32_t s_column(uint32_t n) { return 128u * (n & 1u); }
+__device__ __forceinline__ uint32_t o_column(int m) { return 256u + 128u * (m & 1); }
+
+// Ring slot of Q box 0 of the CTA's pair n: pair 0's Q and K boxes come
+// first, then each pair step adds the next pair's 16 boxes and this pair's 8
+// V boxes.
+__device__ __forceinline__ uint32_t qk_base(uint32_t n) { return n == 0 ? 0u : 16u + 24u * (n - 1u); }
 
 // ------------------------------------------------------------------ loader
+
+__device__ __forceinline__ bool pair_fill(const PairParams &p, uint32_t sbase, PairMisc &ms, volatile int *abrt,
+                                          const PairGeom &g, int i, uint32_t &sl, uint32_t &filled,
+                                          uint32_t &last_par) {
+  const uint32_t pos = sl % kPSlots, ph = slot_phase(sl);
+  if (!mbar_wait(smem_u32(&ms.empty[pos]), ph ^ 1, abrt, p.timeout_ns, p.err, SITE_PR_EMPTY)) return false;
+  const uint32_t dst = slot_addr(sbase, sl), bar = smem_u32(&ms.full[pos]);
+  mbar_arrive_expect_tx(bar, kPSlot);
+  if (i < 16) {
+    const int b = i >> 1;
+    if ((i & 1) == 0)
+      tma_load_3d(dst, &p.tm_q2, bar, 64 * b, 0, g.ta);  // both tokens' heads, dims 64b ..
+    else
+      tma_load_2d(dst, &p.tm_k, bar, 64 * b, g.tile_lo);
+  } else {
+    tma_load_2d(dst, &p.tm_v, bar, 64 * (i - 16), g.tile_lo);
+  }
+  filled |= 1u << pos;
+  last_par = (last_par & ~(1u << pos)) | (ph << pos);
+  ++sl;
+  return true;
+}
 
 __device__ __forceinline__ void pair_loader(const PairParams &p, uint32_t sbase, PairMisc &ms) {
   volatile int *abrt = &ms.abort_flag;
@@ -136,27 +172,19 @@ __device__ __forceinline__ void pair_loader(const PairParams &p, uint32_t sbase,
   uint32_t sl = 0, filled = 0, last_par = 0;
   bool ok = true;
   grid_dependency_wait();  // Q, K and V may come from the previous kernel
+  if ((int)blockIdx.x < n_pairs) {
+    const PairGeom g0 = pair_geom(p, blockIdx.x);
+    for (int i = 0; i < 16 && ok; ++i) ok = pair_fill(p, sbase, ms, abrt, g0, i, sl, filled, last_par);
+  }
   for (int pr = blockIdx.x; pr < n_pairs && ok; pr += gridDim.x) {
+    if (pr + (int)gridDim.x < n_pairs) {  // the next pair's Q and K, then this pair's V
+      const PairGeom gn = pair_geom(p, pr + gridDim.x);
+#pragma unroll 1
+      for (int i = 0; i < 16 && ok; ++i) ok = pair_fill(p, sbase, ms, abrt, gn, i, sl, filled, last_par);
+    }
     const PairGeom g = pair_geom(p, pr);
 #pragma unroll 1
-    for (int i = 0; i < kPSlotsPerPair && ok; ++i, ++sl) {
-      const uint32_t pos = sl % kPSlots, ph = slot_phase(sl);
-      ok = mbar_wait(smem_u32(&ms.empty[pos]), ph ^ 1, abrt, p.timeout_ns, p.err, SITE_PR_EMPTY);
-      if (!ok) break;
-      const uint32_t dst = slot_addr(sbase, sl), bar = smem_u32(&ms.full[pos]);
-      mbar_arrive_expect_tx(bar, kPSlot);
-      if (i < 16) {
-        const int b = i >> 1;
-        if ((i & 1) == 0)
-          tma_load_3d(dst, &p.tm_q2, bar, 64 * b, 0, g.ta);  // both tokens' heads, dims 64b ..
-        else
-          tma_load_2d(dst, &p.tm_k, bar, 64 * b, g.tile_lo);
-      } else {
-        tma_load_2d(dst, &p.tm_v, bar, 64 * (i - 16), g.tile_lo);
-      }
-      filled |= 1u << pos;
-      last_par = (last_par & ~(1u << pos)) | (ph << pos);
-    }
+    for (int i = 16; i < kPSlotsPerPair && ok; ++i) ok = pair_fill(p, sbase, ms, abrt, g, i, sl, filled, last_par);
   }
   if (!ok) {
     // Let every copy already issued land before the shared memory goes away.
@@ -169,76 +197,94 @@ __device__ __forceinline__ void pair_loader(const PairParams &p, uint32_t sbase,
 
 // ------------------------------------------------------------------ MMA issuer
 
-__device__ __forceinline__ void pair_mma(const PairParams &p, uint32_t sbase, uint32_t tmem, PairMisc &ms) {
-  volatile int *abrt = &ms.abort_flag;
+// QK^T of the CTA's pair j into S^T buffer j & 1, from the pair's 16 Q and K
+// slots starting at `sl`.
+__device__ __forceinline__ bool pair_qk(const PairParams &p, uint32_t sbase, uint32_t tmem, PairMisc &ms,
+                                        volatile int *abrt, uint32_t j, uint32_t &sl) {
   constexpr uint32_t kIdescQK = idesc_f16_f32(128, 128, false, false);
-  constexpr uint32_t kIdescPV = idesc_f16_f32(128, 128, true, true);
-  // K and Q boxes: K-major, SBO = one 8-row group.  V^T: MN-major, its two
-  // 64-dim atoms in adjacent slots (LBO = one slot).  P^T: MN-major, token a's
-  // heads then token b's (LBO = one box).
+  // K and Q boxes: K-major, SBO = one 8-row group.
   const uint64_t kq_desc = sdesc_sw128(sbase + kPOffRing, 16, 1024);
+  if (!mbar_wait(smem_u32(&ms.s_empty[j & 1]), ((j >> 1) & 1) ^ 1, abrt, p.timeout_ns, p.err, SITE_PR_S_EMPTY))
+    return false;
+  tc_fence_after();
+  const uint32_t d = tmem + s_column(j);
+  for (int b = 0; b < 8; ++b, sl += 2) {
+    const uint32_t pq = sl % kPSlots, pk = (sl + 1) % kPSlots;
+    if (!mbar_wait(smem_u32(&ms.full[pq]), slot_phase(sl), abrt, p.timeout_ns, p.err, SITE_PR_FULL) ||
+        !mbar_wait(smem_u32(&ms.full[pk]), slot_phase(sl + 1), abrt, p.timeout_ns, p.err, SITE_PR_FULL))
+      return false;
+    tc_fence_after();
+    const uint64_t a0 = sdesc_add(kq_desc, pk * kPSlot), b0 = sdesc_add(kq_desc, pq * kPSlot);
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+      if (b == 0 && ks == 0)
+        umma_f16(d, sdesc_add(a0, ks * 32), sdesc_add(b0, ks * 32), kIdescQK, 0u);
+      else
+        umma_f16_acc(d, sdesc_add(a0, ks * 32), sdesc_add(b0, ks * 32), kIdescQK);
+    }
+    // The extra-row warp may read Q box b once it is done with box b of the
+    // previous pair (so qx[b] never runs two phases ahead of it).
+    if (j > 0 && !mbar_wait(smem_u32(&ms.xdone[b]), (j - 1) & 1, abrt, p.timeout_ns, p.err, SITE_PR_X_EMPTY))
+      return false;
+    mbar_arrive(smem_u32(&ms.qx[b]));
+    umma_commit(smem_u32(&ms.empty[pq]));  // the extra-row warp gives the Q slot's second arrival
+    umma_commit(smem_u32(&ms.empty[pk]));
+    mbar_arrive(smem_u32(&ms.empty[pk]));
+  }
+  umma_commit(smem_u32(&ms.s_full[j & 1]));
+  return true;
+}
+
+// PV of the CTA's pair n once P^T is written: O^T block m into buffer m & 1
+// (after the epilogue drained block m - 2), from the V slots starting at `sl`.
+__device__ __forceinline__ bool pair_pv(const PairParams &p, uint32_t sbase, uint32_t tmem, PairMisc &ms,
+                                        volatile int *abrt, uint32_t n, uint32_t &sl) {
+  constexpr uint32_t kIdescPV = idesc_f16_f32(128, 128, true, true);
+  // V^T: MN-major, its two 64-dim atoms in adjacent slots (LBO = one slot).
+  // P^T: MN-major, token a's heads then token b's (LBO = one box).
   const uint64_t v_desc = sdesc_sw128(sbase + kPOffRing, kPSlot, 1024);
   const uint64_t p_desc = sdesc_sw128(sbase + kPOffP, kPSlot, 1024);
+  if (!mbar_wait(smem_u32(&ms.p_full), n & 1, abrt, p.timeout_ns, p.err, SITE_PR_P_FULL)) return false;
+  tc_fence_after();
+  for (int m = 0; m < 4; ++m, sl += 2) {
+    const uint32_t gb = 4 * n + m, buf = gb & 1;
+    const uint32_t pa = sl % kPSlots, pb = (sl + 1) % kPSlots;  // pa even: pb = pa + 1
+    if (!mbar_wait(smem_u32(&ms.o_empty[buf]), ((gb >> 1) & 1) ^ 1, abrt, p.timeout_ns, p.err, SITE_PR_O_EMPTY) ||
+        !mbar_wait(smem_u32(&ms.full[pa]), slot_phase(sl), abrt, p.timeout_ns, p.err, SITE_PR_FULL) ||
+        !mbar_wait(smem_u32(&ms.full[pb]), slot_phase(sl + 1), abrt, p.timeout_ns, p.err, SITE_PR_FULL))
+      return false;
+    tc_fence_after();
+    const uint64_t a0 = sdesc_add(v_desc, pa * kPSlot);
+    const uint32_t d = tmem + o_column(m);
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      if (ks == 0)
+        umma_f16(d, a0, p_desc, kIdescPV, 0u);
+      else
+        umma_f16_acc(d, sdesc_add(a0, ks * 2048), sdesc_add(p_desc, ks * 2048), kIdescPV);
+    }
+    umma_commit(smem_u32(&ms.empty[pa]));
+    umma_commit(smem_u32(&ms.empty[pb]));
+    mbar_arrive(smem_u32(&ms.empty[pa]));
+    mbar_arrive(smem_u32(&ms.empty[pb]));
+    umma_commit(smem_u32(&ms.o_full[buf]));
+  }
+  umma_commit(smem_u32(&ms.p_empty));
+  return true;
+}
+
+// The MMA thread takes the slots in the loader's order: QK^T of pair 0, then
+// for each pair n the QK^T of pair n+1 (while the softmax works on pair n)
+// and the PV of pair n.
+__device__ __forceinline__ void pair_mma(const PairParams &p, uint32_t sbase, uint32_t tmem, PairMisc &ms) {
+  volatile int *abrt = &ms.abort_flag;
   const int n_pairs = (p.T + 1) / 2;
   uint32_t sl = 0, n = 0;
   bool ok = true;
+  if ((int)blockIdx.x < n_pairs) ok = pair_qk(p, sbase, tmem, ms, abrt, 0, sl);
   for (int pr = blockIdx.x; pr < n_pairs && ok; pr += gridDim.x, ++n) {
-    ok = mbar_wait(smem_u32(&ms.s_empty), (n & 1) ^ 1, abrt, p.timeout_ns, p.err, SITE_PR_S_EMPTY);
-    if (!ok) break;
-    tc_fence_after();
-    for (int b = 0; b < 8 && ok; ++b, sl += 2) {
-      const uint32_t pq = sl % kPSlots, pk = (sl + 1) % kPSlots;
-      ok = mbar_wait(smem_u32(&ms.full[pq]), slot_phase(sl), abrt, p.timeout_ns, p.err, SITE_PR_FULL) &&
-           mbar_wait(smem_u32(&ms.full[pk]), slot_phase(sl + 1), abrt, p.timeout_ns, p.err, SITE_PR_FULL);
-      if (!ok) break;
-      tc_fence_after();
-      const uint64_t a0 = sdesc_add(kq_desc, pk * kPSlot), b0 = sdesc_add(kq_desc, pq * kPSlot);
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {
-        if (b == 0 && ks == 0)
-          umma_f16(tmem, sdesc_add(a0, ks * 32), sdesc_add(b0, ks * 32), kIdescQK, 0u);
-        else
-          umma_f16_acc(tmem, sdesc_add(a0, ks * 32), sdesc_add(b0, ks * 32), kIdescQK);
-      }
-      mbar_arrive(smem_u32(&ms.qx[b]));      // the extra-row warp may read Q box b
-      umma_commit(smem_u32(&ms.empty[pq]));  // the extra-row warp gives the Q slot's second arrival
-      umma_commit(smem_u32(&ms.empty[pk]));
-      mbar_arrive(smem_u32(&ms.empty[pk]));
-    }
-    if (!ok) break;
-    umma_commit(smem_u32(&ms.s_full));
-    // P^T written means S^T has been read and every O^T block of the previous
-    // pair drained: all four blocks go out at once, block 3 (the last V boxes)
-    // first into S^T's columns, which the epilogue drains first.
-    ok = mbar_wait(smem_u32(&ms.p_full), n & 1, abrt, p.timeout_ns, p.err, SITE_PR_P_FULL);
-    if (!ok) break;
-    tc_fence_after();
-    for (int k = 0; k < 4 && ok; ++k) {
-      const int m = (k + 3) & 3;
-      const uint32_t sv = sl + 2 * m;
-      const uint32_t pa = sv % kPSlots, pb = (sv + 1) % kPSlots;  // pa even: pb = pa + 1
-      ok = mbar_wait(smem_u32(&ms.full[pa]), slot_phase(sv), abrt, p.timeout_ns, p.err, SITE_PR_FULL) &&
-           mbar_wait(smem_u32(&ms.full[pb]), slot_phase(sv + 1), abrt, p.timeout_ns, p.err, SITE_PR_FULL);
-      if (!ok) break;
-      tc_fence_after();
-      const uint64_t a0 = sdesc_add(v_desc, pa * kPSlot);
-      const uint32_t d = tmem + o_column(m);
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        if (ks == 0)
-          umma_f16(d, a0, p_desc, kIdescPV, 0u);
-        else
-          umma_f16_acc(d, sdesc_add(a0, ks * 2048), sdesc_add(p_desc, ks * 2048), kIdescPV);
-      }
-      umma_commit(smem_u32(&ms.empty[pa]));
-      umma_commit(smem_u32(&ms.empty[pb]));
-      mbar_arrive(smem_u32(&ms.empty[pa]));
-      mbar_arrive(smem_u32(&ms.empty[pb]));
-      umma_commit(smem_u32(&ms.o_full[m]));
-    }
-    if (!ok) break;
-    sl += 8;
-    umma_commit(smem_u32(&ms.p_empty));
+    if (pr + (int)gridDim.x < n_pairs) ok = pair_qk(p, sbase, tmem, ms, abrt, n + 1, sl);
+    ok = ok && pair_pv(p, sbase, tmem, ms, abrt, n, sl);
   }
   // Every MMA issued so far must finish before TMEM is released.
   umma_commit(smem_u32(&ms.mma_done));
@@ -299,17 +345,17 @@ __device__ __forceinline__ void pair_compute(const PairParams &p, uint8_t *smem,
     const __half *vx = reinterpret_cast<const __half *>(smem + kPOffX + 2048 * (n & 1)) + 512;
     // The extra-row warp's scores of this pair (every pair, so the phases
     // stay in step).
-    bad = bad || !mbar_wait(smem_u32(&ms.x_full), n & 1, abrt, p.timeout_ns, p.err, SITE_PR_X_FULL);
+    bad = bad || !mbar_wait(smem_u32(&ms.x_full[n & 1]), (n >> 1) & 1, abrt, p.timeout_ns, p.err, SITE_PR_X_FULL);
 
     // Softmax of the pair's tile.  Pass 1: column maxima.
-    bad = bad || !mbar_wait(smem_u32(&ms.s_full), n & 1, abrt, p.timeout_ns, p.err, SITE_PR_S_FULL);
+    bad = bad || !mbar_wait(smem_u32(&ms.s_full[n & 1]), (n >> 1) & 1, abrt, p.timeout_ns, p.err, SITE_PR_S_FULL);
     tc_fence_after();
     const int row = g.tile_lo + r;
     const bool vis = has_tok && row >= g.lo[tau] && row < g.hi[tau];
 #pragma unroll 1
     for (int u = 0; u < 2; ++u) {
       float s[32];
-      tmem_ld32(tmem + 64 * tau + 32 * u + lane_base, s);
+      tmem_ld32(tmem + s_column(n) + 64 * tau + 32 * u + lane_base, s);
       tmem_wait_ld();
 #pragma unroll
       for (int h = 0; h < 32; ++h) s[h] = vis ? s[h] * p.scale_log2 : -INFINITY;
@@ -332,7 +378,7 @@ __device__ __forceinline__ void pair_compute(const PairParams &p, uint8_t *smem,
 #pragma unroll 1
     for (int u = 0; u < 2; ++u) {
       float s[32];
-      tmem_ld32(tmem + 64 * tau + 32 * u + lane_base, s);
+      tmem_ld32(tmem + s_column(n) + 64 * tau + 32 * u + lane_base, s);
       tmem_wait_ld();
       const float *mu = ms.m_use + 64 * tau + 32 * u;
 #pragma unroll
@@ -354,7 +400,8 @@ __device__ __forceinline__ void pair_compute(const PairParams &p, uint8_t *smem,
       }
       ms.red[q][64 * tau + 32 * u + l] = reduce_scatter32<false>(s, l);
     }
-    tc_fence_before();  // S^T read for the last time
+    tc_fence_before();
+    mbar_arrive(smem_u32(&ms.s_empty[n & 1]));  // S^T read for the last time
     fence_proxy_async_smem();
     mbar_arrive(smem_u32(&ms.p_full));
     if (bar_red_or(1, kPThreadsC, bad)) break;
@@ -372,18 +419,17 @@ __device__ __forceinline__ void pair_compute(const PairParams &p, uint8_t *smem,
     }
     csync();
 
-    // Epilogue: O^T block m [128 dims][128] -> o of both tokens, block 3
-    // first (it frees S^T's columns for the next pair).  Lanes 2k and 2k+1
-    // hold adjacent dims: for each pair of heads they swap one value, so the
-    // even lane writes both dims of the first head and the odd lane both dims
-    // of the second (32-bit stores).
+    // Epilogue: O^T block m [128 dims][128] -> o of both tokens, as each
+    // block completes.  Lanes 2k and 2k+1 hold adjacent dims: for each pair
+    // of heads they swap one value, so the even lane writes both dims of the
+    // first head and the odd lane both dims of the second (32-bit stores).
     const bool odd = l & 1;
     const bool with_x = tau == 0 && g.extra;  // token a folds in its extra row
     __half *obase = p.o + (long long)(g.ta + tau) * p.o_tok_stride + (r & ~1);
 #pragma unroll 1
-    for (int k = 0; k < 4; ++k) {
-      const int m = (k + 3) & 3;
-      bad = bad || !mbar_wait(smem_u32(&ms.o_full[m]), n & 1, abrt, p.timeout_ns, p.err, SITE_PR_O_FULL);
+    for (int m = 0; m < 4; ++m) {
+      const uint32_t gb = 4 * n + m;
+      bad = bad || !mbar_wait(smem_u32(&ms.o_full[m & 1]), (gb >> 1) & 1, abrt, p.timeout_ns, p.err, SITE_PR_O_FULL);
       tc_fence_after();
       const float xv = with_x ? __half2float(vx[128 * m + r]) : 0.f;
 #pragma unroll 1
@@ -391,9 +437,9 @@ __device__ __forceinline__ void pair_compute(const PairParams &p, uint8_t *smem,
         float o[32];
         tmem_ld32(tmem + o_column(m) + 64 * tau + 32 * u + lane_base, o);
         tmem_wait_ld();
-        if (k == 0 && u == 1) {
+        if (u == 1) {
           tc_fence_before();
-          mbar_arrive(smem_u32(&ms.s_empty));  // S^T's columns may take the next pair's scores
+          mbar_arrive(smem_u32(&ms.o_empty[m & 1]));  // the buffer may take block m + 2
         }
         if (has_tok) {
           const float4 *iv4 = reinterpret_cast<const float4 *>(ms.inv_l + 64 * tau + 32 * u);
@@ -439,7 +485,7 @@ __device__ __forceinline__ void pair_compute(const PairParams &p, uint8_t *smem,
 __device__ __forceinline__ void pair_extra_row(const PairParams &p, uint8_t *smem, PairMisc &ms, int lane) {
   volatile int *abrt = &ms.abort_flag;
   const int n_pairs = (p.T + 1) / 2;
-  uint32_t sl = 0, n = 0;
+  uint32_t n = 0;
   bool ok = true;
   grid_dependency_wait();  // the extra rows are read from global memory
   for (int pr = blockIdx.x; pr < n_pairs && ok; pr += gridDim.x, ++n) {
@@ -459,6 +505,7 @@ __device__ __forceinline__ void pair_extra_row(const PairParams &p, uint8_t *sme
     }
     const __half *kx = reinterpret_cast<const __half *>(xb);
     float acc0 = 0.f, acc1 = 0.f;
+    uint32_t sl = qk_base(n);
     for (int b = 0; b < 8; ++b, sl += 2) {
       const uint32_t pq = sl % kPSlots;
       ok = mbar_wait(smem_u32(&ms.qx[b]), n & 1, abrt, p.timeout_ns, p.err, SITE_PR_FULL);
@@ -487,14 +534,16 @@ __device__ __forceinline__ void pair_extra_row(const PairParams &p, uint8_t *sme
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&ms.empty[pq]));
+      if (lane == 0) {
+        mbar_arrive(smem_u32(&ms.empty[pq]));
+        mbar_arrive(smem_u32(&ms.xdone[b]));
+      }
     }
     if (!ok) break;
-    sl += 8;  // the V slots
     ms.sx[n & 1][2 * lane] = acc0 * p.scale_log2;
     ms.sx[n & 1][2 * lane + 1] = acc1 * p.scale_log2;
     __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&ms.x_full));
+    if (lane == 0) mbar_arrive(smem_u32(&ms.x_full[n & 1]));
   }
 }
 
@@ -509,16 +558,21 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_pair_kernel(const __grid_co
       mbar_init(smem_u32(&ms.full[s]), 1);
       mbar_init(smem_u32(&ms.empty[s]), 2);
     }
-    mbar_init(smem_u32(&ms.s_full), 1);
-    mbar_init(smem_u32(&ms.s_empty), kPThreadsC);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&ms.s_full[b]), 1);
+      mbar_init(smem_u32(&ms.s_empty[b]), kPThreadsC);
+      mbar_init(smem_u32(&ms.o_full[b]), 1);
+      mbar_init(smem_u32(&ms.o_empty[b]), kPThreadsC);
+      mbar_init(smem_u32(&ms.x_full[b]), 1);
+      mbar_init(smem_u32(&ms.x_empty[b]), 1);
+    }
     mbar_init(smem_u32(&ms.p_full), kPThreadsC);
     mbar_init(smem_u32(&ms.p_empty), 1);
-    for (int b = 0; b < 4; ++b) mbar_init(smem_u32(&ms.o_full[b]), 1);
     mbar_init(smem_u32(&ms.mma_done), 1);
-    mbar_init(smem_u32(&ms.x_full), 1);
-    mbar_init(smem_u32(&ms.x_empty[0]), 1);
-    mbar_init(smem_u32(&ms.x_empty[1]), 1);
-    for (int b = 0; b < 8; ++b) mbar_init(smem_u32(&ms.qx[b]), 1);
+    for (int b = 0; b < 8; ++b) {
+      mbar_init(smem_u32(&ms.qx[b]), 1);
+      mbar_init(smem_u32(&ms.xdone[b]), 1);
+    }
     ms.abort_flag = 0;
     for (int i = 0; i < 64; ++i) ms.px[i] = 0.f;
     fence_barrier_init();
