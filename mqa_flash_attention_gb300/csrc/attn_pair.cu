@@ -33,8 +33,9 @@
 //              handles one row (or dim) and that token's 64 heads in two halves
 //   warp  8    loader (one thread issues every TMA copy)
 //   warp  9    TMEM allocator and tcgen05.mma issuer
-//   warp 10    extra row: loads its K and V rows and takes token a's scores
-//              against it from the Q boxes as they pass through the ring
+//   warp 10    extra row: reads its K and V rows (one pair ahead) and takes
+//              token a's scores against it from the Q boxes as they pass
+//              through the ring
 // A Q slot is released by the MMA's commit and by the extra-row warp (it reads
 // it), a K or V slot by the commit and a plain arrival of the MMA thread:
 // every slot's "free" barrier counts two arrivals.  The extra-row warp learns
@@ -478,29 +479,39 @@ __device__ __forceinline__ void pair_compute(const PairParams &p, uint8_t *smem,
 }
 
 // Warp 10: for each pair, token a's row below the tile (when there is one):
-// its K and V rows into this parity's buffer (once the softmax warps are done
-// with the pair two back), then token a's scores against it, taken from the Q
-// boxes as they pass through the ring (lane l: heads 2l and 2l+1), and the
-// second release of every Q slot.
+// its K and V rows, read from global memory one pair ahead into registers;
+// token a's scores against the K row, taken from the Q boxes as they pass
+// through the ring (lane l: heads 2l and 2l+1), with the second release of
+// every Q slot; then the V row into this parity's buffer once the softmax
+// warps are done with the pair two back.  Only the V row waits for them, so
+// the Q slots go back to the ring as soon as the MMA has read them.
+__device__ __forceinline__ void load_extra_row(const PairParams &p, const PairGeom &g, int lane, uint4 (&kr)[2],
+                                               uint4 (&vr)[2]) {
+  if (!g.extra) return;
+  const long long off = (long long)(g.tile_lo - 1) * p.raw_row_stride;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int c = lane + 32 * i;  // 16-byte chunk of the 1024-byte row
+    kr[i] = *reinterpret_cast<const uint4 *>(p.k_raw + off + 16 * c);
+    vr[i] = *reinterpret_cast<const uint4 *>(p.v_raw + off + 16 * c);
+  }
+}
+
 __device__ __forceinline__ void pair_extra_row(const PairParams &p, uint8_t *smem, PairMisc &ms, int lane) {
   volatile int *abrt = &ms.abort_flag;
   const int n_pairs = (p.T + 1) / 2;
   uint32_t n = 0;
   bool ok = true;
   grid_dependency_wait();  // the extra rows are read from global memory
+  uint4 kr[2], vr[2];
+  if ((int)blockIdx.x < n_pairs) load_extra_row(p, pair_geom(p, blockIdx.x), lane, kr, vr);
   for (int pr = blockIdx.x; pr < n_pairs && ok; pr += gridDim.x, ++n) {
     const PairGeom g = pair_geom(p, pr);
     uint8_t *xb = smem + kPOffX + 2048 * (n & 1);
     if (g.extra) {
-      ok = mbar_wait(smem_u32(&ms.x_empty[n & 1]), ((n >> 1) & 1) ^ 1, abrt, p.timeout_ns, p.err, SITE_PR_X_EMPTY);
-      if (!ok) break;
-      const long long off = (long long)(g.tile_lo - 1) * p.raw_row_stride;
+      // The K half of this parity's buffer is read only by this warp.
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const int c = lane + 32 * i;  // 16-byte chunk of the 1024-byte row
-        *reinterpret_cast<uint4 *>(xb + 16 * c) = *reinterpret_cast<const uint4 *>(p.k_raw + off + 16 * c);
-        *reinterpret_cast<uint4 *>(xb + 1024 + 16 * c) = *reinterpret_cast<const uint4 *>(p.v_raw + off + 16 * c);
-      }
+      for (int i = 0; i < 2; ++i) *reinterpret_cast<uint4 *>(xb + 16 * (lane + 32 * i)) = kr[i];
       __syncwarp();
     }
     const __half *kx = reinterpret_cast<const __half *>(xb);
@@ -540,6 +551,14 @@ __device__ __forceinline__ void pair_extra_row(const PairParams &p, uint8_t *sme
       }
     }
     if (!ok) break;
+    if (g.extra) {
+      ok = mbar_wait(smem_u32(&ms.x_empty[n & 1]), ((n >> 1) & 1) ^ 1, abrt, p.timeout_ns, p.err, SITE_PR_X_EMPTY);
+      if (!ok) break;
+#pragma unroll
+      for (int i = 0; i < 2; ++i) *reinterpret_cast<uint4 *>(xb + 1024 + 16 * (lane + 32 * i)) = vr[i];
+    }
+    // The next pair's rows travel while this pair finishes.
+    if (pr + (int)gridDim.x < n_pairs) load_extra_row(p, pair_geom(p, pr + gridDim.x), lane, kr, vr);
     ms.sx[n & 1][2 * lane] = acc0 * p.scale_log2;
     ms.sx[n & 1][2 * lane + 1] = acc1 * p.scale_log2;
     __syncwarp();
