@@ -433,41 +433,42 @@ __device__ __forceinline__ void pair_compute(const PairParams &p, uint8_t *smem,
       bad = bad || !mbar_wait(smem_u32(&ms.o_full[m & 1]), (gb >> 1) & 1, abrt, p.timeout_ns, p.err, SITE_PR_O_FULL);
       tc_fence_after();
       const float xv = with_x ? __half2float(vx[128 * m + r]) : 0.f;
-#pragma unroll 1
-      for (int u = 0; u < 2; ++u) {
-        float o[32];
-        tmem_ld32(tmem + o_column(m) + 64 * tau + 32 * u + lane_base, o);
-        tmem_wait_ld();
-        if (u == 1) {
-          tc_fence_before();
-          mbar_arrive(smem_u32(&ms.o_empty[m & 1]));  // the buffer may take block m + 2
-        }
-        if (has_tok) {
+      // Both halves of the block leave TMEM before the buffer is handed back,
+      // so the next PV into it need not wait for the stores.
+      float o[2][32];
+      tmem_ld32(tmem + o_column(m) + 64 * tau + lane_base, o[0]);
+      tmem_ld32(tmem + o_column(m) + 64 * tau + 32 + lane_base, o[1]);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&ms.o_empty[m & 1]));  // the buffer may take block m + 2
+      if (has_tok) {
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
           const float4 *iv4 = reinterpret_cast<const float4 *>(ms.inv_l + 64 * tau + 32 * u);
           if (with_x) {
             const float4 *px4 = reinterpret_cast<const float4 *>(ms.px + 32 * u);
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
               const float4 iv = iv4[j], px = px4[j];
-              o[4 * j] = fmaf(px.x, xv, o[4 * j]) * iv.x;
-              o[4 * j + 1] = fmaf(px.y, xv, o[4 * j + 1]) * iv.y;
-              o[4 * j + 2] = fmaf(px.z, xv, o[4 * j + 2]) * iv.z;
-              o[4 * j + 3] = fmaf(px.w, xv, o[4 * j + 3]) * iv.w;
+              o[u][4 * j] = fmaf(px.x, xv, o[u][4 * j]) * iv.x;
+              o[u][4 * j + 1] = fmaf(px.y, xv, o[u][4 * j + 1]) * iv.y;
+              o[u][4 * j + 2] = fmaf(px.z, xv, o[u][4 * j + 2]) * iv.z;
+              o[u][4 * j + 3] = fmaf(px.w, xv, o[u][4 * j + 3]) * iv.w;
             }
           } else {
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
               const float4 iv = iv4[j];
-              o[4 * j] *= iv.x;
-              o[4 * j + 1] *= iv.y;
-              o[4 * j + 2] *= iv.z;
-              o[4 * j + 3] *= iv.w;
+              o[u][4 * j] *= iv.x;
+              o[u][4 * j + 1] *= iv.y;
+              o[u][4 * j + 2] *= iv.z;
+              o[u][4 * j + 3] *= iv.w;
             }
           }
 #pragma unroll
           for (int h = 0; h < 32; h += 2) {
-            const float got = __shfl_xor_sync(0xffffffffu, odd ? o[h] : o[h + 1], 1);
-            const __half2 v = odd ? __floats2half2_rn(got, o[h + 1]) : __floats2half2_rn(o[h], got);
+            const float got = __shfl_xor_sync(0xffffffffu, odd ? o[u][h] : o[u][h + 1], 1);
+            const __half2 v = odd ? __floats2half2_rn(got, o[u][h + 1]) : __floats2half2_rn(o[u][h], got);
             *reinterpret_cast<__half2 *>(obase + (32 * u + h + (odd ? 1 : 0)) * kD + 128 * m) = v;
           }
         }
@@ -481,10 +482,12 @@ __device__ __forceinline__ void pair_compute(const PairParams &p, uint8_t *smem,
 // Warp 10: for each pair, token a's row below the tile (when there is one):
 // its K and V rows, read from global memory one pair ahead into registers;
 // token a's scores against the K row, taken from the Q boxes as they pass
-// through the ring (lane l: heads 2l and 2l+1), with the second release of
+// through the ring (lane l: heads l and l + 32), with the second release of
 // every Q slot; then the V row into this parity's buffer once the softmax
 // warps are done with the pair two back.  Only the V row waits for them, so
-// the Q slots go back to the ring as soon as the MMA has read them.
+// the Q slots go back to the ring as soon as the MMA has read them.  Lane l
+// takes heads l and l + 32: the eight lanes of a group then read eight
+// different 16-byte columns of the swizzled box, all 32 banks.
 __device__ __forceinline__ void load_extra_row(const PairParams &p, const PairGeom &g, int lane, uint4 (&kr)[2],
                                                uint4 (&vr)[2]) {
   if (!g.extra) return;
@@ -530,7 +533,7 @@ __device__ __forceinline__ void pair_extra_row(const PairParams &p, uint8_t *sme
           const __half2 *k2 = reinterpret_cast<const __half2 *>(&kv);
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
-            const int h = 2 * lane + j;
+            const int h = lane + 32 * j;
             const uint4 qv = *reinterpret_cast<const uint4 *>(smem + kPOffRing + pq * kPSlot + h * 128 +
                                                               ((c ^ (h & 7)) << 4));
             const __half2 *q2 = reinterpret_cast<const __half2 *>(&qv);
@@ -559,8 +562,8 @@ __device__ __forceinline__ void pair_extra_row(const PairParams &p, uint8_t *sme
     }
     // The next pair's rows travel while this pair finishes.
     if (pr + (int)gridDim.x < n_pairs) load_extra_row(p, pair_geom(p, pr + gridDim.x), lane, kr, vr);
-    ms.sx[n & 1][2 * lane] = acc0 * p.scale_log2;
-    ms.sx[n & 1][2 * lane + 1] = acc1 * p.scale_log2;
+    ms.sx[n & 1][lane] = acc0 * p.scale_log2;
+    ms.sx[n & 1][lane + 32] = acc1 * p.scale_log2;
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&ms.x_full[n & 1]));
   }
