@@ -5,10 +5,13 @@
 namespace ds4a {
 
 cudaError_t prepare_attn_kernel() {
-  cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)kSmemBytes);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(attn_fwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  const void *k[4] = {(const void *)attn_fwd_kernel<false, false>, (const void *)attn_fwd_kernel<false, true>,
+                      (const void *)attn_fwd_kernel<true, false>, (const void *)attn_fwd_kernel<true, true>};
+  for (const void *f : k) {
+    const cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 // Launched with programmatic stream serialization: the kernel's prologue may
@@ -25,7 +28,12 @@ cudaError_t launch_attn(const AttnParams &p, int grid, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return p.comp_fp8 ? cudaLaunchKernelEx(&cfg, attn_fwd_kernel<true>, p) : cudaLaunchKernelEx(&cfg, attn_fwd_kernel<false>, p);
+  const bool la = look_ahead_suits(p);
+  if (p.comp_fp8)
+    return la ? cudaLaunchKernelEx(&cfg, attn_fwd_kernel<true, true>, p)
+              : cudaLaunchKernelEx(&cfg, attn_fwd_kernel<true, false>, p);
+  return la ? cudaLaunchKernelEx(&cfg, attn_fwd_kernel<false, true>, p)
+            : cudaLaunchKernelEx(&cfg, attn_fwd_kernel<false, false>, p);
 }
 
 }  // namespace ds4a

@@ -250,6 +250,21 @@ struct Ring {
 
 // ------------------------------------------------------------------ loaders
 
+// Ring order of an item's parts (the kernel's LA parameter).  With look-ahead
+// the K parts of the next tile come before the V parts of this one, so the
+// next QK^T runs while the softmax works on this tile and the ring keeps
+// loading meanwhile: K(0), then K(j+1) and V(j) for each tile j.  Without it
+// each tile's parts come together (always when parts are held from QK^T until
+// PV: K = V rows, paired stages).  Measured (one GB300): look-ahead takes the
+// indexed r4 prefill chunk from 366 to 332 us and the E4M3 256K decode from
+// 102 to 98 us, but slows the long fp16 decodes (8K rows 13.7 -> 14.4 us)
+// and the E4M3 prefill (106 -> 117 us), so it is a separate instantiation
+// chosen per call (launch_attn), which leaves the code of the others as it
+// was.
+__host__ __device__ __forceinline__ bool look_ahead_suits(const AttnParams &p) {
+  return !p.alias_kv && !p.kv_pair && (p.mode == MODE_INDEXED || (p.comp_fp8 && p.partial));
+}
+
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
@@ -326,7 +341,7 @@ __device__ __noinline__ void q_copy_role(const AttnParams &p, uint32_t sbase, Mi
 // copies and stages stay in flight up to the ring depth.  In this mode a
 // stage barrier expects one arrival per loader thread (TMA stages: thread 0's
 // arrive.expect_tx plus a plain arrival from every other thread).
-template <bool FP8>
+template <bool FP8, bool LA>
 __device__ __forceinline__ void loader_role(const AttnParams &p, uint32_t sbase, Misc &ms, int ltid) {
   volatile int *abrt = &ms.abort_flag;
   const bool group = p.mode == MODE_INDEXED && p.n_comp > 0;  // all loader threads needed
@@ -369,82 +384,113 @@ __device__ __forceinline__ void loader_role(const AttnParams &p, uint32_t sbase,
     }
     q_issued = !q_lsu;
     q_par = n_item & 1;
-    for (int j = ip.j0; j < ip.j1 && ok; ++j) {
-      const Tile tl = ip.cur.next(p);
-      if (tl.seg == 2) {
-        named_bar_sync(2, kLoaderThreads);  // every thread is done with the previous list
-        const int32_t *lst = p.idx + (long long)ip.t * p.idx_stride;
-        for (int k = ltid; k < 128; k += kLoaderThreads) {
-          const int slot = tl.start + k;
-          const int c = slot < p.top_k ? __ldg(lst + slot) : -1;
-          ms.idx_s[k] = (c >= 0 && c < p.n_comp) ? c : 0;  // empty slots load row 0, masked later
+    // One K/V part of tile `tl` into the next ring stage (parts 0-3: K dims
+    // 128*part, parts 4-7: V); gathered tiles read their rows from list `ib`.
+    auto emit = [&](const Tile &tl, int part, int ib) -> bool {
+      // Every thread waits for the slot itself (bounded); a thread that gives
+      // up stops filling, and the group meets at the next tile's barrier.
+      if (!mbar_wait(smem_u32(&ms.kv_empty[ring.st]), ring.ph ^ 1, abrt, p.timeout_ns, p.err, SITE_KV_EMPTY))
+        return false;
+      const uint32_t stage = sbase + kOffKV + ring.st * kStageBytes;
+      const uint32_t b_full = smem_u32(&ms.kv_full[ring.st]);
+      if (FP8 && tile_codes(p, tl)) {
+        // E4M3 rows: the codes of this part (128 rows x 128 bytes) land in
+        // the stage's upper half; the converter warps turn them into the
+        // fp16 stage and arrive on kv_full.
+        if (ltid == 0) {
+          const uint32_t b_code = smem_u32(&ms.code_full[ring.st]);
+          mbar_arrive_expect_tx(b_code, kBoxBytes);
+          tma_load_2d(stage + kBoxBytes, part >= 4 ? &p.tm_v8[tl.seg] : &p.tm_k8[tl.seg], b_code, 128 * (part & 3),
+                      tl.start);
+          cfilled |= 1u << ring.st;
+          clast_par = (clast_par & ~(1u << ring.st)) | (((code_ph >> ring.st) & 1u) << ring.st);
+          code_ph ^= 1u << ring.st;
         }
-        named_bar_sync(2, kLoaderThreads);
+      } else if (tl.seg != 2) {
+        if (ltid == 0) {
+          const int dim0 = 128 * (part & 3);
+          const CUtensorMap *m = part >= 4 ? &p.tm_v[tl.seg] : &p.tm_k[tl.seg];
+          mbar_arrive_expect_tx(b_full, kStageBytes);
+          if (p.kv_pair) {
+            // 64-row tile: the K and the V slice of dims dim0 .. dim0+127 in
+            // one stage, four [64 rows][64 dims] boxes of 8 KB (two copies:
+            // the maps' boxes span two 64-dim blocks).
+            tma_load_3d(stage, &p.tm_k[tl.seg], b_full, 0, tl.start, dim0 / 64);
+            tma_load_3d(stage + kBoxBytes, &p.tm_v[tl.seg], b_full, 0, tl.start, dim0 / 64);
+          } else if (p.batch_geom != nullptr) {  // [sequences][rows][512]: the sequence is the third coordinate
+            tma_load_3d(stage, m, b_full, dim0, tl.start, ip.t);
+            tma_load_3d(stage + kBoxBytes, m, b_full, dim0 + 64, tl.start, ip.t);
+          } else {
+            tma_load_3d(stage, m, b_full, 0, tl.start, dim0 / 64);  // both 64-dim boxes of the part
+          }
+          filled |= 1u << ring.st;
+          last_par = (last_par & ~(1u << ring.st)) | (ring.ph << ring.st);
+        } else {
+          mbar_arrive(b_full);
+        }
+      } else {
+        const uint8_t *base = (part >= 4 ? vbase : kbase) + 256 * (part & 3) + 16 * c8;
+        const uint32_t dst0 = stage + rsub * 128 + ((c8 ^ (rsub & 7)) << 4);  // row & 7 == rsub & 7
+#pragma unroll
+        for (int it = 0; it < 128 / kRowStep; ++it) {
+          const uint8_t *src = base + (long long)ms.idx_s[ib][kRowStep * it + rsub] * p.comp_row_stride;
+          const uint32_t dst = dst0 + it * (kRowStep * 128);
+          cp_async16(dst, src);                    // dims 0-63 of the part: the first box
+          cp_async16(dst + kBoxBytes, src + 128);  // dims 64-127: the second box
+        }
+        cp_async_arrive_noinc(b_full);
       }
+      ring.advance();
+      return true;
+    };
+    // The compressed rows a gathered tile lists, into list `ib`.  The list
+    // may be rewritten once every thread has issued the copies of the tile
+    // that used it last (a copy takes its address when it is issued).
+    auto load_list = [&](const Tile &tl, int ib) {
+      named_bar_sync(2, kLoaderThreads);
+      const int32_t *lst = p.idx + (long long)ip.t * p.idx_stride;
+      for (int k = ltid; k < 128; k += kLoaderThreads) {
+        const int slot = tl.start + k;
+        const int c = slot < p.top_k ? __ldg(lst + slot) : -1;
+        ms.idx_s[ib][k] = (c >= 0 && c < p.n_comp) ? c : 0;  // empty slots load row 0, masked later
+      }
+      named_bar_sync(2, kLoaderThreads);
+    };
+    const int nt = ip.j1 - ip.j0;
+    Tile cur = ip.cur.next(p);
+    if (cur.seg == 2) load_list(cur, 0);
+    if (LA) {
+      // Ring order: the K parts of tile 0, then for each tile the K parts of
+      // the next tile before its own V parts (see mma_role).
+      for (int part = 0; part < 4; ++part) ok = ok && emit(cur, part, 0);
+      for (int jj = 0; jj < nt; ++jj) {
+        if (group) ok = !bar_red_or(2, kLoaderThreads, !ok);  // uniform decision before the next list
+        if (!ok) break;
+        Tile nxt = cur;
+        if (jj + 1 < nt) {
+          nxt = ip.cur.next(p);
+          if (nxt.seg == 2) load_list(nxt, (jj + 1) & 1);
+          for (int part = 0; part < 4; ++part) ok = ok && emit(nxt, part, (jj + 1) & 1);
+        }
+        for (int part = 4; part < 8; ++part) ok = ok && emit(cur, part, jj & 1);
+        cur = nxt;
+      }
+    } else {
       // K/V parts of a tile in ring order: 4 K parts then 4 V parts, or only
       // the 4 K parts when K and V are the same rows (see mma_role).
       const int n_parts = (p.alias_kv | p.kv_pair) ? 4 : 8;
+      for (int jj = 0; jj < nt; ++jj) {
+        if (jj > 0) {
+          cur = ip.cur.next(p);
+          if (cur.seg == 2) load_list(cur, 0);
+        }
 #pragma unroll 1
-      for (int part = 0; part < n_parts; ++part) {  // parts 0-3: K dims 128*part, parts 4-7: V
-        // Every thread waits for the slot itself (bounded); a thread that gives
-        // up stops filling, and the group meets at the next tile's barrier.
-        if (!mbar_wait(smem_u32(&ms.kv_empty[ring.st]), ring.ph ^ 1, abrt, p.timeout_ns, p.err, SITE_KV_EMPTY)) {
-          ok = false;
-          break;
-        }
-        const uint32_t stage = sbase + kOffKV + ring.st * kStageBytes;
-        const uint32_t b_full = smem_u32(&ms.kv_full[ring.st]);
-        if (FP8 && tile_codes(p, tl)) {
-          // E4M3 rows: the codes of this part (128 rows x 128 bytes) land in
-          // the stage's upper half; the converter warps turn them into the
-          // fp16 stage and arrive on kv_full.
-          if (ltid == 0) {
-            const uint32_t b_code = smem_u32(&ms.code_full[ring.st]);
-            mbar_arrive_expect_tx(b_code, kBoxBytes);
-            tma_load_2d(stage + kBoxBytes, part >= 4 ? &p.tm_v8[tl.seg] : &p.tm_k8[tl.seg], b_code, 128 * (part & 3),
-                        tl.start);
-            cfilled |= 1u << ring.st;
-            clast_par = (clast_par & ~(1u << ring.st)) | (((code_ph >> ring.st) & 1u) << ring.st);
-            code_ph ^= 1u << ring.st;
-          }
-        } else if (tl.seg != 2) {
-          if (ltid == 0) {
-            const int dim0 = 128 * (part & 3);
-            const CUtensorMap *m = part >= 4 ? &p.tm_v[tl.seg] : &p.tm_k[tl.seg];
-            mbar_arrive_expect_tx(b_full, kStageBytes);
-            if (p.kv_pair) {
-              // 64-row tile: the K and the V slice of dims dim0 .. dim0+127 in
-              // one stage, four [64 rows][64 dims] boxes of 8 KB (two copies:
-              // the maps' boxes span two 64-dim blocks).
-              tma_load_3d(stage, &p.tm_k[tl.seg], b_full, 0, tl.start, dim0 / 64);
-              tma_load_3d(stage + kBoxBytes, &p.tm_v[tl.seg], b_full, 0, tl.start, dim0 / 64);
-            } else if (p.batch_geom != nullptr) {  // [sequences][rows][512]: the sequence is the third coordinate
-              tma_load_3d(stage, m, b_full, dim0, tl.start, ip.t);
-              tma_load_3d(stage + kBoxBytes, m, b_full, dim0 + 64, tl.start, ip.t);
-            } else {
-              tma_load_3d(stage, m, b_full, 0, tl.start, dim0 / 64);  // both 64-dim boxes of the part
-            }
-            filled |= 1u << ring.st;
-            last_par = (last_par & ~(1u << ring.st)) | (ring.ph << ring.st);
-          } else {
-            mbar_arrive(b_full);
-          }
-        } else {
-          const uint8_t *base = (part >= 4 ? vbase : kbase) + 256 * (part & 3) + 16 * c8;
-          const uint32_t dst0 = stage + rsub * 128 + ((c8 ^ (rsub & 7)) << 4);  // row & 7 == rsub & 7
-#pragma unroll
-          for (int it = 0; it < 128 / kRowStep; ++it) {
-            const uint8_t *src = base + (long long)ms.idx_s[kRowStep * it + rsub] * p.comp_row_stride;
-            const uint32_t dst = dst0 + it * (kRowStep * 128);
-            cp_async16(dst, src);                    // dims 0-63 of the part: the first box
-            cp_async16(dst + kBoxBytes, src + 128);  // dims 64-127: the second box
-          }
-          cp_async_arrive_noinc(b_full);
-        }
-        ring.advance();
+        for (int part = 0; part < n_parts; ++part) ok = ok && emit(cur, part, 0);
+        if (group) ok = !bar_red_or(2, kLoaderThreads, !ok);  // uniform decision before the next list
+        if (!ok) break;
       }
-      if (group) ok = !bar_red_or(2, kLoaderThreads, !ok);  // uniform decision before the next list
     }
+    if (group && ok) ok = !bar_red_or(2, kLoaderThreads, !ok);
     ++n_item;
   }
   if (group) cp_async_wait<0>();  // no gathered copy may still be landing at exit
@@ -474,6 +520,7 @@ __device__ __forceinline__ void loader_role(const AttnParams &p, uint32_t sbase,
 // agree on stage and phase.
 constexpr int kConvThreads = kLoaderThreads - 32;
 
+template <bool LA>
 __device__ __forceinline__ void converter_role(const AttnParams &p, uint32_t sbase, Misc &ms, int ctid) {
   volatile int *abrt = &ms.abort_flag;
   Ring ring;
@@ -484,54 +531,69 @@ __device__ __forceinline__ void converter_role(const AttnParams &p, uint32_t sba
   for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
     ItemPlan ip = plan_item(p, item);
     if (ip.j1 == ip.j0) continue;
-    for (int j = ip.j0; j < ip.j1 && ok; ++j) {
-      const Tile tl = ip.cur.next(p);
-      const int n_parts = p.alias_kv ? 4 : 8;  // the E4M3 path never aliases
+    // One part of tile `tl` in ring order: convert its codes if it has any.
+    auto convert = [&](const Tile &tl, int part) -> bool {
+      (void)part;
+      if (tile_codes(p, tl)) {
+        const uint32_t st = ring.st;
+        bool w = mbar_wait(smem_u32(&ms.code_full[st]), (code_ph >> st) & 1u, abrt, p.timeout_ns, p.err,
+                           SITE_KV_FULL);
+        code_ph ^= 1u << st;
+        if (bar_red_or(3, kConvThreads, !w)) return false;
+        const uint32_t stage = sbase + kOffKV + st * kStageBytes;
 #pragma unroll 1
-      for (int part = 0; part < n_parts; ++part) {
-        if (tile_codes(p, tl)) {
-          const uint32_t st = ring.st;
-          ok = mbar_wait(smem_u32(&ms.code_full[st]), (code_ph >> st) & 1u, abrt, p.timeout_ns, p.err,
-                         SITE_KV_FULL);
-          code_ph ^= 1u << st;
-          if (bar_red_or(3, kConvThreads, !ok)) {
-            ok = false;
-            break;
+        for (int row = ctid; row < kTile; row += kConvThreads) {
+          uint4 raw[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int c = (k + row) & 7;
+            const uint32_t a = stage + kBoxBytes + row * 128 + 16 * c;
+            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(raw[k].x), "=r"(raw[k].y), "=r"(raw[k].z), "=r"(raw[k].w)
+                         : "r"(a));
           }
-          const uint32_t stage = sbase + kOffKV + st * kStageBytes;
-#pragma unroll 1
-          for (int row = ctid; row < kTile; row += kConvThreads) {
-            uint4 raw[8];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              const int c = (k + row) & 7;
-              const uint32_t a = stage + kBoxBytes + row * 128 + 16 * c;
-              asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                           : "=r"(raw[k].x), "=r"(raw[k].y), "=r"(raw[k].z), "=r"(raw[k].w)
-                           : "r"(a));
+          for (int k = 0; k < 8; ++k) {
+            const int c = (k + row) & 7;
+            const uint32_t w4[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
+            uint32_t h[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              h[2 * i] = e4m3x2_to_f16x2(static_cast<uint16_t>(w4[i] & 0xFFFFu));
+              h[2 * i + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(w4[i] >> 16));
             }
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              const int c = (k + row) & 7;
-              const uint32_t w[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
-              uint32_t h[8];
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                h[2 * i] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[i] & 0xFFFFu));
-                h[2 * i + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[i] >> 16));
-              }
-              // dims 16c .. 16c+15 of the part: box c/4, 16-byte chunks 2(c%4), 2(c%4)+1
-              const uint32_t drow = stage + (c >> 2) * kBoxBytes + row * 128;
-              const int col = 2 * (c & 3);
-              sts_v4(drow + ((col ^ (row & 7)) << 4), h[0], h[1], h[2], h[3]);
-              sts_v4(drow + (((col + 1) ^ (row & 7)) << 4), h[4], h[5], h[6], h[7]);
-            }
+            // dims 16c .. 16c+15 of the part: box c/4, 16-byte chunks 2(c%4), 2(c%4)+1
+            const uint32_t drow = stage + (c >> 2) * kBoxBytes + row * 128;
+            const int col = 2 * (c & 3);
+            sts_v4(drow + ((col ^ (row & 7)) << 4), h[0], h[1], h[2], h[3]);
+            sts_v4(drow + (((col + 1) ^ (row & 7)) << 4), h[4], h[5], h[6], h[7]);
           }
-          fence_proxy_async_smem();  // generic stores -> visible to the tensor core
-          named_bar_sync(3, kConvThreads);
-          if (ctid == 0) mbar_arrive(smem_u32(&ms.kv_full[st]));
         }
-        ring.advance();
+        fence_proxy_async_smem();  // generic stores -> visible to the tensor core
+        named_bar_sync(3, kConvThreads);
+        if (ctid == 0) mbar_arrive(smem_u32(&ms.kv_full[st]));
+      }
+      ring.advance();
+      return true;
+    };
+    const int nt = ip.j1 - ip.j0;
+    Tile cur = ip.cur.next(p);
+    if (LA) {  // the loader's order: K(0), then K(j+1) and V(j) for each tile j
+      for (int part = 0; part < 4 && ok; ++part) ok = convert(cur, part);
+      for (int jj = 0; jj < nt && ok; ++jj) {
+        Tile nxt = cur;
+        if (jj + 1 < nt) {
+          nxt = ip.cur.next(p);
+          for (int part = 0; part < 4 && ok; ++part) ok = convert(nxt, part);
+        }
+        for (int part = 4; part < 8 && ok; ++part) ok = convert(cur, part);
+        cur = nxt;
+      }
+    } else {
+      const int n_parts = p.alias_kv ? 4 : 8;  // the E4M3 path never aliases
+      for (int jj = 0; jj < nt && ok; ++jj) {
+        if (jj > 0) cur = ip.cur.next(p);
+        for (int part = 0; part < n_parts && ok; ++part) ok = convert(cur, part);
       }
     }
   }
@@ -539,6 +601,7 @@ __device__ __forceinline__ void converter_role(const AttnParams &p, uint32_t sba
 
 // ------------------------------------------------------------------ MMA issuer
 
+template <bool LA>
 __device__ __forceinline__ void mma_role(const AttnParams &p, uint32_t sbase, uint32_t tmem, Misc &ms, int lane) {
   if (lane == 0) {
     volatile int *abrt = &ms.abort_flag;
@@ -567,27 +630,26 @@ __device__ __forceinline__ void mma_role(const AttnParams &p, uint32_t sbase, ui
       ok = mbar_wait(smem_u32(&ms.q_full), n_item & 1, abrt, p.timeout_ns, p.err, SITE_Q_FULL);
       if (!ok) break;
       const int nt = ip.j1 - ip.j0;
-      for (int jj = 0; jj < nt && ok; ++jj) {
-        // K and V the same rows: each K part stays in the ring after QK^T and
-        // serves PV as V^T.  A part holds 128 dims of every row of the tile,
-        // the K-major A operand of QK^T and the MN-major A operand of PV alike,
-        // so each row crosses into the SM once.  Paired stages hold the K and
-        // the V slice of a 64-row tile: they too stay from QK^T until PV.  With
-        // 64 rows the M = 128 QK^T reads 64 more rows (the next boxes of the
-        // stage): their scores are dropped by the mask, and PV only takes the
-        // tile's own rows.
-        const bool alias = p.alias_kv != 0;
-        const bool hold = alias || p.kv_pair != 0;
-        const uint32_t k0 = ring.st;  // held: part m sits in stage (k0 + m) % kStages until PV m
-        const uint32_t sb = g & 1;
-        ok = mbar_wait(smem_u32(&ms.s_empty[sb]), ((g >> 1) & 1) ^ 1, abrt, p.timeout_ns, p.err, SITE_S_EMPTY);
-        if (!ok) break;
+      // K and V the same rows: each K part stays in the ring after QK^T and
+      // serves PV as V^T.  A part holds 128 dims of every row of the tile,
+      // the K-major A operand of QK^T and the MN-major A operand of PV alike,
+      // so each row crosses into the SM once.  Paired stages hold the K and
+      // the V slice of a 64-row tile: they too stay from QK^T until PV.  With
+      // 64 rows the M = 128 QK^T reads 64 more rows (the next boxes of the
+      // stage): their scores are dropped by the mask, and PV only takes the
+      // tile's own rows.
+      const bool hold = p.alias_kv != 0 || p.kv_pair != 0;
+      uint32_t k0 = 0;  // held: part m sits in stage (k0 + m) % kStages until PV m
+      // S^T of tile jj (global tile gj) = K_tile . Q^T over the 512 dims, 128 dims per stage.
+      auto qk = [&](uint32_t gj, int jj) -> bool {
+        k0 = ring.st;
+        const uint32_t sb = gj & 1;
+        if (!mbar_wait(smem_u32(&ms.s_empty[sb]), ((gj >> 1) & 1) ^ 1, abrt, p.timeout_ns, p.err, SITE_S_EMPTY))
+          return false;
         tc_fence_after();
         const uint32_t d_s = tmem + kTmemS + 64 * sb;
-        // S^T = K_tile . Q^T over the 512 dims, 128 dims per stage.
-        for (int c = 0; c < 4 && ok; ++c) {
-          ok = mbar_wait(smem_u32(&ms.kv_full[ring.st]), ring.ph, abrt, p.timeout_ns, p.err, SITE_KV_FULL);
-          if (!ok) break;
+        for (int c = 0; c < 4; ++c) {
+          if (!mbar_wait(smem_u32(&ms.kv_full[ring.st]), ring.ph, abrt, p.timeout_ns, p.err, SITE_KV_FULL)) return false;
           tc_fence_after();
           const uint64_t a0 = sdesc_add(k_desc, ring.st * kStageBytes);
           const uint64_t b0 = sdesc_add(q_desc, 2 * c * kQBoxBytes);
@@ -606,22 +668,22 @@ __device__ __forceinline__ void mma_role(const AttnParams &p, uint32_t sbase, ui
           if (!hold) umma_commit(smem_u32(&ms.kv_empty[ring.st]));  // held for PV otherwise
           ring.advance();
         }
-        if (!ok) break;
         umma_commit(smem_u32(&ms.s_full[sb]));
         if (jj == nt - 1) umma_commit(smem_u32(&ms.q_empty));
-        ok = mbar_wait(smem_u32(&ms.p_full), g & 1, abrt, p.timeout_ns, p.err, SITE_P_FULL);
-        if (!ok) break;
-        if (jj == 0) {
-          ok = mbar_wait(smem_u32(&ms.o_empty), (n_item & 1) ^ 1, abrt, p.timeout_ns, p.err, SITE_O_EMPTY);
-          if (!ok) break;
-        }
+        return true;
+      };
+      // O^T[m] += V_tile^T[dims 128m..] . P^T of tile jj (global tile gj), 16 rows per instruction.
+      auto pv = [&](uint32_t gj, int jj) -> bool {
+        if (!mbar_wait(smem_u32(&ms.p_full), gj & 1, abrt, p.timeout_ns, p.err, SITE_P_FULL)) return false;
+        if (jj == 0 &&
+            !mbar_wait(smem_u32(&ms.o_empty), (n_item & 1) ^ 1, abrt, p.timeout_ns, p.err, SITE_O_EMPTY))
+          return false;
         tc_fence_after();
-        // O^T[m] += V_tile^T[dims 128m..] . P^T, 16 rows per instruction.
-        for (int m = 0; m < 4 && ok; ++m) {
+        for (int m = 0; m < 4; ++m) {
           uint32_t vst = (k0 + m) % kStages;  // held: the part of the same dims, already landed
           if (!hold) {
-            ok = mbar_wait(smem_u32(&ms.kv_full[ring.st]), ring.ph, abrt, p.timeout_ns, p.err, SITE_KV_FULL);
-            if (!ok) break;
+            if (!mbar_wait(smem_u32(&ms.kv_full[ring.st]), ring.ph, abrt, p.timeout_ns, p.err, SITE_KV_FULL))
+              return false;
             tc_fence_after();
             vst = ring.st;
           }
@@ -642,9 +704,20 @@ __device__ __forceinline__ void mma_role(const AttnParams &p, uint32_t sbase, ui
           if (jj == nt - 1) umma_commit(smem_u32(&ms.o_full[m]));
           if (!hold) ring.advance();
         }
-        if (!ok) break;
         umma_commit(smem_u32(&ms.p_empty));
-        ++g;
+        return true;
+      };
+      if (LA) {
+        // The loader's order: QK^T of tile 0, then per tile the QK^T of the
+        // next tile (into the other S^T buffer, while the softmax works on
+        // this one) and the PV of this one.
+        ok = qk(g, 0);
+        for (int jj = 0; jj < nt && ok; ++jj, ++g) {
+          if (jj + 1 < nt) ok = qk(g + 1, jj + 1);
+          ok = ok && pv(g, jj);
+        }
+      } else {
+        for (int jj = 0; jj < nt && ok; ++jj, ++g) ok = qk(g, jj) && pv(g, jj);
       }
       if (!ok) break;
       ++n_item;
@@ -883,7 +956,7 @@ __device__ __forceinline__ void compute_role(const AttnParams &p, uint8_t *smem,
 
 // ------------------------------------------------------------------ kernel
 
-template <bool FP8>
+template <bool FP8, bool LA>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ AttnParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // Align by pointer arithmetic on the __shared__ array (not through an
@@ -952,13 +1025,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   if (warp < kComputeWarps) {
     compute_role<FP8>(p, smem, tmem, ms, threadIdx.x);
   } else if (warp == kMmaWarp) {
-    mma_role(p, sbase, tmem, ms, lane);
+    mma_role<LA>(p, sbase, tmem, ms, lane);
   } else {
     const int ltid = threadIdx.x - 32 * kLoaderWarp0;
     if (FP8 && ltid >= 32)
-      converter_role(p, sbase, ms, ltid - 32);
+      converter_role<LA>(p, sbase, ms, ltid - 32);
     else
-      loader_role<FP8>(p, sbase, ms, ltid);
+      loader_role<FP8, LA>(p, sbase, ms, ltid);
   }
 
   tc_fence_before();

@@ -53,7 +53,7 @@ struct Misc {
   alignas(16) float m_use[kH];    // reference max used for P (log2 units)
   alignas(16) float alpha[kH];    // rescale factor of the previous reference
   alignas(16) float inv_l[kH];
-  alignas(16) int idx_s[128];     // compressed rows of the tile being gathered
+  alignas(16) int idx_s[2][128];  // compressed rows of the gathered tiles, by tile parity
   alignas(8) uint64_t q_full, q_empty;
   uint64_t kv_full[kStages], kv_empty[kStages];
   uint64_t code_full[kStages];    // E4M3 codes of a part landed (upper half of the stage)
