@@ -202,6 +202,50 @@ def test_prefill_ragged(torch, ds4a, case):
     assert_lse_close(host(lse), wlse, f"ragged {case} lse")
 
 
+def _pair_cases():
+    """Raw-only layouts with a window of at most 128 and T >= 2: the prefill
+    path that serves two consecutive tokens per 128-row tile."""
+    return [
+        make_layout(T=2, q_pos0=500, n_raw=400, raw_pos0=200),                # one pair, extra row present
+        make_layout(T=2, q_pos0=127, n_raw=128, raw_pos0=0),                  # token a's window starts at row 0
+        make_layout(T=2, q_pos0=127, n_raw=129, raw_pos0=0),                  # the extra row is row 0
+        make_layout(T=7, q_pos0=60, n_raw=100, raw_pos0=0),                   # tiles start below row 0, odd T
+        make_layout(T=9, q_pos0=400, n_raw=300, raw_pos0=250, window=37),     # short window: no extra row
+        make_layout(T=6, q_pos0=1000, n_raw=40, raw_pos0=950),                # rows end before the tokens
+        make_layout(T=311, q_pos0=3000, n_raw=500, raw_pos0=2700),            # > one pair per CTA, odd last token
+    ]
+
+
+@pytest.mark.parametrize("case", range(7))
+def test_prefill_pairs(torch, ds4a, case):
+    L = _pair_cases()[case]
+    wl = W.draw(f"pairs{case}", 90 + case, L)
+    d = upload(torch, wl)
+    o = torch.full_like(d["q"], float("nan"))
+    lse = torch.full((L["T"], 64), float("nan"), dtype=torch.float32, device="cuda")
+    ds4a.attn_prefill(L, d["q"], d["k_raw"], d["v_raw"], out=o, lse=lse)
+    want, wlse = oracle_out(wl)
+    assert_close(host(o), want, f"pairs {case}")
+    assert_lse_close(host(lse), wlse, f"pairs {case} lse")
+
+
+def test_prefill_pairs_strided(torch, ds4a):
+    """The pair path with Q/O token strides and K/V row strides larger than the packed ones."""
+    L = make_layout(T=5, q_pos0=300, n_raw=260, raw_pos0=50)
+    wl = W.draw("pairs_strided", 99, L)
+    qbig = torch.zeros((5, 72, 512), dtype=torch.float16, device="cuda")
+    qbig[:, :64] = dev(torch, wl.q)
+    kbig = torch.zeros((260, 640), dtype=torch.float16, device="cuda")
+    vbig = torch.zeros((260, 640), dtype=torch.float16, device="cuda")
+    kbig[:, :512] = dev(torch, wl.k_raw)
+    vbig[:, :512] = dev(torch, wl.v_raw)
+    obig = torch.full((5, 66, 512), 7.0, dtype=torch.float16, device="cuda")
+    ds4a.attn_prefill(L, qbig[:, :64], kbig[:, :512], vbig[:, :512], out=obig[:, :64])
+    want, _ = oracle_out(wl)
+    assert_close(host(obig[:, :64]), want, "pairs strided")
+    assert bool((obig[:, 64:] == 7.0).all()), "a write landed outside the output rows"
+
+
 def test_prefill_strided_tokens_and_rows(torch, ds4a):
     """Q/O token strides and K/V row strides larger than the packed ones."""
     L = make_layout(T=6, q_pos0=150, n_raw=160, raw_pos0=0, n_comp=40, ratio=4)
