@@ -490,7 +490,9 @@ __device__ __forceinline__ void loader_role(const AttnParams &p, uint32_t sbase,
         if (!ok) break;
       }
     }
-    if (group && ok) ok = !bar_red_or(2, kLoaderThreads, !ok);
+    // Every group thread reaches this point (the loops above leave together),
+    // so the last step's outcome is made uniform here too.
+    if (group) ok = !bar_red_or(2, kLoaderThreads, !ok);
     ++n_item;
   }
   if (group) cp_async_wait<0>();  // no gathered copy may still be landing at exit
