@@ -484,7 +484,12 @@ int32_t ds4a_attn_decode_default_splits(const ds4a_layout *L) {
   int32_t s = ceil_div(sms, L->T);
   const int32_t mt = max_tiles_per_token(L, short_decode(L, sms) ? 64 : 128);
   if (s > mt) s = mt;
-  return s < 1 ? 1 : s;
+  if (s < 1) return 1;
+  // The fewest splits whose longest range has as many tiles as with s splits:
+  // the same longest chain, fewer partials to write and merge (65,536
+  // compressed rows, 513 tiles: 129 splits of at most 4 tiles 37.1 us per
+  // call, 152 splits 39.6 us; 262,144 rows: 147 splits 97.8 us, 152 98.9 us).
+  return ceil_div(mt, ceil_div(mt, s));
 }
 
 size_t ds4a_attn_decode_workspace_size(const ds4a_layout *L, int32_t n_splits) {

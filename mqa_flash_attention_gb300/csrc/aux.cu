@@ -208,12 +208,30 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __half *
 }
 
 // Many splits (a long decode): one block per (token, head, 64-dim chunk), 512
-// blocks per token.  Warp w sums the splits w, w+8, w+16, ... over the chunk's
-// 64 dims (a half2 per lane, four loads in flight), and the eight warp sums
-// are added in shared memory: the per-thread chains are 1/8 as long and four
-// times as many blocks load at once as in combine_kernel.
-constexpr int kWideChunks = 8;        // 64-dim chunks per head
-constexpr int kWideMinSplits = 17;    // below this the one-dim-per-thread merge is as fast
+// blocks per token.  Thread (warp w, lane l) owns dims 8 (l & 7) .. +7 of the
+// chunk (one 16-byte load per split) for the splits g, g + 32, g + 64, ... with
+// g = 4 w + (l >> 3).  The loads of the first 256 splits are issued before the
+// split weights are known, together with the (m, l) pairs, so that up to 256
+// splits cost one round of memory latency; the per-thread sums are then added
+// across the lanes of a dim group (shuffles) and across warps (shared memory).
+constexpr int kWideChunks = 8;      // 64-dim chunks per head
+constexpr int kWideMinSplits = 17;  // below this the one-dim-per-thread merge is as fast
+constexpr int kWideGroups = kCombineThreads / 8;  // split groups: 8 threads of 16 bytes cover a chunk
+constexpr int kWideLoads = 8;                     // loads in registers per thread and round
+constexpr int kWideRound = kWideGroups * kWideLoads;
+
+__device__ __forceinline__ void add_weighted(float (&acc)[8], const uint4 &v, float wgt) {
+  const __half2 *h2 = reinterpret_cast<const __half2 *>(&v);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 f = __half22float2(h2[e]);
+    // A split without visible rows left its o_part slot unwritten (stale bytes,
+    // possibly NaN): its weight is 0 and the select (never a multiply, which
+    // would turn 0 * NaN into NaN) drops it.
+    acc[2 * e] += wgt != 0.f ? wgt * f.x : 0.f;
+    acc[2 * e + 1] += wgt != 0.f ? wgt * f.y : 0.f;
+  }
+}
 
 __global__ void __launch_bounds__(kCombineThreads) combine_wide_kernel(const __half *__restrict__ ws_o,
                                                                        const float2 *__restrict__ ws_ml,
@@ -222,64 +240,82 @@ __global__ void __launch_bounds__(kCombineThreads) combine_wide_kernel(const __h
                                                                        float *__restrict__ lse) {
   __shared__ float w_s[kCombineMaxSplits];
   __shared__ float red[kCombineThreads / 32];
-  __shared__ float2 part[kCombineThreads / 32][32];
+  __shared__ float part[kCombineThreads / 32][64];
   grid_dependency_wait();  // the partials come from the previous kernel
   grid_launch_dependents();
   const int chunk = blockIdx.x, h = blockIdx.y, t = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = 4 * warp + (lane >> 3), c8 = lane & 7;
   const long long base = (long long)t * n_splits;
-  float mx = -INFINITY;
-  for (int s = threadIdx.x; s < n_splits; s += kCombineThreads) mx = fmaxf(mx, ws_ml[(base + s) * 64 + h].x);
+  const __half *src = ws_o + (base * 64 + h) * 512 + 64 * chunk + 8 * c8;
+  const long long step = 64LL * 512;
+  uint4 x[kWideLoads];
+#pragma unroll
+  for (int k = 0; k < kWideLoads; ++k) {
+    const int s = g + kWideGroups * k;
+    x[k] = s < n_splits ? __ldg(reinterpret_cast<const uint4 *>(src + s * step)) : make_uint4(0u, 0u, 0u, 0u);
+  }
+  const float2 ml0 = tid < n_splits ? ws_ml[(base + tid) * 64 + h] : make_float2(-INFINITY, 0.f);
+  float mx = ml0.x;
+  for (int s = tid + kCombineThreads; s < n_splits; s += kCombineThreads)
+    mx = fmaxf(mx, ws_ml[(base + s) * 64 + h].x);
   const float M = block_reduce(mx, true, red);
   float lsum = 0.f;
-  for (int s = threadIdx.x; s < n_splits; s += kCombineThreads) {
+  if (tid < n_splits) {
+    const float wgt = (ml0.x == -INFINITY || M == -INFINITY) ? 0.f : exp2f(ml0.x - M) * ml0.y;
+    w_s[tid] = wgt;
+    lsum = wgt;
+  }
+  for (int s = tid + kCombineThreads; s < n_splits; s += kCombineThreads) {
     const float2 ml = ws_ml[(base + s) * 64 + h];
     const float wgt = (ml.x == -INFINITY || M == -INFINITY) ? 0.f : exp2f(ml.x - M) * ml.y;
     w_s[s] = wgt;
     lsum += wgt;
   }
   const float L = block_reduce(lsum, false, red);  // also orders the w_s writes before the reads below
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr int kW = kCombineThreads / 32;
-  const int d = 64 * chunk + 2 * lane;
-  const __half *src = ws_o + (base * 64 + h) * 512 + d;
-  const long long step = 64LL * 512;
-  // A split without visible rows left its o_part slot unwritten (stale bytes,
-  // possibly NaN): the value is loaded, but its weight is 0 and the select
-  // (never a multiply, which would turn 0 * NaN into NaN) drops it.
-  float2 acc = make_float2(0.f, 0.f);
-  int s = warp;
-  for (; s + 3 * kW < n_splits; s += 4 * kW) {
-    float2 x[4];
+  float acc[8];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-      x[i] = __half22float2(__ldg(reinterpret_cast<const __half2 *>(src + (long long)(s + i * kW) * step)));
+  for (int e = 0; e < 8; ++e) acc[e] = 0.f;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float wgt = w_s[s + i * kW];
-      acc.x += wgt != 0.f ? wgt * x[i].x : 0.f;
-      acc.y += wgt != 0.f ? wgt * x[i].y : 0.f;
+  for (int k = 0; k < kWideLoads; ++k) {
+    const int s = g + kWideGroups * k;
+    if (s < n_splits) add_weighted(acc, x[k], w_s[s]);
+  }
+  for (int r = kWideRound; r < n_splits; r += kWideRound) {
+#pragma unroll
+    for (int k = 0; k < kWideLoads; ++k) {
+      const int s = r + g + kWideGroups * k;
+      x[k] = s < n_splits ? __ldg(reinterpret_cast<const uint4 *>(src + s * step)) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int k = 0; k < kWideLoads; ++k) {
+      const int s = r + g + kWideGroups * k;
+      if (s < n_splits) add_weighted(acc, x[k], w_s[s]);
     }
   }
-  for (; s < n_splits; s += kW) {
-    const float2 x = __half22float2(__ldg(reinterpret_cast<const __half2 *>(src + (long long)s * step)));
-    const float wgt = w_s[s];
-    acc.x += wgt != 0.f ? wgt * x.x : 0.f;
-    acc.y += wgt != 0.f ? wgt * x.y : 0.f;
-  }
-  part[warp][lane] = acc;
-  __syncthreads();
-  if (warp == 0) {
-    float2 sum = part[0][lane];
+  // the four split groups of a warp hold the same dims in lanes l, l ^ 8, l ^ 16, l ^ 24
 #pragma unroll
-    for (int w = 1; w < kW; ++w) {
-      sum.x += part[w][lane].x;
-      sum.y += part[w][lane].y;
+  for (int e = 0; e < 8; ++e) {
+    acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], 8);
+    acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], 16);
+  }
+  if (lane < 8) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) part[warp][8 * c8 + e] = acc[e];
+  }
+  __syncthreads();
+  if (tid < 32) {
+    float2 sum = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < kCombineThreads / 32; ++w) {
+      sum.x += part[w][2 * tid];
+      sum.y += part[w][2 * tid + 1];
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
-    *reinterpret_cast<__half2 *>(o + (long long)t * o_tok_stride + h * 512 + d) =
+    *reinterpret_cast<__half2 *>(o + (long long)t * o_tok_stride + h * 512 + 64 * chunk + 2 * tid) =
         __floats2half2_rn(sum.x * inv, sum.y * inv);
   }
-  if (lse != nullptr && chunk == 0 && threadIdx.x == 0)
+  if (lse != nullptr && chunk == 0 && tid == 0)
     lse[(long long)t * 64 + h] = L > 0.f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
 }
 
