@@ -30,18 +30,19 @@
 // 2^8 and are stored as fp16, and the row sums add the same fp16 values, so
 // o = sum(p v) / sum(p) is an exact convex combination up to fp32 rounding.
 //
-// Warp roles (416 threads, one CTA per SM, persistent over work items):
+// Warp roles (512 threads, one CTA per SM, persistent over work items):
 //   warps 0-7   softmax + epilogue: warp w owns TMEM lane quarter w % 4 (32
 //               KV rows or dims) and heads 32*(w/4) .. +31
-//   warps 8-11  loaders: Q once per item, every K/V stage in ring order (TMA
-//               tiles, or 16-byte cp.async gathers of index-listed rows: a
-//               TMA gather moves only 512 bytes per instruction); in a CTA
-//               with a single item warps 9-11 copy its Q.  With E4M3 rows
-//               (the FP8 instantiation) the codes of each part land in the
-//               upper half of its stage and warps 9-11 convert them in place
+//   warps 8-14  loaders: Q once per item, every K/V stage in ring order (TMA
+//               tiles, or 16-byte cp.async gathers of index-listed rows by
+//               all seven warps: a TMA gather moves only 512 bytes per
+//               instruction); in a CTA with a single item warps 9-14 copy its
+//               Q.  With E4M3 rows (the FP8 instantiation) the codes of each
+//               part land in the upper half of its stage and warps 9-12
+//               convert them in place, one row per thread
 //   epilogue    a whole token: o (fp16) and its log-sum-exp; a split of a
 //               token: the split's own normalised o (fp16) and (m, l)
-//   warp  12    TMEM allocator and tcgen05.mma issuer
+//   warp  15    TMEM allocator and tcgen05.mma issuer
 // Each mbarrier is waited on only by a role that cannot fall more than one
 // phase behind it, which a parity wait needs.
 #pragma once
@@ -281,7 +282,7 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
 
 // Q through the load/store path, for a CTA with a single work item (a short
 // decode: Q's latency is then paid once, at the head of the chain).  Loader
-// warps 9-11 copy the item's Q while thread 0 issues the K/V tiles, so Q does
+// warps 9-14 copy the item's Q while thread 0 issues the K/V tiles, so Q does
 // not queue in front of them on the SM's TMA engine: 8.8 -> 8.5 us for a
 // 384-row decode split over 3 CTAs.  (In a long prefill, where each CTA runs
 // many items, it made no difference: there every TMA load takes ~2.7 us under
@@ -329,7 +330,8 @@ __device__ __noinline__ void q_copy_role(const AttnParams &p, uint32_t sbase, Mi
 // span two 64-dim blocks), Q in one 64 KB copy.
 // Gathered tiles (index-listed compressed rows): per stage (128 rows x 128
 // dims) the loader threads copy 2048 chunks of 16 bytes: thread (row group
-// rsub, column c8) copies column c8 of both 64-dim boxes of its 8 rows, so a
+// rsub, column c8) copies column c8 of both 64-dim boxes of rows rsub,
+// rsub + 28, rsub + 56, ... (224 threads: four or five rows each), so a
 // warp instruction covers four rows x 128 contiguous bytes and each listed
 // row's address is formed once per stage for two copies (forming it for
 // every copy held the gather rate near 43 GB/s per SM: indexed attention
@@ -430,11 +432,12 @@ __device__ __forceinline__ void loader_role(const AttnParams &p, uint32_t sbase,
         }
       } else {
         const uint8_t *base = (part >= 4 ? vbase : kbase) + 256 * (part & 3) + 16 * c8;
-        const uint32_t dst0 = stage + rsub * 128 + ((c8 ^ (rsub & 7)) << 4);  // row & 7 == rsub & 7
 #pragma unroll
-        for (int it = 0; it < 128 / kRowStep; ++it) {
-          const uint8_t *src = base + (long long)ms.idx_s[ib][kRowStep * it + rsub] * p.comp_row_stride;
-          const uint32_t dst = dst0 + it * (kRowStep * 128);
+        for (int it = 0; it < (kTile + kRowStep - 1) / kRowStep; ++it) {
+          const int row = kRowStep * it + rsub;
+          if (kTile % kRowStep != 0 && row >= kTile) break;  // the last pass covers part of the rows
+          const uint8_t *src = base + (long long)ms.idx_s[ib][row] * p.comp_row_stride;
+          const uint32_t dst = stage + row * 128 + ((c8 ^ (row & 7)) << 4);
           cp_async16(dst, src);                    // dims 0-63 of the part: the first box
           cp_async16(dst + kBoxBytes, src + 128);  // dims 64-127: the second box
         }
@@ -512,7 +515,7 @@ __device__ __forceinline__ void loader_role(const AttnParams &p, uint32_t sbase,
 // ------------------------------------------------------------------ E4M3 converters
 
 
-// Warps 9..11 when K/V rows are E4M3: for each such K/V part,
+// Warps 9..12 when K/V rows are E4M3 (one row of a part per thread): for each such K/V part,
 // wait for its codes (upper half of the stage), then convert them (exactly)
 // into the fp16 stage in the swizzled layout the TMA would have produced, and
 // arrive on kv_full.  A thread converts whole rows: row r's fp16 values in the
@@ -520,7 +523,7 @@ __device__ __forceinline__ void loader_role(const AttnParams &p, uint32_t sbase,
 // first; chunks are visited in a per-thread rotated order (no bank
 // conflicts).  The same walk of items, tiles and parts as the loader, so both
 // agree on stage and phase.
-constexpr int kConvThreads = kLoaderThreads - 32;
+constexpr int kConvThreads = kTile;
 
 template <bool LA>
 __device__ __forceinline__ void converter_role(const AttnParams &p, uint32_t sbase, Misc &ms, int ctid) {
@@ -1030,9 +1033,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     mma_role<LA>(p, sbase, tmem, ms, lane);
   } else {
     const int ltid = threadIdx.x - 32 * kLoaderWarp0;
-    if (FP8 && ltid >= 32)
-      converter_role<LA>(p, sbase, ms, ltid - 32);
-    else
+    if (FP8 && ltid >= 32) {
+      if (ltid < 32 + kConvThreads) converter_role<LA>(p, sbase, ms, ltid - 32);
+    } else
       loader_role<FP8, LA>(p, sbase, ms, ltid);
   }
 
