@@ -52,9 +52,9 @@
  *     apart), token stride in bytes (>= 65536, multiple of 16).
  *   - K and V may alias (k == v), as in an engine that stores one KV row.
  *     When they alias in every segment that has rows, every row is read once
- *     and serves both Q.K and the V weighting (fp16 rows; E4M3 rows are read
- *     as two arrays even when they alias, and so are calls where only one
- *     segment aliases).
+ *     and serves both Q.K and the V weighting (fp16 rows in prefill and
+ *     decode; E4M3 rows and ds4a_attn_indexed read K and V as two arrays even
+ *     when they alias, and so do calls where only one segment aliases).
  *   - Rows that a token cannot see must still hold finite values (pad rows
  *     written by ds4a_pad_kv are +0.0): an invisible row gets weight 0, and
  *     0 * inf or 0 * nan would poison the sum.

@@ -882,6 +882,13 @@ ds4a_status ds4a_attn_indexed(const ds4a_layout *L, const ds4a_tensors *X, const
   AttnParams p;
   st = fill_params(p, L, X, ds4a::MODE_INDEXED, d);
   if (st != DS4A_OK) return st;
+  // Gathered rows come from L2, where the look-ahead ring order (the K parts
+  // of the next tile before the V parts of this one) gains more than loading
+  // each row once for both products, which holds a tile's parts in the ring
+  // from QK^T to PV (2048 tokens, top-512 of 8192 rows, K = V rows: 343 us
+  // loaded once, 313 us read apart): K and V are read apart even when they
+  // are the same rows.
+  p.alias_kv = 0;
   p.idx = idx;
   p.idx_stride = idx_row_stride / 4;
   p.top_k = top_k;

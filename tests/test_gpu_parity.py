@@ -469,6 +469,24 @@ def test_decode_equals_last_prefill_row(torch, ds4a):
     assert err.max() <= 2 * MAX_ABS
 
 
+def test_calls_on_the_same_buffers_with_other_shapes(torch, ds4a):
+    """Calls on the same device buffers with fewer compressed or raw rows,
+    then the first shape again: each matches the oracle on exactly the rows it
+    names (state carried from one call to the next, such as a tensor map of an
+    earlier shape, would read the wrong rows or none)."""
+    L0 = make_layout(T=3, q_pos0=9000, n_raw=200, raw_pos0=8850, n_comp=70, ratio=128)
+    wl = W.draw("same_bufs", 81, L0)
+    d = upload(torch, wl)
+    for n_comp, n_raw in ((70, 200), (40, 200), (70, 140), (33, 151), (70, 200)):
+        L = dict(L0, n_comp=n_comp, n_raw=n_raw)
+        want, _ = oracle.attention(L, wl.q, wl.k_raw[:n_raw], wl.v_raw[:n_raw], wl.k_comp[:n_comp],
+                                   wl.v_comp[:n_comp])
+        o = ds4a.attn_decode(L, d["q"], d["k_raw"], d["v_raw"], d["k_comp"], d["v_comp"], n_splits=3)
+        assert_close(host(o), want, f"decode n_comp={n_comp} n_raw={n_raw}")
+        o = ds4a.attn_prefill(L, d["q"], d["k_raw"], d["v_raw"], d["k_comp"], d["v_comp"])
+        assert_close(host(o), want, f"prefill n_comp={n_comp} n_raw={n_raw}")
+
+
 def test_decode_several_tokens(torch, ds4a):
     L = make_layout(T=3, q_pos0=5000, n_raw=200, raw_pos0=4850, n_comp=39, ratio=128)
     wl = W.draw("dec3", 67, L)
