@@ -271,6 +271,7 @@ ds4a_status prefill_pairs(const ds4a_layout *L, const ds4a_tensors *X, DeviceSta
     ds4a_status st = encode(&p.tm_q2, X->q, 3, dims, strides, box);
     if (st != DS4A_OK) return st;
   }
+
   ds4a_status st = encode_rows(&p.tm_k, X->k_raw, L->n_raw, X->raw_row_stride, 128);
   if (st == DS4A_OK) st = encode_rows(&p.tm_v, X->v_raw, L->n_raw, X->raw_row_stride, 128);
   if (st != DS4A_OK) return st;
@@ -285,6 +286,7 @@ ds4a_status prefill_pairs(const ds4a_layout *L, const ds4a_tensors *X, DeviceSta
   p.raw_row_stride = X->raw_row_stride;
   p.o = static_cast<__half *>(X->o);
   p.o_tok_stride = X->o_tok_stride / 2;
+  p.o_v8 = (aligned(X->o, 32) && X->o_tok_stride % 32 == 0) ? 1 : 0;
   p.lse = X->lse;
   p.timeout_ns = kDefaultTimeoutNs;
   p.err = d->err;

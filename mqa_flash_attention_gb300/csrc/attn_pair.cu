@@ -11,26 +11,42 @@
 // the earlier token's one remaining row (below the tile) is folded in on the
 // CUDA cores.  Every K/V row then enters the SM once per two tokens (Q 64 KB
 // + K 64 KB + V 64 KB per token instead of 64 + 128 + 128), and both
-// products run as N = 128 MMAs (two tokens x 64 heads), at the tensor core's
-// full rate where a single token's N = 64 runs near half of it:
-//   S^T[128 rows][128]      = K_tile[128][512] . Q_pair[128][512]^T   (K-major A, K-major B)
-//   O^T_m[128 dims][128]    = V_tile^T[dims 128m..][128] . P^T          (MN-major A, MN-major B)
-// TMEM: two S^T buffers (columns 0-127 and 128-255, by pair parity) and two
-// 128-column O^T buffers (256-383 and 384-511) through which the four 128-dim
-// blocks of a pair's O^T pass, drained by the epilogue as they complete; no
-// block accumulates across tiles (the pair has one tile).  With two S^T
-// buffers the QK^T of the next pair runs while the softmax reads this one.
+// products run as N = 128 MMAs at the tensor core's full rate, with the
+// pair's 128 query rows (two tokens x 64 heads) on the M side:
+//   S[128 q][128 rows]      = Q_pair[128][512] . K_tile[128][512]^T        (K-major A and B, shared memory)
+//   O_m[128 q][128 dims]    = P[128 q][128 rows] . V_tile[rows][dims 128m..] (A = P in tensor memory, MN-major B)
+// A query row lives in one TMEM lane, so its softmax needs no exchange
+// between threads: the thread that owns the lane reads the row's 128 scores,
+// writes the row of P (fp16, two per 32-bit column) over the first 64
+// columns of the same S buffer, and PV takes P from there as its A operand.
+// TMEM: two S buffers (columns 0-127 and 128-255, by pair parity; a buffer is
+// free again once the pair's PV has read its P) and two 128-column O buffers
+// (256-383 and 384-511) through which the four 128-dim blocks of a pair's O
+// pass, drained by the epilogue as they complete; no block accumulates across
+// tiles (the pair has one tile).  With two S buffers the QK^T of the next
+// pair runs while the softmax reads this one.
 //
 // Shared memory: a ring of 10 slots of 16 KB through which every box streams
 // in the order the MMAs take them: the Q and K boxes of pair 0, then for each
 // pair n the Q and K boxes of pair n+1 (Q box b, K box b for b = 0..7) before
 // the V boxes of pair n (0..7; a PV block takes two adjacent V slots), so the
 // next pair's loads are not queued behind V boxes that wait for this pair's
-// softmax.  Also P^T of a pair (32 KB), the extra row's K and V (two 2 KB
-// buffers, by pair parity) and bookkeeping.
+// softmax.  Also the extra row's K and V (two 2 KB buffers, by pair parity)
+// and bookkeeping; P needs no shared memory.  (12 slots ran no faster.)
+//
+// Measured against the earlier form of this kernel (S^T with the rows on the
+// lanes, the softmax reducing over lanes and warps, P^T in shared memory, the
+// eight compute warps doing softmax and epilogue in turn): 66.7 -> 64.0 us for
+// the 2048-token chunk.  The output stores are what remains: without them
+// the same kernel takes 57.5 us.  Each epilogue thread owns a (token, head)
+// row of o, so a warp's store touches 32 rows; 32-byte stores
+// (st.global.v8) halve the transactions of 16-byte ones (72.0 us), and
+// staging the rows in shared memory for TMA stores cost more than it saved
+// (66.9-69.3 us: the staging writes, proxy fences and barriers).
 // Warp roles (352 threads):
-//   warps 0-7  softmax + epilogue; thread (TMEM lane quarter w % 4, token w / 4)
-//              handles one row (or dim) and that token's 64 heads in two halves
+//   warps 0-3  softmax: thread 32w + l owns query row r = 32w + l (token r / 64,
+//              head r % 64) in TMEM lane r
+//   warps 4-7  epilogue: thread 32(w-4) + l drains row r of each O block
 //   warp  8    loader (one thread issues every TMA copy)
 //   warp  9    TMEM allocator and tcgen05.mma issuer
 //   warp 10    extra row: reads its K and V rows (one pair ahead) and takes
@@ -54,8 +70,9 @@
 namespace ds4a {
 namespace {
 
-constexpr int kPWarps = 8;
-constexpr int kPThreadsC = 32 * kPWarps;
+constexpr int kPSoftWarps = 4;    // warps 0-3
+constexpr int kPEpiWarp0 = 4;     // warps 4-7
+constexpr int kPRowThreads = 128;  // one thread per query row in each of the two roles
 constexpr int kPLoaderWarp = 8;
 constexpr int kPMmaWarp = 9;
 constexpr int kPXWarp = 10;
@@ -64,21 +81,18 @@ constexpr int kPSlots = 10;
 constexpr uint32_t kPSlot = 16384;
 constexpr int kPSlotsPerPair = 24;  // 8 Q + 8 K + 8 V boxes
 constexpr uint32_t kPOffRing = 0;
-constexpr uint32_t kPOffP = kPSlots * kPSlot;      // P^T: token a's box, then token b's
-constexpr uint32_t kPOffX = kPOffP + 2 * kPSlot;   // extra rows by pair parity: K [512] fp16, then V [512]
+constexpr uint32_t kPOffX = kPSlots * kPSlot;  // extra rows by pair parity: K [512] fp16, then V [512]
 constexpr uint32_t kPOffMisc = kPOffX + 2 * 2048;
 static_assert(kPSlots % 2 == 0 && kPSlotsPerPair % 2 == 0, "V slot pairs must stay adjacent in the ring");
 
 struct PairMisc {
-  alignas(16) float red[4][128];  // per lane quarter: partial max, then partial sum, of each column
-  alignas(16) float m_use[128];   // reference max of each column (log2 units), 0 when nothing is visible
-  alignas(16) float m_true[128];  // the max itself (-inf when nothing is visible)
-  alignas(16) float inv_l[128];
-  alignas(16) float sx[2][64];    // extra row, by pair parity: scaled score of token a per head (log2 units)
-  alignas(16) float px[64];       // extra row: its weight
+  alignas(16) float inv_l[2][128];  // by pair parity: 1 / row sum of each query row (0 when nothing is visible)
+  alignas(16) float px[2][64];      // by pair parity: token a's extra-row weight per head
+  alignas(16) float sx[2][64];      // extra row, by pair parity: scaled score of token a per head (log2 units)
   alignas(8) uint64_t full[kPSlots], empty[kPSlots];
-  uint64_t s_full[2], s_empty[2], p_full, p_empty, o_full[2], o_empty[2], mma_done;
-  uint64_t x_full[2], x_empty[2]; // by pair parity: extra-row scores ready; the row buffer free again
+  uint64_t s_full[2], s_empty[2], p_full[2], o_full[2], o_empty[2], mma_done;  // p_full by pair parity
+  uint64_t x_full[2], x_empty[2];  // by pair parity: extra-row scores ready; the row buffer free again
+  uint64_t st_full[2], st_empty[2];  // by pair parity: inv_l / px written; read by the epilogue
   uint64_t qx[8];                 // Q box b of the current pair has landed (passed on by the MMA thread)
   uint64_t xdone[8];              // the extra-row warp is done with Q box b of its current pair
   uint32_t tmem_base;
@@ -89,7 +103,8 @@ static_assert(kPSmemBytes <= 232448, "pair kernel shared memory");
 
 enum : unsigned int {
   SITE_PR_EMPTY = 0x20, SITE_PR_FULL, SITE_PR_S_EMPTY, SITE_PR_S_FULL, SITE_PR_P_FULL, SITE_PR_P_EMPTY,
-  SITE_PR_O_EMPTY, SITE_PR_O_FULL, SITE_PR_DRAIN, SITE_PR_X_FULL, SITE_PR_X_EMPTY
+  SITE_PR_O_EMPTY, SITE_PR_O_FULL, SITE_PR_DRAIN, SITE_PR_X_FULL, SITE_PR_X_EMPTY, SITE_PR_ST_FULL,
+  SITE_PR_ST_EMPTY
 };
 
 // The pair's tokens and rows.  Token a = 2 * pair, token b = a + 1 (absent for
@@ -134,7 +149,7 @@ __device__ __forceinline__ uint32_t slot_addr(uint32_t sbase, uint32_t sl) {
   return sbase + kPOffRing + (sl % kPSlots) * kPSlot;
 }
 __device__ __forceinline__ uint32_t slot_phase(uint32_t sl) { return (sl / kPSlots) & 1u; }
-// TMEM columns: S^T of pair parity i at 128 i; O^T block m in buffer m & 1 at 256 + 128 (m & 1).
+// TMEM columns: S (then P) of pair parity i at 128 i; O block m in buffer m & 1 at 256 + 128 (m & 1).
 __device__ __forceinline__ uint32_t s_column(uint32_t n) { return 128u * (n & 1u); }
 __device__ __forceinline__ uint32_t o_column(int m) { return 256u + 128u * (m & 1); }
 
@@ -198,12 +213,26 @@ __device__ __forceinline__ void pair_loader(const PairParams &p, uint32_t sbase,
 
 // ------------------------------------------------------------------ MMA issuer
 
-// QK^T of the CTA's pair j into S^T buffer j & 1, from the pair's 16 Q and K
-// slots starting at `sl`.
+// D(tmem) (+)= A(tmem) * B(smem desc)^T: A in tensor memory, row i of A in
+// lane i of the 128 lanes, K packed along the 32-bit columns (two fp16 values
+// per column, the lower K index in the low half).
+__device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// QK^T of the CTA's pair j into S buffer j & 1 (query rows on the lanes), from
+// the pair's 16 Q and K slots starting at `sl`.  The buffer is free once the
+// PV of pair j - 2 has read the P written over it.
 __device__ __forceinline__ bool pair_qk(const PairParams &p, uint32_t sbase, uint32_t tmem, PairMisc &ms,
                                         volatile int *abrt, uint32_t j, uint32_t &sl) {
   constexpr uint32_t kIdescQK = idesc_f16_f32(128, 128, false, false);
-  // K and Q boxes: K-major, SBO = one 8-row group.
+  // Q and K boxes: K-major, SBO = one 8-row group.
   const uint64_t kq_desc = sdesc_sw128(sbase + kPOffRing, 16, 1024);
   if (!mbar_wait(smem_u32(&ms.s_empty[j & 1]), ((j >> 1) & 1) ^ 1, abrt, p.timeout_ns, p.err, SITE_PR_S_EMPTY))
     return false;
@@ -215,7 +244,7 @@ __device__ __forceinline__ bool pair_qk(const PairParams &p, uint32_t sbase, uin
         !mbar_wait(smem_u32(&ms.full[pk]), slot_phase(sl + 1), abrt, p.timeout_ns, p.err, SITE_PR_FULL))
       return false;
     tc_fence_after();
-    const uint64_t a0 = sdesc_add(kq_desc, pk * kPSlot), b0 = sdesc_add(kq_desc, pq * kPSlot);
+    const uint64_t a0 = sdesc_add(kq_desc, pq * kPSlot), b0 = sdesc_add(kq_desc, pk * kPSlot);
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks) {
       if (b == 0 && ks == 0)
@@ -236,16 +265,18 @@ __device__ __forceinline__ bool pair_qk(const PairParams &p, uint32_t sbase, uin
   return true;
 }
 
-// PV of the CTA's pair n once P^T is written: O^T block m into buffer m & 1
-// (after the epilogue drained block m - 2), from the V slots starting at `sl`.
+// PV of the CTA's pair n once P is written over its S buffer: O block m into
+// buffer m & 1 (after the epilogue drained block m - 2), from the V slots
+// starting at `sl`; then the S buffer is free for pair n + 2.
 __device__ __forceinline__ bool pair_pv(const PairParams &p, uint32_t sbase, uint32_t tmem, PairMisc &ms,
                                         volatile int *abrt, uint32_t n, uint32_t &sl) {
-  constexpr uint32_t kIdescPV = idesc_f16_f32(128, 128, true, true);
-  // V^T: MN-major, its two 64-dim atoms in adjacent slots (LBO = one slot).
-  // P^T: MN-major, token a's heads then token b's (LBO = one box).
+  constexpr uint32_t kIdescPV = idesc_f16_f32(128, 128, false, true);
+  // V: MN-major B (dims contiguous), its two 64-dim atoms in adjacent slots
+  // (LBO = one slot), 16 rows of K per MMA = two 8-row groups of 1024 bytes.
   const uint64_t v_desc = sdesc_sw128(sbase + kPOffRing, kPSlot, 1024);
-  const uint64_t p_desc = sdesc_sw128(sbase + kPOffP, kPSlot, 1024);
-  if (!mbar_wait(smem_u32(&ms.p_full), n & 1, abrt, p.timeout_ns, p.err, SITE_PR_P_FULL)) return false;
+  const uint32_t p_tmem = tmem + s_column(n);  // P: 64 columns, 8 per 16 rows of K
+  // By pair parity: the softmax of pair n + 1 may finish before this wait.
+  if (!mbar_wait(smem_u32(&ms.p_full[n & 1]), (n >> 1) & 1, abrt, p.timeout_ns, p.err, SITE_PR_P_FULL)) return false;
   tc_fence_after();
   for (int m = 0; m < 4; ++m, sl += 2) {
     const uint32_t gb = 4 * n + m, buf = gb & 1;
@@ -255,22 +286,17 @@ __device__ __forceinline__ bool pair_pv(const PairParams &p, uint32_t sbase, uin
         !mbar_wait(smem_u32(&ms.full[pb]), slot_phase(sl + 1), abrt, p.timeout_ns, p.err, SITE_PR_FULL))
       return false;
     tc_fence_after();
-    const uint64_t a0 = sdesc_add(v_desc, pa * kPSlot);
+    const uint64_t b0 = sdesc_add(v_desc, pa * kPSlot);
     const uint32_t d = tmem + o_column(m);
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      if (ks == 0)
-        umma_f16(d, a0, p_desc, kIdescPV, 0u);
-      else
-        umma_f16_acc(d, sdesc_add(a0, ks * 2048), sdesc_add(p_desc, ks * 2048), kIdescPV);
-    }
+    for (int ks = 0; ks < 8; ++ks) umma_f16_ts(d, p_tmem + 8 * ks, sdesc_add(b0, ks * 2048), kIdescPV, ks > 0);
     umma_commit(smem_u32(&ms.empty[pa]));
     umma_commit(smem_u32(&ms.empty[pb]));
     mbar_arrive(smem_u32(&ms.empty[pa]));
     mbar_arrive(smem_u32(&ms.empty[pb]));
     umma_commit(smem_u32(&ms.o_full[buf]));
   }
-  umma_commit(smem_u32(&ms.p_empty));
+  umma_commit(smem_u32(&ms.s_empty[n & 1]));
   return true;
 }
 
@@ -295,187 +321,179 @@ __device__ __forceinline__ void pair_mma(const PairParams &p, uint32_t sbase, ui
 
 // ------------------------------------------------------------------ softmax and epilogue
 
-// Lane l ends with the max (or sum) over the warp's 32 rows of column l of the
-// 32 columns held in s[0..31].
-template <bool kMax>
-__device__ __forceinline__ float reduce_scatter32(const float (&s)[32], int lane) {
-  float a[16];
-  {
-    const bool up = lane & 16;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const float send = up ? s[i] : s[i + 16];
-      const float keep = up ? s[i + 16] : s[i];
-      const float got = __shfl_xor_sync(0xffffffffu, send, 16);
-      a[i] = kMax ? fmaxf(keep, got) : keep + got;
-    }
+// The visible columns [c0, c1) of a query row of token tau in the pair's tile.
+__device__ __forceinline__ void visible_columns(const PairGeom &g, int tau, int &c0, int &c1) {
+  if (tau == 1 && !g.has_b) {
+    c0 = c1 = 0;
+    return;
   }
-#pragma unroll
-  for (int c = 16; c >= 2; c >>= 1) {
-    const int half = c / 2;
-    const bool up = lane & half;
-#pragma unroll
-    for (int i = 0; i < half; ++i) {
-      const float send = up ? a[i] : a[i + half];
-      const float keep = up ? a[i + half] : a[i];
-      const float got = __shfl_xor_sync(0xffffffffu, send, half);
-      a[i] = kMax ? fmaxf(keep, got) : keep + got;
-    }
-  }
-  return a[0];
+  c0 = max(g.lo[tau] - g.tile_lo, 0);
+  c1 = min(g.hi[tau] - g.tile_lo, 128);
+  if (c1 < c0) c1 = c0;
 }
 
-__device__ __forceinline__ void csync() { asm volatile("bar.sync 1, %0;" ::"n"(kPThreadsC) : "memory"); }
-
-__device__ __forceinline__ void pair_compute(const PairParams &p, uint8_t *smem, uint32_t tmem, PairMisc &ms,
-                                             int tid) {
+// Warps 0-3: thread r owns query row r (token tau = r / 64, head h = r % 64)
+// in TMEM lane r.  Pass 1 takes the row's maximum over its visible scores
+// (and token a's extra-row score), pass 2 writes P = 2^(s - m) in fp16 over
+// the first 64 columns of the S buffer (columns 32u .. 32u+31 hold rows
+// 64u .. 64u+63 of the tile, two per column) and sums the same fp16 values.
+// A thread rewrites only its own lane, and only columns it has already read.
+__device__ __forceinline__ void pair_softmax(const PairParams &p, uint32_t tmem, PairMisc &ms, int r) {
   volatile int *abrt = &ms.abort_flag;
-  const int w = tid >> 5, l = tid & 31;
-  const int q = w & 3;       // TMEM lane quarter: rows (or dims) 32q .. 32q+31
-  const int tau = w >> 2;    // token of the pair whose columns this thread takes
-  const int r = 32 * q + l;  // this thread's TMEM lane
-  const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+  const int tau = r >> 6, h = r & 63;
+  const uint32_t lane_base = static_cast<uint32_t>(r & ~31) << 16;
   const int n_pairs = (p.T + 1) / 2;
   uint32_t n = 0;
-  bool bad = false;
+  grid_dependency_wait();  // lse may still be read by the previous kernel
+  for (int pr = blockIdx.x; pr < n_pairs; pr += gridDim.x, ++n) {
+    const PairGeom g = pair_geom(p, pr);
+    int c0, c1;
+    visible_columns(g, tau, c0, c1);
+    const bool with_x = tau == 0 && g.extra;
+    // The extra-row warp's scores of this pair (every pair, so the phases
+    // stay in step), then the pair's S.
+    // (Decisions to leave are made per warp: the TMEM accesses below are
+    // warp-collective.)
+    const bool ready =
+        mbar_wait(smem_u32(&ms.x_full[n & 1]), (n >> 1) & 1, abrt, p.timeout_ns, p.err, SITE_PR_X_FULL) &&
+        mbar_wait(smem_u32(&ms.s_full[n & 1]), (n >> 1) & 1, abrt, p.timeout_ns, p.err, SITE_PR_S_FULL);
+    if (!__all_sync(0xffffffffu, ready)) break;
+    tc_fence_after();
+    const uint32_t sb = tmem + s_column(n) + lane_base;
+    const float sxv = with_x ? ms.sx[n & 1][h] : -INFINITY;
+    float mx = sxv;
+#pragma unroll 1
+    for (int u = 0; u < 2; ++u) {
+      float s[64];
+      tmem_ld64(sb + 64 * u, s);
+      tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        const int col = 64 * u + c;
+        if (col >= c0 && col < c1) mx = fmaxf(mx, s[c] * p.scale_log2);
+      }
+    }
+    const float mu = mx == -INFINITY ? 0.f : mx;
+    float lsum = 0.f;
+#pragma unroll 1
+    for (int u = 0; u < 2; ++u) {
+      float s[64];
+      tmem_ld64(sb + 64 * u, s);
+      tmem_wait_ld();
+      float pk[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int col = 64 * u + 2 * i;
+        const float e0 = (col >= c0 && col < c1) ? exp2f(s[2 * i] * p.scale_log2 - mu) : 0.f;
+        const float e1 = (col + 1 >= c0 && col + 1 < c1) ? exp2f(s[2 * i + 1] * p.scale_log2 - mu) : 0.f;
+        const __half2 hp = __floats2half2_rn(e0, e1);
+        const float2 f = __half22float2(hp);
+        lsum += f.x + f.y;
+        pk[i] = __uint_as_float(*reinterpret_cast<const uint32_t *>(&hp));
+      }
+      tmem_st32(sb + 32 * u, pk);
+    }
+    tmem_wait_st();
+    tc_fence_before();
+    mbar_arrive(smem_u32(&ms.p_full[n & 1]));
+    float px = 0.f;
+    if (with_x) {
+      px = exp2f(sxv - mu);
+      lsum += px;
+    }
+    // Row statistics for the epilogue, once it is done with this parity's
+    // previous pair.
+    const bool free_st =
+        mbar_wait(smem_u32(&ms.st_empty[n & 1]), ((n >> 1) & 1) ^ 1, abrt, p.timeout_ns, p.err, SITE_PR_ST_EMPTY);
+    if (!__all_sync(0xffffffffu, free_st)) break;
+    ms.inv_l[n & 1][r] = lsum > 0.f ? 1.f / lsum : 0.f;
+    if (tau == 0) ms.px[n & 1][h] = px;
+    mbar_arrive(smem_u32(&ms.st_full[n & 1]));
+    if (p.lse != nullptr && (tau == 0 || g.has_b))
+      p.lse[(long long)(g.ta + tau) * kH + h] = lsum > 0.f ? (mx + log2f(lsum)) * kLn2 : -INFINITY;
+  }
+}
+
+// 32 bytes to global memory (the address 32-byte aligned).
+__device__ __forceinline__ void stg_v8(void *p, const uint32_t (&w)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+               "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
+// Warps 4-7: thread r drains query row r of each O block [128 q][128 dims]
+// as the PV completes it, scales it by 1 / l (adding token a's extra row,
+// weight px times the V row) and writes the block's 128 dims (256 bytes) of
+// its (token, head) row of o, 32 bytes per store when o allows it.
+__device__ __forceinline__ void pair_epilogue(const PairParams &p, uint8_t *smem, uint32_t tmem, PairMisc &ms,
+                                              int r) {
+  volatile int *abrt = &ms.abort_flag;
+  const int tau = r >> 6, h = r & 63;
+  const uint32_t lane_base = static_cast<uint32_t>(r & ~31) << 16;
+  const int n_pairs = (p.T + 1) / 2;
+  uint32_t n = 0;
   grid_dependency_wait();  // the outputs may still be read by the previous kernel
   for (int pr = blockIdx.x; pr < n_pairs; pr += gridDim.x, ++n) {
     const PairGeom g = pair_geom(p, pr);
     const bool has_tok = tau == 0 || g.has_b;
-    const float *sx = ms.sx[n & 1];
+    const bool with_x = tau == 0 && g.extra;
     const __half *vx = reinterpret_cast<const __half *>(smem + kPOffX + 2048 * (n & 1)) + 512;
-    // The extra-row warp's scores of this pair (every pair, so the phases
-    // stay in step).
-    bad = bad || !mbar_wait(smem_u32(&ms.x_full[n & 1]), (n >> 1) & 1, abrt, p.timeout_ns, p.err, SITE_PR_X_FULL);
-
-    // Softmax of the pair's tile.  Pass 1: column maxima.
-    bad = bad || !mbar_wait(smem_u32(&ms.s_full[n & 1]), (n >> 1) & 1, abrt, p.timeout_ns, p.err, SITE_PR_S_FULL);
-    tc_fence_after();
-    const int row = g.tile_lo + r;
-    const bool vis = has_tok && row >= g.lo[tau] && row < g.hi[tau];
-#pragma unroll 1
-    for (int u = 0; u < 2; ++u) {
-      float s[32];
-      tmem_ld32(tmem + s_column(n) + 64 * tau + 32 * u + lane_base, s);
-      tmem_wait_ld();
-#pragma unroll
-      for (int h = 0; h < 32; ++h) s[h] = vis ? s[h] * p.scale_log2 : -INFINITY;
-      ms.red[q][64 * tau + 32 * u + l] = reduce_scatter32<true>(s, l);
-    }
-    if (bar_red_or(1, kPThreadsC, bad)) break;
-    if (tid < 128) {
-      const int tt = tid >> 6, h = tid & 63;
-      float mx = fmaxf(fmaxf(ms.red[0][tid], ms.red[1][tid]), fmaxf(ms.red[2][tid], ms.red[3][tid]));
-      if (tt == 0 && g.extra) mx = fmaxf(mx, sx[h]);
-      ms.m_true[tid] = mx;
-      ms.m_use[tid] = mx == -INFINITY ? 0.f : mx;
-    }
-    csync();
-    // Pass 2: P = 2^(s - m) in fp16 (P^T row r of token tau's box, 16-byte
-    // chunk c at c ^ (r & 7): the 128-byte swizzle) and the row sums of the
-    // same fp16 values.  P may be rewritten once the previous pair's PV is done.
-    bad = bad || !mbar_wait(smem_u32(&ms.p_empty), (n & 1) ^ 1, abrt, p.timeout_ns, p.err, SITE_PR_P_EMPTY);
-    uint8_t *prow = smem + kPOffP + tau * kPSlot + r * 128;
-#pragma unroll 1
-    for (int u = 0; u < 2; ++u) {
-      float s[32];
-      tmem_ld32(tmem + s_column(n) + 64 * tau + 32 * u + lane_base, s);
-      tmem_wait_ld();
-      const float *mu = ms.m_use + 64 * tau + 32 * u;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t w4[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int h = 8 * c + 2 * i;
-          const float e0 = vis ? exp2f(s[h] * p.scale_log2 - mu[h]) : 0.f;
-          const float e1 = vis ? exp2f(s[h + 1] * p.scale_log2 - mu[h + 1]) : 0.f;
-          const __half2 hp = __floats2half2_rn(e0, e1);
-          const float2 f = __half22float2(hp);
-          s[h] = f.x;
-          s[h + 1] = f.y;
-          w4[i] = *reinterpret_cast<const uint32_t *>(&hp);
-        }
-        const int chunk = 4 * u + c;
-        *reinterpret_cast<uint4 *>(prow + ((chunk ^ (r & 7)) << 4)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-      }
-      ms.red[q][64 * tau + 32 * u + l] = reduce_scatter32<false>(s, l);
-    }
-    tc_fence_before();
-    mbar_arrive(smem_u32(&ms.s_empty[n & 1]));  // S^T read for the last time
-    fence_proxy_async_smem();
-    mbar_arrive(smem_u32(&ms.p_full));
-    if (bar_red_or(1, kPThreadsC, bad)) break;
-    if (tid < 128) {
-      const int tt = tid >> 6, h = tid & 63;
-      float lsum = ms.red[0][tid] + ms.red[1][tid] + ms.red[2][tid] + ms.red[3][tid];
-      if (tt == 0 && g.extra) {
-        const float px = exp2f(sx[h] - ms.m_use[tid]);
-        ms.px[h] = px;
-        lsum += px;
-      }
-      ms.inv_l[tid] = lsum > 0.f ? 1.f / lsum : 0.f;
-      if (p.lse != nullptr && (tt == 0 || g.has_b))
-        p.lse[(long long)(g.ta + tt) * kH + h] = lsum > 0.f ? (ms.m_true[tid] + log2f(lsum)) * kLn2 : -INFINITY;
-    }
-    csync();
-
-    // Epilogue: O^T block m [128 dims][128] -> o of both tokens, as each
-    // block completes.  Lanes 2k and 2k+1 hold adjacent dims: for each pair
-    // of heads they swap one value, so the even lane writes both dims of the
-    // first head and the odd lane both dims of the second (32-bit stores).
-    const bool odd = l & 1;
-    const bool with_x = tau == 0 && g.extra;  // token a folds in its extra row
-    __half *obase = p.o + (long long)(g.ta + tau) * p.o_tok_stride + (r & ~1);
+    const bool ready =
+        mbar_wait(smem_u32(&ms.st_full[n & 1]), (n >> 1) & 1, abrt, p.timeout_ns, p.err, SITE_PR_ST_FULL);
+    if (!__all_sync(0xffffffffu, ready)) break;  // per warp: the TMEM loads are warp-collective
+    const float il = ms.inv_l[n & 1][r];
+    const float px = with_x ? ms.px[n & 1][h] : 0.f;
+    __half *orow = p.o + (long long)(g.ta + tau) * p.o_tok_stride + (long long)h * kD;
+    bool bad = false;
 #pragma unroll 1
     for (int m = 0; m < 4; ++m) {
       const uint32_t gb = 4 * n + m;
-      bad = bad || !mbar_wait(smem_u32(&ms.o_full[m & 1]), (gb >> 1) & 1, abrt, p.timeout_ns, p.err, SITE_PR_O_FULL);
+      const bool done =
+          mbar_wait(smem_u32(&ms.o_full[m & 1]), (gb >> 1) & 1, abrt, p.timeout_ns, p.err, SITE_PR_O_FULL);
+      if (!__all_sync(0xffffffffu, done)) {
+        bad = true;
+        break;
+      }
       tc_fence_after();
-      const float xv = with_x ? __half2float(vx[128 * m + r]) : 0.f;
-      // Both halves of the block leave TMEM before the buffer is handed back,
-      // so the next PV into it need not wait for the stores.
-      float o[2][32];
-      tmem_ld32(tmem + o_column(m) + 64 * tau + lane_base, o[0]);
-      tmem_ld32(tmem + o_column(m) + 64 * tau + 32 + lane_base, o[1]);
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(smem_u32(&ms.o_empty[m & 1]));  // the buffer may take block m + 2
-      if (has_tok) {
+#pragma unroll 1
+      for (int u = 0; u < 2; ++u) {
+        float o[64];
+        tmem_ld64(tmem + o_column(m) + 64 * u + lane_base, o);
+        tmem_wait_ld();
+        if (u == 1) {
+          tc_fence_before();
+          mbar_arrive(smem_u32(&ms.o_empty[m & 1]));  // the buffer may take block m + 2
+        }
+        if (!has_tok) continue;
+        const int d0 = 128 * m + 64 * u;
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const float4 *iv4 = reinterpret_cast<const float4 *>(ms.inv_l + 64 * tau + 32 * u);
-          if (with_x) {
-            const float4 *px4 = reinterpret_cast<const float4 *>(ms.px + 32 * u);
+        for (int c = 0; c < 4; ++c) {
+          uint32_t w8[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const float4 iv = iv4[j], px = px4[j];
-              o[u][4 * j] = fmaf(px.x, xv, o[u][4 * j]) * iv.x;
-              o[u][4 * j + 1] = fmaf(px.y, xv, o[u][4 * j + 1]) * iv.y;
-              o[u][4 * j + 2] = fmaf(px.z, xv, o[u][4 * j + 2]) * iv.z;
-              o[u][4 * j + 3] = fmaf(px.w, xv, o[u][4 * j + 3]) * iv.w;
+          for (int i = 0; i < 8; ++i) {
+            const int e = 16 * c + 2 * i;
+            float a = o[e], b = o[e + 1];
+            if (with_x) {
+              const float2 v = __half22float2(*reinterpret_cast<const __half2 *>(vx + d0 + e));
+              a = fmaf(px, v.x, a);
+              b = fmaf(px, v.y, b);
             }
-          } else {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const float4 iv = iv4[j];
-              o[u][4 * j] *= iv.x;
-              o[u][4 * j + 1] *= iv.y;
-              o[u][4 * j + 2] *= iv.z;
-              o[u][4 * j + 3] *= iv.w;
-            }
+            const __half2 hv = __floats2half2_rn(a * il, b * il);
+            w8[i] = *reinterpret_cast<const uint32_t *>(&hv);
           }
-#pragma unroll
-          for (int h = 0; h < 32; h += 2) {
-            const float got = __shfl_xor_sync(0xffffffffu, odd ? o[u][h] : o[u][h + 1], 1);
-            const __half2 v = odd ? __floats2half2_rn(got, o[u][h + 1]) : __floats2half2_rn(o[u][h], got);
-            *reinterpret_cast<__half2 *>(obase + (32 * u + h + (odd ? 1 : 0)) * kD + 128 * m) = v;
+          __half *dst = orow + d0 + 16 * c;
+          if (p.o_v8) {
+            stg_v8(dst, w8);
+          } else {
+            reinterpret_cast<uint4 *>(dst)[0] = make_uint4(w8[0], w8[1], w8[2], w8[3]);
+            reinterpret_cast<uint4 *>(dst)[1] = make_uint4(w8[4], w8[5], w8[6], w8[7]);
           }
         }
       }
     }
-    if (bar_red_or(1, kPThreadsC, bad)) break;
-    if (tid == 0) mbar_arrive(smem_u32(&ms.x_empty[n & 1]));  // every thread is done with this parity's rows
+    if (bad) break;
+    mbar_arrive(smem_u32(&ms.st_empty[n & 1]));
+    mbar_arrive(smem_u32(&ms.x_empty[n & 1]));  // done with this parity's extra V row
   }
 }
 
@@ -582,21 +600,21 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_pair_kernel(const __grid_co
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&ms.s_full[b]), 1);
-      mbar_init(smem_u32(&ms.s_empty[b]), kPThreadsC);
+      mbar_init(smem_u32(&ms.s_empty[b]), 1);
       mbar_init(smem_u32(&ms.o_full[b]), 1);
-      mbar_init(smem_u32(&ms.o_empty[b]), kPThreadsC);
+      mbar_init(smem_u32(&ms.o_empty[b]), kPRowThreads);
       mbar_init(smem_u32(&ms.x_full[b]), 1);
-      mbar_init(smem_u32(&ms.x_empty[b]), 1);
+      mbar_init(smem_u32(&ms.x_empty[b]), kPRowThreads);
+      mbar_init(smem_u32(&ms.st_full[b]), kPRowThreads);
+      mbar_init(smem_u32(&ms.st_empty[b]), kPRowThreads);
     }
-    mbar_init(smem_u32(&ms.p_full), kPThreadsC);
-    mbar_init(smem_u32(&ms.p_empty), 1);
+    for (int b = 0; b < 2; ++b) mbar_init(smem_u32(&ms.p_full[b]), kPRowThreads);
     mbar_init(smem_u32(&ms.mma_done), 1);
     for (int b = 0; b < 8; ++b) {
       mbar_init(smem_u32(&ms.qx[b]), 1);
       mbar_init(smem_u32(&ms.xdone[b]), 1);
     }
     ms.abort_flag = 0;
-    for (int i = 0; i < 64; ++i) ms.px[i] = 0.f;
     fence_barrier_init();
   }
   if (warp == kPMmaWarp) {
@@ -613,8 +631,10 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_pair_kernel(const __grid_co
   tc_fence_after();
   const uint32_t tmem = ms.tmem_base;
   grid_launch_dependents();
-  if (warp < kPWarps) {
-    pair_compute(p, smem, tmem, ms, threadIdx.x);
+  if (warp < kPSoftWarps) {
+    pair_softmax(p, tmem, ms, threadIdx.x);
+  } else if (warp < kPEpiWarp0 + 4) {
+    pair_epilogue(p, smem, tmem, ms, threadIdx.x - 32 * kPEpiWarp0);
   } else if (warp == kPLoaderWarp) {
     if (lane == 0) pair_loader(p, sbase, ms);
     __syncwarp();

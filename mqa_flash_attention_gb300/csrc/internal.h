@@ -28,6 +28,7 @@ struct PairParams {
   long long raw_row_stride;      // bytes
   __half *o;
   long long o_tok_stride;        // elements
+  int o_v8;                      // o and its token stride are 32-byte aligned: 32-byte stores
   float *lse;
   unsigned long long timeout_ns;
   unsigned int *err;

@@ -246,6 +246,26 @@ def test_prefill_pairs_strided(torch, ds4a):
     assert bool((obig[:, 64:] == 7.0).all()), "a write landed outside the output rows"
 
 
+def test_prefill_pairs_output_16_byte_aligned(torch, ds4a):
+    """The pair path writes o with 32-byte stores when o and its token stride
+    allow them, else with 16-byte ones: here o starts 16 bytes past a 32-byte
+    boundary and its token stride is an odd multiple of 16 bytes."""
+    L = make_layout(T=7, q_pos0=400, n_raw=300, raw_pos0=200)
+    wl = W.draw("pairs_o16", 98, L)
+    tok = 64 * 512 + 24                      # elements: 65,584 bytes per token
+    flat = torch.full((8 + 7 * tok,), 7.0, dtype=torch.float16, device="cuda")
+    out = torch.as_strided(flat, (7, 64, 512), (tok, 512, 1), storage_offset=8)
+    assert out.data_ptr() % 32 == 16 and (tok * 2) % 32 == 16
+    d = upload(torch, wl)
+    ds4a.attn_prefill(L, d["q"], d["k_raw"], d["v_raw"], out=out)
+    want, _ = oracle_out(wl)
+    assert_close(host(out.contiguous()), want, "pairs, 16-byte aligned o")
+    mask = torch.ones_like(flat, dtype=torch.bool)
+    for t in range(7):
+        mask[8 + t * tok: 8 + t * tok + 64 * 512] = False
+    assert bool((flat[mask] == 7.0).all()), "a write landed outside the output rows"
+
+
 def test_prefill_strided_tokens_and_rows(torch, ds4a):
     """Q/O token strides and K/V row strides larger than the packed ones."""
     L = make_layout(T=6, q_pos0=150, n_raw=160, raw_pos0=0, n_comp=40, ratio=4)
