@@ -489,10 +489,17 @@ ds4a_status ds4a_device_status(ds4a_stream_t stream, int clear);
 /*
  * ds4a_device_error_word - like ds4a_device_status, but returns the raw error
  * word in *word (0 = no error).  For a wait that ran out the word is
- * 0x01000000 | site, where site names the barrier that was waited on (1 Q
- * buffer free, 2 K/V stage free, 3 Q loaded, 4 S buffer free, 5 K/V stage
- * loaded, 6 P written, 7 O read, 8 S computed, 9 P consumed, 10 O complete,
- * 11 draining copies, 12 self test).  clear != 0 resets the word.
+ * 0x01000000 | site, where site names the barrier that was waited on.
+ * Attention kernel: 1 Q buffer free, 2 K/V stage free, 3 Q loaded, 4 S buffer
+ * free, 5 K/V stage loaded, 6 P written, 7 O read, 8 S computed, 9 P consumed,
+ * 10 O complete, 11 draining copies, 12 self test.  Raw-prefill pair kernel:
+ * 0x20 ring slot free, 0x21 ring slot loaded, 0x22 S buffer free, 0x23 S
+ * computed, 0x24 P written, 0x26 O buffer drained, 0x27 O block complete,
+ * 0x28 draining copies, 0x29 extra-row scores ready, 0x2A extra-row buffer or
+ * Q box free, 0x2B row statistics ready, 0x2C row statistics read.  Indexer
+ * scores: 0x40 q free, 0x41 k stage free, 0x42 q loaded, 0x43 accumulator
+ * free, 0x44 k stage loaded, 0x45 accumulator complete, 0x46 draining.
+ * clear != 0 resets the word.
  */
 ds4a_status ds4a_device_error_word(ds4a_stream_t stream, uint32_t *word, int clear);
 

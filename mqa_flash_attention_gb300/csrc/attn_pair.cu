@@ -102,7 +102,8 @@ constexpr uint32_t kPSmemBytes = kPOffMisc + ((sizeof(PairMisc) + 127) / 128) * 
 static_assert(kPSmemBytes <= 232448, "pair kernel shared memory");
 
 enum : unsigned int {
-  SITE_PR_EMPTY = 0x20, SITE_PR_FULL, SITE_PR_S_EMPTY, SITE_PR_S_FULL, SITE_PR_P_FULL, SITE_PR_P_EMPTY,
+  SITE_PR_EMPTY = 0x20, SITE_PR_FULL, SITE_PR_S_EMPTY, SITE_PR_S_FULL, SITE_PR_P_FULL,
+  SITE_PR_P_EMPTY,  // (no longer waited on: P lives in its S buffer)
   SITE_PR_O_EMPTY, SITE_PR_O_FULL, SITE_PR_DRAIN, SITE_PR_X_FULL, SITE_PR_X_EMPTY, SITE_PR_ST_FULL,
   SITE_PR_ST_EMPTY
 };
