@@ -812,7 +812,7 @@ def run_also(torch, ds4a, W, dev, stream, pk, pk_kind):
 # ------------------------------------------------------------------ profiling cases
 
 CASES = ("tiny", "decode_r128_32k", "prefill_raw_2048", "indexed_r4_2048", "decode_long_262144",
-         "indexer_r4_2048", "compressor_r4_2048", "compressor_r128_2048")
+         "decode_long_262144_fp8kv", "indexer_r4_2048", "compressor_r4_2048", "compressor_r128_2048")
 
 
 def run_case(name: str, calls: int) -> None:
@@ -844,6 +844,21 @@ def run_case(name: str, calls: int) -> None:
         for _ in range(calls):
             ds4a.compress_append(kv, sc, st_kv, st_s, 0, ratio)
         torch.cuda.synchronize()
+        print(f"{name}: {calls} calls ok")
+        return
+    if name == "decode_long_262144_fp8kv":
+        # the 262,144-row decode over E4M3 compressed rows (codes + one fp32 scale per row)
+        wl = W.decode_long(262144)
+        up = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
+        q, kr, vr = up(wl.q), up(wl.k_raw), up(wl.v_raw)
+        kc, ks = ds4a.quantize_kv_fp8(up(wl.k_comp))
+        vc, vs = ds4a.quantize_kv_fp8(up(wl.v_comp))
+        outs = [torch.empty_like(q) for _ in range(calls)]
+        for i in range(calls):
+            ds4a.attn_decode_fp8(wl.layout, q, kr, vr, kc, ks, vc, vs, out=outs[i])
+        torch.cuda.synchronize()
+        if ds4a.device_status() != ds4a.OK:
+            raise RuntimeError("device wait ran out")
         print(f"{name}: {calls} calls ok")
         return
     wl = W.decode_long(262144) if name == "decode_long_262144" else getattr(W, name)()
