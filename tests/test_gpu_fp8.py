@@ -206,3 +206,36 @@ def test_prefill_fp8kv(torch, ds4a, name):
     _check(host(o), want, f"prefill fp8kv {name}")
     fin = np.isfinite(wlse)
     assert np.abs(host(lse)[fin] - wlse[fin]).max() <= 1e-3
+
+
+# Raw-only layouts with a window of at most 128 and T >= 2 (the shapes the
+# fp16 prefill serves two tokens per tile): one pair with and without the
+# extra row, the extra row at row 0, tiles below row 0 with odd T, a short
+# window, rows ending before the tokens, more pairs than CTAs with an odd last
+# token.
+_PAIR_LAYOUTS = [
+    dict(T=2, q_pos0=500, n_raw=400, raw_pos0=200),
+    dict(T=2, q_pos0=127, n_raw=128, raw_pos0=0),
+    dict(T=2, q_pos0=127, n_raw=129, raw_pos0=0),
+    dict(T=7, q_pos0=60, n_raw=100, raw_pos0=0),
+    dict(T=9, q_pos0=400, n_raw=300, raw_pos0=250, window=37),
+    dict(T=6, q_pos0=1000, n_raw=40, raw_pos0=950),
+    dict(T=311, q_pos0=3000, n_raw=500, raw_pos0=2700),
+]
+
+
+@pytest.mark.parametrize("case", range(len(_PAIR_LAYOUTS)))
+def test_prefill_fp8kv_pairs(torch, ds4a, case):
+    """E4M3 raw rows on those layouts against the oracle over the decoded
+    rows; outputs and log-sum-exp start as NaN."""
+    wl = W.draw(f"fp8_pairs{case}", 120 + case, make_layout(**_PAIR_LAYOUTS[case]))
+    ops, want, wlse = _fp8kv_case(torch, wl, raw_fp8=True)
+    q = dev(torch, wl.q)
+    out = torch.full_like(q, float("nan"))
+    lse = torch.full((wl.layout["T"], 64), float("nan"), dtype=torch.float32, device="cuda")
+    o, lse = _call(ds4a, ds4a.attn_prefill_fp8kv, wl, q, ops, out=out, lse=lse)
+    _check(host(o), want, f"fp8 pairs {case}")
+    got = host(lse)
+    fin = np.isfinite(wlse)
+    assert np.array_equal(np.isfinite(got), fin), f"fp8 pairs {case}: lse finiteness"
+    assert np.abs(got[fin] - wlse[fin]).max() <= 1e-3
