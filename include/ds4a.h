@@ -395,6 +395,20 @@ ds4a_status ds4a_attn_indexed(const ds4a_layout *L, const ds4a_tensors *X,
                               ds4a_stream_t stream);
 
 /*
+ * ds4a_attn_indexed_fp8kv - ds4a_attn_indexed over E4M3 rows: the compressed
+ * rows the lists name are E4M3 codes with per-row scales (required), the raw
+ * rows too when their scales are given ([P2] "Layer Compression": top-512
+ * lists on the ratio-4 layers; "Whole-Model Graph Execution": K/V rows are
+ * quantised to FP8 before they are stored).  Operands as for
+ * ds4a_attn_prefill_fp8kv (X->k_comp / X->v_comp uint8 [n_comp][512] codes,
+ * S->k_comp / S->v_comp their fp32 scales; S->k_raw / S->v_raw both given or
+ * both NULL), lists as for ds4a_attn_indexed.  A listed row's value is
+ * decode(code) * scale of that row.
+ */
+ds4a_status ds4a_attn_indexed_fp8kv(const ds4a_layout *L, const ds4a_tensors *X, const ds4a_fp8_scales *S,
+                                   const int32_t *idx, int64_t idx_row_stride, int32_t top_k, ds4a_stream_t stream);
+
+/*
  * ds4a_indexer_scores - [P2] "Layer Compression" (on ratio-4 layers a learned
  * indexer selects the top-512 compressed rows for each query) and "GPU
  * Backend Architecture" (indexer scoring among the GPU ops).  The pages give

@@ -630,7 +630,7 @@ ds4a_status encode_codes(CUtensorMap *m, const void *codes, int rows, int64_t st
 // Checks and kernel parameters of an attention call whose compressed rows (and
 // raw rows, when S->k_raw is given) are E4M3 codes with per-row scales.
 ds4a_status e4m3_params(AttnParams &p, const ds4a_layout *L, const ds4a_tensors *X, const ds4a_fp8_scales *S,
-                        DeviceState **dev) {
+                        DeviceState **dev, int mode = ds4a::MODE_STRUCT) {
   ds4a_status st = check_layout(L);
   if (st != DS4A_OK) return st;
   if (X == nullptr || S == nullptr) return DS4A_ERR_INVALID_ARG;
@@ -647,7 +647,7 @@ ds4a_status e4m3_params(AttnParams &p, const ds4a_layout *L, const ds4a_tensors 
     return DS4A_ERR_INVALID_ARG;
   st = current_device(dev);
   if (st != DS4A_OK) return st;
-  st = fill_params(p, &L0, X, ds4a::MODE_STRUCT, *dev);  // fp16 tensor maps only for fp16 segments
+  st = fill_params(p, &L0, X, mode, *dev);  // fp16 tensor maps only for fp16 segments
   if (st != DS4A_OK) return st;
   p.n_raw = L->n_raw;
   p.n_comp = L->n_comp;
@@ -891,6 +891,27 @@ ds4a_status ds4a_attn_indexed(const ds4a_layout *L, const ds4a_tensors *X, const
   // loaded once, 313 us read apart): K and V are read apart even when they
   // are the same rows.
   p.alias_kv = 0;
+  p.idx = idx;
+  p.idx_stride = idx_row_stride / 4;
+  p.top_k = top_k;
+  const int grid = L->T < d->sm_count ? L->T : d->sm_count;
+  return launched(ds4a::launch_attn(p, grid, as_cuda(stream)));
+}
+
+ds4a_status ds4a_attn_indexed_fp8kv(const ds4a_layout *L, const ds4a_tensors *X, const ds4a_fp8_scales *S,
+                                   const int32_t *idx, int64_t idx_row_stride, int32_t top_k, ds4a_stream_t stream) {
+  ds4a_status st = check_layout(L);
+  if (st != DS4A_OK) return st;
+  if (top_k < 1 || top_k > 4096) return DS4A_ERR_INVALID_ARG;
+  if (L->T == 0) return DS4A_OK;
+  if (S == nullptr || (L->n_comp > 0 && (S->k_comp == nullptr || S->v_comp == nullptr)))
+    return DS4A_ERR_INVALID_ARG;  // the listed rows are E4M3
+  if (idx == nullptr || !aligned(idx, 16) || idx_row_stride < 4LL * top_k || idx_row_stride % 16 != 0)
+    return DS4A_ERR_INVALID_ARG;
+  AttnParams p;
+  DeviceState *d = nullptr;
+  st = e4m3_params(p, L, X, S, &d, ds4a::MODE_INDEXED);
+  if (st != DS4A_OK) return st;
   p.idx = idx;
   p.idx_stride = idx_row_stride / 4;
   p.top_k = top_k;

@@ -291,6 +291,17 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
 // column (c%8) ^ (h%8) (the 128-byte swizzle TMA applies).  Each thread's
 // copies arrive on q_full by themselves when they land.
 constexpr int kQCopyThreads = kLoaderThreads - 32;
+constexpr int kConvThreads = kTile;  // E4M3 converters: one row of a part per thread (warps 9-12)
+
+// Loader threads that gather index-listed rows: all of them, or with E4M3
+// rows (where warps 9-12 convert) warps 8, 13 and 14.  A ring stage's
+// barriers then count one arrival per gathering thread.
+template <bool FP8>
+__host__ __device__ constexpr int gather_threads() { return FP8 ? kLoaderThreads - kConvThreads : kLoaderThreads; }
+template <bool FP8>
+__device__ __forceinline__ uint32_t stage_fill_count(const AttnParams &p) {
+  return (p.mode == MODE_INDEXED && p.n_comp > 0) ? (uint32_t)gather_threads<FP8>() : 1u;
+}
 
 __device__ __forceinline__ bool q_by_lsu(const AttnParams &p, bool fp8) {
   return !fp8 && !(p.mode == MODE_INDEXED && p.n_comp > 0) && p.q_ptr != nullptr &&
@@ -360,9 +371,11 @@ __device__ __forceinline__ void loader_role(const AttnParams &p, uint32_t sbase,
   bool q_issued = false;
   uint32_t q_par = 0;
   bool ok = true;
-  constexpr int kRowStep = kLoaderThreads / 8;  // rows copied per pass of the group
-  const int c8 = ltid & 7;     // 16-byte column c8 of both 128-byte boxes of a stage's 256-byte row slice
-  const int rsub = ltid >> 3;  // row within each group of kRowStep
+  constexpr int kGroup = gather_threads<FP8>();
+  const int gtid = (FP8 && ltid >= 32) ? ltid - kConvThreads : ltid;  // 0 .. kGroup-1 (warps 8, 13, 14 with E4M3)
+  constexpr int kRowStep = kGroup / 8;  // rows copied per pass of the group
+  const int c8 = gtid & 7;     // 16-byte column c8 of both 128-byte boxes of a stage's 256-byte row slice
+  const int rsub = gtid >> 3;  // row within each group of kRowStep
   const uint8_t *kbase = reinterpret_cast<const uint8_t *>(p.k_comp);
   const uint8_t *vbase = reinterpret_cast<const uint8_t *>(p.v_comp);
 
@@ -375,7 +388,7 @@ __device__ __forceinline__ void loader_role(const AttnParams &p, uint32_t sbase,
     if (n_item == 0 && !plan_reads_status) grid_dependency_wait();  // first global read follows
     bool bad = false;
     if (ltid == 0 && !q_lsu) bad = !mbar_wait(b_q_empty, (n_item & 1) ^ 1, abrt, p.timeout_ns, p.err, SITE_Q_EMPTY);
-    if (group) bad = bar_red_or(2, kLoaderThreads, bad);
+    if (group) bad = bar_red_or(2, kGroup, bad);
     if (bad) {
       ok = false;
       break;
@@ -399,14 +412,29 @@ __device__ __forceinline__ void loader_role(const AttnParams &p, uint32_t sbase,
         // E4M3 rows: the codes of this part (128 rows x 128 bytes) land in
         // the stage's upper half; the converter warps turn them into the
         // fp16 stage and arrive on kv_full.
-        if (ltid == 0) {
-          const uint32_t b_code = smem_u32(&ms.code_full[ring.st]);
+        const uint32_t b_code = smem_u32(&ms.code_full[ring.st]);
+        if (tl.seg == 2) {
+          // Gathered E4M3 rows: thread (rsub, c8) copies codes 16 c8 .. +15 of
+          // the part's 128 codes of its rows, into the dense [row][128 codes]
+          // layout the TMA copy of a code box produces.
+          const uint8_t *cbase = (part >= 4 ? vbase : kbase) + 128 * (part & 3) + 16 * c8;
+#pragma unroll
+          for (int it = 0; it < (kTile + kRowStep - 1) / kRowStep; ++it) {
+            const int row = kRowStep * it + rsub;
+            if (kTile % kRowStep != 0 && row >= kTile) break;
+            cp_async16(stage + kBoxBytes + row * 128 + 16 * c8,
+                       cbase + (long long)ms.idx_s[ib][row] * p.comp_row_stride);
+          }
+          cp_async_arrive_noinc(b_code);
+        } else if (ltid == 0) {
           mbar_arrive_expect_tx(b_code, kBoxBytes);
           tma_load_2d(stage + kBoxBytes, part >= 4 ? &p.tm_v8[tl.seg] : &p.tm_k8[tl.seg], b_code, 128 * (part & 3),
                       tl.start);
           cfilled |= 1u << ring.st;
           clast_par = (clast_par & ~(1u << ring.st)) | (((code_ph >> ring.st) & 1u) << ring.st);
           code_ph ^= 1u << ring.st;
+        } else {
+          mbar_arrive(b_code);  // a gathering group: one arrival per thread
         }
       } else if (tl.seg != 2) {
         if (ltid == 0) {
@@ -450,14 +478,14 @@ __device__ __forceinline__ void loader_role(const AttnParams &p, uint32_t sbase,
     // may be rewritten once every thread has issued the copies of the tile
     // that used it last (a copy takes its address when it is issued).
     auto load_list = [&](const Tile &tl, int ib) {
-      named_bar_sync(2, kLoaderThreads);
+      named_bar_sync(2, kGroup);
       const int32_t *lst = p.idx + (long long)ip.t * p.idx_stride;
-      for (int k = ltid; k < 128; k += kLoaderThreads) {
+      for (int k = gtid; k < 128; k += kGroup) {
         const int slot = tl.start + k;
         const int c = slot < p.top_k ? __ldg(lst + slot) : -1;
         ms.idx_s[ib][k] = (c >= 0 && c < p.n_comp) ? c : 0;  // empty slots load row 0, masked later
       }
-      named_bar_sync(2, kLoaderThreads);
+      named_bar_sync(2, kGroup);
     };
     const int nt = ip.j1 - ip.j0;
     Tile cur = ip.cur.next(p);
@@ -467,7 +495,7 @@ __device__ __forceinline__ void loader_role(const AttnParams &p, uint32_t sbase,
       // the next tile before its own V parts (see mma_role).
       for (int part = 0; part < 4; ++part) ok = ok && emit(cur, part, 0);
       for (int jj = 0; jj < nt; ++jj) {
-        if (group) ok = !bar_red_or(2, kLoaderThreads, !ok);  // uniform decision before the next list
+        if (group) ok = !bar_red_or(2, kGroup, !ok);  // uniform decision before the next list
         if (!ok) break;
         Tile nxt = cur;
         if (jj + 1 < nt) {
@@ -489,13 +517,13 @@ __device__ __forceinline__ void loader_role(const AttnParams &p, uint32_t sbase,
         }
 #pragma unroll 1
         for (int part = 0; part < n_parts; ++part) ok = ok && emit(cur, part, 0);
-        if (group) ok = !bar_red_or(2, kLoaderThreads, !ok);  // uniform decision before the next list
+        if (group) ok = !bar_red_or(2, kGroup, !ok);  // uniform decision before the next list
         if (!ok) break;
       }
     }
     // Every group thread reaches this point (the loops above leave together),
     // so the last step's outcome is made uniform here too.
-    if (group) ok = !bar_red_or(2, kLoaderThreads, !ok);
+    if (group) ok = !bar_red_or(2, kGroup, !ok);
     ++n_item;
   }
   if (group) cp_async_wait<0>();  // no gathered copy may still be landing at exit
@@ -523,8 +551,6 @@ __device__ __forceinline__ void loader_role(const AttnParams &p, uint32_t sbase,
 // first; chunks are visited in a per-thread rotated order (no bank
 // conflicts).  The same walk of items, tiles and parts as the loader, so both
 // agree on stage and phase.
-constexpr int kConvThreads = kTile;
-
 template <bool LA>
 __device__ __forceinline__ void converter_role(const AttnParams &p, uint32_t sbase, Misc &ms, int ctid) {
   volatile int *abrt = &ms.abort_flag;
@@ -576,7 +602,7 @@ __device__ __forceinline__ void converter_role(const AttnParams &p, uint32_t sba
         }
         fence_proxy_async_smem();  // generic stores -> visible to the tensor core
         named_bar_sync(3, kConvThreads);
-        if (ctid == 0) mbar_arrive(smem_u32(&ms.kv_full[st]));
+        if (ctid == 0) mbar_arrive_cnt(smem_u32(&ms.kv_full[st]), stage_fill_count<true>(p));
       }
       ring.advance();
       return true;
@@ -816,8 +842,11 @@ __device__ __forceinline__ void compute_role(const AttnParams &p, uint8_t *smem,
       const bool f8 = FP8 && tile_codes(p, tl);
       const float *ksc = tl.seg == 0 ? p.k_scale[0] : p.k_scale[1];
       const float *vsp = tl.seg == 0 ? p.v_scale[0] : p.v_scale[1];
-      const float sl2 = f8 && vis ? p.scale_log2 * __ldg(ksc + tl.start + r) : p.scale_log2;
-      const float vsc = f8 && vis ? __ldg(vsp + tl.start + r) : 1.f;
+      // (a gathered row's scale is that of the compressed row it lists)
+      const int srow = (f8 && vis && tl.seg == 2) ? __ldg(p.idx + (long long)t * p.idx_stride + tl.start + r)
+                                                  : tl.start + r;
+      const float sl2 = f8 && vis ? p.scale_log2 * __ldg(ksc + srow) : p.scale_log2;
+      const float vsc = f8 && vis ? __ldg(vsp + srow) : 1.f;
 #pragma unroll
       for (int h = 0; h < 32; ++h) s[h] = vis ? fmaf(s[h], sl2, bias) : -INFINITY;
 
@@ -974,11 +1003,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&ms.q_full), q_by_lsu(p, FP8) ? kQCopyThreads : 1);
     mbar_init(smem_u32(&ms.q_empty), 1);
-    const uint32_t fill_count = (p.mode == MODE_INDEXED && p.n_comp > 0) ? kLoaderThreads : 1;
+    const uint32_t fill_count = stage_fill_count<FP8>(p);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&ms.kv_full[s]), fill_count);
       mbar_init(smem_u32(&ms.kv_empty[s]), 1);
-      mbar_init(smem_u32(&ms.code_full[s]), 1);
+      mbar_init(smem_u32(&ms.code_full[s]), fill_count);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&ms.s_full[s]), 1);
@@ -1033,9 +1062,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     mma_role<LA>(p, sbase, tmem, ms, lane);
   } else {
     const int ltid = threadIdx.x - 32 * kLoaderWarp0;
-    if (FP8 && ltid >= 32) {
-      if (ltid < 32 + kConvThreads) converter_role<LA>(p, sbase, ms, ltid - 32);
-    } else
+    if (FP8 && ltid >= 32 && ltid < 32 + kConvThreads)
+      converter_role<LA>(p, sbase, ms, ltid - 32);
+    else
       loader_role<FP8, LA>(p, sbase, ms, ltid);
   }
 

@@ -114,6 +114,8 @@ def lib() -> ctypes.CDLL:
         L.ds4a_attn_decode_fp8kv.argtypes = [PL, PT, ctypes.POINTER(Fp8Scales), i32, vp, ctypes.c_size_t, vp]
         L.ds4a_attn_prefill_fp8kv.restype = st
         L.ds4a_attn_prefill_fp8kv.argtypes = [PL, PT, ctypes.POINTER(Fp8Scales), vp]
+        L.ds4a_attn_indexed_fp8kv.restype = st
+        L.ds4a_attn_indexed_fp8kv.argtypes = [PL, PT, ctypes.POINTER(Fp8Scales), vp, i64, i32, vp]
         L.ds4a_quantize_kv_fp8.restype = st
         L.ds4a_quantize_kv_fp8.argtypes = [vp, i64, i32, vp, i64, vp, vp]
         L.ds4a_compress_rows.restype = i32
@@ -583,6 +585,26 @@ def attn_indexed(layout, q, k_raw, v_raw, k_comp, v_comp, idx, *, out=None, lse=
     _on_device(idx=idx)
     _check(lib().ds4a_attn_indexed(ctypes.byref(L), ctypes.byref(X), _ptr(idx), idx.stride(0) * 4, idx.shape[1],
                                    _stream(stream)), "ds4a_attn_indexed")
+    return (out, lse) if (want_lse or lse is not None) else out
+
+
+def attn_indexed_fp8kv(layout, q, k_raw, v_raw, k_comp, v_comp, idx, *, k_comp_scale, v_comp_scale,
+                       k_raw_scale=None, v_raw_scale=None, out=None, lse=None, want_lse=False, stream=None):
+    """:func:`attn_indexed` over E4M3 rows: the listed compressed rows as uint8
+    codes [n_comp, 512] with fp32 row scales; raw rows as codes too when their
+    scales are given, else fp16 [n_raw, 512]."""
+    import torch
+    L = make_layout(layout)
+    if idx.dtype != torch.int32 or idx.dim() != 2 or idx.stride(1) != 1:
+        raise ValueError("idx must be int32 [T, top_k] with contiguous rows")
+    if idx.shape[0] < L.T:
+        raise ValueError(f"idx has {idx.shape[0]} lists, the layout has T = {L.T}")
+    out, lse = _outputs(q, out, lse, want_lse)
+    X, S = _fp8kv(L, q, k_raw, v_raw, k_comp, v_comp, out, lse, k_raw_scale, v_raw_scale, k_comp_scale,
+                  v_comp_scale)
+    _on_device(idx=idx)
+    _check(lib().ds4a_attn_indexed_fp8kv(ctypes.byref(L), ctypes.byref(X), ctypes.byref(S), _ptr(idx),
+                                         idx.stride(0) * 4, idx.shape[1], _stream(stream)), "ds4a_attn_indexed_fp8kv")
     return (out, lse) if (want_lse or lse is not None) else out
 
 

@@ -131,6 +131,22 @@ def test_decode_workspace_is_checked(lib):
                                 None) == ds4a.ERR_WORKSPACE
 
 
+def test_indexed_fp8kv_arguments_are_checked(lib):
+    """Rejected before any device access: no scales, a missing compressed-row
+    scale, top_k out of 1..4096, no lists, a list stride below 4 * top_k."""
+    L = _layout(n_comp=64, ratio=4)
+    X = _tensors(k_comp=FAKE, v_comp=FAKE)
+    S = ds4a.Fp8Scales(None, None, FAKE, FAKE)
+    f = lib.ds4a_attn_indexed_fp8kv
+    assert f(ctypes.byref(L), ctypes.byref(X), None, FAKE, 2048, 512, None) == ds4a.ERR_INVALID_ARG
+    S1 = ds4a.Fp8Scales(None, None, None, FAKE)
+    assert f(ctypes.byref(L), ctypes.byref(X), ctypes.byref(S1), FAKE, 2048, 512, None) == ds4a.ERR_INVALID_ARG
+    assert f(ctypes.byref(L), ctypes.byref(X), ctypes.byref(S), FAKE, 2048, 0, None) == ds4a.ERR_INVALID_ARG
+    assert f(ctypes.byref(L), ctypes.byref(X), ctypes.byref(S), FAKE, 2048, 4097, None) == ds4a.ERR_INVALID_ARG
+    assert f(ctypes.byref(L), ctypes.byref(X), ctypes.byref(S), None, 2048, 512, None) == ds4a.ERR_INVALID_ARG
+    assert f(ctypes.byref(L), ctypes.byref(X), ctypes.byref(S), FAKE, 2040, 512, None) == ds4a.ERR_INVALID_ARG
+
+
 def test_indexed_arguments_are_checked(lib):
     L = _layout(n_comp=64, ratio=4)
     X = _tensors(k_comp=FAKE, v_comp=FAKE)

@@ -2,7 +2,8 @@
 
 * ds4a_quantize_kv_fp8: codes and scales bit for bit against the oracle (the
   fp32 quotients, product and E4M3 rounding are the same operations).
-* ds4a_attn_decode_fp8 / _fp8kv and ds4a_attn_prefill_fp8kv: against the
+* ds4a_attn_decode_fp8 / _fp8kv, ds4a_attn_prefill_fp8kv and
+  ds4a_attn_indexed_fp8kv: against the
   fp64 attention oracle run on the rows' values decode(code) * scale, within
   max abs 5e-3 and mean abs 5e-4.  The codes and scales the GPU reads are the
   oracle's own quantisation of the rows (uploaded), so no expected value
@@ -239,3 +240,57 @@ def test_prefill_fp8kv_pairs(torch, ds4a, case):
     fin = np.isfinite(wlse)
     assert np.array_equal(np.isfinite(got), fin), f"fp8 pairs {case}: lse finiteness"
     assert np.abs(got[fin] - wlse[fin]).max() <= 1e-3
+
+
+def _indexed_fp8(torch, ds4a, wl, idx, raw_fp8):
+    """E4M3 indexed attention (listed compressed rows as codes; raw rows as
+    codes too with raw_fp8) against the oracle over the decoded rows, the
+    outputs pre-filled with NaN; returns the GPU output."""
+    L = wl.layout
+    ops = {}
+    kr, vr = wl.k_raw, wl.v_raw
+    if raw_fp8:
+        ops["k_raw"], ops["k_raw_scale"], kr = _quantized(torch, wl.k_raw)
+        ops["v_raw"], ops["v_raw_scale"], vr = _quantized(torch, wl.v_raw)
+    else:
+        ops["k_raw"], ops["v_raw"] = dev(torch, wl.k_raw), dev(torch, wl.v_raw)
+    kc_codes, kcs, kc = _quantized(torch, wl.k_comp)
+    vc_codes, vcs, vc = _quantized(torch, wl.v_comp)
+    want, wlse = oracle.attention(L, wl.q, kr, vr, kc, vc, idx=idx)
+    q = dev(torch, wl.q)
+    out = torch.full_like(q, float("nan"))
+    lse = torch.full((L["T"], 64), float("nan"), dtype=torch.float32, device="cuda")
+    ds4a.attn_indexed_fp8kv(L, q, ops["k_raw"], ops["v_raw"], kc_codes, vc_codes, dev(torch, idx),
+                            k_comp_scale=kcs, v_comp_scale=vcs, k_raw_scale=ops.get("k_raw_scale"),
+                            v_raw_scale=ops.get("v_raw_scale"), out=out, lse=lse)
+    got = host(out)
+    _check(got, want, f"indexed fp8 {wl.name}")
+    gl = host(lse)
+    fin = np.isfinite(wlse)
+    assert np.array_equal(np.isfinite(gl), fin), "indexed fp8: lse finiteness"
+    assert np.abs(gl[fin] - wlse[fin]).max() <= 1e-3
+    return got
+
+
+@pytest.mark.parametrize("raw_fp8", [False, True])
+def test_indexed_fp8kv_all_tokens(torch, ds4a, raw_fp8):
+    """The full indexed ratio-4 chunk (2048 tokens, top-512 of 8192 rows) over
+    E4M3 compressed rows (and E4M3 raw rows), every token against the oracle."""
+    wl = W.indexed_r4_2048()
+    _indexed_fp8(torch, ds4a, wl, wl.idx, raw_fp8)
+
+
+def test_indexed_fp8kv_edge_cases(torch, ds4a):
+    """Duplicates, -1 around entries, every row, entries past the last row
+    (empty slots), lists with no valid entry; E4M3 raw and compressed rows."""
+    L = make_layout(T=7, q_pos0=700, n_raw=140, raw_pos0=600, n_comp=175, ratio=4)
+    wl = W.draw("idx_fp8_edge", 69, L)
+    idx = np.full((7, 200), -1, np.int32)
+    idx[0, :3] = [4, 4, 9]
+    idx[1, 50:60] = np.arange(10)
+    idx[2, :] = np.arange(200) % 175
+    idx[3, 0] = 174
+    idx[4, 199] = 0
+    idx[5, :6] = [175, 3, 176, 2 ** 31 - 1, 8, 100000]
+    idx[6, 10:140] = np.arange(175, 305)
+    _indexed_fp8(torch, ds4a, wl, idx, raw_fp8=True)
