@@ -294,8 +294,9 @@ constexpr int kQCopyThreads = kLoaderThreads - 32;
 constexpr int kConvThreads = kTile;  // E4M3 converters: one row of a part per thread (warps 9-12)
 
 // Loader threads that gather index-listed rows: all of them, or with E4M3
-// rows (where warps 9-12 convert) warps 8, 13 and 14.  A ring stage's
-// barriers then count one arrival per gathering thread.
+// rows (where warps 9-12 convert) warps 8, 13 and 14.  The barrier the
+// gathered copies complete (kv_full in the fp16 kernel, code_full in the
+// E4M3 one) then counts one arrival per gathering thread.
 template <bool FP8>
 __host__ __device__ constexpr int gather_threads() { return FP8 ? kLoaderThreads - kConvThreads : kLoaderThreads; }
 template <bool FP8>
@@ -441,6 +442,7 @@ __device__ __forceinline__ void loader_role(const AttnParams &p, uint32_t sbase,
           const int dim0 = 128 * (part & 3);
           const CUtensorMap *m = part >= 4 ? &p.tm_v[tl.seg] : &p.tm_k[tl.seg];
           mbar_arrive_expect_tx(b_full, kStageBytes);
+          if (FP8) mbar_arrive_cnt(b_full, kConvThreads - 1);  // the stage counts the converter threads
           if (p.kv_pair) {
             // 64-row tile: the K and the V slice of dims dim0 .. dim0+127 in
             // one stage, four [64 rows][64 dims] boxes of 8 KB (two copies:
@@ -455,7 +457,7 @@ __device__ __forceinline__ void loader_role(const AttnParams &p, uint32_t sbase,
           }
           filled |= 1u << ring.st;
           last_par = (last_par & ~(1u << ring.st)) | (ring.ph << ring.st);
-        } else {
+        } else if (!FP8) {
           mbar_arrive(b_full);
         }
       } else {
@@ -549,8 +551,12 @@ __device__ __forceinline__ void loader_role(const AttnParams &p, uint32_t sbase,
 // arrive on kv_full.  A thread converts whole rows: row r's fp16 values in the
 // upper box overwrite only row r's own codes, which the thread has read
 // first; chunks are visited in a per-thread rotated order (no bank
-// conflicts).  The same walk of items, tiles and parts as the loader, so both
-// agree on stage and phase.
+// conflicts).  The threads never wait for one another: each arrives on
+// kv_full after its own row (a stage of the E4M3 kernel counts 128
+// arrivals; an fp16 stage gets them from the loader thread at once), which
+// made the 262,144-row E4M3 decode 78.8 -> 75.1 us against a barrier among the
+// converters per part.  The same walk of items, tiles and parts as the
+// loader, so both agree on stage and phase.
 template <bool LA>
 __device__ __forceinline__ void converter_role(const AttnParams &p, uint32_t sbase, Misc &ms, int ctid) {
   volatile int *abrt = &ms.abort_flag;
@@ -570,7 +576,7 @@ __device__ __forceinline__ void converter_role(const AttnParams &p, uint32_t sba
         bool w = mbar_wait(smem_u32(&ms.code_full[st]), (code_ph >> st) & 1u, abrt, p.timeout_ns, p.err,
                            SITE_KV_FULL);
         code_ph ^= 1u << st;
-        if (bar_red_or(3, kConvThreads, !w)) return false;
+        if (!w) return false;
         const uint32_t stage = sbase + kOffKV + st * kStageBytes;
 #pragma unroll 1
         for (int row = ctid; row < kTile; row += kConvThreads) {
@@ -601,8 +607,7 @@ __device__ __forceinline__ void converter_role(const AttnParams &p, uint32_t sba
           }
         }
         fence_proxy_async_smem();  // generic stores -> visible to the tensor core
-        named_bar_sync(3, kConvThreads);
-        if (ctid == 0) mbar_arrive_cnt(smem_u32(&ms.kv_full[st]), stage_fill_count<true>(p));
+        mbar_arrive(smem_u32(&ms.kv_full[st]));
       }
       ring.advance();
       return true;
@@ -1005,7 +1010,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     mbar_init(smem_u32(&ms.q_empty), 1);
     const uint32_t fill_count = stage_fill_count<FP8>(p);
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_u32(&ms.kv_full[s]), fill_count);
+      mbar_init(smem_u32(&ms.kv_full[s]), FP8 ? (uint32_t)kConvThreads : fill_count);
       mbar_init(smem_u32(&ms.kv_empty[s]), 1);
       mbar_init(smem_u32(&ms.code_full[s]), fill_count);
     }
