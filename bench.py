@@ -626,11 +626,13 @@ def run_also(torch, ds4a, W, dev, stream, pk, pk_kind):
             kr, vr = up(wl.k_raw), up(wl.v_raw)
             kc, ks = ds4a.quantize_kv_fp8(kr, stream=stream)
             vc, vs = ds4a.quantize_kv_fp8(vr, stream=stream)
-            sets.append([up(wl.q), kc, ks, vc, vs, torch.empty(wl.q.shape, dtype=torch.float16, device=dev)])
+            ws = torch.empty(ds4a.prefill_fp8kv_workspace_size(wl.layout), dtype=torch.uint8, device=dev)
+            sets.append([up(wl.q), kc, ks, vc, vs, torch.empty(wl.q.shape, dtype=torch.float16, device=dev), ws])
         torch.cuda.synchronize()
         sec = timed(lambda i: ds4a.attn_prefill_fp8kv(wl.layout, sets[i % 2][0], sets[i % 2][1], sets[i % 2][3],
                                                       k_raw_scale=sets[i % 2][2], v_raw_scale=sets[i % 2][4],
-                                                      out=sets[i % 2][5], stream=stream), 10)
+                                                      out=sets[i % 2][5], workspace=sets[i % 2][6], stream=stream),
+                    10)
         fl = attn_flops(wl.layout)
         n = wl.layout["n_raw"]
         by = 2 * wl.q.nbytes + 2 * n * (512 + 4)

@@ -317,6 +317,25 @@ ds4a_status ds4a_attn_prefill_fp8kv(const ds4a_layout *L, const ds4a_tensors *X,
                                     ds4a_stream_t stream);
 
 /*
+ * ds4a_attn_prefill_fp8kv_ws - ds4a_attn_prefill_fp8kv with a workspace, same
+ * operands and result.  When the raw rows are E4M3 (S->k_raw given), the call
+ * has no compressed rows, window <= 128 and T >= 2, each raw row that some
+ * query sees is decoded once into fp16 rows of the workspace (exact: every
+ * E4M3 value is an fp16 value) and the prefill runs as pairs of consecutive
+ * queries over one 128-row tile (the kernel of ds4a_attn_prefill), the row
+ * scales applied in the kernel.  Other calls ignore the workspace and run as
+ * ds4a_attn_prefill_fp8kv.
+ *   workspace  device memory, 256-byte aligned, at least
+ *              ds4a_attn_prefill_fp8kv_workspace_size(L) bytes (may be NULL
+ *              when that is 0); overwritten; must not overlap the operands.
+ * Returns DS4A_ERR_WORKSPACE when the workspace is missing, short or
+ * misaligned.
+ */
+size_t ds4a_attn_prefill_fp8kv_workspace_size(const ds4a_layout *L);
+ds4a_status ds4a_attn_prefill_fp8kv_ws(const ds4a_layout *L, const ds4a_tensors *X, const ds4a_fp8_scales *S,
+                                       void *workspace, size_t workspace_bytes, ds4a_stream_t stream);
+
+/*
  * ds4a_attn_decode_batch - one decode step for n_seq independent sequences in
  * one launch (the pages' "serving many requests in parallel", page 4): each
  * sequence has one query token, its own position and row counts, and its own

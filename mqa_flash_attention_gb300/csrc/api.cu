@@ -260,8 +260,11 @@ bool short_decode(const ds4a_layout *L, int sm_count) {
 }
 
 // Raw rows only, window <= 128, T >= 2: pairs of consecutive tokens share one
-// 128-row tile (attn_pair.cu); the result is the structural attention.
-ds4a_status prefill_pairs(const ds4a_layout *L, const ds4a_tensors *X, DeviceState *d, ds4a_stream_t stream) {
+// 128-row tile (attn_pair.cu); the result is the structural attention.  With
+// k_scale / v_scale the rows are decoded E4M3 codes (exact in fp16) whose
+// per-row scales the kernel applies (K's to the scores, V's to P).
+ds4a_status prefill_pairs(const ds4a_layout *L, const ds4a_tensors *X, DeviceState *d, ds4a_stream_t stream,
+                          const float *k_scale = nullptr, const float *v_scale = nullptr) {
   ds4a::PairParams p;
   std::memset(&p, 0, sizeof(p));
   {
@@ -283,6 +286,8 @@ ds4a_status prefill_pairs(const ds4a_layout *L, const ds4a_tensors *X, DeviceSta
   p.scale_log2 = L->scale * 1.4426950408889634f;
   p.k_raw = static_cast<const uint8_t *>(X->k_raw);
   p.v_raw = static_cast<const uint8_t *>(X->v_raw);
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
   p.raw_row_stride = X->raw_row_stride;
   p.o = static_cast<__half *>(X->o);
   p.o_tok_stride = X->o_tok_stride / 2;
@@ -725,6 +730,70 @@ ds4a_status ds4a_attn_prefill_fp8kv(const ds4a_layout *L, const ds4a_tensors *X,
   if (st != DS4A_OK) return st;
   const int grid = L->T < d->sm_count ? L->T : d->sm_count;
   return launched(ds4a::launch_attn(p, grid, as_cuda(stream)));
+}
+
+}  // extern "C"
+
+namespace {
+
+// The raw rows [lo, hi) that some query of a raw-only E4M3 prefill sees, when
+// the call takes the pair kernel (window <= 128, T >= 2; the window rule
+// t - window < position <= t); false otherwise.
+bool fp8_pair_rows(const ds4a_layout *L, int64_t *lo, int64_t *hi) {
+  if (L->n_comp != 0 || L->n_raw <= 0 || L->window > 128 || L->T < 2) return false;
+  const int64_t a = (int64_t)L->q_pos0 - L->window + 1 - L->raw_pos0;
+  const int64_t b = (int64_t)L->q_pos0 + L->T - L->raw_pos0;
+  *lo = a < 0 ? 0 : a;
+  *hi = b > L->n_raw ? L->n_raw : b;
+  return *hi > *lo;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t ds4a_attn_prefill_fp8kv_workspace_size(const ds4a_layout *L) {
+  int64_t lo = 0, hi = 0;
+  if (check_layout(L) != DS4A_OK || !fp8_pair_rows(L, &lo, &hi)) return 0;
+  return (size_t)(hi - lo) * 2 * DS4A_ROW_BYTES;
+}
+
+ds4a_status ds4a_attn_prefill_fp8kv_ws(const ds4a_layout *L, const ds4a_tensors *X, const ds4a_fp8_scales *S,
+                                       void *workspace, size_t workspace_bytes, ds4a_stream_t stream) {
+  ds4a_status st = check_layout(L);
+  if (st != DS4A_OK) return st;
+  if (L->T == 0) return DS4A_OK;
+  int64_t lo = 0, hi = 0;
+  if (X == nullptr || S == nullptr || S->k_raw == nullptr || !fp8_pair_rows(L, &lo, &hi))
+    return ds4a_attn_prefill_fp8kv(L, X, S, stream);
+  // Q and O as usual (checked with the E4M3 rows left out), then the codes.
+  ds4a_layout L0 = *L;
+  L0.n_raw = 0;
+  st = check_tensors(&L0, X);
+  if (st != DS4A_OK) return st;
+  if (!e4m3_rows_ok(X->k_raw, X->v_raw, X->raw_row_stride) || !scales_ok(S->k_raw, S->v_raw))
+    return DS4A_ERR_INVALID_ARG;
+  const int32_t rows = (int32_t)(hi - lo);
+  const size_t need = (size_t)rows * 2 * DS4A_ROW_BYTES;
+  if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256)) return DS4A_ERR_WORKSPACE;
+  DeviceState *d = nullptr;
+  st = current_device(&d);
+  if (st != DS4A_OK) return st;
+  // Each visible row decoded once, into fp16 rows of the workspace (K then V).
+  __half *kw = static_cast<__half *>(workspace);
+  __half *vw = kw + (size_t)rows * DS4A_HEAD_DIM;
+  const uint8_t *kc = static_cast<const uint8_t *>(X->k_raw) + lo * X->raw_row_stride;
+  const uint8_t *vc = static_cast<const uint8_t *>(X->v_raw) + lo * X->raw_row_stride;
+  st = launched(ds4a::launch_widen_e4m3_rows(kc, vc, X->raw_row_stride, rows, kw, vw, as_cuda(stream)));
+  if (st != DS4A_OK) return st;
+  ds4a_layout L1 = *L;
+  L1.raw_pos0 = (int32_t)(L->raw_pos0 + lo);
+  L1.n_raw = rows;
+  ds4a_tensors X1 = *X;
+  X1.k_raw = kw;
+  X1.v_raw = vw;
+  X1.raw_row_stride = DS4A_ROW_BYTES;
+  return prefill_pairs(&L1, &X1, d, stream, S->k_raw + lo, S->v_raw + lo);
 }
 
 // ------------------------------------------------------------------ batched decode

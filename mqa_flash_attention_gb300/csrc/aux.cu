@@ -459,6 +459,47 @@ __global__ void quantize_fp8_kernel(const uint8_t *__restrict__ src, long long s
   }
 }
 
+// ------------------------------------------------------------------ E4M3 rows -> fp16 codes' values
+// Rows of K and V codes to their decoded values decode(code) in fp16 (exact:
+// every E4M3 value is an fp16 value; the row scales stay apart), [n][512]
+// each.  Thread i handles 16 codes (one 16-byte load, two 16-byte stores),
+// grid-stride over both arrays.
+
+__global__ void widen_e4m3_rows_kernel(const uint8_t *__restrict__ kc, const uint8_t *__restrict__ vc,
+                                       long long stride, int n_rows, __half *__restrict__ ko,
+                                       __half *__restrict__ vo) {
+  const long long per = (long long)n_rows * 32;  // 16-code chunks per array
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < 2 * per;
+       i += (long long)gridDim.x * blockDim.x) {
+    const bool is_v = i >= per;
+    const long long j = is_v ? i - per : i;
+    const int row = (int)(j >> 5), c = (int)(j & 31);
+    const uint4 w = __ldg(reinterpret_cast<const uint4 *>((is_v ? vc : kc) + row * stride) + c);
+    const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
+    uint32_t h[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      h[2 * k] = e4m3x2_to_f16x2(static_cast<uint16_t>(wd[k] & 0xFFFFu));
+      h[2 * k + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(wd[k] >> 16));
+    }
+    uint4 *dst = reinterpret_cast<uint4 *>((is_v ? vo : ko) + (long long)row * 512 + 16 * c);
+    dst[0] = make_uint4(h[0], h[1], h[2], h[3]);
+    dst[1] = make_uint4(h[4], h[5], h[6], h[7]);
+  }
+}
+
+cudaError_t launch_widen_e4m3_rows(const void *k_codes, const void *v_codes, long long stride, int n_rows,
+                                   __half *k_out, __half *v_out, cudaStream_t s) {
+  if (n_rows <= 0) return cudaSuccess;
+  const int threads = 256;
+  long long blocks = ((long long)n_rows * 64 + threads - 1) / threads;
+  if (blocks > 4096) blocks = 4096;
+  widen_e4m3_rows_kernel<<<(unsigned)blocks, threads, 0, s>>>(static_cast<const uint8_t *>(k_codes),
+                                                              static_cast<const uint8_t *>(v_codes), stride, n_rows,
+                                                              k_out, v_out);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_quantize_fp8(const void *src, long long src_stride, int n_rows, void *dst, long long dst_stride,
                                 float *scales, cudaStream_t s) {
   const int threads = 256, rows_per_block = threads / 32;

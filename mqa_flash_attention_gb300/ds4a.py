@@ -114,6 +114,10 @@ def lib() -> ctypes.CDLL:
         L.ds4a_attn_decode_fp8kv.argtypes = [PL, PT, ctypes.POINTER(Fp8Scales), i32, vp, ctypes.c_size_t, vp]
         L.ds4a_attn_prefill_fp8kv.restype = st
         L.ds4a_attn_prefill_fp8kv.argtypes = [PL, PT, ctypes.POINTER(Fp8Scales), vp]
+        L.ds4a_attn_prefill_fp8kv_workspace_size.restype = ctypes.c_size_t
+        L.ds4a_attn_prefill_fp8kv_workspace_size.argtypes = [PL]
+        L.ds4a_attn_prefill_fp8kv_ws.restype = st
+        L.ds4a_attn_prefill_fp8kv_ws.argtypes = [PL, PT, ctypes.POINTER(Fp8Scales), vp, ctypes.c_size_t, vp]
         L.ds4a_attn_indexed_fp8kv.restype = st
         L.ds4a_attn_indexed_fp8kv.argtypes = [PL, PT, ctypes.POINTER(Fp8Scales), vp, i64, i32, vp]
         L.ds4a_quantize_kv_fp8.restype = st
@@ -480,15 +484,38 @@ def attn_decode_fp8kv(layout, q, k_raw, v_raw, k_comp, v_comp, *, k_comp_scale, 
     return (out, lse) if (want_lse or lse is not None) else out
 
 
+def prefill_fp8kv_workspace_size(layout) -> int:
+    """Workspace bytes of :func:`attn_prefill_fp8kv` with E4M3 raw rows (0: none needed)."""
+    return int(lib().ds4a_attn_prefill_fp8kv_workspace_size(ctypes.byref(make_layout(layout))))
+
+
 def attn_prefill_fp8kv(layout, q, k_raw, v_raw, k_comp=None, v_comp=None, *, k_comp_scale=None, v_comp_scale=None,
-                       k_raw_scale=None, v_raw_scale=None, out=None, lse=None, want_lse=False, stream=None):
-    """Structural prefill over E4M3 rows (operands as in :func:`attn_decode_fp8kv`)."""
+                       k_raw_scale=None, v_raw_scale=None, workspace=None, out=None, lse=None, want_lse=False,
+                       stream=None):
+    """Structural prefill over E4M3 rows (operands as in :func:`attn_decode_fp8kv`).
+
+    With E4M3 raw rows and no compressed rows (window <= 128, T >= 2) the rows
+    are decoded once into ``workspace`` (allocated here when None) and the
+    prefill runs on the pair kernel; ``workspace=False`` keeps the call on the
+    one-token kernel without a workspace."""
+    import torch
     L = make_layout(layout)
     out, lse = _outputs(q, out, lse, want_lse)
     X, S = _fp8kv(L, q, k_raw, v_raw, k_comp, v_comp, out, lse, k_raw_scale, v_raw_scale, k_comp_scale,
                   v_comp_scale)
-    _check(lib().ds4a_attn_prefill_fp8kv(ctypes.byref(L), ctypes.byref(X), ctypes.byref(S), _stream(stream)),
-           "ds4a_attn_prefill_fp8kv")
+    if workspace is False:
+        _check(lib().ds4a_attn_prefill_fp8kv(ctypes.byref(L), ctypes.byref(X), ctypes.byref(S), _stream(stream)),
+               "ds4a_attn_prefill_fp8kv")
+    else:
+        need = lib().ds4a_attn_prefill_fp8kv_workspace_size(ctypes.byref(L)) if k_raw_scale is not None else 0
+        if workspace is None and need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        wp, wb = None, 0
+        if workspace is not None:
+            _on_device(workspace=workspace)
+            wp, wb = _ptr(workspace), workspace.numel() * workspace.element_size()
+        _check(lib().ds4a_attn_prefill_fp8kv_ws(ctypes.byref(L), ctypes.byref(X), ctypes.byref(S), wp, wb,
+                                                _stream(stream)), "ds4a_attn_prefill_fp8kv_ws")
     return (out, lse) if (want_lse or lse is not None) else out
 
 

@@ -131,6 +131,46 @@ def test_decode_workspace_is_checked(lib):
                                 None) == ds4a.ERR_WORKSPACE
 
 
+def test_prefill_fp8kv_workspace_size(lib):
+    """Two fp16 rows (K and V) per raw row that some query sees, when the call
+    takes the pair kernel (no compressed rows, window <= 128, T >= 2); else 0."""
+    f = lib.ds4a_attn_prefill_fp8kv_workspace_size
+    # Queries at 1000..1063 with a 128-row window see positions 873..1063.
+    L = _layout(T=64, q_pos0=1000, n_raw=2000, raw_pos0=0, n_comp=0, window=128)
+    assert f(ctypes.byref(L)) == (1063 - 873 + 1) * 2 * 1024
+    # Rows clipped at both ends: positions 950..989 exist, all of them seen.
+    L = _layout(T=6, q_pos0=1000, n_raw=40, raw_pos0=950, n_comp=0, window=128)
+    assert f(ctypes.byref(L)) == 40 * 2 * 1024
+    # Rows that no query sees (all after the last query).
+    L = _layout(T=4, q_pos0=100, n_raw=50, raw_pos0=500, n_comp=0, window=128)
+    assert f(ctypes.byref(L)) == 0
+    for kw in (dict(T=1), dict(window=129), dict(n_comp=8, ratio=4), dict(n_raw=0), dict(window=0)):
+        base = dict(T=64, q_pos0=1000, n_raw=2000, raw_pos0=0, n_comp=0, window=128)
+        base.update(kw)
+        assert f(ctypes.byref(_layout(**base))) == 0, kw
+    assert f(None) == 0
+
+
+def test_prefill_fp8kv_workspace_is_checked(lib):
+    """The pair path rejects a missing, short or misaligned workspace and bad
+    code rows or scales before any device access."""
+    L = _layout(T=6, q_pos0=1000, n_raw=40, raw_pos0=950, n_comp=0, window=128)
+    X = _tensors()
+    S = ds4a.Fp8Scales(FAKE, FAKE, None, None)
+    f = lib.ds4a_attn_prefill_fp8kv_ws
+    need = lib.ds4a_attn_prefill_fp8kv_workspace_size(ctypes.byref(L))
+    assert f(ctypes.byref(L), ctypes.byref(X), ctypes.byref(S), None, 0, None) == ds4a.ERR_WORKSPACE
+    assert f(ctypes.byref(L), ctypes.byref(X), ctypes.byref(S), FAKE, need - 1, None) == ds4a.ERR_WORKSPACE
+    assert f(ctypes.byref(L), ctypes.byref(X), ctypes.byref(S), ctypes.c_void_p((1 << 20) + 128), need,
+             None) == ds4a.ERR_WORKSPACE
+    S1 = ds4a.Fp8Scales(FAKE, None, None, None)
+    assert f(ctypes.byref(L), ctypes.byref(X), ctypes.byref(S1), FAKE, need, None) == ds4a.ERR_INVALID_ARG
+    X1 = _tensors(raw_row_stride=520)
+    assert f(ctypes.byref(L), ctypes.byref(X1), ctypes.byref(S), FAKE, need, None) == ds4a.ERR_INVALID_ARG
+    X2 = _tensors(o=MISALIGNED)
+    assert f(ctypes.byref(L), ctypes.byref(X2), ctypes.byref(S), FAKE, need, None) == ds4a.ERR_INVALID_ARG
+
+
 def test_indexed_fp8kv_arguments_are_checked(lib):
     """Rejected before any device access: no scales, a missing compressed-row
     scale, top_k out of 1..4096, no lists, a list stride below 4 * top_k."""

@@ -225,20 +225,28 @@ _PAIR_LAYOUTS = [
 ]
 
 
+@pytest.mark.parametrize("path", ["pairs", "one_token"])
 @pytest.mark.parametrize("case", range(len(_PAIR_LAYOUTS)))
-def test_prefill_fp8kv_pairs(torch, ds4a, case):
+def test_prefill_fp8kv_pairs(torch, ds4a, case, path):
     """E4M3 raw rows on those layouts against the oracle over the decoded
-    rows; outputs and log-sum-exp start as NaN."""
+    rows, through the workspace call (rows decoded once, pair kernel) and the
+    call without one (one-token kernel); outputs and log-sum-exp start as
+    NaN, and the workspace starts as NaN rows."""
     wl = W.draw(f"fp8_pairs{case}", 120 + case, make_layout(**_PAIR_LAYOUTS[case]))
     ops, want, wlse = _fp8kv_case(torch, wl, raw_fp8=True)
     q = dev(torch, wl.q)
     out = torch.full_like(q, float("nan"))
     lse = torch.full((wl.layout["T"], 64), float("nan"), dtype=torch.float32, device="cuda")
-    o, lse = _call(ds4a, ds4a.attn_prefill_fp8kv, wl, q, ops, out=out, lse=lse)
-    _check(host(o), want, f"fp8 pairs {case}")
+    ws = False
+    if path == "pairs":
+        need = ds4a.prefill_fp8kv_workspace_size(wl.layout)
+        assert need > 0
+        ws = torch.full((need // 2,), float("nan"), dtype=torch.float16, device="cuda")
+    o, lse = _call(ds4a, ds4a.attn_prefill_fp8kv, wl, q, ops, out=out, lse=lse, workspace=ws)
+    _check(host(o), want, f"fp8 pairs {case} {path}")
     got = host(lse)
     fin = np.isfinite(wlse)
-    assert np.array_equal(np.isfinite(got), fin), f"fp8 pairs {case}: lse finiteness"
+    assert np.array_equal(np.isfinite(got), fin), f"fp8 pairs {case} {path}: lse finiteness"
     assert np.abs(got[fin] - wlse[fin]).max() <= 1e-3
 
 
