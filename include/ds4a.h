@@ -320,10 +320,10 @@ ds4a_status ds4a_attn_prefill_fp8kv(const ds4a_layout *L, const ds4a_tensors *X,
  * ds4a_attn_prefill_fp8kv_ws - ds4a_attn_prefill_fp8kv with a workspace, same
  * operands and result.  When the raw rows are E4M3 (S->k_raw given), the call
  * has no compressed rows, window <= 128 and T >= 2, each raw row that some
- * query sees is decoded once into fp16 rows of the workspace (exact: every
- * E4M3 value is an fp16 value) and the prefill runs as pairs of consecutive
- * queries over one 128-row tile (the kernel of ds4a_attn_prefill), the row
- * scales applied in the kernel.  Other calls ignore the workspace and run as
+ * query sees is decoded once into an fp16 row of the workspace, its values
+ * decode(code) * scale rounded once to fp16, and the prefill runs over those
+ * rows as ds4a_attn_prefill does (pairs of consecutive queries over one
+ * 128-row tile).  Other calls ignore the workspace and run as
  * ds4a_attn_prefill_fp8kv.
  *   workspace  device memory, 256-byte aligned, at least
  *              ds4a_attn_prefill_fp8kv_workspace_size(L) bytes (may be NULL

@@ -260,11 +260,8 @@ bool short_decode(const ds4a_layout *L, int sm_count) {
 }
 
 // Raw rows only, window <= 128, T >= 2: pairs of consecutive tokens share one
-// 128-row tile (attn_pair.cu); the result is the structural attention.  With
-// k_scale / v_scale the rows are decoded E4M3 codes (exact in fp16) whose
-// per-row scales the kernel applies (K's to the scores, V's to P).
-ds4a_status prefill_pairs(const ds4a_layout *L, const ds4a_tensors *X, DeviceState *d, ds4a_stream_t stream,
-                          const float *k_scale = nullptr, const float *v_scale = nullptr) {
+// 128-row tile (attn_pair.cu); the result is the structural attention.
+ds4a_status prefill_pairs(const ds4a_layout *L, const ds4a_tensors *X, DeviceState *d, ds4a_stream_t stream) {
   ds4a::PairParams p;
   std::memset(&p, 0, sizeof(p));
   {
@@ -286,8 +283,6 @@ ds4a_status prefill_pairs(const ds4a_layout *L, const ds4a_tensors *X, DeviceSta
   p.scale_log2 = L->scale * 1.4426950408889634f;
   p.k_raw = static_cast<const uint8_t *>(X->k_raw);
   p.v_raw = static_cast<const uint8_t *>(X->v_raw);
-  p.k_scale = k_scale;
-  p.v_scale = v_scale;
   p.raw_row_stride = X->raw_row_stride;
   p.o = static_cast<__half *>(X->o);
   p.o_tok_stride = X->o_tok_stride / 2;
@@ -779,12 +774,13 @@ ds4a_status ds4a_attn_prefill_fp8kv_ws(const ds4a_layout *L, const ds4a_tensors 
   DeviceState *d = nullptr;
   st = current_device(&d);
   if (st != DS4A_OK) return st;
-  // Each visible row decoded once, into fp16 rows of the workspace (K then V).
+  // Each visible row's values decoded once, into fp16 rows of the workspace (K then V).
   __half *kw = static_cast<__half *>(workspace);
   __half *vw = kw + (size_t)rows * DS4A_HEAD_DIM;
   const uint8_t *kc = static_cast<const uint8_t *>(X->k_raw) + lo * X->raw_row_stride;
   const uint8_t *vc = static_cast<const uint8_t *>(X->v_raw) + lo * X->raw_row_stride;
-  st = launched(ds4a::launch_widen_e4m3_rows(kc, vc, X->raw_row_stride, rows, kw, vw, as_cuda(stream)));
+  st = launched(ds4a::launch_widen_e4m3_rows(kc, vc, S->k_raw + lo, S->v_raw + lo, X->raw_row_stride, rows, kw, vw,
+                                             as_cuda(stream)));
   if (st != DS4A_OK) return st;
   ds4a_layout L1 = *L;
   L1.raw_pos0 = (int32_t)(L->raw_pos0 + lo);
@@ -793,7 +789,7 @@ ds4a_status ds4a_attn_prefill_fp8kv_ws(const ds4a_layout *L, const ds4a_tensors 
   X1.k_raw = kw;
   X1.v_raw = vw;
   X1.raw_row_stride = DS4A_ROW_BYTES;
-  return prefill_pairs(&L1, &X1, d, stream, S->k_raw + lo, S->v_raw + lo);
+  return prefill_pairs(&L1, &X1, d, stream);
 }
 
 // ------------------------------------------------------------------ batched decode

@@ -86,7 +86,6 @@ constexpr uint32_t kPOffMisc = kPOffX + 2 * 2048;
 static_assert(kPSlots % 2 == 0 && kPSlotsPerPair % 2 == 0, "V slot pairs must stay adjacent in the ring");
 
 struct PairMisc {
-  alignas(16) float ksc[2][128], vsc[2][128];  // scaled rows, by pair parity: the tile rows' K and V scales
   alignas(16) float inv_l[2][128];  // by pair parity: 1 / row sum of each query row (0 when nothing is visible)
   alignas(16) float px[2][64];      // by pair parity: token a's extra-row weight per head
   alignas(16) float sx[2][64];      // extra row, by pair parity: scaled score of token a per head (log2 units)
@@ -340,42 +339,28 @@ __device__ __forceinline__ void visible_columns(const PairGeom &g, int tau, int 
 // the first 64 columns of the S buffer (columns 32u .. 32u+31 hold rows
 // 64u .. 64u+63 of the tile, two per column) and sums the same fp16 values.
 // A thread rewrites only its own lane, and only columns it has already read.
-// SC (rows given as decoded E4M3 codes with per-row scales): row c's K scale
-// multiplies column c's score and its V scale the P fed to PV (the sums keep
-// P); the tile's 128 scales are read once per pair (one per thread) and
-// shared through shared memory, and the four warps then leave together.
-template <bool SC>
 __device__ __forceinline__ void pair_softmax(const PairParams &p, uint32_t tmem, PairMisc &ms, int r) {
   volatile int *abrt = &ms.abort_flag;
   const int tau = r >> 6, h = r & 63;
   const uint32_t lane_base = static_cast<uint32_t>(r & ~31) << 16;
   const int n_pairs = (p.T + 1) / 2;
   uint32_t n = 0;
-  // Leaving is decided per warp (the TMEM accesses are warp-collective), or
-  // by all four warps at their named barrier when there is one.
-  auto leave = [&](bool bad) { return SC ? bar_red_or(4, kPRowThreads, bad) : !__all_sync(0xffffffffu, !bad); };
-  grid_dependency_wait();  // lse may still be read by the previous kernel; the scales are inputs
+  grid_dependency_wait();  // lse may still be read by the previous kernel
   for (int pr = blockIdx.x; pr < n_pairs; pr += gridDim.x, ++n) {
     const PairGeom g = pair_geom(p, pr);
     int c0, c1;
     visible_columns(g, tau, c0, c1);
     const bool with_x = tau == 0 && g.extra;
-    if (SC) {
-      const int row = g.tile_lo + r;
-      const bool in = row >= 0 && row < p.n_raw;
-      ms.ksc[n & 1][r] = in ? __ldg(p.k_scale + row) : 0.f;
-      ms.vsc[n & 1][r] = in ? __ldg(p.v_scale + row) : 0.f;
-    }
     // The extra-row warp's scores of this pair (every pair, so the phases
     // stay in step), then the pair's S.
+    // (Decisions to leave are made per warp: the TMEM accesses below are
+    // warp-collective.)
     const bool ready =
         mbar_wait(smem_u32(&ms.x_full[n & 1]), (n >> 1) & 1, abrt, p.timeout_ns, p.err, SITE_PR_X_FULL) &&
         mbar_wait(smem_u32(&ms.s_full[n & 1]), (n >> 1) & 1, abrt, p.timeout_ns, p.err, SITE_PR_S_FULL);
-    if (leave(!ready)) break;  // (the barrier also publishes the scales)
+    if (!__all_sync(0xffffffffu, ready)) break;
     tc_fence_after();
     const uint32_t sb = tmem + s_column(n) + lane_base;
-    const float *ksc = ms.ksc[n & 1];
-    const float *vsc = ms.vsc[n & 1];
     const float sxv = with_x ? ms.sx[n & 1][h] : -INFINITY;
     float mx = sxv;
 #pragma unroll 1
@@ -386,8 +371,7 @@ __device__ __forceinline__ void pair_softmax(const PairParams &p, uint32_t tmem,
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
         const int col = 64 * u + c;
-        const float sl2 = SC ? p.scale_log2 * ksc[col] : p.scale_log2;
-        if (col >= c0 && col < c1) mx = fmaxf(mx, s[c] * sl2);
+        if (col >= c0 && col < c1) mx = fmaxf(mx, s[c] * p.scale_log2);
       }
     }
     const float mu = mx == -INFINITY ? 0.f : mx;
@@ -401,19 +385,12 @@ __device__ __forceinline__ void pair_softmax(const PairParams &p, uint32_t tmem,
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
         const int col = 64 * u + 2 * i;
-        const float sl0 = SC ? p.scale_log2 * ksc[col] : p.scale_log2;
-        const float sl1 = SC ? p.scale_log2 * ksc[col + 1] : p.scale_log2;
-        const float e0 = (col >= c0 && col < c1) ? exp2f(s[2 * i] * sl0 - mu) : 0.f;
-        const float e1 = (col + 1 >= c0 && col + 1 < c1) ? exp2f(s[2 * i + 1] * sl1 - mu) : 0.f;
+        const float e0 = (col >= c0 && col < c1) ? exp2f(s[2 * i] * p.scale_log2 - mu) : 0.f;
+        const float e1 = (col + 1 >= c0 && col + 1 < c1) ? exp2f(s[2 * i + 1] * p.scale_log2 - mu) : 0.f;
         const __half2 hp = __floats2half2_rn(e0, e1);
         const float2 f = __half22float2(hp);
         lsum += f.x + f.y;
-        if (SC) {  // P times the row's V scale feeds the MMA; the sums keep P
-          const __half2 hv = __floats2half2_rn(e0 * vsc[col], e1 * vsc[col + 1]);
-          pk[i] = __uint_as_float(*reinterpret_cast<const uint32_t *>(&hv));
-        } else {
-          pk[i] = __uint_as_float(*reinterpret_cast<const uint32_t *>(&hp));
-        }
+        pk[i] = __uint_as_float(*reinterpret_cast<const uint32_t *>(&hp));
       }
       tmem_st32(sb + 32 * u, pk);
     }
@@ -429,10 +406,9 @@ __device__ __forceinline__ void pair_softmax(const PairParams &p, uint32_t tmem,
     // previous pair.
     const bool free_st =
         mbar_wait(smem_u32(&ms.st_empty[n & 1]), ((n >> 1) & 1) ^ 1, abrt, p.timeout_ns, p.err, SITE_PR_ST_EMPTY);
-    if (leave(!free_st)) break;
+    if (!__all_sync(0xffffffffu, free_st)) break;
     ms.inv_l[n & 1][r] = lsum > 0.f ? 1.f / lsum : 0.f;
-    // (SC: the extra row's weight times its V scale meets its decoded V row in the epilogue)
-    if (tau == 0) ms.px[n & 1][h] = (SC && with_x) ? px * __ldg(p.v_scale + g.tile_lo - 1) : px;
+    if (tau == 0) ms.px[n & 1][h] = px;
     mbar_arrive(smem_u32(&ms.st_full[n & 1]));
     if (p.lse != nullptr && (tau == 0 || g.has_b))
       p.lse[(long long)(g.ta + tau) * kH + h] = lsum > 0.f ? (mx + log2f(lsum)) * kLn2 : -INFINITY;
@@ -543,7 +519,6 @@ __device__ __forceinline__ void load_extra_row(const PairParams &p, const PairGe
   }
 }
 
-template <bool SC>
 __device__ __forceinline__ void pair_extra_row(const PairParams &p, uint8_t *smem, PairMisc &ms, int lane) {
   volatile int *abrt = &ms.abort_flag;
   const int n_pairs = (p.T + 1) / 2;
@@ -606,16 +581,13 @@ __device__ __forceinline__ void pair_extra_row(const PairParams &p, uint8_t *sme
     }
     // The next pair's rows travel while this pair finishes.
     if (pr + (int)gridDim.x < n_pairs) load_extra_row(p, pair_geom(p, pr + gridDim.x), lane, kr, vr);
-    // (SC: the row's K scale multiplies its scores)
-    const float sl2 = (SC && g.extra) ? p.scale_log2 * __ldg(p.k_scale + g.tile_lo - 1) : p.scale_log2;
-    ms.sx[n & 1][lane] = acc0 * sl2;
-    ms.sx[n & 1][lane + 32] = acc1 * sl2;
+    ms.sx[n & 1][lane] = acc0 * p.scale_log2;
+    ms.sx[n & 1][lane + 32] = acc1 * p.scale_log2;
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&ms.x_full[n & 1]));
   }
 }
 
-template <bool SC>
 __global__ void __launch_bounds__(kPThreads, 1) attn_pair_kernel(const __grid_constant__ PairParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -661,7 +633,7 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_pair_kernel(const __grid_co
   const uint32_t tmem = ms.tmem_base;
   grid_launch_dependents();
   if (warp < kPSoftWarps) {
-    pair_softmax<SC>(p, tmem, ms, threadIdx.x);
+    pair_softmax(p, tmem, ms, threadIdx.x);
   } else if (warp < kPEpiWarp0 + 4) {
     pair_epilogue(p, smem, tmem, ms, threadIdx.x - 32 * kPEpiWarp0);
   } else if (warp == kPLoaderWarp) {
@@ -671,7 +643,7 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_pair_kernel(const __grid_co
     if (lane == 0) pair_mma(p, sbase, tmem, ms);
     __syncwarp();
   } else {
-    pair_extra_row<SC>(p, smem, ms, lane);
+    pair_extra_row(p, smem, ms, lane);
   }
   tc_fence_before();
   __syncthreads();
@@ -682,10 +654,7 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_pair_kernel(const __grid_co
 }  // namespace
 
 cudaError_t prepare_pair_kernel() {
-  cudaError_t e = cudaFuncSetAttribute(attn_pair_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)kPSmemBytes);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(attn_pair_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPSmemBytes);
+  return cudaFuncSetAttribute(attn_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPSmemBytes);
 }
 
 cudaError_t launch_pair(const PairParams &p, int grid, cudaStream_t s) {
@@ -699,8 +668,7 @@ cudaError_t launch_pair(const PairParams &p, int grid, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return p.k_scale != nullptr ? cudaLaunchKernelEx(&cfg, attn_pair_kernel<true>, p)
-                              : cudaLaunchKernelEx(&cfg, attn_pair_kernel<false>, p);
+  return cudaLaunchKernelEx(&cfg, attn_pair_kernel, p);
 }
 
 }  // namespace ds4a

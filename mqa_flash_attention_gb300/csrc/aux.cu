@@ -459,15 +459,17 @@ __global__ void quantize_fp8_kernel(const uint8_t *__restrict__ src, long long s
   }
 }
 
-// ------------------------------------------------------------------ E4M3 rows -> fp16 codes' values
-// Rows of K and V codes to their decoded values decode(code) in fp16 (exact:
-// every E4M3 value is an fp16 value; the row scales stay apart), [n][512]
-// each.  Thread i handles 16 codes (one 16-byte load, two 16-byte stores),
-// grid-stride over both arrays.
+// ------------------------------------------------------------------ E4M3 rows -> fp16 row values
+// Rows of K and V codes to their values decode(code) * scale rounded to fp16
+// (decode(code) itself is exact in fp16; the product is rounded once, as an
+// fp16 row of the same values would be), [n][512] each.  Thread i handles 16
+// codes (one 16-byte load, two 16-byte stores), grid-stride over both arrays.
+// The next kernel may start at once: it waits for this grid before its reads.
 
 __global__ void widen_e4m3_rows_kernel(const uint8_t *__restrict__ kc, const uint8_t *__restrict__ vc,
-                                       long long stride, int n_rows, __half *__restrict__ ko,
-                                       __half *__restrict__ vo) {
+                                       const float *__restrict__ ks, const float *__restrict__ vs, long long stride,
+                                       int n_rows, __half *__restrict__ ko, __half *__restrict__ vo) {
+  grid_launch_dependents();
   const long long per = (long long)n_rows * 32;  // 16-code chunks per array
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < 2 * per;
        i += (long long)gridDim.x * blockDim.x) {
@@ -475,12 +477,15 @@ __global__ void widen_e4m3_rows_kernel(const uint8_t *__restrict__ kc, const uin
     const long long j = is_v ? i - per : i;
     const int row = (int)(j >> 5), c = (int)(j & 31);
     const uint4 w = __ldg(reinterpret_cast<const uint4 *>((is_v ? vc : kc) + row * stride) + c);
+    const float sc = __ldg((is_v ? vs : ks) + row);
     const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
     uint32_t h[8];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      h[2 * k] = e4m3x2_to_f16x2(static_cast<uint16_t>(wd[k] & 0xFFFFu));
-      h[2 * k + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(wd[k] >> 16));
+    for (int k = 0; k < 8; ++k) {
+      const uint32_t d = e4m3x2_to_f16x2(static_cast<uint16_t>(k & 1 ? wd[k >> 1] >> 16 : wd[k >> 1] & 0xFFFFu));
+      const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&d));
+      const __half2 r = __floats2half2_rn(f.x * sc, f.y * sc);
+      h[k] = *reinterpret_cast<const uint32_t *>(&r);
     }
     uint4 *dst = reinterpret_cast<uint4 *>((is_v ? vo : ko) + (long long)row * 512 + 16 * c);
     dst[0] = make_uint4(h[0], h[1], h[2], h[3]);
@@ -488,15 +493,16 @@ __global__ void widen_e4m3_rows_kernel(const uint8_t *__restrict__ kc, const uin
   }
 }
 
-cudaError_t launch_widen_e4m3_rows(const void *k_codes, const void *v_codes, long long stride, int n_rows,
-                                   __half *k_out, __half *v_out, cudaStream_t s) {
+cudaError_t launch_widen_e4m3_rows(const void *k_codes, const void *v_codes, const float *k_scale,
+                                   const float *v_scale, long long stride, int n_rows, __half *k_out, __half *v_out,
+                                   cudaStream_t s) {
   if (n_rows <= 0) return cudaSuccess;
   const int threads = 256;
   long long blocks = ((long long)n_rows * 64 + threads - 1) / threads;
   if (blocks > 4096) blocks = 4096;
   widen_e4m3_rows_kernel<<<(unsigned)blocks, threads, 0, s>>>(static_cast<const uint8_t *>(k_codes),
-                                                              static_cast<const uint8_t *>(v_codes), stride, n_rows,
-                                                              k_out, v_out);
+                                                              static_cast<const uint8_t *>(v_codes), k_scale, v_scale,
+                                                              stride, n_rows, k_out, v_out);
   return cudaGetLastError();
 }
 

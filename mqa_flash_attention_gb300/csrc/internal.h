@@ -25,7 +25,6 @@ struct PairParams {
   int T, q_pos0, n_raw, raw_pos0, window;
   float scale_log2;
   const uint8_t *k_raw, *v_raw;  // the row below a pair's tile is read directly
-  const float *k_scale, *v_scale;  // per-row scales of rows given as decoded E4M3 codes (else null)
   long long raw_row_stride;      // bytes
   __half *o;
   long long o_tok_stride;        // elements
@@ -46,8 +45,9 @@ cudaError_t launch_block_mask_dense(const GeomScalars &g, const __half *mask, lo
 cudaError_t launch_combine(const __half *ws_o, const float2 *ws_ml, int n_splits, int T, __half *o,
                            long long o_tok_stride, float *lse, cudaStream_t s);
 cudaError_t launch_selftest_wait(unsigned long long timeout_ns, unsigned int *err, cudaStream_t s);
-cudaError_t launch_widen_e4m3_rows(const void *k_codes, const void *v_codes, long long stride, int n_rows,
-                                   __half *k_out, __half *v_out, cudaStream_t s);
+cudaError_t launch_widen_e4m3_rows(const void *k_codes, const void *v_codes, const float *k_scale,
+                                   const float *v_scale, long long stride, int n_rows, __half *k_out, __half *v_out,
+                                   cudaStream_t s);
 cudaError_t launch_quantize_fp8(const void *src, long long src_stride, int n_rows, void *dst, long long dst_stride,
                                 float *scales, cudaStream_t s);
 
