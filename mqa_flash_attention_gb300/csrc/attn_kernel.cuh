@@ -257,13 +257,14 @@ struct Ring {
 // loading meanwhile: K(0), then K(j+1) and V(j) for each tile j.  Without it
 // each tile's parts come together (always when parts are held from QK^T until
 // PV: K = V rows, paired stages).  Measured (one GB300): look-ahead takes the
-// indexed r4 prefill chunk from 366 to 332 us and the E4M3 256K decode from
-// 102 to 98 us, but slows the long fp16 decodes (8K rows 13.7 -> 14.4 us)
-// and the E4M3 prefill (106 -> 117 us), so it is a separate instantiation
+// indexed r4 prefill chunk from 366 to 332 us, the E4M3 256K decode from 102
+// to 98 us and, with the sixteen-warp layout, the fp16 split-KV decodes too
+// (65,536 rows 33.8 -> 32.2 us, 64 batched sequences 22.9 -> 21.8 us), but
+// slows the E4M3 prefill (106 -> 117 us), so it is a separate instantiation
 // chosen per call (launch_attn), which leaves the code of the others as it
-// was.
+// was: split-KV decode and indexed calls.
 __host__ __device__ __forceinline__ bool look_ahead_suits(const AttnParams &p) {
-  return !p.alias_kv && !p.kv_pair && (p.mode == MODE_INDEXED || (p.comp_fp8 && p.partial));
+  return !p.alias_kv && !p.kv_pair && (p.mode == MODE_INDEXED || p.partial);
 }
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
