@@ -545,6 +545,41 @@ ds4a_status ds4a_device_error_word(ds4a_stream_t stream, uint32_t *word, int cle
  */
 ds4a_status ds4a_selftest_wait_timeout(uint64_t timeout_ns, ds4a_stream_t stream);
 
+/*
+ * ds4a_graph_begin / ds4a_graph_end / ds4a_graph_launch / ds4a_graph_destroy -
+ * record the ds4a calls a thread makes on one stream and replay them as one
+ * CUDA graph (a serving step issued as one launch instead of each call's host
+ * work: argument checks, tensor maps, one launch per kernel).
+ *   ds4a_graph_begin(stream)   starts the recording.  stream must be a created
+ *                              stream (NULL, the legacy default stream, is
+ *                              rejected).  The first call on a device loads
+ *                              every kernel of the library first: a kernel's
+ *                              first launch loads its code, which a recording
+ *                              does not allow.
+ *   ds4a calls on stream       checked as usual; a call that returns an error
+ *                              records nothing.  Their kernels are recorded,
+ *                              not run.  Calls that read results back to the
+ *                              host (ds4a_device_status, ds4a_device_error_word)
+ *                              cannot be recorded.
+ *   ds4a_graph_end(stream, &g) ends the recording (always) and instantiates
+ *                              it into *g; DS4A_ERR_CUDA and *g = NULL when a
+ *                              recorded launch failed.
+ *   ds4a_graph_launch(g, s)    runs the recorded kernels on stream s with the
+ *                              arguments they were recorded with: the same
+ *                              buffers, sizes and layouts, whatever those
+ *                              buffers hold then.  A recorded call's workspace
+ *                              is reused by every launch, so launches that
+ *                              share one must not overlap (one stream, or
+ *                              events between streams).
+ *   ds4a_graph_destroy(g)      frees the graph (NULL: no-op); launches already
+ *                              issued complete, none may be issued after.
+ */
+typedef struct ds4a_graph_s *ds4a_graph;
+ds4a_status ds4a_graph_begin(ds4a_stream_t stream);
+ds4a_status ds4a_graph_end(ds4a_stream_t stream, ds4a_graph *graph);
+ds4a_status ds4a_graph_launch(ds4a_graph graph, ds4a_stream_t stream);
+void ds4a_graph_destroy(ds4a_graph graph);
+
 #ifdef __cplusplus
 }
 #endif

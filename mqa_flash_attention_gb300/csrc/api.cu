@@ -9,6 +9,7 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <new>
 
 #include "ds4a.h"
 #include "internal.h"
@@ -37,6 +38,7 @@ struct DeviceState {
   int sm_count = 0;
   unsigned int *err = nullptr;
   void *scratch = nullptr;  // device address of g_decode_scratch
+  bool loaded = false;      // every kernel's code loaded (before a recording)
 };
 
 std::mutex g_mu;
@@ -1119,3 +1121,75 @@ ds4a_status ds4a_indexer_topk(const ds4a_layout *L, const float *scores, int64_t
   p.cached_keys = (max_n <= top_k || max_n > ds4a::kTopkMaxCachedKeys) ? 0 : (int)max_n;
   return launched(ds4a::launch_indexer_topk(p, p.cached_keys * 4, as_cuda(stream)));
 }
+
+// ------------------------------------------------------------------ recorded call sequences
+
+struct ds4a_graph_s {
+  cudaGraph_t graph;
+  cudaGraphExec_t exec;
+};
+
+extern "C" {
+
+ds4a_status ds4a_graph_begin(ds4a_stream_t stream) {
+  if (stream == nullptr) return DS4A_ERR_INVALID_ARG;  // the legacy default stream cannot be recorded
+  DeviceState *d = nullptr;
+  ds4a_status st = current_device(&d);
+  if (st != DS4A_OK) return st;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!d->loaded) {
+      // A kernel's first launch loads its code, which a recording does not allow.
+      DS4A_CUDA_TRY(ds4a::preload_aux_kernels());
+      DS4A_CUDA_TRY(ds4a::preload_indexer_kernels());
+      DS4A_CUDA_TRY(ds4a::preload_compressor_kernels());
+      d->loaded = true;
+    }
+  }
+  DS4A_CUDA_TRY(cudaStreamBeginCapture(as_cuda(stream), cudaStreamCaptureModeThreadLocal));
+  return DS4A_OK;
+}
+
+ds4a_status ds4a_graph_end(ds4a_stream_t stream, ds4a_graph *graph) {
+  if (graph != nullptr) *graph = nullptr;
+  if (stream == nullptr) return DS4A_ERR_INVALID_ARG;
+  cudaGraph_t g = nullptr;
+  const cudaError_t e = cudaStreamEndCapture(as_cuda(stream), &g);  // ends the recording in every case
+  if (e != cudaSuccess) {
+    if (g != nullptr) cudaGraphDestroy(g);
+    return cuda_failed("cudaStreamEndCapture", e);
+  }
+  if (graph == nullptr) {
+    cudaGraphDestroy(g);
+    return DS4A_ERR_INVALID_ARG;
+  }
+  cudaGraphExec_t x = nullptr;
+  const cudaError_t ei = cudaGraphInstantiate(&x, g, 0);
+  if (ei != cudaSuccess) {
+    cudaGraphDestroy(g);
+    return cuda_failed("cudaGraphInstantiate", ei);
+  }
+  ds4a_graph h = new (std::nothrow) ds4a_graph_s{g, x};
+  if (h == nullptr) {
+    cudaGraphExecDestroy(x);
+    cudaGraphDestroy(g);
+    return cuda_failed("allocation of the graph handle", (int)cudaErrorMemoryAllocation, nullptr);
+  }
+  *graph = h;
+  return DS4A_OK;
+}
+
+ds4a_status ds4a_graph_launch(ds4a_graph graph, ds4a_stream_t stream) {
+  if (graph == nullptr) return DS4A_ERR_INVALID_ARG;
+  const cudaError_t e = cudaGraphLaunch(graph->exec, as_cuda(stream));
+  return e == cudaSuccess ? DS4A_OK : cuda_failed("cudaGraphLaunch", e);
+}
+
+void ds4a_graph_destroy(ds4a_graph graph) {
+  if (graph == nullptr) return;
+  cudaGraphExecDestroy(graph->exec);
+  cudaGraphDestroy(graph->graph);
+  delete graph;
+}
+
+}  // extern "C"

@@ -516,4 +516,20 @@ cudaError_t launch_quantize_fp8(const void *src, long long src_stride, int n_row
   return cudaGetLastError();
 }
 
+// Loads the code of every kernel listed (lazy module loading would otherwise
+// do it at a kernel's first launch, which may fall inside a stream capture).
+cudaError_t preload_aux_kernels() {
+  const void *k[] = {(const void *)pad_kernel,          (const void *)block_mask_struct_kernel,
+                     (const void *)block_mask_dense_kernel, (const void *)combine_kernel,
+                     (const void *)combine_wide_kernel, (const void *)combine_small_kernel,
+                     (const void *)selftest_wait_kernel, (const void *)quantize_fp8_kernel,
+                     (const void *)widen_e4m3_rows_kernel};
+  for (const void *f : k) {
+    cudaFuncAttributes a;
+    const cudaError_t e = cudaFuncGetAttributes(&a, f);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
 }  // namespace ds4a

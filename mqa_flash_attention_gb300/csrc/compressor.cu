@@ -198,4 +198,13 @@ cudaError_t launch_compress(const CompressParams &p, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+// Loads the code of every kernel listed (lazy module loading would otherwise
+// do it at a kernel's first launch, which may fall inside a stream capture).
+cudaError_t preload_compressor_kernels() {
+  cudaFuncAttributes a;
+  cudaError_t e = cudaFuncGetAttributes(&a, (const void *)compress_pool_kernel);
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, (const void *)compress_append_kernel);
+  return e;
+}
+
 }  // namespace ds4a

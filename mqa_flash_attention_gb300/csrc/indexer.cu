@@ -595,4 +595,25 @@ cudaError_t launch_indexer_scores(const ScoreParams &p, int n_heads, int grid, c
   return p.relu ? launch_scores_relu<true>(p, n_heads, grid, s) : launch_scores_relu<false>(p, n_heads, grid, s);
 }
 
+// Loads the code of every kernel listed (lazy module loading would otherwise
+// do it at a kernel's first launch, which may fall inside a stream capture).
+cudaError_t preload_indexer_kernels() {
+  const void *k[] = {
+      (const void *)indexer_topk_kernel<true>,          (const void *)indexer_topk_kernel<false>,
+      (const void *)indexer_scores_kernel<1, false>,   (const void *)indexer_scores_kernel<1, true>,
+      (const void *)indexer_scores_kernel<2, false>,   (const void *)indexer_scores_kernel<2, true>,
+      (const void *)indexer_scores_kernel<4, false>,   (const void *)indexer_scores_kernel<4, true>,
+      (const void *)indexer_scores_kernel<8, false>,   (const void *)indexer_scores_kernel<8, true>,
+      (const void *)indexer_scores_kernel<16, false>,  (const void *)indexer_scores_kernel<16, true>,
+      (const void *)indexer_scores_kernel<32, false>,  (const void *)indexer_scores_kernel<32, true>,
+      (const void *)indexer_scores_kernel<64, false>,  (const void *)indexer_scores_kernel<64, true>,
+      (const void *)indexer_scores_kernel<128, false>, (const void *)indexer_scores_kernel<128, true>};
+  for (const void *f : k) {
+    cudaFuncAttributes a;
+    const cudaError_t e = cudaFuncGetAttributes(&a, f);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
 }  // namespace ds4a

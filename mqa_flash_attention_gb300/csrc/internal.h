@@ -48,6 +48,7 @@ cudaError_t launch_selftest_wait(unsigned long long timeout_ns, unsigned int *er
 cudaError_t launch_widen_e4m3_rows(const void *k_codes, const void *v_codes, const float *k_scale,
                                    const float *v_scale, long long stride, int n_rows, __half *k_out, __half *v_out,
                                    cudaStream_t s);
+cudaError_t preload_aux_kernels();
 cudaError_t launch_quantize_fp8(const void *src, long long src_stride, int n_rows, void *dst, long long dst_stride,
                                 float *scales, cudaStream_t s);
 
@@ -55,6 +56,7 @@ cudaError_t launch_quantize_fp8(const void *src, long long src_stride, int n_row
 constexpr int kTopkMaxCachedKeys = 32768;  // candidate keys a top-k CTA keeps in shared memory
 cudaError_t launch_indexer_topk(const TopkParams &p, int dyn_smem, cudaStream_t s);
 cudaError_t launch_indexer_scores(const ScoreParams &p, int n_heads, int grid, cudaStream_t s);
+cudaError_t preload_indexer_kernels();
 
 // compressor.cu
 // One append of n_new rows to a compressor state holding n_state rows
@@ -74,5 +76,6 @@ struct CompressParams {
 };
 void compress_shape(int ratio, int *splits, int *slots);
 cudaError_t launch_compress(const CompressParams &p, cudaStream_t s);
+cudaError_t preload_compressor_kernels();
 
 }  // namespace ds4a

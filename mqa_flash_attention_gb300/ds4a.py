@@ -134,6 +134,14 @@ def lib() -> ctypes.CDLL:
         L.ds4a_device_error_word.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
         L.ds4a_selftest_wait_timeout.restype = st
         L.ds4a_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
+        L.ds4a_graph_begin.restype = st
+        L.ds4a_graph_begin.argtypes = [vp]
+        L.ds4a_graph_end.restype = st
+        L.ds4a_graph_end.argtypes = [vp, ctypes.POINTER(vp)]
+        L.ds4a_graph_launch.restype = st
+        L.ds4a_graph_launch.argtypes = [vp, vp]
+        L.ds4a_graph_destroy.restype = None
+        L.ds4a_graph_destroy.argtypes = [vp]
         _lib = L
     return _lib
 
@@ -368,6 +376,59 @@ class PreparedCall:
         st = self._fn(*self._args)
         if st != OK:
             raise Ds4aError(st, self._name)
+
+
+class Graph:
+    """The library calls made on ``stream`` inside ``with graph:``, recorded
+    once and replayed by ``graph()`` as one CUDA graph launch
+    (``ds4a_graph_begin`` / ``_end`` / ``_launch``).  Each replay runs the
+    recorded kernels on the same buffers, sizes and layouts with whatever the
+    buffers hold then.  Give every recorded call its outputs and workspace
+    explicitly (an allocation inside the recording would be freed while the
+    graph still uses it), keep the tensors alive while the graph is used, and
+    do not overlap replays that share a workspace."""
+
+    def __init__(self, stream):
+        if stream is None:
+            raise ValueError("a graph records a created stream, not the default stream")
+        self._stream = stream
+        self._h = ctypes.c_void_p()
+        self._args = None
+
+    def __enter__(self):
+        if self._h:
+            raise RuntimeError("this graph was already recorded")
+        _check(lib().ds4a_graph_begin(_stream(self._stream)), "ds4a_graph_begin")
+        return self
+
+    def __exit__(self, exc_type, exc, tb):
+        st = lib().ds4a_graph_end(_stream(self._stream), ctypes.byref(self._h))
+        if exc_type is None:
+            _check(st, "ds4a_graph_end")
+        self._args = (self._h, _stream(self._stream))
+        self._fn = lib().ds4a_graph_launch
+        return False
+
+    def __call__(self, stream=None) -> None:
+        """One replay on the recording stream (or on ``stream``)."""
+        args = self._args if stream is None else (self._h, _stream(stream))
+        if args is None or not self._h:
+            raise RuntimeError("the graph holds no recording")
+        st = self._fn(*args)
+        if st != OK:
+            raise Ds4aError(st, "ds4a_graph_launch")
+
+    def close(self) -> None:
+        if self._h:
+            lib().ds4a_graph_destroy(self._h)
+            self._h = ctypes.c_void_p()
+            self._args = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def prepare_decode(layout, q, k_raw, v_raw, k_comp=None, v_comp=None, *, n_splits=0, workspace, out, lse=None,

@@ -171,6 +171,17 @@ def test_prefill_fp8kv_workspace_is_checked(lib):
     assert f(ctypes.byref(L), ctypes.byref(X2), ctypes.byref(S), FAKE, need, None) == ds4a.ERR_INVALID_ARG
 
 
+def test_graph_arguments_are_checked(lib):
+    """Recording needs a created stream and a handle slot; launching needs a
+    graph; destroying NULL is a no-op.  All refused before any CUDA call."""
+    assert lib.ds4a_graph_begin(None) == ds4a.ERR_INVALID_ARG
+    h = ctypes.c_void_p()
+    assert lib.ds4a_graph_end(None, ctypes.byref(h)) == ds4a.ERR_INVALID_ARG
+    assert not h
+    assert lib.ds4a_graph_launch(None, FAKE) == ds4a.ERR_INVALID_ARG
+    lib.ds4a_graph_destroy(None)
+
+
 def test_indexed_fp8kv_arguments_are_checked(lib):
     """Rejected before any device access: no scales, a missing compressed-row
     scale, top_k out of 1..4096, no lists, a list stride below 4 * top_k."""
