@@ -477,9 +477,9 @@ __device__ __forceinline__ void loader_role(const AttnParams &p, uint32_t sbase,
       ring.advance();
       return true;
     };
-    // The compressed rows a gathered tile lists, into list `ib`.  The list
-    // may be rewritten once every thread has issued the copies of the tile
-    // that used it last (a copy takes its address when it is issued).
+    // The compressed rows a gathered tile lists, into list `ib`.  A list may
+    // be rewritten once every thread has issued the copies of the tile that
+    // used it last (a copy takes its address when it is issued).
     auto load_list = [&](const Tile &tl, int ib) {
       named_bar_sync(2, kGroup);
       const int32_t *lst = p.idx + (long long)ip.t * p.idx_stride;
@@ -490,9 +490,51 @@ __device__ __forceinline__ void loader_role(const AttnParams &p, uint32_t sbase,
       }
       named_bar_sync(2, kGroup);
     };
+    // With E4M3 rows the group is 96 threads and each reads two slots of a
+    // list: there the slots are read into registers one tile ahead of their
+    // use (fetch_list), so the reads' latency passes while the group copies
+    // the tile before, and store_list writes them into the list (indexed
+    // E4M3 chunk 457 -> 423 us).  The fp16 kernel keeps load_list: the same
+    // read-ahead left its indexed time unchanged and, by its mere presence,
+    // slowed its long decodes by 1-2%.
+    auto fetch_list = [&](const Tile &tl, int (&v)[2]) {
+      const int32_t *lst = p.idx + (long long)ip.t * p.idx_stride;
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int k = gtid + u * kGroup, slot = tl.start + k;
+        v[u] = (k < 128 && slot < p.top_k) ? __ldg(lst + slot) : -1;
+      }
+    };
+    auto store_list = [&](const int (&v)[2], int ib) {
+      named_bar_sync(2, kGroup);
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int k = gtid + u * kGroup;
+        if (k < 128) ms.idx_s[ib][k] = (v[u] >= 0 && v[u] < p.n_comp) ? v[u] : 0;  // empty slots: row 0, masked
+      }
+      named_bar_sync(2, kGroup);
+    };
+    static_assert(!FP8 || 2 * kGroup >= 128, "two list slots per thread cover a tile");
+    // The tile after the cursor's position, without moving the cursor.
+    auto peek = [&]() -> Tile {
+      TileCursor c = ip.cur;
+      return c.next(p);
+    };
     const int nt = ip.j1 - ip.j0;
+    int lv[2] = {-1, -1};  // (E4M3) list slots of the next gathered tile, read ahead
     Tile cur = ip.cur.next(p);
-    if (cur.seg == 2) load_list(cur, 0);
+    if (cur.seg == 2) {
+      if (FP8) {
+        fetch_list(cur, lv);
+        store_list(lv, 0);
+      } else {
+        load_list(cur, 0);
+      }
+    }
+    if (FP8 && group && nt > 1) {
+      const Tile t1 = peek();
+      if (t1.seg == 2) fetch_list(t1, lv);
+    }
     if (LA) {
       // Ring order: the K parts of tile 0, then for each tile the K parts of
       // the next tile before its own V parts (see mma_role).
@@ -503,7 +545,16 @@ __device__ __forceinline__ void loader_role(const AttnParams &p, uint32_t sbase,
         Tile nxt = cur;
         if (jj + 1 < nt) {
           nxt = ip.cur.next(p);
-          if (nxt.seg == 2) load_list(nxt, (jj + 1) & 1);
+          if (nxt.seg == 2) {
+            if (FP8)
+              store_list(lv, (jj + 1) & 1);
+            else
+              load_list(nxt, (jj + 1) & 1);
+          }
+          if (FP8 && group && jj + 2 < nt) {
+            const Tile t2 = peek();
+            if (t2.seg == 2) fetch_list(t2, lv);
+          }
           for (int part = 0; part < 4; ++part) ok = ok && emit(nxt, part, (jj + 1) & 1);
         }
         for (int part = 4; part < 8; ++part) ok = ok && emit(cur, part, jj & 1);
@@ -516,7 +567,16 @@ __device__ __forceinline__ void loader_role(const AttnParams &p, uint32_t sbase,
       for (int jj = 0; jj < nt; ++jj) {
         if (jj > 0) {
           cur = ip.cur.next(p);
-          if (cur.seg == 2) load_list(cur, 0);
+          if (cur.seg == 2) {
+            if (FP8)
+              store_list(lv, 0);
+            else
+              load_list(cur, 0);
+          }
+          if (FP8 && group && jj + 1 < nt) {
+            const Tile t1 = peek();
+            if (t1.seg == 2) fetch_list(t1, lv);
+          }
         }
 #pragma unroll 1
         for (int part = 0; part < n_parts; ++part) ok = ok && emit(cur, part, 0);
