@@ -250,6 +250,40 @@ def test_prefill_fp8kv_pairs(torch, ds4a, case, path):
     assert np.abs(got[fin] - wlse[fin]).max() <= 1e-3
 
 
+def test_prefill_fp8kv_padded_code_rows(torch, ds4a):
+    """E4M3 raw rows at a 1024-byte row stride (codes in the first 512 bytes,
+    the rest 0xFF, an E4M3 NaN code that must never be read) through the
+    workspace call, the workspace pre-filled with NaN rows: against the oracle
+    over the decoded rows.  A workspace one byte short is refused."""
+    wl = W.draw("fp8_padded", 131, make_layout(T=45, q_pos0=900, n_raw=400, raw_pos0=700))
+    L = wl.layout
+    ops, dec = {}, {}
+    for nm in ("k_raw", "v_raw"):
+        codes, scales = f8.quantize_rows(getattr(wl, nm))
+        padded = np.full((codes.shape[0], 1024), 0xFF, dtype=np.uint8)
+        padded[:, :512] = codes
+        ops[nm] = dev(torch, padded)[:, :512]
+        ops[nm + "_scale"] = dev(torch, scales)
+        dec[nm] = f8.dequantize_rows(codes, scales)
+    assert ops["k_raw"].stride(0) == 1024
+    want, wlse = oracle.attention(L, wl.q, dec["k_raw"], dec["v_raw"], None, None)
+    q = dev(torch, wl.q)
+    need = ds4a.prefill_fp8kv_workspace_size(L)
+    assert need == (945 - 900 + 127) * 2 * 1024  # positions 773 .. 944 are seen
+    ws = torch.full((need // 2,), float("nan"), dtype=torch.float16, device="cuda")
+    out = torch.full_like(q, float("nan"))
+    o, lse = ds4a.attn_prefill_fp8kv(L, q, ops["k_raw"], ops["v_raw"], k_raw_scale=ops["k_raw_scale"],
+                                     v_raw_scale=ops["v_raw_scale"], workspace=ws, out=out, want_lse=True)
+    _check(host(o), want, "fp8 padded code rows")
+    fin = np.isfinite(wlse)
+    assert np.abs(host(lse)[fin] - wlse[fin]).max() <= 1e-3
+    short = torch.empty(need - 1, dtype=torch.uint8, device="cuda")
+    with pytest.raises(ds4a.Ds4aError) as e:
+        ds4a.attn_prefill_fp8kv(L, q, ops["k_raw"], ops["v_raw"], k_raw_scale=ops["k_raw_scale"],
+                                v_raw_scale=ops["v_raw_scale"], workspace=short, out=out)
+    assert e.value.status == ds4a.ERR_WORKSPACE
+
+
 def _indexed_fp8(torch, ds4a, wl, idx, raw_fp8):
     """E4M3 indexed attention (listed compressed rows as codes; raw rows as
     codes too with raw_fp8) against the oracle over the decoded rows, the
