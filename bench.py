@@ -833,8 +833,9 @@ def run_also(torch, ds4a, W, dev, stream, pk, pk_kind):
 
 # ------------------------------------------------------------------ profiling cases
 
-CASES = ("tiny", "decode_r128_32k", "prefill_raw_2048", "indexed_r4_2048", "decode_long_262144",
-         "decode_long_262144_fp8kv", "indexer_r4_2048", "compressor_r4_2048", "compressor_r128_2048")
+CASES = ("tiny", "decode_r128_32k", "prefill_raw_2048", "prefill_raw_2048_fp8kv", "indexed_r4_2048",
+         "decode_long_262144", "decode_long_262144_fp8kv", "indexer_r4_2048", "compressor_r4_2048",
+         "compressor_r128_2048")
 
 
 def run_case(name: str, calls: int) -> None:
@@ -878,6 +879,23 @@ def run_case(name: str, calls: int) -> None:
         outs = [torch.empty_like(q) for _ in range(calls)]
         for i in range(calls):
             ds4a.attn_decode_fp8(wl.layout, q, kr, vr, kc, ks, vc, vs, out=outs[i])
+        torch.cuda.synchronize()
+        if ds4a.device_status() != ds4a.OK:
+            raise RuntimeError("device wait ran out")
+        print(f"{name}: {calls} calls ok")
+        return
+    if name == "prefill_raw_2048_fp8kv":
+        # the 2048-token raw prefill over E4M3 raw rows: widening pass into the workspace, pair kernel
+        wl = W.prefill_raw_2048()
+        up = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
+        q = up(wl.q)
+        kc, ks = ds4a.quantize_kv_fp8(up(wl.k_raw))
+        vc, vs = ds4a.quantize_kv_fp8(up(wl.v_raw))
+        ws = torch.empty(ds4a.prefill_fp8kv_workspace_size(wl.layout), dtype=torch.uint8, device="cuda")
+        outs = [torch.empty_like(q) for _ in range(calls)]
+        for i in range(calls):
+            ds4a.attn_prefill_fp8kv(wl.layout, q, kc, vc, k_raw_scale=ks, v_raw_scale=vs, workspace=ws,
+                                    out=outs[i])
         torch.cuda.synchronize()
         if ds4a.device_status() != ds4a.OK:
             raise RuntimeError("device wait ran out")
