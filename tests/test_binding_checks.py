@@ -137,3 +137,20 @@ def test_indexer_sizes():
     s = torch.zeros((4, 300), dtype=torch.float32)
     raises("scores is", ds4a.indexer_topk, L, s[:, :299], 16)
     raises("out must be", ds4a.indexer_topk, L, s, 16, out=torch.zeros((4, 15), dtype=torch.int32))
+
+
+def test_fp8_prefill_and_graph_arguments():
+    """E4M3 raw rows shorter than the layout, or on the host, are refused
+    before any workspace is sized or allocated; a recording needs a created
+    stream."""
+    o = ops(n_comp=0)
+    L = layout(n_comp=0)
+    codes = torch.zeros((200, D), dtype=torch.uint8)
+    scales = torch.zeros(200, dtype=torch.float32)
+    raises("k_raw holds", ds4a.attn_prefill_fp8kv, L, o["q"], codes[:150], codes, k_raw_scale=scales,
+           v_raw_scale=scales)
+    raises("k_raw_scale must be", ds4a.attn_prefill_fp8kv, L, o["q"], codes, codes, k_raw_scale=scales[:10],
+           v_raw_scale=scales)
+    raises("must be a CUDA tensor", ds4a.attn_prefill_fp8kv, L, o["q"], codes, codes, k_raw_scale=scales,
+           v_raw_scale=scales)
+    raises("created stream", ds4a.Graph, None)
