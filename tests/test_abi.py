@@ -32,6 +32,30 @@ def test_header_declares_the_calls():
         assert n in names
 
 
+def test_header_is_plain_c(tmp_path):
+    """The boundary header compiles as ISO C99 (no C++ or CUDA types), and a C
+    program that calls every declared function links against the library."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    names = declared_functions()
+    src = tmp_path / "uses_header.c"
+    src.write_text('#include "ds4a.h"\n#include <stddef.h>\ntypedef void (*fn)(void);\n'
+                   "fn table[] = {\n" + ",\n".join(f"  (fn)&{n}" for n in names) + "\n};\n"
+                   "int main(void) { return table[0] == NULL; }\n")
+    ds4a_build.build()
+    libdir = os.path.dirname(ds4a._LIB_PATH)
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-pedantic",
+                        "-I", os.path.join(ROOT, "include"), "-c", str(src), "-o", str(tmp_path / "u.o")],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([cc, str(tmp_path / "u.o"), "-o", str(tmp_path / "u"), "-L", libdir, "-lds4a",
+                        "-Wl,--allow-shlib-undefined"], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+
+
 def test_every_declared_symbol_is_exported(lib):
     missing = [n for n in declared_functions() if not hasattr(lib, n)]
     assert not missing, missing
