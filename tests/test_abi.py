@@ -34,7 +34,8 @@ def test_header_declares_the_calls():
 
 def test_header_is_plain_c(tmp_path):
     """The boundary header compiles as ISO C99 (no C++ or CUDA types), and a C
-    program that calls every declared function links against the library."""
+    program that takes the address of every declared function links against
+    the library."""
     import shutil
     import subprocess
     cc = shutil.which("gcc") or shutil.which("cc")
