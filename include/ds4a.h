@@ -549,7 +549,9 @@ ds4a_status ds4a_selftest_wait_timeout(uint64_t timeout_ns, ds4a_stream_t stream
  * ds4a_graph_begin / ds4a_graph_end / ds4a_graph_launch / ds4a_graph_destroy -
  * record the ds4a calls a thread makes on one stream and replay them as one
  * CUDA graph (a serving step issued as one launch instead of each call's host
- * work: argument checks, tensor maps, one launch per kernel).
+ * work: argument checks, tensor maps, one launch per kernel; the counterpart
+ * of the engine's one command-buffer chain per layer, [P2] "Whole-Model Graph
+ * Execution").  Runtime plumbing: it computes nothing itself.
  *   ds4a_graph_begin(stream)   starts the recording.  stream must be a created
  *                              stream (NULL, the legacy default stream, is
  *                              rejected).  The first call on a device loads
