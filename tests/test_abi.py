@@ -176,6 +176,31 @@ def test_prefill_fp8kv_workspace_size(lib):
     assert f(None) == 0
 
 
+def test_prefill_fp8kv_workspace_covers_exactly_the_visible_rows(lib):
+    """On random raw-only layouts the workspace holds two fp16 rows for each
+    raw row the oracle's window rule makes visible to at least one query (the
+    union over the queries is one run of rows), and nothing more."""
+    import numpy as np
+    import oracle
+    rng = np.random.default_rng(20261203)
+    f = lib.ds4a_attn_prefill_fp8kv_workspace_size
+    for _ in range(300):
+        T = int(rng.integers(2, 200))
+        window = int(rng.integers(1, 129))
+        n_raw = int(rng.integers(1, 700))
+        raw_pos0 = int(rng.integers(0, 2000))
+        q_pos0 = int(rng.integers(max(0, raw_pos0 - 300), raw_pos0 + n_raw + 300))
+        L = dict(T=T, q_pos0=q_pos0, n_raw=n_raw, raw_pos0=raw_pos0, n_comp=0, ratio=128, window=window)
+        seen = np.zeros(n_raw, dtype=bool)
+        for t in range(T):
+            seen |= oracle.raw_visible(L, q_pos0 + t)
+        idx = np.flatnonzero(seen)
+        if idx.size:
+            assert idx[-1] - idx[0] + 1 == idx.size, L  # one run of rows
+        got = f(ctypes.byref(_layout(**L)))
+        assert got == idx.size * 2 * 1024, (L, got, idx.size)
+
+
 def test_prefill_fp8kv_workspace_is_checked(lib):
     """The pair path rejects a missing, short or misaligned workspace and bad
     code rows or scales before any device access."""
