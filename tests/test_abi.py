@@ -92,6 +92,40 @@ def test_decode_workspace_size(lib):
     assert lib.ds4a_attn_decode_workspace_size(None, 5) == 0
 
 
+def test_default_split_count_is_the_fewest_with_the_shortest_chain(lib):
+    """Without a GPU the library assumes 148 SMs.  For T tokens of n tiles
+    each, s0 = min(ceil(148 / T), n) splits give a longest range of
+    ceil(n / s0) tiles; the default is the fewest splits with no longer a
+    range (one fewer split would lengthen it).  Tiles are 64 rows when every
+    (token, split) item of 64-row tiles fits on its own SM and a token has at
+    most 32 of them, else 128 rows."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("the SM count of a present GPU replaces the 148 assumed here")
+    import numpy as np
+    rng = np.random.default_rng(7)
+    cdiv = lambda a, b: -(-a // b)  # noqa: E731
+    for _ in range(400):
+        T = int(rng.choice([1, 1, 1, 2, 3, 5, 8, 17, 64, 200]))
+        n_raw = int(rng.integers(0, 400))
+        n_comp = int(rng.integers(0, 70000)) if rng.random() < 0.7 else int(rng.integers(0, 600))
+        window = int(rng.integers(1, 300))
+        if n_raw + n_comp == 0:
+            n_comp = 1
+        L = _layout(T=T, q_pos0=10 ** 7, n_raw=n_raw, raw_pos0=10 ** 7 - n_raw + 1, n_comp=n_comp, ratio=128,
+                    window=window)
+        raw = min(window, n_raw)
+        tiles = lambda rows: cdiv(raw, rows) + cdiv(n_comp, rows)  # noqa: E731
+        half = 2 * tiles(128)
+        n = tiles(64) if (half <= 32 and half * T <= 148) else tiles(128)
+        got = lib.ds4a_attn_decode_default_splits(ctypes.byref(L))
+        s0 = min(cdiv(148, T), n)
+        assert 1 <= got <= s0, (T, n, got)
+        assert cdiv(n, got) == cdiv(n, s0), (T, n, got)
+        if got > 1:
+            assert cdiv(n, got - 1) > cdiv(n, s0), (T, n, got)
+
+
 FAKE = ctypes.c_void_p(1 << 20)       # never dereferenced: validation fails first
 MISALIGNED = ctypes.c_void_p((1 << 20) + 8)
 
